@@ -1,0 +1,78 @@
+"""Pins of the oracle's main-KV entry build (compression, RMSNorm, RoPE, FP4)
+against closed forms, library routines and the invariants the pages state."""
+import numpy as np
+import torch
+
+from oracle import csa2_oracle as o
+from serving_lightning_indexer_gb300 import workloads as W
+
+
+def _inputs(n_tok, seed):
+    C, Z, gamma = W.make_compress_inputs(n_tok, seed)
+    return (C.float().numpy().astype(np.float64), Z.float().numpy().astype(np.float64),
+            gamma.numpy().astype(np.float64))
+
+
+def test_m1_weight_is_identically_one():
+    # V4.1 Q&A page: for m=1 the softmax weight is identically 1 (no Z at all)
+    C, Z, gamma = _inputs(6, 0)
+    pos = np.arange(6)
+    a = o.compress_latent(C, None, 1, gamma, 1e-6, pos, 10000.0, apply_rope=False)
+    b = o.compress_latent(C, Z, 1, gamma, 1e-6, pos, 10000.0, apply_rope=False)
+    ref = torch.nn.functional.rms_norm(torch.tensor(C), (512,), torch.tensor(gamma), eps=1e-6).numpy()
+    assert np.allclose(a, ref, rtol=1e-12) and np.array_equal(a, b)
+
+
+def test_m2_equal_gates_give_the_mean_and_library_rmsnorm():
+    C, Z, gamma = _inputs(8, 1)
+    Z[:] = 0.3
+    lat = o.compress_latent(C, Z, 2, gamma, 1e-6, np.zeros(4), 10000.0, apply_rope=False)
+    mean = (C[0::2] + C[1::2]) / 2
+    ref = torch.nn.functional.rms_norm(torch.tensor(mean), (512,), torch.tensor(gamma), eps=1e-6).numpy()
+    assert np.allclose(lat, ref, rtol=1e-12)
+
+
+def test_m2_is_per_channel_softmax_over_two_tokens():
+    C, Z, gamma = _inputs(2, 2)
+    lat = o.compress_latent(C, Z, 2, np.ones(512), 0.0, np.zeros(1), 10000.0, apply_rope=False)
+    wts = torch.softmax(torch.tensor(Z), dim=0).numpy()       # library softmax over the 2 tokens
+    x = (wts * C).sum(0)
+    assert np.allclose(lat[0], x / np.sqrt((x * x).mean()), rtol=1e-12)
+
+
+def test_m2_entries_depend_only_on_their_own_pair():
+    # non-overlapping windows: perturbing tokens outside a pair leaves its entry unchanged
+    C, Z, gamma = _inputs(12, 3)
+    pos = np.arange(6) * 2
+    base = o.compress_latent(C, Z, 2, gamma, 1e-6, pos, 10000.0)
+    C2, Z2 = C.copy(), Z.copy()
+    C2[[0, 1, 4, 5, 10, 11]] += 5.0
+    Z2[[0, 1, 4, 5, 10, 11]] -= 2.0
+    pert = o.compress_latent(C2, Z2, 2, gamma, 1e-6, pos, 10000.0)
+    assert np.array_equal(base[[1, 3, 4]], pert[[1, 3, 4]])
+    assert not np.allclose(base[[0, 2, 5]], pert[[0, 2, 5]])
+
+
+def test_rope_matches_complex_rotation_and_keeps_norm():
+    rng = np.random.default_rng(4)
+    y = rng.normal(size=(5, 512))
+    pos = np.array([0, 1, 7, 1000, 1 << 20])
+    r = o.rope_interleaved(y, pos, 10000.0)
+    assert np.array_equal(r[:, :448], y[:, :448])
+    assert np.array_equal(r[0], y[0])                            # position 0: identity
+    z = y[:, 448::2] + 1j * y[:, 449::2]
+    freq = 10000.0 ** (-np.arange(32) / 32.0)
+    zr = z * np.exp(1j * pos[:, None] * freq[None, :])
+    assert np.allclose(r[:, 448::2], zr.real, atol=1e-12) and np.allclose(r[:, 449::2], zr.imag, atol=1e-12)
+    assert np.allclose(np.linalg.norm(r, axis=1), np.linalg.norm(y, axis=1), rtol=1e-13)   # RoPE keeps the norm
+
+
+def test_records_decode_close_to_latent():
+    C, Z, gamma = _inputs(64, 5)
+    rec, lat = o.compress_records(C, Z, 2, gamma, 1e-6, np.arange(32) * 2, 10000.0)
+    dec = o.main_kv_records(rec, np.arange(32))
+    step = np.repeat(o.ue8m0(rec[:, 256:272]), 32, axis=1)      # e2m1 spacing is <= 2 x 2^k
+    assert np.all(np.abs(dec - lat) <= step + 1e-12)
+    assert rec.shape == (32, 288) and (rec[:, 272:] == 0).all()
+    # the report reading's bound: a unit-RMS 512-vector has |x| <= sqrt(512) << 2688
+    assert np.abs(lat).max() < np.sqrt(512) * 1.5
