@@ -1,0 +1,247 @@
+/*
+ * csa2.h -- C ABI of the CSA2 global-attention step on one GB300 (sm_103a).
+ *
+ * The step, as the web pages on DeepSeek-V4.1 CSA2 describe it (CSA2 page,
+ * zdszero.github.io/csa2.html, "一层 CSA2 的 attention 具体怎么算" and
+ * "Hierarchical Sparse Indexer"; DSA page, zdszero.github.io/dsa.html,
+ * "Lightning Indexer"):
+ *
+ *   1. Lightning-Indexer score  I[t,s] = sum_h w[t,h] * ReLU(q[t,h] . k[s])
+ *      (32 heads x 128 dims, FP8 index-K cache)              -> csa2_index_score
+ *   2. top-512 positions -> physical slots, and (Full layer of the decoder) a
+ *      candidate pool of the 2048 blocks of 8 with the highest block maxima
+ *                                                           -> csa2_topk_with_candidates
+ *   3. Reindex: score only the pool, everything else -inf, top-512
+ *                                                           -> csa2_reindex
+ *   4. MQA sparse attention: 64 heads x 512-dim K=V, one joint softmax over
+ *      128 SWA keys + <= 512 main-KV entries + a per-head sink in the
+ *      denominator                                          -> csa2_sparse_attn
+ *   5. main-KV entry build: m=2 per-channel softmax of two tokens (m=1:
+ *      weight 1), RMSNorm, RoPE on the last 64 dims, FP4  -> csa2_compress_m2
+ *
+ * Conventions shared by every call
+ *   - All pointers in the argument structs are DEVICE pointers to
+ *     caller-owned memory (except the struct itself, which lives on the host
+ *     and is read before the call returns).  The library never allocates or
+ *     frees device memory; scratch comes from the caller's workspace, sized by
+ *     csa2_workspace_size().
+ *   - Every call is asynchronous on the given stream (a cudaStream_t passed
+ *     as void*; NULL = legacy default stream) and never synchronises the host.
+ *   - Arguments are validated on the host before any launch; an invalid
+ *     argument returns a status code and launches nothing.  A failed launch
+ *     returns CSA2_ERR_CUDA.
+ *   - Kernels never trap.  An out-of-range page id or slot met on the device
+ *     is skipped and recorded in a device-side error word that
+ *     csa2_check_device_error() reads (it synchronises the stream).
+ *   - Integer layouts are int32, row-major; "ld" arguments are row strides in
+ *     elements.
+ *
+ * Storage formats (the same bytes the oracle decodes)
+ *   index-K page : 8448 B = 64 keys x 128 e4m3 codes, then 64 fp32 scales
+ *                  (DSA page, "KV pool").  Key s of a sequence is in physical
+ *                  page page_table[b][s / 64], row s % 64.
+ *   main-KV record: 288 B at slot*288 = 256 B of 512 e2m1 codes (element 2i
+ *                  in the low nibble of byte i), 16 ue8m0 scales (one per 32
+ *                  elements, value 2^(u-127)), 16 B padding (CSA2 page,
+ *                  "attention 计算的落点": 288 B per entry).
+ *   SWA record   : 528 B at slot*528 = 512 e4m3 codes, then 4 fp32 scales, one
+ *                  per 128 channels (CSA2 page: 528 B FP8 SWA entry).
+ *   slot         : page_table[b][p / 64] * 64 + p % 64 (DSA page, "logits 与
+ *                  top-k"); -1 marks an empty slot.
+ */
+#ifndef CSA2_H_
+#define CSA2_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define CSA2_API __attribute__((visibility("default")))
+#else
+#define CSA2_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  CSA2_OK = 0,
+  CSA2_ERR_NULL = 1,          /* a required pointer is NULL */
+  CSA2_ERR_SHAPE = 2,         /* a size or count is out of range */
+  CSA2_ERR_ALIGN = 3,         /* a pointer or stride is not 16-byte aligned */
+  CSA2_ERR_UNSUPPORTED = 4,   /* a valid but unsupported combination */
+  CSA2_ERR_CUDA = 5,          /* a CUDA runtime call or launch failed */
+  CSA2_ERR_DEVICE_BOUNDS = 6, /* a kernel met an out-of-range page id or slot */
+  CSA2_ERR_WORKSPACE = 7,     /* workspace missing or smaller than required */
+  CSA2_ERR_DEVICE_TIMEOUT = 8 /* a kernel gave up a bounded wait (internal fault) */
+} csa2_status;
+
+/* Fixed sizes of the method. */
+enum {
+  CSA2_IDX_HEADS = 32, CSA2_IDX_DIM = 128,
+  CSA2_ATT_HEADS = 64, CSA2_ATT_DIM = 512, CSA2_ROPE_DIMS = 64,
+  CSA2_PAGE = 64, CSA2_INDEX_PAGE_BYTES = 8448,
+  CSA2_MAIN_RECORD_BYTES = 288, CSA2_SWA_RECORD_BYTES = 528,
+  CSA2_MAX_TOPK = 2048, CSA2_POOL_BLOCK = 8, CSA2_MAX_SWA = 128
+};
+
+/* Static description of a status code. */
+CSA2_API const char* csa2_status_string(int status);
+/* Human-readable detail of the last error returned on the calling thread
+ * (thread-local; valid until the thread's next call). */
+CSA2_API const char* csa2_last_error_detail(void);
+
+/* Which query rows see which entries.  Row t belongs to sequence
+ * row_seq[t] (row_seq NULL: sequence t, which needs T == B; an id outside
+ * [0, B) makes the row see no entries).  The entries
+ * visible to row t are E_t = n_visible[b] in decode (row_pos NULL), or
+ * E_t = (row_pos[t] + 1) / ratio_m in prefill, clipped to n_visible[b] when
+ * n_visible is given (CSA2 page, "候选池不减少存储": visible = (pos+1)//ratio).
+ * At least one of n_visible, row_pos must be given. */
+typedef struct {
+  int32_t T;                  /* query rows, >= 1 */
+  int32_t B;                  /* sequences, >= 1 */
+  const int32_t* row_seq;     /* [T] in [0,B) or NULL */
+  const int32_t* row_pos;     /* [T] token position or NULL */
+  const int32_t* n_visible;   /* [B] visible entries or NULL */
+  int32_t ratio_m;            /* 1 or 2 (only used with row_pos) */
+} csa2_rows;
+
+/* ---- 1. Lightning-Indexer score (Full layer) --------------------------------
+ * scores[t][s] = k_scale[s] * sum_h (w[t,h] * q_scale[t,h]) * ReLU(q8[t,h] . k8[s])
+ * which equals sum_h w[t,h] * ReLU(q[t,h] . k[s]) on the dequantised q and k
+ * because q_scale, k_scale >= 0 (DSA page, "fp8 与 scale 的吸收").  No
+ * 1/sqrt(H) or 1/sqrt(d) factor is applied.
+ * Written: scores[t][s] for s < round_up(E_t, 128) clipped to ld_scores
+ * (s >= E_t holds -inf); block_max[t][j] = max over the visible positions of
+ * block j (8 positions) for j < ceil(E_t / 8), if block_max is not NULL.
+ * Alignment: q_fp8, index_k 16 B; ld_scores and ld_block_max multiples of 4.
+ * Prefill (row_pos given, B == 1, T >= 64) runs the query-blocked tensor-core
+ * path (8 queries x 32 heads per MMA); everything else the per-row scan. */
+typedef struct {
+  const uint8_t* q_fp8;       /* [T,32,128] e4m3 codes */
+  const float* q_scale;       /* [T,32] >= 0 */
+  const float* w;             /* [T,32] head weights */
+  const uint8_t* index_k;     /* pages of 8448 B */
+  int64_t index_k_pages;      /* number of pages in index_k */
+  const int32_t* page_table;  /* [B, pt_stride] logical page -> physical page */
+  int32_t pt_stride;
+  csa2_rows rows;
+  float* scores; int64_t ld_scores;           /* [T, ld_scores] */
+  float* block_max; int64_t ld_block_max;     /* optional [T, ld_block_max] */
+} csa2_index_score_args;
+CSA2_API int csa2_index_score(const csa2_index_score_args* args, void* workspace, size_t ws_bytes, void* stream);
+
+/* ---- 2. top-k with slot translation and the candidate pool ------------------
+ * Per row: the k (<= 2048) positions s < E_t with the largest finite scores,
+ * ordered by score descending then position ascending (ties go to the lower
+ * position), -1 filled when fewer than k are finite (DSA page, "Top-k：选的是
+ * token，不是 block").  topk_slot[t][i] = slot of topk_pos[t][i] (-1 kept).
+ * Pool (pool_blocks not NULL; CSA2 page, "Hierarchical Sparse Indexer",
+ * "attention 计算的落点" select_candidate_blocks): block scores are
+ * block_max[t][0..ceil(E_t/8)); the newest block ceil(E_t/8)-1 is always kept
+ * and counts toward pool_n; the other places go to the highest block maxima
+ * (ties: lower block id); output ascending block ids, -1 padded; with at most
+ * pool_n blocks every block is kept.
+ * Workspace: csa2_workspace_size(CSA2_CALL_TOPK, args, &bytes). */
+typedef struct {
+  const float* scores; int64_t ld_scores;     /* [T, ld_scores] */
+  const float* block_max; int64_t ld_block_max; /* [T, ld_block_max], needed for the pool */
+  const int32_t* page_table; int32_t pt_stride; /* slot translation; NULL: no slots */
+  csa2_rows rows;
+  int32_t k;                                   /* 1..2048 */
+  int32_t* topk_pos;                           /* [T, ld_topk] */
+  int32_t* topk_slot;                          /* [T, ld_topk] or NULL */
+  int64_t ld_topk;                             /* >= k */
+  int32_t* pool_blocks;                        /* [T, pool_n] or NULL */
+  int32_t pool_n;                              /* 1..2048 when pool_blocks is set */
+} csa2_topk_args;
+CSA2_API int csa2_topk_with_candidates(const csa2_topk_args* args, void* workspace, size_t ws_bytes, void* stream);
+
+/* ---- 3. Reindex: pool-only rescoring and top-k ------------------------------
+ * Candidate i of row t is position p = 8 * pool_blocks[t][i / 8] + i % 8; it
+ * is scored like csa2_index_score when the block id is >= 0 and p < E_t, and
+ * is -inf otherwise (CSA2 page, "Hierarchical Sparse Indexer" item 2: a
+ * Reindex layer scores only the pool).  Then the top-k of those scores, as in
+ * csa2_topk_with_candidates, reported as positions and slots.
+ * pool_scores (optional, [T, 8*pool_n]) receives the candidate scores. */
+typedef struct {
+  const uint8_t* q_fp8; const float* q_scale; const float* w;  /* as in index_score */
+  const uint8_t* index_k; int64_t index_k_pages;
+  const int32_t* page_table; int32_t pt_stride;
+  csa2_rows rows;
+  const int32_t* pool_blocks; int32_t pool_n;  /* [T, pool_n], pool_n <= 2048 */
+  int32_t k;                                   /* 1..2048 */
+  int32_t* topk_pos; int32_t* topk_slot; int64_t ld_topk;
+  float* pool_scores;                          /* optional [T, 8*pool_n] */
+} csa2_reindex_args;
+CSA2_API int csa2_reindex(const csa2_reindex_args* args, void* workspace, size_t ws_bytes, void* stream);
+
+/* ---- 4. MQA sparse attention with SWA keys and an attention sink -----------
+ * For row t and head i (CSA2 page, attention equation):
+ *   logit_j = (q[t,i] . kv_j) * softmax_scale,  j over the valid SWA slots
+ *             swa_slot[t][0..n_swa) and main slots topk_slot[t][0..k) (-1 skipped)
+ *   out[t,i] = sum_j e^(logit_j - M) kv_j / (sum_j e^(logit_j - M) + e^(sink[i] - M))
+ * kv_j is the dequantised 512-vector (K = V); the sink is not scaled.
+ * lse[t,i] = M + ln(denominator) (natural log, sink included).
+ * softmax_scale == 0 selects 1/sqrt(512).  Alignment: q, main_kv, swa_kv, out 16 B. */
+typedef struct {
+  const uint16_t* q;                           /* [T,64,512] bf16 */
+  const uint8_t* main_kv; int64_t main_kv_slots;   /* 288-B records */
+  const int32_t* topk_slot; int32_t k; int64_t ld_topk;  /* [T, ld_topk]; k <= 2048 */
+  const uint8_t* swa_kv; int64_t swa_slots;        /* 528-B records */
+  const int32_t* swa_slot; int32_t n_swa; int64_t ld_swa;  /* [T, ld_swa]; n_swa <= 128 */
+  const float* sink;                           /* [64] */
+  float softmax_scale;
+  int32_t T;
+  int32_t out_bf16;                            /* 0: fp32 out, 1: bf16 out */
+  void* out;                                   /* [T,64,512] */
+  float* lse;                                  /* optional [T,64] */
+} csa2_sparse_attn_args;
+CSA2_API int csa2_sparse_attn(const csa2_sparse_attn_args* args, void* workspace, size_t ws_bytes, void* stream);
+
+/* ---- 5. main-KV entry build (m = 2, or m = 1) -------------------------------
+ * Entry e (0 <= e < n_tokens / m) is built from tokens e*m .. e*m+m-1 of C, Z:
+ *   m=2: x[c] = sum_j softmax_j(Z[2e+j][c]) * C[2e+j][c]  (per channel, no APE)
+ *   m=1: x = C[e]                                         (weight identically 1)
+ *   y = x / sqrt(mean(x^2) + eps) * gamma                 (RMSNorm)
+ *   RoPE on dims 448..511 when apply_rope: pairs (448+2i, 449+2i) rotated by
+ *   pos * rope_theta^(-2i/64), pos = entry_pos[e] if given, else (first_entry + e) * m
+ *   FP4: per 32 elements u = k + 127 with k the smallest integer such that
+ *   6 * 2^k >= amax (u = 127 for amax 0, clamped to [0,254]); codes = e2m1
+ *   round-to-nearest-even of y / 2^k, saturating at 6; sign bit for y < 0.
+ * The 288-B record goes to slot entry_slot[e] if given, else to
+ * page_table[(first_entry + e) / 64] * 64 + (first_entry + e) % 64.
+ * (CSA2 page item 3 and V4.1 Q&A page; V4.1-Flash report reading, section 六:
+ * FP4 after RoPE, no global scale.)  latent_out (optional, fp32 [n_entries,512])
+ * receives y after RoPE, before quantisation.  Alignment: C, Z 16 B. */
+typedef struct {
+  const uint16_t* C; const uint16_t* Z;        /* [n_tokens,512] bf16; Z unused for m=1 */
+  int64_t n_tokens; int32_t ratio_m;
+  const float* gamma; float eps;               /* [512] */
+  int32_t apply_rope; float rope_theta;
+  int64_t first_entry;
+  const int32_t* entry_pos;                    /* optional [n_entries] */
+  uint8_t* main_kv; int64_t main_kv_slots;     /* 288-B records */
+  const int32_t* page_table; int64_t pt_len;   /* [pt_len] of the one sequence, or NULL */
+  const int32_t* entry_slot;                   /* optional [n_entries] direct slots */
+  float* latent_out;                           /* optional [n_entries,512] */
+} csa2_compress_args;
+CSA2_API int csa2_compress_m2(const csa2_compress_args* args, void* stream);
+
+/* ---- workspace, device errors ------------------------------------------------ */
+enum { CSA2_CALL_INDEX_SCORE = 1, CSA2_CALL_TOPK = 2, CSA2_CALL_REINDEX = 3, CSA2_CALL_SPARSE_ATTN = 4 };
+/* Bytes of workspace the call needs with these arguments (0 if none). */
+CSA2_API int csa2_workspace_size(int which_call, const void* args, size_t* bytes);
+/* Synchronises the stream, then returns CSA2_ERR_DEVICE_BOUNDS or
+ * CSA2_ERR_DEVICE_TIMEOUT if a kernel on this device recorded one since the
+ * last check (and clears the record), else CSA2_OK. */
+CSA2_API int csa2_check_device_error(void* stream);
+/* Library version string. */
+CSA2_API const char* csa2_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* CSA2_H_ */

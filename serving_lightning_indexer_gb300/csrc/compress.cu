@@ -1,0 +1,180 @@
+// Main-KV entry build of a Full layer.
+//
+// CSA2 page, "一层 CSA2 的 attention 具体怎么算" item 3, and the V4.1 Q&A page
+// (compression operator): with m = 2 an entry is the per-channel
+// softmax-weighted sum of two adjacent, non-overlapping tokens (no APE); with
+// m = 1 the weight is identically 1.  The result goes through RMSNorm, RoPE on
+// the last 64 dims, and FP4 quantisation after RoPE (V4.1-Flash report
+// reading, section 六), into a 288-B record (e2m1 codes + ue8m0 scale per 32).
+//
+// One warp per entry, lane l owning channels 16l .. 16l+15 (two e2m1 scale
+// groups span a lane pair).  HBM-bound: 2 KB (m=2: 4 KB) read, 288 B written.
+#include <math.h>
+
+#include "csa2_device.cuh"
+#include "csa2_internal.h"
+
+namespace csa2 {
+
+namespace {
+
+struct CompressParams {
+  const __nv_bfloat16* C;
+  const __nv_bfloat16* Z;
+  long long n_entries;
+  int ratio_m;
+  const float* gamma;
+  float eps;
+  int apply_rope;
+  double rope_theta;
+  long long first_entry;
+  const int* entry_pos;
+  uint8_t* main_kv;
+  long long main_slots;
+  const int* page_table;
+  long long pt_len;
+  const int* entry_slot;
+  float* latent_out;
+  uint32_t* err;
+};
+
+__device__ __forceinline__ void load16_bf16(const __nv_bfloat16* src, float (&v)[16]) {
+  const uint4* s = reinterpret_cast<const uint4*>(src);
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const uint4 r = __ldg(s + i);
+    const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&w[j]);
+      const float2 f = __bfloat1622float2(b);
+      v[8 * i + 2 * j] = f.x;
+      v[8 * i + 2 * j + 1] = f.y;
+    }
+  }
+}
+
+// e2m1 code of a value already divided by its group scale: nearest magnitude
+// among 0, .5, 1, 1.5, 2, 3, 4, 6 with ties to the even code, saturating.
+__device__ __forceinline__ uint32_t e2m1_code(float v) {
+  const float a = fabsf(v);
+  uint32_t c = (a > 0.25f) + (a >= 0.75f) + (a > 1.25f) + (a >= 1.75f) + (a > 2.5f) + (a >= 3.5f) + (a > 5.0f);
+  return c | (v < 0.f ? 8u : 0u);
+}
+
+__global__ void __launch_bounds__(256) compress_kernel(const __grid_constant__ CompressParams p) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long e = static_cast<long long>(blockIdx.x) * 8 + warp;
+  if (e >= p.n_entries) return;
+  const int c0 = lane * 16;
+  float x[16];
+  if (p.ratio_m == 1) {
+    load16_bf16(p.C + e * 512 + c0, x);
+  } else {
+    float ca[16], cb[16], za[16], zb[16];
+    const long long r0 = e * 2;
+    load16_bf16(p.C + r0 * 512 + c0, ca);
+    load16_bf16(p.C + (r0 + 1) * 512 + c0, cb);
+    load16_bf16(p.Z + r0 * 512 + c0, za);
+    load16_bf16(p.Z + (r0 + 1) * 512 + c0, zb);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const float zm = fmaxf(za[i], zb[i]);
+      const float ea = expf(za[i] - zm), eb = expf(zb[i] - zm);
+      x[i] = (ea * ca[i] + eb * cb[i]) / (ea + eb);
+    }
+  }
+  // RMSNorm over the 512 channels
+  float ss = 0.f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) ss = fmaf(x[i], x[i], ss);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+  const float inv = 1.0f / sqrtf(ss / 512.0f + p.eps);
+  float y[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) y[i] = x[i] * inv * __ldg(p.gamma + c0 + i);
+  // RoPE on dims 448..511: interleaved pairs, angle pos * theta^(-2i/64)
+  if (p.apply_rope && lane >= 28) {
+    const long long pos = p.entry_pos ? static_cast<long long>(__ldg(p.entry_pos + e)) : (p.first_entry + e) * p.ratio_m;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int i = (c0 - 448) / 2 + j;
+      const double inv_freq = pow(p.rope_theta, -2.0 * i / 64.0);
+      double s, c;
+      sincos(static_cast<double>(pos) * inv_freq, &s, &c);
+      const double a = y[2 * j], b = y[2 * j + 1];
+      y[2 * j] = static_cast<float>(a * c - b * s);
+      y[2 * j + 1] = static_cast<float>(a * s + b * c);
+    }
+  }
+  if (p.latent_out) {
+    float4* lo = reinterpret_cast<float4*>(p.latent_out + e * 512 + c0);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) lo[i] = make_float4(y[4 * i], y[4 * i + 1], y[4 * i + 2], y[4 * i + 3]);
+  }
+  // FP4: group of 32 = lanes (2g, 2g+1)
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(y[i]));
+  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+  int u = 127;
+  if (amax > 0.f) {
+    int ex;
+    const float f = frexpf(amax, &ex);           // amax = f * 2^ex, f in [0.5, 1)
+    const int k = (f <= 0.75f) ? ex - 3 : ex - 2;  // smallest k with 6 * 2^k >= amax
+    u = min(max(k + 127, 0), 254);
+  }
+  uint32_t packed[2] = {0u, 0u};
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const uint32_t code = e2m1_code(ldexpf(y[i], 127 - u));
+    packed[i >> 3] |= code << (4 * (i & 7));
+  }
+  // destination slot
+  long long slot;
+  if (p.entry_slot) {
+    slot = __ldg(p.entry_slot + e);
+  } else {
+    const long long ent = p.first_entry + e;
+    const long long lp = ent >> 6;
+    slot = (lp < p.pt_len) ? static_cast<long long>(__ldg(p.page_table + lp)) * 64 + (ent & 63) : -1;
+  }
+  if (slot < 0 || slot >= p.main_slots) {
+    if (lane == 0) set_error(p.err, kErrBounds);
+    return;
+  }
+  uint8_t* rec = p.main_kv + slot * 288;
+  *reinterpret_cast<uint2*>(rec + lane * 8) = make_uint2(packed[0], packed[1]);
+  if ((lane & 1) == 0) rec[256 + (lane >> 1)] = static_cast<uint8_t>(u);
+  if (lane < 4) *reinterpret_cast<uint32_t*>(rec + 272 + lane * 4) = 0u;
+}
+
+}  // namespace
+
+cudaError_t launch_compress(const CompressLaunch& a, const DeviceCtx& ctx, cudaStream_t st) {
+  CompressParams p;
+  p.C = reinterpret_cast<const __nv_bfloat16*>(a.C);
+  p.Z = reinterpret_cast<const __nv_bfloat16*>(a.Z);
+  p.n_entries = a.n_entries;
+  p.ratio_m = a.ratio_m;
+  p.gamma = a.gamma;
+  p.eps = a.eps;
+  p.apply_rope = a.apply_rope;
+  p.rope_theta = static_cast<double>(a.rope_theta);
+  p.first_entry = a.first_entry;
+  p.entry_pos = a.entry_pos;
+  p.main_kv = a.main_kv;
+  p.main_slots = a.main_slots;
+  p.page_table = a.page_table;
+  p.pt_len = a.pt_len;
+  p.entry_slot = a.entry_slot;
+  p.latent_out = a.latent_out;
+  p.err = ctx.err;
+  if (a.n_entries == 0) return cudaSuccess;
+  const long long blocks = (a.n_entries + 7) / 8;
+  compress_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace csa2

@@ -1,0 +1,456 @@
+// Lightning-Indexer scoring on the 5th-generation tensor cores.
+//
+// Score (CSA2 page, "一层 CSA2 的 attention 具体怎么算" item 4; DSA page,
+// "打分公式" and "fp8 与 scale 的吸收"):
+//     I[t,s] = k_scale[s] * sum_h w'[t,h] * ReLU(q8[t,h] . k8[s]),  w' = w * q_scale
+//
+// One persistent, warp-specialised kernel serves three tilings:
+//   * scan,   NQ=1: decode.  A tile is 128 consecutive entries (two 64-entry
+//                   pages) of one row's sequence x the row's 32 heads.
+//   * scan,   NQ=8: prefill of one sequence.  A tile is 128 entries x 8
+//                   consecutive query rows (256 = 8 x 32 head columns).
+//   * gather, NQ=1: Reindex.  A tile is 16 candidate blocks of 8 entries
+//                   (CSA2 page, "Hierarchical Sparse Indexer": a Reindex
+//                   layer scores only the pool) x the row's 32 heads.
+// The contraction D[key, (query, head)] = K8 . Q8^T (K = 128) runs as
+// tcgen05.mma kind::f8f6f4 with keys on M = 128 and (query, head) on N,
+// both operands TMA-staged in the 128-byte swizzle layout, the fp32
+// accumulator in TMEM (double-buffered).  The epilogue reads one key row per
+// thread (tcgen05.ld 32x32b), applies ReLU, the head weights, the per-key
+// scale, the visibility mask, and emits the 8-entry block maxima used by the
+// candidate pool.
+//
+// Roles (192 threads): warp 0 = TMA producer, warp 1 = TMEM owner + MMA
+// issuer, warps 2..5 = epilogue (warp w reads TMEM lanes 32*(w%4)...).
+#include <math.h>
+
+#include "csa2_device.cuh"
+#include "csa2_internal.h"
+
+namespace csa2 {
+
+namespace {
+
+constexpr int kModeScan = 0;
+constexpr int kModeGather = 1;
+constexpr int kTileKeys = 128;
+constexpr int kRowBytes = 128;                       // one FP8 key / one head of q
+constexpr int kPageRows = 66;                        // an 8448-B page seen as 66 rows of 128 B
+constexpr int kMaxQB = 4096;                         // query blocks per launch
+
+struct IdxParams {
+  const float* q_scale;
+  const float* w;
+  const uint8_t* index_k;
+  long long n_pages;
+  const int* page_table;
+  int pt_stride;
+  RowsDev rows;
+  float* out;
+  long long ld_out;
+  float* block_max;
+  long long ld_bm;
+  const int* pool_blocks;
+  int pool_n;
+  uint32_t* err;
+};
+
+template <int NQ>
+struct IdxCfg {
+  static constexpr int kStages = (NQ == 1) ? 8 : 6;
+  static constexpr int kQBytes = NQ * 32 * kRowBytes;
+  static constexpr int kAccCols = NQ * 32;
+  static constexpr int kTmemCols = 2 * kAccCols < 32 ? 32 : 2 * kAccCols;
+  static constexpr int kKeyBytes = kTileKeys * kRowBytes;
+  static constexpr int kOffKeys = 0;
+  static constexpr int kOffQ = kOffKeys + kStages * kKeyBytes;
+  static constexpr int kOffScales = kOffQ + 2 * kQBytes;
+  static constexpr int kOffW = kOffScales + kStages * kTileKeys * 4;
+  static constexpr int kOffBars = kOffW + NQ * 32 * 4;
+  static constexpr int kNumBars = 2 * kStages + 8;
+  static constexpr int kOffMisc = kOffBars + kNumBars * 8;
+  static constexpr int kOffPrefix = kOffMisc + 16;
+  static size_t smem_bytes(int nqb) { return 1024 + kOffPrefix + static_cast<size_t>(nqb + 1) * 4; }
+};
+static_assert((2 * 32) == IdxCfg<1>::kTmemCols, "decode accumulators: 2 x 32 columns");
+static_assert(512 == IdxCfg<8>::kTmemCols, "prefill accumulators: 2 x 256 columns");
+
+// Entries visible to the rows of a query block and the number of tiles.
+template <int NQ, int MODE>
+__device__ __forceinline__ int qb_tiles(const IdxParams& p, int qb) {
+  if (MODE == kModeGather) return (p.pool_n * 8 + kTileKeys - 1) / kTileKeys;
+  const int t0 = qb * NQ;
+  const int b = row_seq_of(p.rows, t0);
+  int emax = 0;
+#pragma unroll
+  for (int j = 0; j < NQ; ++j)
+    if (t0 + j < p.rows.T) emax = max(emax, visible_of(p.rows, t0 + j, b));
+  return (emax + kTileKeys - 1) / kTileKeys;
+}
+
+__device__ __forceinline__ int find_qb(const int* prefix, int nqb, long long g) {
+  int lo = 0, hi = nqb - 1;  // largest qb with prefix[qb] <= g
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (prefix[mid] <= g) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+template <int NQ, int MODE>
+__global__ void __launch_bounds__(192, 1)
+    index_tiles_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_kv,
+                       const __grid_constant__ IdxParams p) {
+  using Cfg = IdxCfg<NQ>;
+  constexpr int S = Cfg::kStages;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* s_keys = smem + Cfg::kOffKeys;
+  uint8_t* s_q = smem + Cfg::kOffQ;
+  float* s_scales = reinterpret_cast<float*>(smem + Cfg::kOffScales);
+  float* s_w = reinterpret_cast<float*>(smem + Cfg::kOffW);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Cfg::kOffBars);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + S;
+  uint64_t* qfull = bars + 2 * S;
+  uint64_t* qempty = qfull + 2;
+  uint64_t* tfull = qempty + 2;
+  uint64_t* tempty = tfull + 2;
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + Cfg::kOffMisc);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(smem + Cfg::kOffMisc + 4);
+  int* s_prefix = reinterpret_cast<int*>(smem + Cfg::kOffPrefix);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int T = p.rows.T;
+  const int nqb = (MODE == kModeScan) ? (T + NQ - 1) / NQ : T;
+
+  for (int i = threadIdx.x; i < nqb; i += blockDim.x) s_prefix[i + 1] = qb_tiles<NQ, MODE>(p, i);
+  if (threadIdx.x == 0) {
+    s_prefix[0] = 0;
+    *s_abort = 0;
+    for (int i = 0; i < S; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1 + 4);  // MMA commit + one arrival per epilogue warp
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&qfull[i], 1);
+      mbar_init(&qempty[i], 1);
+      mbar_init(&tfull[i], 1);
+      mbar_init(&tempty[i], 4);
+    }
+    fence_mbar_init();
+    prefetch_tmap(&map_q);
+    prefetch_tmap(&map_kv);
+  }
+  if (warp == 1) {
+    tmem_alloc(s_tmem, Cfg::kTmemCols);
+    tmem_relinquish();
+  }
+  __syncthreads();
+  if (warp == 0) {  // inclusive scan of the tile counts by one warp
+    const int per = (nqb + 31) / 32;
+    const int lo = 1 + lane * per;
+    const int hi = min(lo + per, nqb + 1);
+    int sum = 0;
+    for (int i = lo; i < hi; ++i) sum += s_prefix[i];
+    int incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    int run = incl - sum;
+    for (int i = lo; i < hi; ++i) {
+      run += s_prefix[i];
+      s_prefix[i] = run;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *s_tmem;
+  const long long total = s_prefix[nqb];
+  const long long g_begin = total * blockIdx.x / gridDim.x;
+  const long long g_end = total * (blockIdx.x + 1) / gridDim.x;
+
+  if (g_begin < g_end) {
+    if (warp == 0 && lane == 0) {
+      // ------------------------------------------------------------ producer
+      const uint64_t pol_keys = (MODE == kModeScan && NQ > 1) ? l2_policy_evict_last() : l2_policy_evict_first();
+      const uint64_t pol_q = l2_policy_evict_last();
+      int qb = find_qb(s_prefix, nqb, g_begin);
+      int cur_qb = -1, qcount = 0, b = 0, emax = 0, t0 = 0;
+      long long it = 0;
+      bool ok = true;
+      for (long long g = g_begin; g < g_end; ++g, ++it) {
+        while (g >= s_prefix[qb + 1]) ++qb;
+        const int kb = static_cast<int>(g - s_prefix[qb]);
+        if (qb != cur_qb) {
+          cur_qb = qb;
+          const int slot = qcount & 1;
+          if (!(ok = mbar_wait(&qempty[slot], ((qcount >> 1) & 1) ^ 1, s_abort))) break;
+          t0 = (MODE == kModeScan) ? qb * NQ : qb;
+          mbar_arrive_expect_tx(&qfull[slot], Cfg::kQBytes);
+          tma_load_2d(s_q + slot * Cfg::kQBytes, &map_q, 0, t0 * 32, &qfull[slot], pol_q);
+          ++qcount;
+          b = row_seq_of(p.rows, t0);
+          emax = 0;
+          for (int j = 0; j < (MODE == kModeScan ? NQ : 1); ++j)
+            if (t0 + j < T) emax = max(emax, visible_of(p.rows, t0 + j, b));
+        }
+        const int s = static_cast<int>(it % S);
+        if (!(ok = mbar_wait(&empty[s], static_cast<uint32_t>((it / S) & 1) ^ 1u, s_abort))) break;
+        uint8_t* kdst = s_keys + s * Cfg::kKeyBytes;
+        float* sdst = s_scales + s * kTileKeys;
+        const int* ptab = p.page_table + static_cast<long long>(b) * p.pt_stride;
+        if (MODE == kModeScan) {
+          int pg[2];
+          uint32_t bytes = 0;
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int lp = kb * 2 + h;
+            pg[h] = -1;
+            if (lp * 64 < emax) {
+              const int phys = (lp < p.pt_stride) ? __ldg(ptab + lp) : -1;
+              if (phys >= 0 && phys < p.n_pages) {
+                pg[h] = phys;
+                bytes += 64 * kRowBytes + 64 * 4;
+              } else {
+                set_error(p.err, kErrBounds);
+              }
+            }
+          }
+          mbar_arrive_expect_tx(&full[s], bytes);
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            if (pg[h] < 0) continue;
+            tma_load_2d(kdst + h * 64 * kRowBytes, &map_kv, 0, pg[h] * kPageRows, &full[s], pol_keys);
+            bulk_load(sdst + h * 64, p.index_k + static_cast<long long>(pg[h]) * 8448 + 8192, 256, &full[s],
+                      pol_keys);
+          }
+        } else {
+          int rowid[16];
+          uint32_t bytes = 0;
+          const int* pool = p.pool_blocks + static_cast<long long>(t0) * p.pool_n;
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int cb = kb * 16 + j;
+            const int blk = (cb < p.pool_n) ? __ldg(pool + cb) : -1;
+            rowid[j] = -1;
+            if (blk >= 0 && blk * 8 < emax) {
+              const int phys = ((blk >> 3) < p.pt_stride) ? __ldg(ptab + (blk >> 3)) : -1;
+              if (phys >= 0 && phys < p.n_pages) {
+                rowid[j] = phys * kPageRows + (blk & 7) * 8;
+                bytes += 8 * kRowBytes + 8 * 4;
+              } else {
+                set_error(p.err, kErrBounds);
+              }
+            }
+          }
+          mbar_arrive_expect_tx(&full[s], bytes);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            if (rowid[j] < 0) continue;
+            const int phys = rowid[j] / kPageRows;
+            const int r = rowid[j] - phys * kPageRows;
+            tma_load_2d(kdst + j * 8 * kRowBytes, &map_kv, 0, rowid[j], &full[s], pol_keys);
+            bulk_load(sdst + j * 8, p.index_k + static_cast<long long>(phys) * 8448 + 8192 + r * 4, 32, &full[s],
+                      pol_keys);
+          }
+        }
+      }
+      if (!ok) {
+        *s_abort = 1;
+        set_error(p.err, kErrTimeout);
+      }
+      // the copies of the last stages must land before the CTA may exit
+      for (long long i = (it > S ? it - S : 0); i < it; ++i)
+        mbar_wait(&full[i % S], static_cast<uint32_t>((i / S) & 1), nullptr);
+    } else if (warp == 1 && lane == 0) {
+      // ------------------------------------------------------------ MMA issuer
+      constexpr uint32_t idesc = idesc_e4m3_f32(128, NQ * 32);
+      int qb = find_qb(s_prefix, nqb, g_begin);
+      int cur_qb = -1, qcount = 0, slot = 0;
+      long long it = 0;
+      bool ok = true;
+      for (long long g = g_begin; g < g_end; ++g, ++it) {
+        while (g >= s_prefix[qb + 1]) ++qb;
+        if (qb != cur_qb) {
+          if (cur_qb >= 0) mma_commit(&qempty[slot]);
+          cur_qb = qb;
+          slot = qcount & 1;
+          if (!(ok = mbar_wait(&qfull[slot], (qcount >> 1) & 1, s_abort))) break;
+          ++qcount;
+        }
+        const int s = static_cast<int>(it % S);
+        if (!(ok = mbar_wait(&full[s], static_cast<uint32_t>((it / S) & 1), s_abort))) break;
+        const int a = static_cast<int>(it & 1);
+        if (!(ok = mbar_wait(&tempty[a], static_cast<uint32_t>((it >> 1) & 1) ^ 1u, s_abort))) break;
+        tc_fence_after();
+        const uint64_t adesc = smem_desc_sw128(s_keys + s * Cfg::kKeyBytes);
+        const uint64_t bdesc = smem_desc_sw128(s_q + slot * Cfg::kQBytes);
+        const uint32_t d = tmem_base + a * Cfg::kAccCols;
+#pragma unroll
+        for (int k = 0; k < 4; ++k)  // K = 128 bytes = 4 x 32 e4m3
+          mma_e4m3(d, adesc + 2 * k, bdesc + 2 * k, idesc, k > 0 ? 1u : 0u);
+        mma_commit(&tfull[a]);
+        mma_commit(&empty[s]);
+      }
+      if (!ok) {
+        *s_abort = 1;
+        set_error(p.err, kErrTimeout);
+      }
+    } else if (warp >= 2) {
+      // ------------------------------------------------------------ epilogue
+      const int quad = warp & 3;
+      const int r = quad * 32 + lane;  // key row of this thread within the tile
+      int qb = find_qb(s_prefix, nqb, g_begin);
+      int cur_qb = -1, t0 = 0;
+      int E[NQ];
+      long long it = 0;
+      bool ok = true;
+      for (long long g = g_begin; g < g_end; ++g, ++it) {
+        while (g >= s_prefix[qb + 1]) ++qb;
+        const int kb = static_cast<int>(g - s_prefix[qb]);
+        if (qb != cur_qb) {
+          named_bar_sync(1, 128);
+          cur_qb = qb;
+          t0 = (MODE == kModeScan) ? qb * NQ : qb;
+          const int b = row_seq_of(p.rows, t0);
+          for (int i = threadIdx.x - 64; i < NQ * 32; i += 128) {
+            const int t = t0 + i / 32;
+            s_w[i] = (t < T) ? __ldg(p.w + static_cast<long long>(t) * 32 + (i & 31)) *
+                                   __ldg(p.q_scale + static_cast<long long>(t) * 32 + (i & 31))
+                             : 0.f;
+          }
+#pragma unroll
+          for (int j = 0; j < NQ; ++j) E[j] = (t0 + j < T) ? visible_of(p.rows, t0 + j, b) : 0;
+          named_bar_sync(1, 128);
+        }
+        const int a = static_cast<int>(it & 1);
+        const int s = static_cast<int>(it % S);
+        // On a timeout this warp keeps walking the tiles without waiting, so the
+        // other epilogue warps never stall on the named barrier above.
+        if (ok) ok = mbar_wait(&tfull[a], static_cast<uint32_t>((it >> 1) & 1), s_abort);
+        if (ok) ok = mbar_wait(&full[s], static_cast<uint32_t>((it / S) & 1), s_abort);  // acquire the scales
+        if (!ok) continue;
+        tc_fence_after();
+        const float ks = s_scales[s * kTileKeys + r];
+        int pos;
+        long long ci = 0;
+        if (MODE == kModeScan) {
+          pos = kb * kTileKeys + r;
+        } else {
+          ci = static_cast<long long>(kb) * kTileKeys + r;
+          const int cb = static_cast<int>(ci >> 3);
+          const int blk = (cb < p.pool_n) ? __ldg(p.pool_blocks + static_cast<long long>(t0) * p.pool_n + cb) : -1;
+          pos = blk >= 0 ? blk * 8 + static_cast<int>(ci & 7) : -1;
+        }
+#pragma unroll 1
+        for (int j = 0; j < NQ; ++j) {
+          float v[32];
+          tmem_ld32(tmem_base + a * Cfg::kAccCols + j * 32 + (static_cast<uint32_t>(quad * 32) << 16), v);
+          const float4* w4 = reinterpret_cast<const float4*>(s_w + j * 32);
+          float acc0 = 0.f, acc1 = 0.f;
+#pragma unroll
+          for (int h4 = 0; h4 < 8; ++h4) {
+            const float4 ww = w4[h4];
+            acc0 = fmaf(ww.x, fmaxf(v[4 * h4 + 0], 0.f), acc0);
+            acc1 = fmaf(ww.y, fmaxf(v[4 * h4 + 1], 0.f), acc1);
+            acc0 = fmaf(ww.z, fmaxf(v[4 * h4 + 2], 0.f), acc0);
+            acc1 = fmaf(ww.w, fmaxf(v[4 * h4 + 3], 0.f), acc1);
+          }
+          const int t = t0 + j;
+          const bool valid = pos >= 0 && pos < E[j];
+          const float sc = valid ? (acc0 + acc1) * ks : -INFINITY;
+          if (MODE == kModeScan) {
+            if (t < T && pos < p.ld_out) p.out[static_cast<long long>(t) * p.ld_out + pos] = sc;
+            if (p.block_max != nullptr) {
+              float m = sc;
+              m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+              m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+              m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
+              const int blk = pos >> 3;
+              if ((lane & 7) == 0 && t < T && blk < (E[j] + 7) / 8 && blk < p.ld_bm)
+                p.block_max[static_cast<long long>(t) * p.ld_bm + blk] = m;
+            }
+          } else {
+            if (ci < static_cast<long long>(p.pool_n) * 8) p.out[static_cast<long long>(t) * p.pool_n * 8 + ci] = sc;
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&tempty[a]);
+          mbar_arrive(&empty[s]);
+        }
+      }
+      if (!ok) {
+        *s_abort = 1;
+        set_error(p.err, kErrTimeout);
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, Cfg::kTmemCols);
+  }
+}
+
+template <int NQ, int MODE>
+cudaError_t launch_variant(const IndexLaunch& a, const DeviceCtx& ctx, cudaStream_t st, const char** why) {
+  using Cfg = IdxCfg<NQ>;
+  const int nqb = (MODE == kModeScan) ? (a.rows.T + NQ - 1) / NQ : a.rows.T;
+  if (nqb > kMaxQB) {
+    *why = "too many query rows for one launch";
+    return cudaErrorInvalidValue;
+  }
+  CUtensorMap map_q, map_kv;
+  if (encode_tmap_2d_u8(&map_q, a.q_fp8, kRowBytes, static_cast<uint64_t>(a.rows.T) * 32, kRowBytes, kRowBytes,
+                        NQ * 32) != CUDA_SUCCESS) {
+    *why = "tensor map of q could not be encoded";
+    return cudaErrorInvalidValue;
+  }
+  if (encode_tmap_2d_u8(&map_kv, a.index_k, kRowBytes, static_cast<uint64_t>(a.n_pages) * kPageRows, kRowBytes,
+                        kRowBytes, MODE == kModeScan ? 64 : 8) != CUDA_SUCCESS) {
+    *why = "tensor map of the index-K cache could not be encoded";
+    return cudaErrorInvalidValue;
+  }
+  IdxParams p;
+  p.q_scale = a.q_scale;
+  p.w = a.w;
+  p.index_k = a.index_k;
+  p.n_pages = a.n_pages;
+  p.page_table = a.page_table;
+  p.pt_stride = a.pt_stride;
+  p.rows = RowsDev{a.rows.T, a.rows.B, a.rows.row_seq, a.rows.row_pos, a.rows.n_visible, a.rows.ratio_m};
+  p.out = a.out;
+  p.ld_out = a.ld_out;
+  p.block_max = a.block_max;
+  p.ld_bm = a.ld_bm;
+  p.pool_blocks = a.pool_blocks;
+  p.pool_n = a.pool_n;
+  p.err = ctx.err;
+  const size_t smem = Cfg::smem_bytes(nqb);
+  auto kern = index_tiles_kernel<NQ, MODE>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  kern<<<ctx.num_sms, 192, smem, st>>>(map_q, map_kv, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_index_tiles(const IndexLaunch& a, int mode, int nq, const DeviceCtx& ctx, cudaStream_t st,
+                               const char** why) {
+  if (mode == kModeScan && nq == 1) return launch_variant<1, kModeScan>(a, ctx, st, why);
+  if (mode == kModeScan && nq == 8) return launch_variant<8, kModeScan>(a, ctx, st, why);
+  if (mode == kModeGather && nq == 1) return launch_variant<1, kModeGather>(a, ctx, st, why);
+  *why = "unsupported index tiling";
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace csa2

@@ -1,0 +1,127 @@
+"""Host-side checks of the C ABI that need no GPU: the library builds, loads and
+exports every symbol include/csa2.h declares, the ctypes structs match the C
+layout, and argument validation returns status codes without launching."""
+import ctypes as C
+import os
+import re
+import subprocess
+
+import pytest
+
+from conftest import ROOT
+
+HEADER = os.path.join(ROOT, "include", "csa2.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from serving_lightning_indexer_gb300 import _build, csa2
+    _build.build()
+    return csa2.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"CSA2_API\s+[\w\s\*]+?\b(csa2_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_five_calls():
+    names = declared_functions()
+    for n in ("csa2_index_score", "csa2_topk_with_candidates", "csa2_reindex", "csa2_sparse_attn",
+              "csa2_compress_m2"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    from serving_lightning_indexer_gb300 import _build
+    out = subprocess.run(["nm", "-D", "--defined-only", _build.LIB], capture_output=True, text=True).stdout
+    exported = set(re.findall(r"\bT\s+(csa2_\w+)", out))
+    assert set(declared_functions()) <= exported
+    from serving_lightning_indexer_gb300 import csa2
+    assert set(csa2.EXPORTED) == set(declared_functions())
+    # nothing but the ABI is exported
+    assert all(s.startswith("csa2_") for s in exported)
+
+
+def _struct_sizes_from_c():
+    src = r"""
+#include <stdio.h>
+#include <stddef.h>
+#include "csa2.h"
+int main(void) {
+  printf("%zu %zu %zu %zu %zu %zu\n", sizeof(csa2_rows), sizeof(csa2_index_score_args), sizeof(csa2_topk_args),
+         sizeof(csa2_reindex_args), sizeof(csa2_sparse_attn_args), sizeof(csa2_compress_args));
+  printf("%zu %zu %zu %zu\n", offsetof(csa2_index_score_args, rows), offsetof(csa2_topk_args, k),
+         offsetof(csa2_sparse_attn_args, softmax_scale), offsetof(csa2_compress_args, latent_out));
+  return 0;
+}
+"""
+    import tempfile
+    with tempfile.TemporaryDirectory() as d:
+        c = os.path.join(d, "s.c")
+        open(c, "w").write(src)
+        exe = os.path.join(d, "s")
+        subprocess.run(["gcc", "-I", os.path.join(ROOT, "include"), c, "-o", exe], check=True)
+        return [list(map(int, l.split())) for l in subprocess.run([exe], capture_output=True, text=True).stdout.split("\n") if l]
+
+
+def test_ctypes_structs_match_c_layout():
+    from serving_lightning_indexer_gb300 import csa2
+    sizes, offs = _struct_sizes_from_c()
+    assert sizes == [C.sizeof(csa2.Rows), C.sizeof(csa2.IndexScoreArgs), C.sizeof(csa2.TopkArgs),
+                     C.sizeof(csa2.ReindexArgs), C.sizeof(csa2.SparseAttnArgs), C.sizeof(csa2.CompressArgs)]
+    assert offs == [csa2.IndexScoreArgs.rows.offset, csa2.TopkArgs.k.offset, csa2.SparseAttnArgs.softmax_scale.offset,
+                    csa2.CompressArgs.latent_out.offset]
+
+
+FAKE = 0x10000  # a non-null, 16-B aligned address that is never dereferenced
+
+
+def test_validation_returns_codes_without_launch(lib):
+    from serving_lightning_indexer_gb300 import csa2
+    r = csa2.Rows(2, 2, None, None, FAKE, 1)
+    a = csa2.IndexScoreArgs(FAKE, FAKE, FAKE, None, 10, FAKE, 4, r, FAKE, 128, None, 0)
+    assert lib.csa2_index_score(C.byref(a), None, 0, None) == 1                  # NULL index_k
+    a.index_k = FAKE + 8
+    assert lib.csa2_index_score(C.byref(a), None, 0, None) == 3                  # misaligned
+    a.index_k = FAKE
+    a.ld_scores = 130
+    assert lib.csa2_index_score(C.byref(a), None, 0, None) == 3                  # ld not a multiple of 4
+    a.ld_scores = 128
+    a.rows = csa2.Rows(3, 2, None, None, FAKE, 1)
+    assert lib.csa2_index_score(C.byref(a), None, 0, None) == 2                  # T != B without row_seq
+    a.rows = csa2.Rows(2, 2, None, FAKE, None, 3)
+    assert lib.csa2_index_score(C.byref(a), None, 0, None) == 4                  # ratio_m = 3
+    assert b"ratio_m" in lib.csa2_last_error_detail()
+
+    t = csa2.TopkArgs(FAKE, 128, None, 0, None, 0, csa2.Rows(2, 2, None, None, FAKE, 1), 4096, FAKE, None, 4096,
+                      None, 0)
+    assert lib.csa2_topk_with_candidates(C.byref(t), None, 0, None) == 2         # k > 2048
+    t.k, t.ld_topk = 512, 512
+    t.pool_blocks, t.pool_n = FAKE, 2048
+    assert lib.csa2_topk_with_candidates(C.byref(t), None, 0, None) == 1         # pool needs block_max
+    t.block_max, t.ld_block_max = FAKE, 16
+    n = C.c_size_t(0)
+    assert lib.csa2_workspace_size(2, C.cast(C.byref(t), C.c_void_p), C.byref(n)) == 0 and n.value > 0
+    assert lib.csa2_topk_with_candidates(C.byref(t), None, 0, None) == 7         # workspace missing
+
+    s = csa2.SparseAttnArgs(FAKE, FAKE, 10, FAKE, 512, 512, FAKE, 10, FAKE, 129, 129, FAKE, 0.0, 1, 0, FAKE, None)
+    assert lib.csa2_sparse_attn(C.byref(s), None, 0, None) == 2                  # n_swa > 128
+    s.n_swa, s.softmax_scale = 128, -1.0
+    assert lib.csa2_sparse_attn(C.byref(s), None, 0, None) == 2                  # negative scale
+
+    ca = csa2.CompressArgs(FAKE, None, 64, 2, FAKE, 1e-6, 1, 10000.0, 0, None, FAKE, 64, FAKE, 1, None, None)
+    assert lib.csa2_compress_m2(C.byref(ca), None) == 1                          # m=2 needs Z
+    ca.ratio_m = 4
+    assert lib.csa2_compress_m2(C.byref(ca), None) == 4
+    for code in range(9):
+        assert lib.csa2_status_string(code)
+
+
+def test_binding_refuses_cpu_tensors(lib):
+    import torch
+
+    from serving_lightning_indexer_gb300 import csa2
+    x = torch.zeros(4, 32, 128, dtype=torch.uint8)
+    with pytest.raises(ValueError):
+        csa2.index_score(x, x, x, x, x, csa2.Rows(1, 1, None, None, None, 1), x)

@@ -1,0 +1,123 @@
+"""GPU parity of csa2_sparse_attn and csa2_compress_m2."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from gpu_util import assert_attention_close, need_gpu, np_
+from oracle import csa2_oracle as o
+from serving_lightning_indexer_gb300 import csa2
+from serving_lightning_indexer_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+
+def _attn_case(T, k, n_swa, seed, holes=0.0, out_bf16=False, n_entries=5000):
+    dev = need_gpu()
+    pc = W.make_paged_cache([n_entries], seed=seed, device=dev)
+    al = W.make_attn_layer(T, seed=seed + 1, device=dev)
+    rng = np.random.default_rng(seed)
+    slots = np.stack([o.slots_of(rng.choice(n_entries, size=k, replace=False), np_(pc.page_table[0]))
+                      for _ in range(T)]) if k else np.zeros((T, 0), dtype=np.int64)
+    if holes:
+        slots[rng.random(slots.shape) < holes] = -1
+    tks = torch.tensor(slots, dtype=torch.int32, device=dev) if k else None
+    swa = al.swa_slot[:, :n_swa].contiguous() if n_swa else None
+    if n_swa and holes:
+        swa = swa.clone()
+        swa[torch.tensor(rng.random(tuple(swa.shape)) < holes, device=dev)] = -1
+    out = torch.empty(T, 64, 512, dtype=torch.bfloat16 if out_bf16 else torch.float32, device=dev)
+    lse = torch.empty(T, 64, dtype=torch.float32, device=dev)
+    csa2.sparse_attn(al.q, pc.main_kv if k else None, tks, al.swa_kv if n_swa else None, swa, al.sink, out, lse)
+    torch.cuda.synchronize()
+    assert csa2.check_device_error() == 0
+    main_np, swa_np = np_(pc.main_kv), np_(al.swa_kv)
+    for t in range(T):
+        ref, rl = o.attention_row(al.q[t].float().cpu().numpy().astype(np.float64), main_np,
+                                  slots[t] if k else np.zeros(0, dtype=np.int64), swa_np,
+                                  np_(swa[t]) if n_swa else np.zeros(0, dtype=np.int64),
+                                  np_(al.sink).astype(np.float64), 1 / math.sqrt(512))
+        assert_attention_close(out[t].double().cpu().numpy(), ref, f"row {t}")
+        assert np.abs(np_(lse[t]) - rl).max() < 2e-3
+
+
+@pytest.mark.parametrize("T,k,n_swa", [(1, 512, 128), (3, 512, 128), (16, 512, 128), (200, 512, 128),
+                                       (2, 100, 0), (2, 0, 37), (5, 2048, 128), (1, 1, 0)])
+def test_attention_matches_oracle(T, k, n_swa):
+    _attn_case(T, k, n_swa, seed=T * 7 + k + n_swa)
+
+
+def test_attention_with_empty_slots_and_bf16_out():
+    _attn_case(4, 512, 128, seed=99, holes=0.3, out_bf16=True)
+
+
+def test_attention_no_keys_at_all_gives_zero():
+    dev = need_gpu()
+    al = W.make_attn_layer(2, seed=5, device=dev)
+    swa = torch.full((2, 128), -1, dtype=torch.int32, device=dev)
+    out = torch.full((2, 64, 512), 7.0, dtype=torch.float32, device=dev)
+    lse = torch.empty(2, 64, dtype=torch.float32, device=dev)
+    csa2.sparse_attn(al.q, None, None, al.swa_kv, swa, al.sink, out, lse)
+    torch.cuda.synchronize()
+    assert (np_(out) == 0).all()
+    assert np.allclose(np_(lse), np.repeat(np_(al.sink)[None], 2, 0), atol=1e-6)   # only the sink remains
+
+
+def test_attention_bad_slot_is_reported():
+    dev = need_gpu()
+    pc = W.make_paged_cache([256], seed=6, device=dev)
+    al = W.make_attn_layer(1, seed=7, device=dev)
+    tks = torch.arange(512, dtype=torch.int32, device=dev)[None].contiguous()
+    tks[0, 3] = pc.main_kv.shape[0] + 5
+    out = torch.empty(1, 64, 512, dtype=torch.float32, device=dev)
+    csa2.sparse_attn(al.q, pc.main_kv, tks[:, :256].contiguous(), al.swa_kv, al.swa_slot, al.sink, out)
+    assert csa2.check_device_error() == 6
+
+
+@pytest.mark.parametrize("ratio", [1, 2])
+def test_compress_matches_oracle(ratio):
+    dev = need_gpu()
+    n_tok = 4096 + ratio
+    Cm, Z, gamma = W.make_compress_inputs(n_tok, seed=20 + ratio, device=dev)
+    n_ent = n_tok // ratio
+    first = 1000
+    pt = torch.randperm(96, device=dev).to(torch.int32)           # 96 pages hold entries < 6144
+    kv = torch.zeros(96 * 64, 288, dtype=torch.uint8, device=dev)
+    lat = torch.empty(n_ent, 512, dtype=torch.float32, device=dev)
+    csa2.compress_m2(Cm, Z if ratio == 2 else None, ratio, gamma, kv, page_table=pt, first_entry=first,
+                     latent_out=lat)
+    torch.cuda.synchronize()
+    assert csa2.check_device_error() == 0
+    pos = (first + np.arange(n_ent)) * ratio
+    ref = o.compress_latent(Cm.float().cpu().numpy().astype(np.float64), Z.float().cpu().numpy().astype(np.float64),
+                            ratio, np_(gamma).astype(np.float64), 1e-6, pos, 10000.0)
+    got_lat = np_(lat).astype(np.float64)
+    assert np.abs(got_lat - ref).max() <= 1e-4 * np.abs(ref).max()
+    slots = o.slots_of(first + np.arange(n_ent), np_(pt))
+    got = np_(kv)[slots]
+    # the kernel's FP4 decisions equal the oracle's encoder applied to the kernel's own fp32 latent
+    assert np.array_equal(got, o.fp4_encode_records(got_lat.astype(np.float32).astype(np.float64)))
+    # against the float64 oracle: codes may differ only where the float64 value sits next to a rounding midpoint
+    want = o.fp4_encode_records(ref)
+    assert np.array_equal(got[:, 256:], want[:, 256:]) or (got[:, 256:272] != want[:, 256:272]).mean() < 1e-3
+    dec_got = o.main_kv_records(got, np.arange(n_ent))
+    dec_want = o.main_kv_records(want, np.arange(n_ent))
+    step = np.repeat(o.ue8m0(want[:, 256:272]), 32, axis=1)
+    assert np.all(np.abs(dec_got - dec_want) <= 0.5 * step + 1e-12)
+
+
+def test_compress_entry_slots_and_no_rope():
+    dev = need_gpu()
+    Cm, Z, gamma = W.make_compress_inputs(64, seed=30, device=dev)
+    es = torch.tensor(np.random.default_rng(0).permutation(100)[:32], dtype=torch.int32, device=dev)
+    kv = torch.zeros(100, 288, dtype=torch.uint8, device=dev)
+    lat = torch.empty(32, 512, dtype=torch.float32, device=dev)
+    csa2.compress_m2(Cm, Z, 2, gamma, kv, entry_slot=es, apply_rope=False, latent_out=lat)
+    torch.cuda.synchronize()
+    ref = o.compress_latent(Cm.float().cpu().numpy().astype(np.float64), Z.float().cpu().numpy().astype(np.float64),
+                            2, np_(gamma).astype(np.float64), 1e-6, np.zeros(32), 10000.0, apply_rope=False)
+    assert np.abs(np_(lat) - ref).max() <= 1e-4 * np.abs(ref).max()
+    assert np.array_equal(np_(kv)[np_(es)], o.fp4_encode_records(np_(lat).astype(np.float64)))
+    untouched = np.setdiff1d(np.arange(100), np_(es))
+    assert (np_(kv)[untouched] == 0).all()

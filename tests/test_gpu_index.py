@@ -1,0 +1,104 @@
+"""GPU parity of csa2_index_score (decode scan and prefill query-blocked path)."""
+import numpy as np
+import pytest
+import torch
+
+from gpu_util import assert_scores_close, need_gpu, np_
+from oracle import csa2_oracle as o
+from serving_lightning_indexer_gb300 import csa2
+from serving_lightning_indexer_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+
+def _decode(lengths, seed, ld=None, with_bm=True):
+    dev = need_gpu()
+    B = len(lengths)
+    pc = W.make_paged_cache(lengths, seed=seed, device=dev, with_main=False)
+    iq = W.make_indexer_query(B, seed=seed + 1, device=dev)
+    nvis = torch.tensor(lengths, dtype=torch.int32, device=dev)
+    ld = ld or ((max(lengths) + 127) // 128 * 128)
+    scores = torch.full((B, ld), 7.0, dtype=torch.float32, device=dev)
+    bm = torch.full((B, (ld + 7) // 8 + 4), 7.0, dtype=torch.float32, device=dev) if with_bm else None
+    r = csa2.rows(B, B, n_visible=nvis)
+    csa2.index_score(iq.q_fp8, iq.q_scale, iq.w, pc.index_k, pc.page_table, r, scores, bm)
+    torch.cuda.synchronize()
+    assert csa2.check_device_error() == 0
+    return pc, iq, scores, bm
+
+
+@pytest.mark.parametrize("lengths", [[1], [127, 128, 129], [4096], [100, 1000, 4133, 64, 65, 8191]])
+def test_decode_scores_match_oracle(lengths):
+    pc, iq, scores, bm = _decode(lengths, seed=len(lengths))
+    cache, pt = np_(pc.index_k), np_(pc.page_table)
+    for b, n in enumerate(lengths):
+        ref = o.index_scores_row(np_(iq.q_fp8[b]), np_(iq.q_scale[b]), np_(iq.w[b]), cache, pt[b], n)
+        got = np_(scores[b])
+        assert_scores_close(got[:n], ref, f"row {b}")
+        tail = got[n:(n + 127) // 128 * 128]
+        assert np.all(np.isneginf(tail)), "positions past E must hold -inf inside the last tile"
+        # block maxima are exactly the max of the kernel's own scores over visible positions
+        nb = (n + 7) // 8
+        want = [got[8 * j:min(8 * j + 8, n)].max() for j in range(nb)]
+        assert np.array_equal(np_(bm[b, :nb]), np.array(want, dtype=np.float32))
+        assert np.all(np_(bm[b, nb:]) == 7.0) or nb * 8 >= bm.shape[1] * 8
+
+
+def test_decode_row_seq_and_clipped_ld():
+    dev = need_gpu()
+    lengths = [300, 700]
+    pc = W.make_paged_cache(lengths, seed=5, device=dev, with_main=False)
+    iq = W.make_indexer_query(3, seed=6, device=dev)
+    row_seq = torch.tensor([1, 0, 1], dtype=torch.int32, device=dev)
+    nvis = torch.tensor(lengths, dtype=torch.int32, device=dev)
+    ld = 512                                  # shorter than sequence 1: written up to ld only
+    scores = torch.full((3, ld), 7.0, dtype=torch.float32, device=dev)
+    csa2.index_score(iq.q_fp8, iq.q_scale, iq.w, pc.index_k, pc.page_table,
+                     csa2.rows(3, 2, row_seq=row_seq, n_visible=nvis), scores)
+    torch.cuda.synchronize()
+    cache, pt = np_(pc.index_k), np_(pc.page_table)
+    for t, b in enumerate([1, 0, 1]):
+        n = lengths[b]
+        ref = o.index_scores_row(np_(iq.q_fp8[t]), np_(iq.q_scale[t]), np_(iq.w[t]), cache, pt[b], n)
+        m = min(n, ld)
+        assert_scores_close(np_(scores[t, :m]), ref[:m], f"row {t}")
+
+
+def test_bad_page_id_is_reported_not_faulted():
+    dev = need_gpu()
+    lengths = [256]
+    pc = W.make_paged_cache(lengths, seed=7, device=dev, with_main=False)
+    iq = W.make_indexer_query(1, seed=8, device=dev)
+    pt = pc.page_table.clone()
+    pt[0, 2] = 10_000                         # beyond the cache
+    scores = torch.empty(1, 256, dtype=torch.float32, device=dev)
+    csa2.index_score(iq.q_fp8, iq.q_scale, iq.w, pc.index_k, pt,
+                     csa2.rows(1, 1, n_visible=torch.tensor([256], dtype=torch.int32, device=dev)), scores)
+    assert csa2.check_device_error() == 6
+    assert csa2.check_device_error() == 0     # the record is cleared
+
+
+@pytest.mark.parametrize("T,ratio", [(64, 2), (100, 1)])
+def test_prefill_query_blocked_path(T, ratio):
+    dev = need_gpu()
+    n_entries = 3000
+    pc = W.make_paged_cache([n_entries], seed=9, device=dev, with_main=False)
+    iq = W.make_indexer_query(T, seed=10, device=dev)
+    # queries at the end of the context, causal visibility (pos + 1) // m
+    first = n_entries * ratio - T
+    row_pos = torch.arange(first, first + T, dtype=torch.int32, device=dev)
+    ld = (n_entries + 127) // 128 * 128
+    scores = torch.full((T, ld), 7.0, dtype=torch.float32, device=dev)
+    bm = torch.full((T, ld // 8), 7.0, dtype=torch.float32, device=dev)
+    r = csa2.rows(T, 1, row_seq=torch.zeros(T, dtype=torch.int32, device=dev), row_pos=row_pos, ratio_m=ratio)
+    csa2.index_score(iq.q_fp8, iq.q_scale, iq.w, pc.index_k, pc.page_table, r, scores, bm)
+    torch.cuda.synchronize()
+    assert csa2.check_device_error() == 0
+    cache, pt = np_(pc.index_k), np_(pc.page_table)
+    keys = o.index_k_entries(cache, pt[0], n_entries)
+    for t in list(range(0, T, 7)) + [T - 1]:
+        e = o.visible_entries(first + t, ratio)
+        ref = o.index_score_values(o.dequant_q(np_(iq.q_fp8[t]), np_(iq.q_scale[t])), np_(iq.w[t]), keys[:e])
+        got = np_(scores[t])
+        assert_scores_close(got[:e], ref, f"row {t}")
+        assert np.all(np.isneginf(got[e:min(ld, (e + 127) // 128 * 128)]))

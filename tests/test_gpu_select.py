@@ -1,0 +1,181 @@
+"""GPU parity of csa2_topk_with_candidates and csa2_reindex.
+
+Selection on given fp32 scores is bit-exact against the oracle run on the same
+fp32 values (both sides decide in fp32); end-to-end selection from the FP8
+cache follows the near-tie rule."""
+import numpy as np
+import pytest
+import torch
+
+from gpu_util import assert_scores_close, assert_selection_ok, need_gpu, np_
+from oracle import csa2_oracle as o
+from serving_lightning_indexer_gb300 import csa2
+from serving_lightning_indexer_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+
+def _run_topk(scores_np, lengths, k=512, pool_n=2048, pt=None):
+    dev = need_gpu()
+    T, ld = scores_np.shape
+    scores = torch.tensor(scores_np, dtype=torch.float32, device=dev)
+    # block maxima of the given scores over the visible part, as the scorer writes them
+    nbld = (ld + 7) // 8 + 3 & ~3
+    bm_np = np.full((T, nbld), -np.inf, dtype=np.float32)
+    for t, n in enumerate(lengths):
+        for j in range((n + 7) // 8):
+            bm_np[t, j] = scores_np[t, 8 * j:min(8 * j + 8, n)].max()
+    bm = torch.tensor(bm_np, device=dev)
+    if pt is None:
+        pt_np = np.stack([np.random.default_rng(t).permutation(4096 * 4)[: (ld + 63) // 64] for t in range(T)])
+    else:
+        pt_np = pt
+    ptab = torch.tensor(pt_np, dtype=torch.int32, device=dev)
+    nvis = torch.tensor(lengths, dtype=torch.int32, device=dev)
+    pos = torch.full((T, k), -7, dtype=torch.int32, device=dev)
+    slot = torch.full((T, k), -7, dtype=torch.int32, device=dev)
+    pool = torch.full((T, pool_n), -7, dtype=torch.int32, device=dev)
+    csa2.topk_with_candidates(scores, csa2.rows(T, T, n_visible=nvis), k, pos, slot, ptab, bm, pool)
+    torch.cuda.synchronize()
+    assert csa2.check_device_error() == 0
+    return np_(pos), np_(slot), np_(pool), bm_np, pt_np
+
+
+def _check_exact(scores_np, lengths, k=512, pool_n=2048):
+    pos, slot, pool, bm_np, pt = _run_topk(scores_np, lengths, k, pool_n)
+    for t, n in enumerate(lengths):
+        s = scores_np[t, :n]
+        want = o.topk_positions(s, k)
+        assert pos[t].tolist() == want.tolist(), f"row {t}: positions differ"
+        assert slot[t].tolist() == o.slots_of(want, pt[t]).tolist(), f"row {t}: slots differ"
+        wpool = o.candidate_pool(bm_np[t, :(n + 7) // 8].astype(np.float64), pool_n)
+        assert pool[t].tolist() == wpool.tolist(), f"row {t}: pool differs"
+
+
+def test_exact_short_and_ragged_rows():
+    rng = np.random.default_rng(0)
+    lengths = [0, 1, 7, 300, 511, 512, 513, 4000, 16384]
+    ld = 16384
+    s = rng.normal(size=(len(lengths), ld)).astype(np.float32)
+    _check_exact(s, lengths)
+
+
+def test_exact_with_many_ties():
+    rng = np.random.default_rng(1)
+    lengths = [5000, 12000]
+    s = np.round(rng.normal(size=(2, 12000)), 1).astype(np.float32)
+    _check_exact(s, lengths)
+
+
+def test_exact_long_rows_streaming_passes():
+    rng = np.random.default_rng(2)
+    lengths = [300_000, 65_537, 200_003]
+    ld = 300_032
+    s = rng.normal(size=(3, ld)).astype(np.float32)
+    _check_exact(s, lengths)
+
+
+def test_exact_crowded_threshold_bin_refines():
+    # a narrow distribution far from zero puts thousands of scores in one 11-bit bin
+    rng = np.random.default_rng(3)
+    lengths = [400_000, 150_000]
+    s = (100.0 + 0.01 * rng.normal(size=(2, 400_000))).astype(np.float32)
+    _check_exact(s, lengths)
+
+
+def test_exact_massive_ties_fall_back_to_streaming_select():
+    lengths = [100_000, 40_000]
+    s = np.full((2, 100_000), 3.5, dtype=np.float32)
+    s[0, 99_000] = 4.0
+    pos, slot, pool, bm_np, pt = _run_topk(s, lengths)
+    assert pos[0].tolist() == [99_000] + list(range(511))
+    assert pos[1].tolist() == list(range(512))
+    assert pool[0].tolist() == o.candidate_pool(bm_np[0, :12_500].astype(np.float64), 2048).tolist()
+
+
+def test_exact_all_excluded_rows():
+    s = np.full((2, 1024), -np.inf, dtype=np.float32)
+    s[1, 5] = 1.0
+    pos, slot, pool, _, _ = _run_topk(s, [1000, 1000])
+    assert (pos[0] == -1).all() and (slot[0] == -1).all()
+    assert pos[1].tolist() == [5] + [-1] * 511
+
+
+def test_end_to_end_selection_from_cache():
+    dev = need_gpu()
+    lengths = [20000, 17000]
+    pc = W.make_paged_cache(lengths, seed=11, device=dev, with_main=False)
+    iq = W.make_indexer_query(2, seed=12, device=dev)
+    nvis = torch.tensor(lengths, dtype=torch.int32, device=dev)
+    r = csa2.rows(2, 2, n_visible=nvis)
+    scores = torch.empty(2, 20096, dtype=torch.float32, device=dev)
+    bm = torch.empty(2, 2512, dtype=torch.float32, device=dev)
+    csa2.index_score(iq.q_fp8, iq.q_scale, iq.w, pc.index_k, pc.page_table, r, scores, bm)
+    pos = torch.empty(2, 512, dtype=torch.int32, device=dev)
+    pool = torch.empty(2, 2048, dtype=torch.int32, device=dev)
+    csa2.topk_with_candidates(scores, r, 512, pos, None, None, bm, pool)
+    torch.cuda.synchronize()
+    cache, pt = np_(pc.index_k), np_(pc.page_table)
+    for b, n in enumerate(lengths):
+        ref = o.index_scores_row(np_(iq.q_fp8[b]), np_(iq.q_scale[b]), np_(iq.w[b]), cache, pt[b], n)
+        assert_selection_ok(np_(pos[b]), ref, 512)
+        # the newest block is forced: give it a value above every block maximum
+        bmx = o.block_maxima(ref, n)
+        bmx[-1] = bmx.max() + 1.0
+        assert_selection_ok(np_(pool[b]), bmx, 2048, "pool")
+        p = np_(pool[b])
+        assert np.all(np.diff(p[p >= 0]) > 0)
+        assert set((np_(pos[b]) // 8).tolist()) <= set(p.tolist())
+
+
+@pytest.mark.parametrize("lengths", [[3000, 16384], [40000, 1_000_003]])
+def test_reindex_matches_oracle(lengths):
+    dev = need_gpu()
+    B = len(lengths)
+    pc = W.make_paged_cache(lengths, seed=13, device=dev, with_main=False)
+    iq = W.make_indexer_query(B, seed=14, device=dev)
+    pool = W.make_pool(lengths, seed=15, device=dev)
+    nvis = torch.tensor(lengths, dtype=torch.int32, device=dev)
+    r = csa2.rows(B, B, n_visible=nvis)
+    pos = torch.empty(B, 512, dtype=torch.int32, device=dev)
+    slot = torch.empty(B, 512, dtype=torch.int32, device=dev)
+    ps = torch.empty(B, 2048 * 8, dtype=torch.float32, device=dev)
+    csa2.reindex(iq.q_fp8, iq.q_scale, iq.w, pc.index_k, pc.page_table, r, pool, 512, pos, slot, ps)
+    torch.cuda.synchronize()
+    assert csa2.check_device_error() == 0
+    cache, pt = np_(pc.index_k), np_(pc.page_table)
+    for b, n in enumerate(lengths):
+        args = (np_(iq.q_fp8[b]), np_(iq.q_scale[b]), np_(iq.w[b]), cache, pt[b], n)
+        ref = o.reindex_scores(*args, np_(pool[b]))
+        assert_scores_close(np_(ps[b]), ref, f"pool scores {b}")
+        # selection on the kernel's own fp32 pool scores is exact
+        full = np.full(n, -np.inf, dtype=np.float32)
+        pp = o.pool_positions(np_(pool[b]), n)
+        full[pp[pp >= 0]] = np_(ps[b])[pp >= 0]
+        want = o.topk_positions(full, 512)
+        assert np_(pos[b]).tolist() == want.tolist()
+        assert np_(slot[b]).tolist() == o.slots_of(want, pt[b]).tolist()
+        # and against the float64 oracle under the near-tie rule
+        reff = np.full(n, -np.inf)
+        reff[pp[pp >= 0]] = ref[pp >= 0]
+        assert_selection_ok(np_(pos[b]), reff, 512, "reindex")
+
+
+def test_reindex_equals_full_topk_when_pool_covers_all():
+    dev = need_gpu()
+    n = 12000
+    pc = W.make_paged_cache([n], seed=16, device=dev, with_main=False)
+    iq = W.make_indexer_query(1, seed=17, device=dev)
+    nvis = torch.tensor([n], dtype=torch.int32, device=dev)
+    r = csa2.rows(1, 1, n_visible=nvis)
+    scores = torch.empty(1, 12032, dtype=torch.float32, device=dev)
+    bm = torch.empty(1, 1504, dtype=torch.float32, device=dev)
+    csa2.index_score(iq.q_fp8, iq.q_scale, iq.w, pc.index_k, pc.page_table, r, scores, bm)
+    pos = torch.empty(1, 512, dtype=torch.int32, device=dev)
+    pool = torch.empty(1, 2048, dtype=torch.int32, device=dev)
+    csa2.topk_with_candidates(scores, r, 512, pos, None, None, bm, pool)
+    rpos = torch.empty(1, 512, dtype=torch.int32, device=dev)
+    csa2.reindex(iq.q_fp8, iq.q_scale, iq.w, pc.index_k, pc.page_table, r, pool, 512, rpos)
+    torch.cuda.synchronize()
+    assert (np_(pool[0])[:1500] == np.arange(1500)).all()
+    assert np_(rpos[0]).tolist() == np_(pos[0]).tolist()
