@@ -130,6 +130,12 @@ typedef struct {
   csa2_rows rows;
   float* scores; int64_t ld_scores;           /* [T, ld_scores] */
   float* block_max; int64_t ld_block_max;     /* optional [T, ld_block_max] */
+  /* optional [2, T, 2048] uint32, decode path only (else must be NULL): receives
+   * 2048-bin histograms of the top 11 bits of the order-preserving key of every
+   * visible score (rows 0..T-1) and of every block maximum (rows T..2T-1, the
+   * newest block counted as +inf; zero when block_max is NULL).  Passing it on
+   * to csa2_topk_with_candidates saves that call a pass over the scores. */
+  uint32_t* hist;
 } csa2_index_score_args;
 CSA2_API int csa2_index_score(const csa2_index_score_args* args, void* workspace, size_t ws_bytes, void* stream);
 
@@ -156,6 +162,8 @@ typedef struct {
   int64_t ld_topk;                             /* >= k */
   int32_t* pool_blocks;                        /* [T, pool_n] or NULL */
   int32_t pool_n;                              /* 1..2048 when pool_blocks is set */
+  const uint32_t* hist;                        /* optional: the histograms csa2_index_score wrote
+                                                  for these scores and block maxima */
 } csa2_topk_args;
 CSA2_API int csa2_topk_with_candidates(const csa2_topk_args* args, void* workspace, size_t ws_bytes, void* stream);
 

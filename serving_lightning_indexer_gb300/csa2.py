@@ -33,13 +33,13 @@ class Rows(C.Structure):
 class IndexScoreArgs(C.Structure):
     _fields_ = [("q_fp8", _P), ("q_scale", _P), ("w", _P), ("index_k", _P), ("index_k_pages", _I64),
                 ("page_table", _P), ("pt_stride", _I32), ("rows", Rows), ("scores", _P), ("ld_scores", _I64),
-                ("block_max", _P), ("ld_block_max", _I64)]
+                ("block_max", _P), ("ld_block_max", _I64), ("hist", _P)]
 
 
 class TopkArgs(C.Structure):
     _fields_ = [("scores", _P), ("ld_scores", _I64), ("block_max", _P), ("ld_block_max", _I64),
                 ("page_table", _P), ("pt_stride", _I32), ("rows", Rows), ("k", _I32), ("topk_pos", _P),
-                ("topk_slot", _P), ("ld_topk", _I64), ("pool_blocks", _P), ("pool_n", _I32)]
+                ("topk_slot", _P), ("ld_topk", _I64), ("pool_blocks", _P), ("pool_n", _I32), ("hist", _P)]
 
 
 class ReindexArgs(C.Structure):
@@ -149,23 +149,24 @@ def rows(T, B, row_seq=None, row_pos=None, n_visible=None, ratio_m=1) -> Rows:
 
 
 # ---------------------------------------------------------------- calls
-def index_score(q_fp8, q_scale, w, index_k, page_table, r: Rows, scores, block_max=None, stream=None):
-    """Lightning-Indexer scores (csa2_index_score)."""
+def index_score(q_fp8, q_scale, w, index_k, page_table, r: Rows, scores, block_max=None, stream=None, hist=None):
+    """Lightning-Indexer scores (csa2_index_score); `hist` ([2,T,2048] int32) optionally
+    receives the key histograms that csa2_topk_with_candidates can reuse."""
     lib = load()
     a = IndexScoreArgs(_ptr(q_fp8), _ptr(q_scale), _ptr(w), _ptr(index_k), index_k.shape[0], _ptr(page_table),
                        page_table.shape[-1], r, _ptr(scores), scores.shape[-1], _ptr(block_max),
-                       block_max.shape[-1] if block_max is not None else 0)
+                       block_max.shape[-1] if block_max is not None else 0, _ptr(hist))
     _check(lib.csa2_index_score(C.byref(a), None, 0, _stream(stream)), "csa2_index_score")
 
 
 def topk_with_candidates(scores, r: Rows, k, topk_pos, topk_slot=None, page_table=None, block_max=None,
-                         pool_blocks=None, stream=None, ws=None):
+                         pool_blocks=None, stream=None, ws=None, hist=None):
     """Top-k positions / slots and the optional candidate pool (csa2_topk_with_candidates)."""
     lib = load()
     a = TopkArgs(_ptr(scores), scores.shape[-1], _ptr(block_max), block_max.shape[-1] if block_max is not None else 0,
                  _ptr(page_table), page_table.shape[-1] if page_table is not None else 0, r, k, _ptr(topk_pos),
                  _ptr(topk_slot), topk_pos.shape[-1], _ptr(pool_blocks),
-                 pool_blocks.shape[-1] if pool_blocks is not None else 0)
+                 pool_blocks.shape[-1] if pool_blocks is not None else 0, _ptr(hist))
     need = C.c_size_t(0)
     _check(lib.csa2_workspace_size(CALL_TOPK, C.cast(C.byref(a), _P), C.byref(need)), "csa2_workspace_size")
     buf = ws if ws is not None else workspace(need.value, scores.device, "topk")

@@ -26,7 +26,7 @@ struct CompressParams {
   const float* gamma;
   float eps;
   int apply_rope;
-  double rope_theta;
+  double inv_freq[32];     // theta^(-2i/64), computed on the host in double
   long long first_entry;
   const int* entry_pos;
   uint8_t* main_kv;
@@ -64,6 +64,8 @@ __device__ __forceinline__ uint32_t e2m1_code(float v) {
 
 __global__ void __launch_bounds__(256) compress_kernel(const __grid_constant__ CompressParams p) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  pdl_trigger();
+  pdl_wait();
   const long long e = static_cast<long long>(blockIdx.x) * 8 + warp;
   if (e >= p.n_entries) return;
   const int c0 = lane * 16;
@@ -97,15 +99,23 @@ __global__ void __launch_bounds__(256) compress_kernel(const __grid_constant__ C
   // RoPE on dims 448..511: interleaved pairs, angle pos * theta^(-2i/64)
   if (p.apply_rope && lane >= 28) {
     const long long pos = p.entry_pos ? static_cast<long long>(__ldg(p.entry_pos + e)) : (p.first_entry + e) * p.ratio_m;
+    // The angle pos * inv_freq reaches ~1e6 rad: it is formed and reduced
+    // modulo 2 pi in double (2 pi split in two parts), then sin/cos run in fp32
+    // on the reduced angle.
+    constexpr double kTwoPiHi = 6.283185307179586;
+    constexpr double kTwoPiLo = 2.4492935982947064e-16;
+    constexpr double kInvTwoPi = 0.15915494309189535;
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       const int i = (c0 - 448) / 2 + j;
-      const double inv_freq = pow(p.rope_theta, -2.0 * i / 64.0);
-      double s, c;
-      sincos(static_cast<double>(pos) * inv_freq, &s, &c);
-      const double a = y[2 * j], b = y[2 * j + 1];
-      y[2 * j] = static_cast<float>(a * c - b * s);
-      y[2 * j + 1] = static_cast<float>(a * s + b * c);
+      const double ang = static_cast<double>(pos) * p.inv_freq[i];
+      const double kq = rint(ang * kInvTwoPi);
+      const double red = fma(-kq, kTwoPiLo, fma(-kq, kTwoPiHi, ang));
+      float sn, cs;
+      sincosf(static_cast<float>(red), &sn, &cs);
+      const float a = y[2 * j], b = y[2 * j + 1];
+      y[2 * j] = a * cs - b * sn;
+      y[2 * j + 1] = a * sn + b * cs;
     }
   }
   if (p.latent_out) {
@@ -161,7 +171,7 @@ cudaError_t launch_compress(const CompressLaunch& a, const DeviceCtx& ctx, cudaS
   p.gamma = a.gamma;
   p.eps = a.eps;
   p.apply_rope = a.apply_rope;
-  p.rope_theta = static_cast<double>(a.rope_theta);
+  for (int i = 0; i < 32; ++i) p.inv_freq[i] = pow(static_cast<double>(a.rope_theta), -2.0 * i / 64.0);
   p.first_entry = a.first_entry;
   p.entry_pos = a.entry_pos;
   p.main_kv = a.main_kv;
@@ -173,8 +183,9 @@ cudaError_t launch_compress(const CompressLaunch& a, const DeviceCtx& ctx, cudaS
   p.err = ctx.err;
   if (a.n_entries == 0) return cudaSuccess;
   const long long blocks = (a.n_entries + 7) / 8;
-  compress_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(p);
-  return cudaGetLastError();
+  cudaError_t e = prefer_max_smem(compress_kernel, 0);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(compress_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, st, p);
 }
 
 }  // namespace csa2

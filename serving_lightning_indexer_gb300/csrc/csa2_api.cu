@@ -67,6 +67,10 @@ cudaError_t device_ctx(DeviceCtx* out) {
     c.device = dev;
     e = cudaDeviceGetAttribute(&c.num_sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
+    e = cudaDeviceGetAttribute(&c.smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
+    if (e != cudaSuccess) return e;
+    e = cudaDeviceGetAttribute(&c.smem_reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev);
+    if (e != cudaSuccess) return e;
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_device_error);
     if (e != cudaSuccess) return e;
@@ -150,8 +154,11 @@ int csa2_index_score(const csa2_index_score_args* a, void* ws, size_t ws_bytes, 
     return fail(CSA2_ERR_ALIGN, "csa2_index_score: block_max must be 16-B aligned with ld a positive multiple of 4");
   const bool prefill = a->rows.row_pos && a->rows.B == 1 && a->rows.T >= 64;
   const int nq = prefill ? 8 : 1;
-  if ((a->rows.T + nq - 1) / nq > 4096)
-    return fail(CSA2_ERR_SHAPE, "csa2_index_score: at most %d rows per call on this path", 4096 * nq);
+  if ((a->rows.T + nq - 1) / nq > 2048)
+    return fail(CSA2_ERR_SHAPE, "csa2_index_score: at most %d rows per call on this path", 2048 * nq);
+  if (a->hist && prefill)
+    return fail(CSA2_ERR_UNSUPPORTED, "csa2_index_score: hist is produced on the decode path only (pass NULL)");
+  if (a->hist && !aligned16(a->hist)) return fail(CSA2_ERR_ALIGN, "csa2_index_score: hist must be 16-B aligned");
   DeviceCtx ctx;
   cudaError_t e = csa2::device_ctx(&ctx);
   if (e != cudaSuccess) return cuda_fail(e, "csa2_index_score: device");
@@ -168,6 +175,7 @@ int csa2_index_score(const csa2_index_score_args* a, void* ws, size_t ws_bytes, 
   L.ld_out = a->ld_scores;
   L.block_max = a->block_max;
   L.ld_bm = a->ld_block_max;
+  L.hist = a->hist;
   const char* why = "launch";
   e = csa2::launch_index_tiles(L, 0, nq, ctx, static_cast<cudaStream_t>(stream), &why);
   if (e != cudaSuccess) return cuda_fail(e, why);
@@ -206,6 +214,8 @@ static int topk_fill(const csa2_topk_args* a, csa2::SelectLaunch* S) {
   S->ld_topk = a->ld_topk;
   S->pool_out = a->pool_blocks;
   S->pool_n = a->pool_blocks ? a->pool_n : 0;
+  if (a->hist && !aligned16(a->hist)) return fail(CSA2_ERR_ALIGN, "csa2_topk_with_candidates: hist must be 16-B aligned");
+  S->hist = a->hist;
   return CSA2_OK;
 }
 
@@ -234,7 +244,7 @@ int csa2_reindex(const csa2_reindex_args* a, void* ws, size_t ws_bytes, void* st
   int rc = check_index_common(a->q_fp8, a->q_scale, a->w, a->index_k, a->index_k_pages, a->page_table, a->pt_stride,
                               a->rows, "csa2_reindex");
   if (rc) return rc;
-  if (a->rows.T > 4096) return fail(CSA2_ERR_SHAPE, "csa2_reindex: at most 4096 rows per call");
+  if (a->rows.T > 2048) return fail(CSA2_ERR_SHAPE, "csa2_reindex: at most 2048 rows per call");
   if (!a->pool_blocks || !a->topk_pos) return fail(CSA2_ERR_NULL, "csa2_reindex: pool_blocks/topk_pos is NULL");
   if (a->pool_n < 1 || a->pool_n > CSA2_MAX_TOPK) return fail(CSA2_ERR_SHAPE, "csa2_reindex: pool_n=%d not in 1..2048", a->pool_n);
   if (a->k < 1 || a->k > CSA2_MAX_TOPK) return fail(CSA2_ERR_SHAPE, "csa2_reindex: k=%d not in 1..2048", a->k);

@@ -178,6 +178,14 @@ __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
+// ---------------------------------------------------------------- programmatic dependent launch
+// Every kernel of the library is launched with programmatic stream
+// serialisation: it lets the next kernel's CTAs start (pdl_trigger) as soon as
+// all of its own CTAs are running, and touches global memory only after the
+// previous kernel has completed and flushed (pdl_wait).
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ---------------------------------------------------------------- ordering key
 // Order-preserving map float -> uint32 (a < b  <=>  key(a) < key(b) for
 // non-NaN values).  -inf maps to 0x007FFFFF.

@@ -24,8 +24,25 @@ struct RowsHost {
 struct DeviceCtx {
   int device;
   int num_sms;
+  int smem_per_sm;        // shared memory per SM (bytes)
+  int smem_reserved;      // shared memory the runtime reserves per CTA (bytes)
   uint32_t* err;
 };
+// CTAs of `smem_bytes` dynamic shared memory that fit on one SM (shared memory only).
+inline int ctas_per_sm_by_smem(const DeviceCtx& c, size_t smem_bytes) {
+  const long long per = static_cast<long long>(smem_bytes) + c.smem_reserved;
+  const long long n = per > 0 ? c.smem_per_sm / per : 1;
+  return n < 1 ? 1 : static_cast<int>(n);
+}
+// Prefer the largest shared-memory carveout for a kernel, so that consecutive
+// kernels of the library never reconfigure the L1 / shared-memory split.
+template <typename K>
+inline cudaError_t prefer_max_smem(K kern, size_t dyn_smem) {
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                       static_cast<int>(cudaSharedmemCarveoutMaxShared));
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(dyn_smem));
+}
 cudaError_t device_ctx(DeviceCtx* out);
 
 // Lightning-Indexer tiles.  mode 0: scan (scores over consecutive entries),
@@ -43,6 +60,7 @@ struct IndexLaunch {
   long long ld_out;
   float* block_max;
   long long ld_bm;
+  uint32_t* hist;
   const int* pool_blocks;
   int pool_n;
 };
@@ -68,6 +86,7 @@ struct SelectLaunch {
   int pool_n;
   const int* pool_in;     // kind 2: the pool the candidates come from [T, pool_in_n]
   int pool_in_n;
+  const uint32_t* hist;   // optional precomputed key histograms [V][2048]
 };
 size_t select_workspace_bytes(const SelectLaunch& a);
 cudaError_t launch_select(const SelectLaunch& a, void* ws, size_t ws_bytes, const DeviceCtx& ctx, cudaStream_t st);
@@ -117,6 +136,23 @@ struct CompressLaunch {
   float* latent_out;
 };
 cudaError_t launch_compress(const CompressLaunch& a, const DeviceCtx& ctx, cudaStream_t st);
+
+// Launch with programmatic stream serialisation (see pdl_trigger / pdl_wait).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
+}
 
 // Tensor-map encoder from the driver (fetched once through the runtime).
 CUresult encode_tmap_2d_u8(CUtensorMap* map, const void* base, uint64_t inner_bytes, uint64_t rows,

@@ -20,8 +20,10 @@
 // scale, the visibility mask, and emits the 8-entry block maxima used by the
 // candidate pool.
 //
-// Roles (192 threads): warp 0 = TMA producer, warp 1 = TMEM owner + MMA
-// issuer, warps 2..5 = epilogue (warp w reads TMEM lanes 32*(w%4)...).
+// Roles (320 threads): warp 0 = TMA producer, warp 1 = TMEM owner + MMA
+// issuer, warps 2..9 = two epilogue groups taking alternate tiles (warp w
+// reads TMEM lanes 32*(w%4)...).  The accumulator ring (4 buffers in decode,
+// 2 in prefill) lets the MMA run ahead of both groups.
 #include <math.h>
 
 #include "csa2_device.cuh"
@@ -36,7 +38,7 @@ constexpr int kModeGather = 1;
 constexpr int kTileKeys = 128;
 constexpr int kRowBytes = 128;                       // one FP8 key / one head of q
 constexpr int kPageRows = 66;                        // an 8448-B page seen as 66 rows of 128 B
-constexpr int kMaxQB = 4096;                         // query blocks per launch
+constexpr int kMaxQB = 2048;                         // query blocks per launch
 
 struct IdxParams {
   const float* q_scale;
@@ -50,41 +52,60 @@ struct IdxParams {
   long long ld_out;
   float* block_max;
   long long ld_bm;
+  uint32_t* hist;  // optional [2][T][2048]: key histograms of the scores and of the block maxima
   const int* pool_blocks;
   int pool_n;
   uint32_t* err;
 };
 
+constexpr int kHistBins = 2048;  // top 11 bits of the order-preserving key
+
+constexpr int kEpiGroups = 2;                        // epilogue groups of 4 warps, alternating tiles
+constexpr int kThreads = 64 + kEpiGroups * 128;
+
 template <int NQ>
 struct IdxCfg {
-  static constexpr int kStages = (NQ == 1) ? 8 : 6;
+  // decode runs two CTAs per SM (two producers per SM measured ~1.5x the HBM
+  // throughput of one CTA with deeper staging); prefill one CTA with 6 stages
+  static constexpr int kStages = (NQ == 1) ? 4 : 6;
+  static constexpr int kCtasPerSm = (NQ == 1) ? 2 : 1;
+  static constexpr int kNumAcc = (NQ == 1) ? 4 : 2;  // TMEM accumulator ring
   static constexpr int kQBytes = NQ * 32 * kRowBytes;
   static constexpr int kAccCols = NQ * 32;
-  static constexpr int kTmemCols = 2 * kAccCols < 32 ? 32 : 2 * kAccCols;
+  static constexpr int kTmemCols = kNumAcc * kAccCols;
   static constexpr int kKeyBytes = kTileKeys * kRowBytes;
   static constexpr int kOffKeys = 0;
   static constexpr int kOffQ = kOffKeys + kStages * kKeyBytes;
   static constexpr int kOffScales = kOffQ + 2 * kQBytes;
   static constexpr int kOffW = kOffScales + kStages * kTileKeys * 4;
-  static constexpr int kOffBars = kOffW + NQ * 32 * 4;
-  static constexpr int kNumBars = 2 * kStages + 8;
+  static constexpr int kOffBars = kOffW + kEpiGroups * NQ * 32 * 4;
+  static constexpr int kNumBars = 2 * kStages + 4 + 2 * kNumAcc;
   static constexpr int kOffMisc = kOffBars + kNumBars * 8;
-  static constexpr int kOffPrefix = kOffMisc + 16;
-  static size_t smem_bytes(int nqb) { return 1024 + kOffPrefix + static_cast<size_t>(nqb + 1) * 4; }
+  static constexpr int kOffLookup = kOffMisc + 16;         // 32 resolved copy sources of the producer warp
+  // per epilogue group: score and block-max key histograms of the current row (decode only)
+  static constexpr int kHistWords = (NQ == 1) ? 2 * kHistBins : 0;
+  static constexpr int kOffHist = kOffLookup + 32 * 4;
+  static constexpr int kOffPrefix = kOffHist + kEpiGroups * kHistWords * 4;
+  // prefix [nqb+1], then the sequence and the visible entries of every query block [nqb] each
+  static size_t smem_bytes(int nqb) { return 1024 + kOffPrefix + static_cast<size_t>(3 * nqb + 1) * 4; }
 };
-static_assert((2 * 32) == IdxCfg<1>::kTmemCols, "decode accumulators: 2 x 32 columns");
+static_assert(128 == IdxCfg<1>::kTmemCols, "decode accumulators: 4 x 32 columns");
 static_assert(512 == IdxCfg<8>::kTmemCols, "prefill accumulators: 2 x 256 columns");
+static_assert(kEpiGroups == 2 && IdxCfg<1>::kNumAcc % kEpiGroups == 0 && IdxCfg<8>::kNumAcc % kEpiGroups == 0,
+              "each epilogue group owns the accumulators of its tiles");
 
-// Entries visible to the rows of a query block and the number of tiles.
+// Sequence, entries visible to the rows of a query block, and its tile count.
 template <int NQ, int MODE>
-__device__ __forceinline__ int qb_tiles(const IdxParams& p, int qb) {
-  if (MODE == kModeGather) return (p.pool_n * 8 + kTileKeys - 1) / kTileKeys;
-  const int t0 = qb * NQ;
+__device__ __forceinline__ int qb_tiles(const IdxParams& p, int qb, int* seq, int* emax_out) {
+  const int t0 = (MODE == kModeScan) ? qb * NQ : qb;
   const int b = row_seq_of(p.rows, t0);
   int emax = 0;
 #pragma unroll
-  for (int j = 0; j < NQ; ++j)
+  for (int j = 0; j < (MODE == kModeScan ? NQ : 1); ++j)
     if (t0 + j < p.rows.T) emax = max(emax, visible_of(p.rows, t0 + j, b));
+  *seq = b;
+  *emax_out = emax;
+  if (MODE == kModeGather) return (p.pool_n * 8 + kTileKeys - 1) / kTileKeys;
   return (emax + kTileKeys - 1) / kTileKeys;
 }
 
@@ -98,7 +119,7 @@ __device__ __forceinline__ int find_qb(const int* prefix, int nqb, long long g) 
 }
 
 template <int NQ, int MODE>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(kThreads, IdxCfg<NQ>::kCtasPerSm)
     index_tiles_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_kv,
                        const __grid_constant__ IdxParams p) {
   using Cfg = IdxCfg<NQ>;
@@ -115,9 +136,11 @@ __global__ void __launch_bounds__(192, 1)
   uint64_t* qfull = bars + 2 * S;
   uint64_t* qempty = qfull + 2;
   uint64_t* tfull = qempty + 2;
-  uint64_t* tempty = tfull + 2;
+  uint64_t* tempty = tfull + Cfg::kNumAcc;
+  constexpr int NA = Cfg::kNumAcc;
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + Cfg::kOffMisc);
   volatile int* s_abort = reinterpret_cast<volatile int*>(smem + Cfg::kOffMisc + 4);
+  int* s_lookup = reinterpret_cast<int*>(smem + Cfg::kOffLookup);
   int* s_prefix = reinterpret_cast<int*>(smem + Cfg::kOffPrefix);
 
   const int warp = threadIdx.x >> 5;
@@ -125,7 +148,11 @@ __global__ void __launch_bounds__(192, 1)
   const int T = p.rows.T;
   const int nqb = (MODE == kModeScan) ? (T + NQ - 1) / NQ : T;
 
-  for (int i = threadIdx.x; i < nqb; i += blockDim.x) s_prefix[i + 1] = qb_tiles<NQ, MODE>(p, i);
+  int* s_seq = s_prefix + nqb + 1;
+  int* s_emax = s_seq + nqb;
+  pdl_trigger();
+  pdl_wait();  // global memory is touched only after the previous kernel completed
+  for (int i = threadIdx.x; i < nqb; i += blockDim.x) s_prefix[i + 1] = qb_tiles<NQ, MODE>(p, i, &s_seq[i], &s_emax[i]);
   if (threadIdx.x == 0) {
     s_prefix[0] = 0;
     *s_abort = 0;
@@ -136,8 +163,10 @@ __global__ void __launch_bounds__(192, 1)
     for (int i = 0; i < 2; ++i) {
       mbar_init(&qfull[i], 1);
       mbar_init(&qempty[i], 1);
+    }
+    for (int i = 0; i < NA; ++i) {
       mbar_init(&tfull[i], 1);
-      mbar_init(&tempty[i], 4);
+      mbar_init(&tempty[i], 4);   // the four warps of the epilogue group owning this accumulator
     }
     fence_mbar_init();
     prefetch_tmap(&map_q);
@@ -175,98 +204,98 @@ __global__ void __launch_bounds__(192, 1)
   const long long g_end = total * (blockIdx.x + 1) / gridDim.x;
 
   if (g_begin < g_end) {
-    if (warp == 0 && lane == 0) {
+    if (warp == 0) {
       // ------------------------------------------------------------ producer
+      // The warp resolves the copy sources of a group of tiles in parallel (one
+      // page or candidate block per lane), then lane 0 waits for free stages
+      // and issues the TMA / bulk copies.
+      constexpr int SLOTS = (MODE == kModeScan) ? 2 : 16;  // copies per tile
+      constexpr int GT = 32 / SLOTS;                       // tiles per group
       const uint64_t pol_keys = (MODE == kModeScan && NQ > 1) ? l2_policy_evict_last() : l2_policy_evict_first();
       const uint64_t pol_q = l2_policy_evict_last();
-      int qb = find_qb(s_prefix, nqb, g_begin);
-      int cur_qb = -1, qcount = 0, b = 0, emax = 0, t0 = 0;
+      int cur_qb = -1, qcount = 0;
       long long it = 0;
       bool ok = true;
-      for (long long g = g_begin; g < g_end; ++g, ++it) {
-        while (g >= s_prefix[qb + 1]) ++qb;
-        const int kb = static_cast<int>(g - s_prefix[qb]);
-        if (qb != cur_qb) {
-          cur_qb = qb;
-          const int slot = qcount & 1;
-          if (!(ok = mbar_wait(&qempty[slot], ((qcount >> 1) & 1) ^ 1, s_abort))) break;
-          t0 = (MODE == kModeScan) ? qb * NQ : qb;
-          mbar_arrive_expect_tx(&qfull[slot], Cfg::kQBytes);
-          tma_load_2d(s_q + slot * Cfg::kQBytes, &map_q, 0, t0 * 32, &qfull[slot], pol_q);
-          ++qcount;
-          b = row_seq_of(p.rows, t0);
-          emax = 0;
-          for (int j = 0; j < (MODE == kModeScan ? NQ : 1); ++j)
-            if (t0 + j < T) emax = max(emax, visible_of(p.rows, t0 + j, b));
-        }
-        const int s = static_cast<int>(it % S);
-        if (!(ok = mbar_wait(&empty[s], static_cast<uint32_t>((it / S) & 1) ^ 1u, s_abort))) break;
-        uint8_t* kdst = s_keys + s * Cfg::kKeyBytes;
-        float* sdst = s_scales + s * kTileKeys;
-        const int* ptab = p.page_table + static_cast<long long>(b) * p.pt_stride;
-        if (MODE == kModeScan) {
-          int pg[2];
-          uint32_t bytes = 0;
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int lp = kb * 2 + h;
-            pg[h] = -1;
-            if (lp * 64 < emax) {
-              const int phys = (lp < p.pt_stride) ? __ldg(ptab + lp) : -1;
-              if (phys >= 0 && phys < p.n_pages) {
-                pg[h] = phys;
-                bytes += 64 * kRowBytes + 64 * 4;
-              } else {
-                set_error(p.err, kErrBounds);
+      for (long long g0 = g_begin; g0 < g_end; g0 += GT) {
+        {
+          const long long gl = g0 + lane / SLOTS;
+          const int sl = lane % SLOTS;
+          int rid = -1;  // row of the 66-row page view to copy from
+          if (gl < g_end) {
+            const int qbl = find_qb(s_prefix, nqb, gl);
+            const int kb = static_cast<int>(gl - s_prefix[qbl]);
+            const int b = s_seq[qbl], emax = s_emax[qbl];
+            const int* ptab = p.page_table + static_cast<long long>(b) * p.pt_stride;
+            if (MODE == kModeScan) {
+              const int lp = kb * 2 + sl;
+              if (lp * 64 < emax) {
+                const int phys = (lp < p.pt_stride) ? __ldg(ptab + lp) : -1;
+                if (phys >= 0 && phys < p.n_pages) rid = phys * kPageRows;
+                else set_error(p.err, kErrBounds);
+              }
+            } else {
+              const int cb = kb * 16 + sl;
+              const int blk = (cb < p.pool_n) ? __ldg(p.pool_blocks + static_cast<long long>(qbl) * p.pool_n + cb) : -1;
+              if (blk >= 0 && blk * 8 < emax) {
+                const int phys = ((blk >> 3) < p.pt_stride) ? __ldg(ptab + (blk >> 3)) : -1;
+                if (phys >= 0 && phys < p.n_pages) rid = phys * kPageRows + (blk & 7) * 8;
+                else set_error(p.err, kErrBounds);
               }
             }
           }
-          mbar_arrive_expect_tx(&full[s], bytes);
+          s_lookup[lane] = rid;
+        }
+        __syncwarp();
+        if (lane == 0) {
+          int qb = find_qb(s_prefix, nqb, g0);
+          for (int j = 0; j < GT && g0 + j < g_end && ok; ++j, ++it) {
+            const long long g = g0 + j;
+            while (g >= s_prefix[qb + 1]) ++qb;
+            if (qb != cur_qb) {
+              cur_qb = qb;
+              const int slot = qcount & 1;
+              if (!(ok = mbar_wait(&qempty[slot], ((qcount >> 1) & 1) ^ 1, s_abort))) break;
+              const int t0 = (MODE == kModeScan) ? qb * NQ : qb;
+              mbar_arrive_expect_tx(&qfull[slot], Cfg::kQBytes);
+              tma_load_2d(s_q + slot * Cfg::kQBytes, &map_q, 0, t0 * 32, &qfull[slot], pol_q);
+              ++qcount;
+            }
+            const int s = static_cast<int>(it % S);
+            if (!(ok = mbar_wait(&empty[s], static_cast<uint32_t>((it / S) & 1) ^ 1u, s_abort))) break;
+            uint8_t* kdst = s_keys + s * Cfg::kKeyBytes;
+            float* sdst = s_scales + s * kTileKeys;
+            constexpr int kRows = (MODE == kModeScan) ? 64 : 8;  // key rows per copy
+            uint32_t bytes = 0;
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            if (pg[h] < 0) continue;
-            tma_load_2d(kdst + h * 64 * kRowBytes, &map_kv, 0, pg[h] * kPageRows, &full[s], pol_keys);
-            bulk_load(sdst + h * 64, p.index_k + static_cast<long long>(pg[h]) * 8448 + 8192, 256, &full[s],
-                      pol_keys);
-          }
-        } else {
-          int rowid[16];
-          uint32_t bytes = 0;
-          const int* pool = p.pool_blocks + static_cast<long long>(t0) * p.pool_n;
+            for (int c = 0; c < SLOTS; ++c)
+              if (s_lookup[j * SLOTS + c] >= 0) bytes += kRows * (kRowBytes + 4);
+            mbar_arrive_expect_tx(&full[s], bytes);
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const int cb = kb * 16 + j;
-            const int blk = (cb < p.pool_n) ? __ldg(pool + cb) : -1;
-            rowid[j] = -1;
-            if (blk >= 0 && blk * 8 < emax) {
-              const int phys = ((blk >> 3) < p.pt_stride) ? __ldg(ptab + (blk >> 3)) : -1;
-              if (phys >= 0 && phys < p.n_pages) {
-                rowid[j] = phys * kPageRows + (blk & 7) * 8;
-                bytes += 8 * kRowBytes + 8 * 4;
-              } else {
-                set_error(p.err, kErrBounds);
-              }
+            for (int c = 0; c < SLOTS; ++c) {
+              const int rid = s_lookup[j * SLOTS + c];
+              if (rid < 0) continue;
+              const int phys = rid / kPageRows;
+              const int r = rid - phys * kPageRows;
+              tma_load_2d(kdst + c * kRows * kRowBytes, &map_kv, 0, rid, &full[s], pol_keys);
+              bulk_load(sdst + c * kRows, p.index_k + static_cast<long long>(phys) * 8448 + 8192 + r * 4, kRows * 4,
+                        &full[s], pol_keys);
             }
           }
-          mbar_arrive_expect_tx(&full[s], bytes);
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            if (rowid[j] < 0) continue;
-            const int phys = rowid[j] / kPageRows;
-            const int r = rowid[j] - phys * kPageRows;
-            tma_load_2d(kdst + j * 8 * kRowBytes, &map_kv, 0, rowid[j], &full[s], pol_keys);
-            bulk_load(sdst + j * 8, p.index_k + static_cast<long long>(phys) * 8448 + 8192 + r * 4, 32, &full[s],
-                      pol_keys);
-          }
         }
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        it = __shfl_sync(0xffffffffu, it, 0);
+        if (!ok) break;
+        __syncwarp();
       }
-      if (!ok) {
-        *s_abort = 1;
-        set_error(p.err, kErrTimeout);
+      if (lane == 0) {
+        if (!ok) {
+          *s_abort = 1;
+          set_error(p.err, kErrTimeout);
+        }
+        // the copies of the last stages must land before the CTA may exit
+        for (long long i = (it > S ? it - S : 0); i < it; ++i)
+          mbar_wait(&full[i % S], static_cast<uint32_t>((i / S) & 1), nullptr);
       }
-      // the copies of the last stages must land before the CTA may exit
-      for (long long i = (it > S ? it - S : 0); i < it; ++i)
-        mbar_wait(&full[i % S], static_cast<uint32_t>((i / S) & 1), nullptr);
     } else if (warp == 1 && lane == 0) {
       // ------------------------------------------------------------ MMA issuer
       constexpr uint32_t idesc = idesc_e4m3_f32(128, NQ * 32);
@@ -285,8 +314,8 @@ __global__ void __launch_bounds__(192, 1)
         }
         const int s = static_cast<int>(it % S);
         if (!(ok = mbar_wait(&full[s], static_cast<uint32_t>((it / S) & 1), s_abort))) break;
-        const int a = static_cast<int>(it & 1);
-        if (!(ok = mbar_wait(&tempty[a], static_cast<uint32_t>((it >> 1) & 1) ^ 1u, s_abort))) break;
+        const int a = static_cast<int>(it % NA);
+        if (!(ok = mbar_wait(&tempty[a], static_cast<uint32_t>((it / NA) & 1) ^ 1u, s_abort))) break;
         tc_fence_after();
         const uint64_t adesc = smem_desc_sw128(s_keys + s * Cfg::kKeyBytes);
         const uint64_t bdesc = smem_desc_sw128(s_q + slot * Cfg::kQBytes);
@@ -303,8 +332,31 @@ __global__ void __launch_bounds__(192, 1)
       }
     } else if (warp >= 2) {
       // ------------------------------------------------------------ epilogue
+      // Two groups of four warps take alternate tiles; inside a group warp w
+      // reads TMEM lane quadrant w % 4.
+      const int grp = (warp - 2) >> 2;
+      const int gtid = threadIdx.x - 64 - grp * 128;
       const int quad = warp & 3;
       const int r = quad * 32 + lane;  // key row of this thread within the tile
+      float* s_wg = s_w + grp * NQ * 32;
+      constexpr bool kHist = (NQ == 1 && MODE == kModeScan);
+      const bool hist_on = kHist && p.hist != nullptr;
+      uint32_t* hs = reinterpret_cast<uint32_t*>(smem + Cfg::kOffHist) + grp * Cfg::kHistWords;
+      uint32_t* hb = hs + kHistBins;
+      if (hist_on)
+        for (int i = gtid; i < 2 * kHistBins; i += 128) hs[i] = 0u;
+      // adds the group's histograms of row t to the global ones and clears them
+      auto flush_hist = [&](int t) {
+        uint32_t* gs = p.hist + static_cast<long long>(t) * kHistBins;
+        uint32_t* gb = p.hist + (static_cast<long long>(T) + t) * kHistBins;
+        for (int i = gtid; i < kHistBins; i += 128) {
+          const uint32_t a = hs[i], c = hb[i];
+          if (a) atomicAdd(gs + i, a);
+          if (c) atomicAdd(gb + i, c);
+          hs[i] = 0u;
+          hb[i] = 0u;
+        }
+      };
       int qb = find_qb(s_prefix, nqb, g_begin);
       int cur_qb = -1, t0 = 0;
       int E[NQ];
@@ -312,46 +364,51 @@ __global__ void __launch_bounds__(192, 1)
       bool ok = true;
       for (long long g = g_begin; g < g_end; ++g, ++it) {
         while (g >= s_prefix[qb + 1]) ++qb;
+        if ((it & (kEpiGroups - 1)) != grp) continue;
         const int kb = static_cast<int>(g - s_prefix[qb]);
         if (qb != cur_qb) {
-          named_bar_sync(1, 128);
+          named_bar_sync(1 + grp, 128);
+          if (hist_on && cur_qb >= 0) {
+            flush_hist(t0);
+            named_bar_sync(1 + grp, 128);
+          }
           cur_qb = qb;
           t0 = (MODE == kModeScan) ? qb * NQ : qb;
           const int b = row_seq_of(p.rows, t0);
-          for (int i = threadIdx.x - 64; i < NQ * 32; i += 128) {
+          for (int i = gtid; i < NQ * 32; i += 128) {
             const int t = t0 + i / 32;
-            s_w[i] = (t < T) ? __ldg(p.w + static_cast<long long>(t) * 32 + (i & 31)) *
+            s_wg[i] = (t < T) ? __ldg(p.w + static_cast<long long>(t) * 32 + (i & 31)) *
                                    __ldg(p.q_scale + static_cast<long long>(t) * 32 + (i & 31))
                              : 0.f;
           }
 #pragma unroll
           for (int j = 0; j < NQ; ++j) E[j] = (t0 + j < T) ? visible_of(p.rows, t0 + j, b) : 0;
-          named_bar_sync(1, 128);
+          named_bar_sync(1 + grp, 128);
         }
-        const int a = static_cast<int>(it & 1);
+        const int a = static_cast<int>(it % NA);
         const int s = static_cast<int>(it % S);
-        // On a timeout this warp keeps walking the tiles without waiting, so the
-        // other epilogue warps never stall on the named barrier above.
-        if (ok) ok = mbar_wait(&tfull[a], static_cast<uint32_t>((it >> 1) & 1), s_abort);
-        if (ok) ok = mbar_wait(&full[s], static_cast<uint32_t>((it / S) & 1), s_abort);  // acquire the scales
-        if (!ok) continue;
-        tc_fence_after();
-        const float ks = s_scales[s * kTileKeys + r];
         int pos;
         long long ci = 0;
         if (MODE == kModeScan) {
           pos = kb * kTileKeys + r;
-        } else {
+        } else {  // the candidate's block id is loaded before the wait to hide its latency
           ci = static_cast<long long>(kb) * kTileKeys + r;
           const int cb = static_cast<int>(ci >> 3);
           const int blk = (cb < p.pool_n) ? __ldg(p.pool_blocks + static_cast<long long>(t0) * p.pool_n + cb) : -1;
           pos = blk >= 0 ? blk * 8 + static_cast<int>(ci & 7) : -1;
         }
+        // On a timeout this warp keeps walking the tiles without waiting, so the
+        // other warps of its group never stall on the named barrier above.
+        if (ok) ok = mbar_wait(&tfull[a], static_cast<uint32_t>((it / NA) & 1), s_abort);
+        if (ok) ok = mbar_wait(&full[s], static_cast<uint32_t>((it / S) & 1), s_abort);  // acquire the scales
+        if (!ok) continue;
+        tc_fence_after();
+        const float ks = s_scales[s * kTileKeys + r];
 #pragma unroll 1
         for (int j = 0; j < NQ; ++j) {
           float v[32];
           tmem_ld32(tmem_base + a * Cfg::kAccCols + j * 32 + (static_cast<uint32_t>(quad * 32) << 16), v);
-          const float4* w4 = reinterpret_cast<const float4*>(s_w + j * 32);
+          const float4* w4 = reinterpret_cast<const float4*>(s_wg + j * 32);
           float acc0 = 0.f, acc1 = 0.f;
 #pragma unroll
           for (int h4 = 0; h4 < 8; ++h4) {
@@ -366,14 +423,19 @@ __global__ void __launch_bounds__(192, 1)
           const float sc = valid ? (acc0 + acc1) * ks : -INFINITY;
           if (MODE == kModeScan) {
             if (t < T && pos < p.ld_out) p.out[static_cast<long long>(t) * p.ld_out + pos] = sc;
+            if (hist_on && valid) atomicAdd(&hs[ord_key(sc) >> 21], 1u);
             if (p.block_max != nullptr) {
               float m = sc;
               m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
               m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
               m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
               const int blk = pos >> 3;
-              if ((lane & 7) == 0 && t < T && blk < (E[j] + 7) / 8 && blk < p.ld_bm)
+              const int nblk = (E[j] + 7) / 8;
+              if ((lane & 7) == 0 && t < T && blk < nblk && blk < p.ld_bm) {
                 p.block_max[static_cast<long long>(t) * p.ld_bm + blk] = m;
+                // the newest block is always kept by the pool: it counts as +inf
+                if (hist_on) atomicAdd(&hb[(blk == nblk - 1 ? 0xFFFFFFFFu : ord_key(m)) >> 21], 1u);
+              }
             }
           } else {
             if (ci < static_cast<long long>(p.pool_n) * 8) p.out[static_cast<long long>(t) * p.pool_n * 8 + ci] = sc;
@@ -385,6 +447,10 @@ __global__ void __launch_bounds__(192, 1)
           mbar_arrive(&tempty[a]);
           mbar_arrive(&empty[s]);
         }
+      }
+      if (hist_on && cur_qb >= 0) {
+        named_bar_sync(1 + grp, 128);
+        flush_hist(t0);
       }
       if (!ok) {
         *s_abort = 1;
@@ -431,15 +497,28 @@ cudaError_t launch_variant(const IndexLaunch& a, const DeviceCtx& ctx, cudaStrea
   p.ld_out = a.ld_out;
   p.block_max = a.block_max;
   p.ld_bm = a.ld_bm;
+  p.hist = a.hist;
   p.pool_blocks = a.pool_blocks;
   p.pool_n = a.pool_n;
   p.err = ctx.err;
+  if (a.hist) {
+    if (!(NQ == 1 && MODE == kModeScan)) {
+      *why = "score histograms are produced on the decode path only";
+      return cudaErrorInvalidValue;
+    }
+    cudaError_t e0 = cudaMemsetAsync(a.hist, 0, static_cast<size_t>(2) * a.rows.T * kHistBins * 4, st);
+    if (e0 != cudaSuccess) return e0;
+  }
   const size_t smem = Cfg::smem_bytes(nqb);
   auto kern = index_tiles_kernel<NQ, MODE>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  cudaError_t e = prefer_max_smem(kern, smem);
   if (e != cudaSuccess) return e;
-  kern<<<ctx.num_sms, 192, smem, st>>>(map_q, map_kv, p);
-  return cudaGetLastError();
+  // CTAs per SM: bounded by shared memory, the register budget of the launch
+  // bounds and the TMEM columns (kTmemCols per CTA, 512 per SM)
+  int occ = ctas_per_sm_by_smem(ctx, smem);
+  occ = occ > Cfg::kCtasPerSm ? Cfg::kCtasPerSm : occ;
+  static_assert(IdxCfg<1>::kTmemCols * IdxCfg<1>::kCtasPerSm <= 512, "TMEM of the CTAs sharing an SM");
+  return launch_pdl(kern, dim3(ctx.num_sms * occ), dim3(kThreads), smem, st, map_q, map_kv, p);
 }
 
 }  // namespace

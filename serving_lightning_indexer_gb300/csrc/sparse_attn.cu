@@ -107,6 +107,45 @@ __device__ __forceinline__ float2 e4m3x2_to_float2(uint16_t two) {
   return __half22float2(hh);
 }
 
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
+
+// Byte tables of the bf16 bit patterns of the 8 e2m1 magnitudes times 2^(u-127)
+// (0, .5, 1, 1.5, 2, 3, 4, 6): L = low bytes, H = high bytes, entries 0-3 in
+// the first word, 4-7 in the second.  Valid for 2 <= u <= 252 (the scaled
+// magnitudes stay normal bf16 numbers).
+struct E2m1Tables {
+  uint32_t L0, L1, H0, H1;
+};
+__device__ __forceinline__ E2m1Tables e2m1_tables(uint32_t u) {
+  const int k = static_cast<int>(u) - 127;
+  constexpr uint32_t base[8] = {0u, 0x3F00u, 0x3F80u, 0x3FC0u, 0x4000u, 0x4040u, 0x4080u, 0x40C0u};
+  uint32_t P[8];
+#pragma unroll
+  for (int m = 0; m < 8; ++m) P[m] = m ? static_cast<uint32_t>(static_cast<int>(base[m]) + (k << 7)) : 0u;
+  E2m1Tables t;
+  t.L0 = (P[0] & 0xFFu) | ((P[1] & 0xFFu) << 8) | ((P[2] & 0xFFu) << 16) | ((P[3] & 0xFFu) << 24);
+  t.L1 = (P[4] & 0xFFu) | ((P[5] & 0xFFu) << 8) | ((P[6] & 0xFFu) << 16) | ((P[7] & 0xFFu) << 24);
+  t.H0 = (P[0] >> 8) | ((P[1] >> 8) << 8) | ((P[2] >> 8) << 16) | ((P[3] >> 8) << 24);
+  t.H1 = (P[4] >> 8) | ((P[5] >> 8) << 8) | ((P[6] >> 8) << 16) | ((P[7] >> 8) << 24);
+  return t;
+}
+// Four e2m1 codes (the 4 nibbles of c, element 0 lowest) -> two bf16x2 words.
+__device__ __forceinline__ void e2m1x4_bf16(uint32_t c, const E2m1Tables& t, uint32_t& o0, uint32_t& o1) {
+  const uint32_t mag = c & 0x7777u;              // 3-bit magnitude indices
+  const uint32_t lo = prmt(t.L0, t.L1, mag);
+  uint32_t hi = prmt(t.H0, t.H1, mag);
+  // byte i of sm = 0xFF when element i is negative: replicate the bit that
+  // holds the nibble's sign (c << 4 moves the even nibbles' sign to bit 7)
+  const uint32_t sm = prmt(c << 4, c, 0xD9C8u);
+  hi |= sm & 0x80808080u;
+  o0 = prmt(lo, hi, 0x5140u);                    // (lo0,hi0,lo1,hi1): elements 0, 1
+  o1 = prmt(lo, hi, 0x7362u);                    // elements 2, 3
+}
+
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
   return *reinterpret_cast<uint32_t*>(&v);
@@ -127,6 +166,8 @@ __global__ void __launch_bounds__(512, 1) sparse_attn_kernel(const __grid_consta
   const int t = blockIdx.y;
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
+  pdl_trigger();
+  pdl_wait();
   const int L = p.n_swa + p.k;
   const int nchunks = (L + kCK - 1) / kCK;
   const int c0 = split * p.chunks_per_split;
@@ -199,21 +240,33 @@ __global__ void __launch_bounds__(512, 1) sparse_attn_kernel(const __grid_consta
         const uint8_t* rec = p.main_kv + static_cast<long long>(slot) * 288;
         const uint4* src = reinterpret_cast<const uint4*>(rec + part * 32);
         const uint32_t sbytes = __ldg(reinterpret_cast<const unsigned short*>(rec + 256) + part);
-        const float sc0 = ue8m0_value(sbytes & 0xFFu), sc1 = ue8m0_value(sbytes >> 8);
+        const uint4 raw0 = __ldg(src), raw1 = __ldg(src + 1);
 #pragma unroll
         for (int i = 0; i < 2; ++i) {  // 32 elements per 16-B load, one scale each
-          const uint4 raw = __ldg(src + i);
-          const float sc = i ? sc1 : sc0;
+          const uint4 raw = i ? raw1 : raw0;
+          const uint32_t u = i ? (sbytes >> 8) : (sbytes & 0xFFu);
           const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
+          if (u >= 2u && u <= 252u) {
+            const E2m1Tables tb = e2m1_tables(u);
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {  // 8 codes per word
-            uint32_t packed[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const uint32_t byte = (w4[q] >> (8 * e)) & 0xFFu;
-              packed[e] = pack_bf16(e2m1_scaled(byte & 0xFu, sc), e2m1_scaled(byte >> 4, sc));
+            for (int q = 0; q < 4; ++q) {  // 8 codes per word
+              uint32_t o0, o1, o2, o3;
+              e2m1x4_bf16(w4[q] & 0xFFFFu, tb, o0, o1);
+              e2m1x4_bf16(w4[q] >> 16, tb, o2, o3);
+              dst[4 * i + q] = make_uint4(o0, o1, o2, o3);
             }
-            dst[4 * i + q] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+          } else {  // scales at the ends of the ue8m0 range: exact float path
+            const float sc = ue8m0_value(u);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              uint32_t packed[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const uint32_t byte = (w4[q] >> (8 * e)) & 0xFFu;
+                packed[e] = pack_bf16(e2m1_scaled(byte & 0xFu, sc), e2m1_scaled(byte >> 4, sc));
+              }
+              dst[4 * i + q] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+            }
           }
         }
       }
@@ -315,6 +368,7 @@ __global__ void __launch_bounds__(512, 1) sparse_attn_kernel(const __grid_consta
     __syncthreads();
   }
 
+  cp_async_wait_all();  // a CTA without chunks still owns in-flight copies of q
   // ---- epilogue
   const int h0 = 16 * hg + g, h1 = h0 + 8;
   if (p.nsplit == 1) {
@@ -360,36 +414,56 @@ __global__ void __launch_bounds__(512, 1) sparse_attn_kernel(const __grid_consta
   }
 }
 
-// Merge of the per-split (max, sum, O): block (t, 8-head group), thread -> 2 dims.
-__global__ void __launch_bounds__(256) attn_combine_kernel(const __grid_constant__ AttnParams p) {
-  const int t = blockIdx.x;
-  const int d = threadIdx.x * 2;
-  for (int hh = 0; hh < 8; ++hh) {
-    const int h = blockIdx.y * 8 + hh;
-    const float sk = __ldg(p.sink + h) * kLog2e;
-    float M = sk;
-    for (int s = 0; s < p.nsplit; ++s)
-      M = fmaxf(M, p.ws_ml[((static_cast<long long>(t) * p.nsplit + s) * kH + h) * 2]);
-    float den = exp2f(sk - M);
-    float a0 = 0.f, a1 = 0.f;
-    for (int s = 0; s < p.nsplit; ++s) {
-      const long long ps = static_cast<long long>(t) * p.nsplit + s;
-      const float m = p.ws_ml[(ps * kH + h) * 2];
-      if (m == -INFINITY) continue;
-      const float wgt = exp2f(m - M);
-      den += wgt * p.ws_ml[(ps * kH + h) * 2 + 1];
-      const float2 ov = *reinterpret_cast<const float2*>(p.ws_o + (ps * kH + h) * kD + d);
-      a0 += wgt * ov.x;
-      a1 += wgt * ov.y;
+// Merge of the per-split (max, sum, O) of one (row, head): one warp turns the
+// split statistics into normalised weights, then every thread sums its four
+// dims over the splits with independent loads.
+constexpr int kMaxSplits = 32;
+
+__global__ void __launch_bounds__(128) attn_combine_kernel(const __grid_constant__ AttnParams p) {
+  const int t = blockIdx.x, h = blockIdx.y;
+  __shared__ float s_wt[kMaxSplits];
+  pdl_trigger();
+  pdl_wait();
+  const int ns = p.nsplit;
+  const long long base = static_cast<long long>(t) * ns;
+  if (threadIdx.x < 32) {
+    const int s = threadIdx.x;
+    float m = -INFINITY, l = 0.f;
+    if (s < ns) {
+      m = p.ws_ml[((base + s) * kH + h) * 2];
+      l = p.ws_ml[((base + s) * kH + h) * 2 + 1];
     }
-    const float inv = 1.f / den;
-    const long long o = (static_cast<long long>(t) * kH + h) * kD + d;
-    if (p.out_bf16)
-      *reinterpret_cast<__nv_bfloat162*>(static_cast<__nv_bfloat16*>(p.out) + o) =
-          __floats2bfloat162_rn(a0 * inv, a1 * inv);
-    else
-      *reinterpret_cast<float2*>(static_cast<float*>(p.out) + o) = make_float2(a0 * inv, a1 * inv);
-    if (p.lse && threadIdx.x == 0) p.lse[static_cast<long long>(t) * kH + h] = (M + log2f(den)) * kLn2;
+    const float sk = __ldg(p.sink + h) * kLog2e;
+    float M = fmaxf(m, sk);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    const float w = (s < ns && m != -INFINITY) ? exp2f(m - M) : 0.f;
+    float den = w * l;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+    den += exp2f(sk - M);
+    s_wt[s] = w / den;
+    if (s == 0 && p.lse) p.lse[static_cast<long long>(t) * kH + h] = (M + log2f(den)) * kLn2;
+  }
+  __syncthreads();
+  const int d = threadIdx.x * 4;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 8
+  for (int s = 0; s < ns; ++s) {
+    const float w = s_wt[s];
+    const float4 v = *reinterpret_cast<const float4*>(p.ws_o + ((base + s) * kH + h) * kD + d);
+    acc.x = fmaf(w, v.x, acc.x);
+    acc.y = fmaf(w, v.y, acc.y);
+    acc.z = fmaf(w, v.z, acc.z);
+    acc.w = fmaf(w, v.w, acc.w);
+  }
+  const long long o = (static_cast<long long>(t) * kH + h) * kD + d;
+  if (p.out_bf16) {
+    __nv_bfloat162* out = reinterpret_cast<__nv_bfloat162*>(static_cast<__nv_bfloat16*>(p.out) + o);
+    out[0] = __floats2bfloat162_rn(acc.x, acc.y);
+    out[1] = __floats2bfloat162_rn(acc.z, acc.w);
+  } else {
+    *reinterpret_cast<float4*>(static_cast<float*>(p.out) + o) = acc;
   }
 }
 
@@ -401,6 +475,7 @@ int attn_num_splits(int T, int n_keys, int num_sms) {
   int s = (2 * num_sms + T - 1) / T;
   if (s < 1) s = 1;
   if (s > nchunks) s = nchunks;
+  if (s > kMaxSplits) s = kMaxSplits;
   // equalise the chunk count per split
   const int cps = (nchunks + s - 1) / s;
   return (nchunks + cps - 1) / cps;
@@ -443,12 +518,13 @@ cudaError_t launch_sparse_attn(const AttnLaunch& a, void* ws, size_t ws_bytes, c
     p.ws_o = static_cast<float*>(ws);
     p.ws_ml = p.ws_o + static_cast<size_t>(a.T) * nsplit * kH * kD;
   }
-  cudaError_t e = cudaFuncSetAttribute(sparse_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       AttnSmem::kBytes);
+  cudaError_t e = prefer_max_smem(sparse_attn_kernel, AttnSmem::kBytes);
   if (e != cudaSuccess) return e;
-  sparse_attn_kernel<<<dim3(nsplit, a.T), 512, AttnSmem::kBytes, st>>>(p);
-  if (nsplit > 1) attn_combine_kernel<<<dim3(a.T, kH / 8), 256, 0, st>>>(p);
-  return cudaGetLastError();
+  if ((e = prefer_max_smem(attn_combine_kernel, 0)) != cudaSuccess) return e;
+  e = launch_pdl(sparse_attn_kernel, dim3(nsplit, a.T), dim3(512), AttnSmem::kBytes, st, p);
+  if (e != cudaSuccess) return e;
+  if (nsplit > 1) e = launch_pdl(attn_combine_kernel, dim3(a.T, kH), dim3(128), 0, st, p);
+  return e;
 }
 
 }  // namespace csa2

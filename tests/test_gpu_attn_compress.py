@@ -121,3 +121,31 @@ def test_compress_entry_slots_and_no_rope():
     assert np.array_equal(np_(kv)[np_(es)], o.fp4_encode_records(np_(lat).astype(np.float64)))
     untouched = np.setdiff1d(np.arange(100), np_(es))
     assert (np_(kv)[untouched] == 0).all()
+
+
+def test_attention_main_kv_with_varied_block_scales():
+    # e2m1 records whose 32-element groups carry scales 2^(u-127) with u spread
+    # over a wide range (the table-lookup dequantisation) and at the ends of the
+    # ue8m0 range (the exact float path); compared relative to the output scale.
+    dev = need_gpu()
+    rng = np.random.default_rng(7)
+    n = 600
+    rec = np.zeros((n, 288), dtype=np.uint8)
+    rec[:, :256] = rng.integers(0, 256, size=(n, 256), dtype=np.uint8)
+    u = rng.integers(118, 137, size=(n, 16))
+    u[::7, 3] = 0
+    u[::11, 5] = 1
+    u[::13, 9] = 2
+    rec[:, 256:272] = u.astype(np.uint8)
+    main = torch.tensor(rec, device=dev)
+    al = W.make_attn_layer(2, seed=8, device=dev)
+    slots = np.stack([rng.choice(n, size=512, replace=False) for _ in range(2)])
+    tks = torch.tensor(slots, dtype=torch.int32, device=dev)
+    out = torch.empty(2, 64, 512, dtype=torch.float32, device=dev)
+    csa2.sparse_attn(al.q, main, tks, al.swa_kv, al.swa_slot, al.sink, out, softmax_scale=1e-3)
+    torch.cuda.synchronize()
+    for t in range(2):
+        ref, _ = o.attention_row(al.q[t].float().cpu().numpy().astype(np.float64), rec, slots[t], np_(al.swa_kv),
+                                 np_(al.swa_slot[t]), np_(al.sink).astype(np.float64), 1e-3)
+        err = np.abs(np_(out[t]).astype(np.float64) - ref).max() / np.abs(ref).max()
+        assert err < 1e-2, err

@@ -179,3 +179,41 @@ def test_reindex_equals_full_topk_when_pool_covers_all():
     torch.cuda.synchronize()
     assert (np_(pool[0])[:1500] == np.arange(1500)).all()
     assert np_(rpos[0]).tolist() == np_(pos[0]).tolist()
+
+
+def test_fused_histograms_give_identical_selection():
+    # the decode scan's key histograms, passed on to the top-k, must not change any result
+    dev = need_gpu()
+    lengths = [70000, 140001, 20000]
+    B = len(lengths)
+    pc = W.make_paged_cache(lengths, seed=21, device=dev, with_main=False)
+    iq = W.make_indexer_query(B, seed=22, device=dev)
+    r = csa2.rows(B, B, n_visible=torch.tensor(lengths, dtype=torch.int32, device=dev))
+    ld = 140032
+    scores = torch.empty(B, ld, dtype=torch.float32, device=dev)
+    bm = torch.empty(B, ld // 8, dtype=torch.float32, device=dev)
+    hist = torch.full((2, B, 2048), 99, dtype=torch.int32, device=dev)
+    csa2.index_score(iq.q_fp8, iq.q_scale, iq.w, pc.index_k, pc.page_table, r, scores, bm, hist=hist)
+    outs = []
+    for h in (None, hist):
+        pos = torch.empty(B, 512, dtype=torch.int32, device=dev)
+        slot = torch.empty_like(pos)
+        pool = torch.empty(B, 2048, dtype=torch.int32, device=dev)
+        csa2.topk_with_candidates(scores, r, 512, pos, slot, pc.page_table, bm, pool, hist=h)
+        outs.append((np_(pos), np_(slot), np_(pool)))
+    torch.cuda.synchronize()
+    assert csa2.check_device_error() == 0
+    for a, b in zip(*outs):
+        assert np.array_equal(a, b)
+    # the histograms count exactly the visible scores and block maxima, in their top-11-bit bins
+    h = np_(hist).astype(np.int64)
+    for b_, n in enumerate(lengths):
+        s = np_(scores[b_, :n])
+        key = s.view(np.uint32).astype(np.int64)
+        key = np.where(key & 0x80000000, ~key & 0xFFFFFFFF, key | 0x80000000)
+        assert np.array_equal(h[0, b_], np.bincount(key >> 21, minlength=2048))
+        nb = (n + 7) // 8
+        bmk = np_(bm[b_, :nb]).view(np.uint32).astype(np.int64)
+        bmk = np.where(bmk & 0x80000000, ~bmk & 0xFFFFFFFF, bmk | 0x80000000)
+        bmk[-1] = 0xFFFFFFFF
+        assert np.array_equal(h[1, b_], np.bincount(bmk >> 21, minlength=2048))
