@@ -167,6 +167,21 @@ typedef struct {
 } csa2_topk_args;
 CSA2_API int csa2_topk_with_candidates(const csa2_topk_args* args, void* workspace, size_t ws_bytes, void* stream);
 
+/* ---- top-k without workspace or allocation ------------------------------------
+ * The pages have no counterpart of this call: it is a deployment convenience.
+ * Same arguments, semantics and results as csa2_topk_with_candidates, but no
+ * workspace: for callers that cannot provide or allocate device scratch (an
+ * operator interface that passes only inputs and outputs, an engine whose
+ * allocator cannot serve extra buffers, a path that must not call cudaMalloc).
+ * The scratch is a static device array of CSA2_TOPK_NOALLOC_SCRATCH_BYTES that
+ * every GPU loading the library holds until exit; rows needing more (about 60
+ * rows when long rows and pools are selected) return CSA2_ERR_WORKSPACE.  The
+ * library allocates nothing during the call.  The first call on each device
+ * looks up the array's device address, so make it before any stream capture.
+ * All calls share the array: calls that overlap on the GPU race. */
+#define CSA2_TOPK_NOALLOC_SCRATCH_BYTES ((size_t)8 << 20)
+CSA2_API int csa2_topk_with_candidates_noalloc(const csa2_topk_args* args, void* stream);
+
 /* ---- 3. Reindex: pool-only rescoring and top-k ------------------------------
  * Candidate i of row t is position p = 8 * pool_blocks[t][i / 8] + i % 8; it
  * is scored like csa2_index_score when the block id is >= 0 and p < E_t, and

@@ -65,7 +65,7 @@ class CompressArgs(C.Structure):
 CALL_INDEX_SCORE, CALL_TOPK, CALL_REINDEX, CALL_SPARSE_ATTN = 1, 2, 3, 4
 EXPORTED = ("csa2_status_string", "csa2_last_error_detail", "csa2_index_score", "csa2_topk_with_candidates",
             "csa2_reindex", "csa2_sparse_attn", "csa2_compress_m2", "csa2_workspace_size",
-            "csa2_check_device_error", "csa2_version")
+            "csa2_check_device_error", "csa2_version", "csa2_topk_with_candidates_noalloc")
 
 _lib = None
 
@@ -94,6 +94,8 @@ def load(build_if_missing: bool = False) -> C.CDLL:
         f = getattr(lib, name)
         f.restype = C.c_int
         f.argtypes = [C.POINTER(st), _P, C.c_size_t, _P]
+    lib.csa2_topk_with_candidates_noalloc.restype = C.c_int
+    lib.csa2_topk_with_candidates_noalloc.argtypes = [C.POINTER(TopkArgs), _P]
     lib.csa2_compress_m2.restype = C.c_int
     lib.csa2_compress_m2.argtypes = [C.POINTER(CompressArgs), _P]
     lib.csa2_workspace_size.restype = C.c_int
@@ -172,6 +174,19 @@ def topk_with_candidates(scores, r: Rows, k, topk_pos, topk_slot=None, page_tabl
     buf = ws if ws is not None else workspace(need.value, scores.device, "topk")
     _check(lib.csa2_topk_with_candidates(C.byref(a), _ptr(buf), buf.numel() if buf is not None else 0,
                                          _stream(stream)), "csa2_topk_with_candidates")
+
+
+def topk_with_candidates_noalloc(scores, r: Rows, k, topk_pos, topk_slot=None, page_table=None, block_max=None,
+                                 pool_blocks=None, stream=None, hist=None):
+    """csa2_topk_with_candidates_noalloc: the same selection without a workspace; its
+    scratch is a static device array inside the library (for callers that cannot
+    allocate device memory)."""
+    lib = load()
+    a = TopkArgs(_ptr(scores), scores.shape[-1], _ptr(block_max), block_max.shape[-1] if block_max is not None else 0,
+                 _ptr(page_table), page_table.shape[-1] if page_table is not None else 0, r, k, _ptr(topk_pos),
+                 _ptr(topk_slot), topk_pos.shape[-1], _ptr(pool_blocks),
+                 pool_blocks.shape[-1] if pool_blocks is not None else 0, _ptr(hist))
+    _check(lib.csa2_topk_with_candidates_noalloc(C.byref(a), _stream(stream)), "csa2_topk_with_candidates_noalloc")
 
 
 def reindex(q_fp8, q_scale, w, index_k, page_table, r: Rows, pool_blocks, k, topk_pos, topk_slot=None,

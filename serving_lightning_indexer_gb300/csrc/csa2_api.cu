@@ -28,6 +28,18 @@ int fail(int code, const char* fmt, ...) {
   return code;
 }
 
+}  // namespace
+
+namespace csa2 {
+// Records the detail string of an error returned on this thread.
+int set_error_detail(int code, const char* detail) {
+  g_detail = detail;
+  return code;
+}
+}  // namespace csa2
+
+namespace {
+
 int cuda_fail(cudaError_t e, const char* what) {
   return fail(CSA2_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
 }
@@ -182,7 +194,11 @@ int csa2_index_score(const csa2_index_score_args* a, void* ws, size_t ws_bytes, 
   return CSA2_OK;
 }
 
-static int topk_fill(const csa2_topk_args* a, csa2::SelectLaunch* S) {
+}  // extern "C"
+
+// Validates top-k arguments and fills the internal launch description; shared
+// by every top-k entry point.
+int csa2::topk_prepare(const csa2_topk_args* a, csa2::SelectLaunch* S) {
   if (!a) return fail(CSA2_ERR_NULL, "csa2_topk_with_candidates: args is NULL");
   int rc = rows_check(a->rows, "csa2_topk_with_candidates");
   if (rc) return rc;
@@ -219,9 +235,11 @@ static int topk_fill(const csa2_topk_args* a, csa2::SelectLaunch* S) {
   return CSA2_OK;
 }
 
+extern "C" {
+
 int csa2_topk_with_candidates(const csa2_topk_args* a, void* ws, size_t ws_bytes, void* stream) {
   csa2::SelectLaunch S;
-  int rc = topk_fill(a, &S);
+  int rc = csa2::topk_prepare(a, &S);
   if (rc) return rc;
   const size_t need = csa2::select_workspace_bytes(S);
   if (!ws || ws_bytes < need)
@@ -389,7 +407,7 @@ int csa2_workspace_size(int which, const void* args, size_t* bytes) {
       return CSA2_OK;
     case CSA2_CALL_TOPK: {
       csa2::SelectLaunch S;
-      int rc = topk_fill(static_cast<const csa2_topk_args*>(args), &S);
+      int rc = csa2::topk_prepare(static_cast<const csa2_topk_args*>(args), &S);
       if (rc) return rc;
       *bytes = csa2::select_workspace_bytes(S);
       return CSA2_OK;

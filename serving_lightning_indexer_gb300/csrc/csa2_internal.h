@@ -137,6 +137,11 @@ struct CompressLaunch {
 };
 cudaError_t launch_compress(const CompressLaunch& a, const DeviceCtx& ctx, cudaStream_t st);
 
+// Shared by the top-k entry points: argument checks + launch description.
+int topk_prepare(const csa2_topk_args* a, SelectLaunch* S);
+// Records the per-thread detail string returned by csa2_last_error_detail().
+int set_error_detail(int code, const char* detail);
+
 // Launch with programmatic stream serialisation (see pdl_trigger / pdl_wait).
 template <typename... KArgs, typename... Args>
 cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
