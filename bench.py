@@ -41,6 +41,26 @@ WORKLOAD = "csa2-decode-38layer-b8-ctx{32K,256K,1M,1M}x2"
 INDEX_KEY_BYTES = 132   # 128 e4m3 codes + one fp32 scale per key
 
 
+def _scan_traffic_per_key():
+    """DRAM bytes per key of the decode scan from the committed ncu capture
+    (profiles/index_scan_decode_b8x262k.md), or None when the kernel source has
+    changed since that capture was taken."""
+    import hashlib
+    import re
+    csrc = os.path.join(ROOT, "serving_lightning_indexer_gb300", "csrc")
+    src = b"".join(open(os.path.join(csrc, f), "rb").read() for f in ("index_score.cu", "csa2_device.cuh"))
+    digest = hashlib.sha256(src).hexdigest()[:16]
+    try:
+        text = open(os.path.join(ROOT, "profiles", "index_scan_decode_b8x262k.md")).read()
+    except OSError:
+        return None
+    per_key = re.search(r"dram_bytes_per_key:\s*([0-9.]+)", text)
+    sha = re.search(r"source_sha256:\s*([0-9a-f]+)", text)
+    if not per_key or not sha or sha.group(1) != digest:
+        return None
+    return float(per_key.group(1))
+
+
 def _peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -300,6 +320,7 @@ def main():
         return
 
     peak, peak_kind = _peaks()
+    traffic_per_key = _scan_traffic_per_key()
     ms_per_step = ms_total / K
     value = keys_per_step * K * world / (ms_total / 1e3)
     scan_launches = len(scan_ms)
@@ -326,7 +347,11 @@ def main():
         "attn_query_layers_per_s": attn_per_step * K * world / (ms_total / 1e3),
         "roofline": {"bound": "hbm", "kernel": "index_tiles_kernel<1,scan> (decode Lightning-Indexer scan)",
                      "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "peak_source": peak_kind, "traffic": None,
+                     "peak_source": peak_kind,
+                     "traffic": (None if traffic_per_key is None
+                                 else traffic_per_key * scan_bytes_per_launch / INDEX_KEY_BYTES),
+                     "traffic_source": "ncu dram bytes per key of the committed scan capture, scaled to the "
+                                       "keys of an average launch",
                      "algorithmic_bytes_per_launch": scan_bytes_per_launch,
                      "avg_launch_ms": scan_ms_total / scan_launches, "launches_timed": scan_launches,
                      "per_layer_ms": {str(l): statistics.mean(v) for l, v in per_layer.items()}},
