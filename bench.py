@@ -326,12 +326,13 @@ def main():
     scan_launches = len(scan_ms)
     scan_bytes_per_launch = scan_bytes_per_step * K / scan_launches
     achieved = scan_bytes_per_step * K / (scan_ms_total / 1e3) / 1e9
-    # our kernels launched per step (the attention split-K merge and the select
-    # passes included; memsets are not kernels)
+    # our kernels launched per step: a Full layer runs compress, the scan and the
+    # two select passes (filter, final); a Reindex layer the pool gather and the
+    # final select; every layer one clustered attention launch (memsets are not kernels)
     from serving_lightning_indexer_gb300 import decode_step as ds
     n_full = sum(1 for l in step.layers if ds.role_of(l) == "full")
     n_reidx = sum(1 for l in step.layers if ds.role_of(l) == "reindex")
-    launches_per_step = n_full * (1 + 1 + 4) + n_reidx * 2 + len(step.layers) * 2
+    launches_per_step = n_full * 4 + n_reidx * 2 + len(step.layers)
     cpu = None
     if not args.no_cpu_baseline:
         v, cores, sample = cpu_baseline(step, args.cpu_budget, lambda t: t.detach().cpu().numpy())

@@ -5,14 +5,20 @@
 // <= k main-KV entries of the row's top-k, with the per-head sink s_i only in
 // the denominator; K = V is one shared 512-vector (MQA, 64 heads).
 //
-// A CTA takes one query row and a contiguous range of 64-key chunks of the
-// row's key list [SWA slots..., main slots...].  Per chunk it gathers the
-// records (FP8 SWA, FP4 main KV), dequantises them to bf16 in shared memory,
-// computes S = q K^T on the tensor cores (mma.sync m16n8k16 bf16, fp32
-// accumulation; 16 warps, each a 16-head x 16-key tile over all 512 dims),
-// updates a running max / sum per head, and accumulates O += P V (each warp a
-// 16-head x 128-dim tile).  Small batches split the key list over several
-// CTAs and merge the partial (max, sum, O) by log-sum-exp in a second kernel.
+// The key list of a row is [SWA slots..., main slots...], cut into chunks of
+// 64 keys.  A thread-block cluster of S CTAs works on one row, CTA r taking a
+// contiguous range of chunks.  Per chunk a CTA
+//   * gathers the records with bulk async copies (one per key, completing on an
+//     mbarrier) into a staging area, the row's q arriving the same way,
+//   * dequantises them to bf16 rows in shared memory (FP8 e4m3 x fp32 scale for
+//     SWA, e2m1 x ue8m0 through byte-permute tables for main KV),
+//   * computes S = q K^T on the tensor cores (mma.sync m16n8k16 bf16, fp32
+//     accumulate; 16 warps, each 16 heads x 16 keys over all 512 dims), a
+//     running max / sum per head, and O += P V (each warp 16 heads x 128 dims),
+// gathering the next chunk's records meanwhile.  The partial results of a row
+// are merged through distributed shared memory: the CTAs exchange their (max,
+// sum) per head, scale their O by exp(max - M) / denominator, and each CTA sums
+// a share of the heads over the cluster and writes it.  No global scratch.
 #include <math.h>
 
 #include "csa2_device.cuh"
@@ -28,6 +34,9 @@ constexpr int kCK = 64;              // keys per chunk
 constexpr int kQStride = kD + 8;     // bf16 per shared row (1040 B: conflict-free ldmatrix)
 constexpr int kSStride = kCK + 4;    // floats
 constexpr int kPStride = kCK + 8;    // bf16
+constexpr int kRawStride = 528;      // staging bytes per key (largest record)
+constexpr int kOStride = kD + 4;     // floats per row of the O partial in the merge
+constexpr int kMaxCluster = 16;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
@@ -49,22 +58,30 @@ struct AttnParams {
   int out_bf16;
   void* out;
   float* lse;
-  int nsplit;
+  int nsplit;             // CTAs per row = cluster size
   int chunks_per_split;
-  float* ws_o;    // [T][nsplit][64][512]
-  float* ws_ml;   // [T][nsplit][64][2]
   uint32_t* err;
 };
 
 struct AttnSmem {
   static constexpr int kOffQ = 0;
   static constexpr int kOffK = kOffQ + kH * kQStride * 2;
-  static constexpr int kOffS = kOffK + kCK * kQStride * 2;
+  static constexpr int kOffRaw = kOffK + kCK * kQStride * 2;
+  static constexpr int kOffS = kOffRaw + kCK * kRawStride;
   static constexpr int kOffP = kOffS + kH * kSStride * 4;
   static constexpr int kOffStats = kOffP + kH * kPStride * 2;  // m, l, alpha [64] each
-  static constexpr int kOffValid = kOffStats + 3 * kH * 4;
-  static constexpr int kBytes = kOffValid + kCK * 4;
+  static constexpr int kOffKind = kOffStats + 3 * kH * 4;       // [64] 0 none, 1 SWA, 2 main
+  static constexpr int kOffBars = kOffKind + kCK * 4;           // q, records, merge receive
+  static constexpr int kBytes = kOffBars + 24;
+  // merge: send rows [64][kQStride] bf16 over q, receive rows [ns][ceil(64/ns)][512] bf16 after them
+  static constexpr int kRecvRowsMax = 75;                       // max over ns of ns * ceil(64 / ns)
+  static constexpr int kOffSend = 0;
+  static constexpr int kOffRecv = kOffSend + kH * kQStride * 2;
+  static_assert(kOffRecv + kRecvRowsMax * kD * 2 <= kOffS, "the merge buffers fit over q, K and the staging");
 };
+// ns * recv_rows_per_rank(ns) peaks at 75 (ns = 15) for 1 <= ns <= 16.
+__host__ __device__ constexpr int recv_rows_per_rank(int ns) { return (kH + ns - 1) / ns; }
+static_assert(15 * ((kH + 14) / 15) == AttnSmem::kRecvRowsMax, "receive rows");
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
@@ -84,29 +101,47 @@ __device__ __forceinline__ void mma_bf16(float (&c)[4], uint32_t a0, uint32_t a1
       : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
-__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem)), "l"(gmem) : "memory");
-}
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
-// e2m1 code (4 bits) times a power-of-two scale.
-__device__ __forceinline__ float e2m1_scaled(uint32_t c, float scale) {
-  const uint32_t e = (c >> 1) & 3u, m = c & 1u;
-  const float mag = e ? __uint_as_float(((e + 126u) << 23) | (m << 22)) : (m ? 0.5f : 0.f);
-  const float v = mag * scale;
-  return (c & 8u) ? -v : v;
+// ---------------------------------------------------------------- cluster helpers
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
 }
-__device__ __forceinline__ float ue8m0_value(uint32_t u) {
-  return u ? __uint_as_float(u << 23) : __uint_as_float(0x00400000u);  // 2^(u-127)
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
-// Two e4m3 codes (low byte first) -> two floats, exactly (e4m3 is a subset of f16).
-__device__ __forceinline__ float2 e4m3x2_to_float2(uint16_t two) {
-  uint32_t h2;
-  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(two));
-  __half2 hh = *reinterpret_cast<__half2*>(&h2);
-  return __half22float2(hh);
+// Address of the same shared-memory location in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t map_rank(uint32_t smem_addr, uint32_t rank) {
+  uint32_t d;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(d) : "r"(smem_addr), "r"(rank));
+  return d;
+}
+__device__ __forceinline__ float ld_cluster_f32(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr));
+  return v;
+}
+// Bulk asynchronous copy from this CTA's shared memory into a cluster peer's,
+// completing on the peer's mbarrier (dst and mbar in the cluster window).
+__device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst, const void* src, uint32_t bytes, uint32_t mbar) {
+  asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+                   "r"(dst),
+               "r"(smem_u32(src)), "r"(bytes), "r"(mbar)
+               : "memory");
+}
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ float4 ld_cluster_f32x4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0,%1,%2,%3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr));
+  return v;
 }
 
+// ---------------------------------------------------------------- dequantisation
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
   uint32_t d;
   asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
@@ -145,45 +180,129 @@ __device__ __forceinline__ void e2m1x4_bf16(uint32_t c, const E2m1Tables& t, uin
   o0 = prmt(lo, hi, 0x5140u);                    // (lo0,hi0,lo1,hi1): elements 0, 1
   o1 = prmt(lo, hi, 0x7362u);                    // elements 2, 3
 }
-
+// e2m1 code (4 bits) times a power-of-two scale (exact float path).
+__device__ __forceinline__ float e2m1_scaled(uint32_t c, float scale) {
+  const uint32_t e = (c >> 1) & 3u, m = c & 1u;
+  const float mag = e ? __uint_as_float(((e + 126u) << 23) | (m << 22)) : (m ? 0.5f : 0.f);
+  const float v = mag * scale;
+  return (c & 8u) ? -v : v;
+}
+__device__ __forceinline__ float ue8m0_value(uint32_t u) {
+  return u ? __uint_as_float(u << 23) : __uint_as_float(0x00400000u);  // 2^(u-127)
+}
+// Two e4m3 codes (low byte first) -> two floats, exactly (e4m3 is a subset of f16).
+__device__ __forceinline__ float2 e4m3x2_to_float2(uint32_t two) {
+  uint32_t h2;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(static_cast<uint16_t>(two)));
+  __half2 hh = *reinterpret_cast<__half2*>(&h2);
+  return __half22float2(hh);
+}
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// 16-B chunk c (elements 8c .. 8c+7) of a staged record -> 8 bf16.
+__device__ __forceinline__ uint4 dequant_chunk(const uint8_t* raw, int kind, int c) {
+  if (kind == 2) {  // main KV: 512 e2m1 codes, ue8m0 per 32 elements
+    const uint32_t w = *reinterpret_cast<const uint32_t*>(raw + 4 * c);
+    const uint32_t u = raw[256 + (c >> 2)];
+    uint4 o;
+    if (u >= 2u && u <= 252u) {
+      const E2m1Tables tb = e2m1_tables(u);
+      e2m1x4_bf16(w & 0xFFFFu, tb, o.x, o.y);
+      e2m1x4_bf16(w >> 16, tb, o.z, o.w);
+    } else {
+      const float sc = ue8m0_value(u);
+      uint32_t pk[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const uint32_t byte = (w >> (8 * e)) & 0xFFu;
+        pk[e] = pack_bf16(e2m1_scaled(byte & 0xFu, sc), e2m1_scaled(byte >> 4, sc));
+      }
+      o = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+    }
+    return o;
+  }
+  if (kind == 1) {  // SWA: 512 e4m3 codes, fp32 scale per 128 channels
+    const uint2 w = *reinterpret_cast<const uint2*>(raw + 8 * c);
+    const float sc = *reinterpret_cast<const float*>(raw + 512 + (c >> 4) * 4);
+    const float2 a = e4m3x2_to_float2(w.x & 0xFFFFu), b = e4m3x2_to_float2(w.x >> 16);
+    const float2 d = e4m3x2_to_float2(w.y & 0xFFFFu), e = e4m3x2_to_float2(w.y >> 16);
+    return make_uint4(pack_bf16(a.x * sc, a.y * sc), pack_bf16(b.x * sc, b.y * sc), pack_bf16(d.x * sc, d.y * sc),
+                      pack_bf16(e.x * sc, e.y * sc));
+  }
+  return make_uint4(0u, 0u, 0u, 0u);
+}
+
+// Slot and kind of key j of row t (kind 0: empty or out of range).
+__device__ __forceinline__ int key_slot(const AttnParams& p, int t, int j, int* kind) {
+  int slot = -1;
+  *kind = 0;
+  if (j < p.n_swa) {
+    slot = __ldg(p.swa_slot + static_cast<long long>(t) * p.ld_swa + j);
+    if (slot >= p.swa_slots) {
+      set_error(p.err, kErrBounds);
+      slot = -1;
+    }
+    if (slot >= 0) *kind = 1;
+  } else if (j < p.n_swa + p.k) {
+    slot = __ldg(p.topk_slot + static_cast<long long>(t) * p.ld_topk + (j - p.n_swa));
+    if (slot >= p.main_slots) {
+      set_error(p.err, kErrBounds);
+      slot = -1;
+    }
+    if (slot >= 0) *kind = 2;
+  }
+  return slot;
+}
+
 __global__ void __launch_bounds__(512, 1) sparse_attn_kernel(const __grid_constant__ AttnParams p) {
-  extern __shared__ __align__(16) uint8_t sm[];
+  extern __shared__ __align__(128) uint8_t sm[];
   __nv_bfloat16* sQ = reinterpret_cast<__nv_bfloat16*>(sm + AttnSmem::kOffQ);
   __nv_bfloat16* sK = reinterpret_cast<__nv_bfloat16*>(sm + AttnSmem::kOffK);
+  uint8_t* sRaw = sm + AttnSmem::kOffRaw;
   float* sS = reinterpret_cast<float*>(sm + AttnSmem::kOffS);
   __nv_bfloat16* sP = reinterpret_cast<__nv_bfloat16*>(sm + AttnSmem::kOffP);
   float* sM = reinterpret_cast<float*>(sm + AttnSmem::kOffStats);
   float* sL = sM + kH;
   float* sA = sL + kH;
-  int* sValid = reinterpret_cast<int*>(sm + AttnSmem::kOffValid);
+  int* sKind = reinterpret_cast<int*>(sm + AttnSmem::kOffKind);
+  uint64_t* bar_q = reinterpret_cast<uint64_t*>(sm + AttnSmem::kOffBars);
+  uint64_t* bar_raw = bar_q + 1;
+  uint64_t* bar_recv = bar_q + 2;
 
-  const int split = blockIdx.x;
-  const int t = blockIdx.y;
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
-  pdl_trigger();
-  pdl_wait();
+  const int t = blockIdx.y;
+  const uint32_t rank = (p.nsplit > 1) ? cluster_rank() : 0u;
   const int L = p.n_swa + p.k;
   const int nchunks = (L + kCK - 1) / kCK;
-  const int c0 = split * p.chunks_per_split;
+  const int c0 = static_cast<int>(rank) * p.chunks_per_split;
   const int c1 = min(c0 + p.chunks_per_split, nchunks);
 
-  // q -> shared (async), stats init
-  {
-    const __nv_bfloat16* gq = p.q + static_cast<long long>(t) * kH * kD;
-    for (int i = tid; i < kH * (kD / 8); i += blockDim.x) {
-      const int h = i / (kD / 8), c = i % (kD / 8);
-      cp_async16(sQ + h * kQStride + c * 8, gq + h * kD + c * 8);
-    }
+  if (tid == 0) {
+    mbar_init(bar_q, kH);     // one arrival per q row copy
+    mbar_init(bar_raw, kCK);  // one arrival per key of a chunk
+    mbar_init(bar_recv, 1);   // the merge: one local arrival + the bytes pushed by the cluster
+    fence_mbar_init();
   }
   if (tid < kH) {
     sM[tid] = -INFINITY;
     sL[tid] = 0.f;
+  }
+  __syncthreads();
+  pdl_trigger();
+  pdl_wait();
+
+  const uint64_t pol = l2_policy_evict_first();
+  // q rows and the first chunk's records: bulk copies, one per thread of the first 64
+  int next_slot = -1, next_kind = 0;
+  if (tid < kCK) {
+    mbar_arrive_expect_tx(bar_q, kD * 2);
+    bulk_load(sQ + tid * kQStride, p.q + (static_cast<long long>(t) * kH + tid) * kD, kD * 2, bar_q,
+              l2_policy_evict_last());
+    if (c0 < c1) next_slot = key_slot(p, t, c0 * kCK + tid, &next_kind);
   }
   float o[16][4];
 #pragma unroll
@@ -191,89 +310,50 @@ __global__ void __launch_bounds__(512, 1) sparse_attn_kernel(const __grid_consta
   const int hg = warp & 3;       // 16-head group
   const int xg = warp >> 2;      // S: 16-key group; PV: 128-dim group
   const int g = lane >> 2, cq = lane & 3;
+  bool ok = true;
 
-  for (int ch = c0; ch < c1; ++ch) {
-    // ---- gather + dequantise 64 keys: thread -> (key kk, 64-dim part)
-    {
-      const int kk = tid >> 3, part = tid & 7;
-      const int j = ch * kCK + kk;
-      int slot = -1;
-      bool swa = false;
-      if (j < p.n_swa) {
-        slot = __ldg(p.swa_slot + static_cast<long long>(t) * p.ld_swa + j);
-        swa = true;
-        if (slot >= p.swa_slots) {
-          set_error(p.err, kErrBounds);
-          slot = -1;
-        }
-      } else if (j < L) {
-        slot = __ldg(p.topk_slot + static_cast<long long>(t) * p.ld_topk + (j - p.n_swa));
-        if (slot >= p.main_slots) {
-          set_error(p.err, kErrBounds);
-          slot = -1;
-        }
-      }
-      uint4* dst = reinterpret_cast<uint4*>(sK + kk * kQStride + part * 64);
-      if (slot < 0) {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) dst[i] = make_uint4(0, 0, 0, 0);
-      } else if (swa) {
-        const uint8_t* rec = p.swa_kv + static_cast<long long>(slot) * 528;
-        const float sc = __ldg(reinterpret_cast<const float*>(rec + 512) + (part >> 1));
-        const uint4* src = reinterpret_cast<const uint4*>(rec + part * 64);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const uint4 raw = __ldg(src + i);  // 16 codes
-          const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
-          uint32_t packed[8];
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const float2 lo = e4m3x2_to_float2(static_cast<uint16_t>(w4[q] & 0xFFFFu));
-            const float2 hi = e4m3x2_to_float2(static_cast<uint16_t>(w4[q] >> 16));
-            packed[2 * q] = pack_bf16(lo.x * sc, lo.y * sc);
-            packed[2 * q + 1] = pack_bf16(hi.x * sc, hi.y * sc);
-          }
-          dst[2 * i] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
-          dst[2 * i + 1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
-        }
-      } else {
-        const uint8_t* rec = p.main_kv + static_cast<long long>(slot) * 288;
-        const uint4* src = reinterpret_cast<const uint4*>(rec + part * 32);
-        const uint32_t sbytes = __ldg(reinterpret_cast<const unsigned short*>(rec + 256) + part);
-        const uint4 raw0 = __ldg(src), raw1 = __ldg(src + 1);
-#pragma unroll
-        for (int i = 0; i < 2; ++i) {  // 32 elements per 16-B load, one scale each
-          const uint4 raw = i ? raw1 : raw0;
-          const uint32_t u = i ? (sbytes >> 8) : (sbytes & 0xFFu);
-          const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
-          if (u >= 2u && u <= 252u) {
-            const E2m1Tables tb = e2m1_tables(u);
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {  // 8 codes per word
-              uint32_t o0, o1, o2, o3;
-              e2m1x4_bf16(w4[q] & 0xFFFFu, tb, o0, o1);
-              e2m1x4_bf16(w4[q] >> 16, tb, o2, o3);
-              dst[4 * i + q] = make_uint4(o0, o1, o2, o3);
-            }
-          } else {  // scales at the ends of the ue8m0 range: exact float path
-            const float sc = ue8m0_value(u);
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              uint32_t packed[4];
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const uint32_t byte = (w4[q] >> (8 * e)) & 0xFFu;
-                packed[e] = pack_bf16(e2m1_scaled(byte & 0xFu, sc), e2m1_scaled(byte >> 4, sc));
-              }
-              dst[4 * i + q] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
-            }
-          }
-        }
-      }
-      if (part == 0) sValid[kk] = slot >= 0 ? 1 : 0;
+  // records of one chunk, key = tid (threads 0..63)
+  auto issue_records = [&](int slot, int kind) {
+    sKind[tid] = kind;
+    if (kind == 0) {
+      mbar_arrive(bar_raw);
+    } else {
+      const uint32_t bytes = kind == 1 ? 528u : 288u;
+      const uint8_t* src = (kind == 1 ? p.swa_kv : p.main_kv) + static_cast<long long>(slot) * bytes;
+      mbar_arrive_expect_tx(bar_raw, bytes);
+      bulk_load(sRaw + tid * kRawStride, src, bytes, bar_raw, pol);
     }
-    cp_async_wait_all();
-    __syncthreads();
+  };
+  if (tid < kCK && c0 < c1) issue_records(next_slot, next_kind);
+
+  int it = 0;
+  for (int ch = c0; ch < c1; ++ch, ++it) {
+    // the next chunk's slots load now; its records are issued once this chunk is dequantised
+    if (tid < kCK) {
+      next_slot = -1;
+      next_kind = 0;
+      if (ch + 1 < c1) next_slot = key_slot(p, t, (ch + 1) * kCK + tid, &next_kind);
+    }
+    if (ok) ok = mbar_wait(bar_raw, static_cast<uint32_t>(it & 1), nullptr);
+    if (!ok) set_error(p.err, kErrTimeout);
+    // ---- dequantise: warp w owns keys 4w..4w+3, lane l the 16-B chunks l and l+32 of each
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+      const int key = warp * 4 + kk;
+      const int kind = ok ? sKind[key] : 0;
+      const uint8_t* raw = sRaw + key * kRawStride;
+      uint4* dst = reinterpret_cast<uint4*>(sK + key * kQStride);
+      dst[lane] = dequant_chunk(raw, kind, lane);
+      dst[lane + 32] = dequant_chunk(raw, kind, lane + 32);
+    }
+    const unsigned kmask_lo = __ballot_sync(0xffffffffu, ok && sKind[lane] != 0);
+    const unsigned kmask_hi = __ballot_sync(0xffffffffu, ok && sKind[32 + lane] != 0);
+    __syncthreads();  // sK ready; the staging area and sKind are free again
+    if (tid < kCK && ch + 1 < c1) issue_records(next_slot, next_kind);
+    if (it == 0) {
+      if (ok) ok = mbar_wait(bar_q, 0u, nullptr);
+      if (!ok) set_error(p.err, kErrTimeout);
+    }
 
     // ---- S tile: heads 16hg.., keys 16xg.., all 512 dims
     {
@@ -305,10 +385,11 @@ __global__ void __launch_bounds__(512, 1) sparse_attn_kernel(const __grid_consta
       const int h = tid >> 3, sub = tid & 7;
       float x[8];
       float cmax = -INFINITY;
+      const unsigned km = (sub < 4) ? kmask_lo : kmask_hi;
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const int key = sub * 8 + i;
-        x[i] = sValid[key] ? sS[h * kSStride + key] * p.scale_log2 : -INFINITY;
+        x[i] = ((km >> (key & 31)) & 1u) ? sS[h * kSStride + key] * p.scale_log2 : -INFINITY;
         cmax = fmaxf(cmax, x[i]);
       }
       cmax = fmaxf(cmax, __shfl_xor_sync(0xffffffffu, cmax, 1));
@@ -367,10 +448,13 @@ __global__ void __launch_bounds__(512, 1) sparse_attn_kernel(const __grid_consta
     }
     __syncthreads();
   }
+  if (c0 >= c1 && ok) {  // a CTA without chunks still owns the copies of q
+    ok = mbar_wait(bar_q, 0u, nullptr);
+    if (!ok) set_error(p.err, kErrTimeout);
+  }
 
-  cp_async_wait_all();  // a CTA without chunks still owns in-flight copies of q
-  // ---- epilogue
   const int h0 = 16 * hg + g, h1 = h0 + 8;
+  const long long obase = static_cast<long long>(t) * kH * kD;
   if (p.nsplit == 1) {
     const float s0 = __ldg(p.sink + h0) * kLog2e, s1 = __ldg(p.sink + h1) * kLog2e;
     const float m0 = sM[h0], m1 = sM[h1];
@@ -380,16 +464,15 @@ __global__ void __launch_bounds__(512, 1) sparse_attn_kernel(const __grid_consta
     const float d0 = sL[h0] * w0 + exp2f(s0 - M0);
     const float d1 = sL[h1] * w1 + exp2f(s1 - M1);
     const float f0 = w0 / d0, f1 = w1 / d1;
-    const long long base = static_cast<long long>(t) * kH * kD;
 #pragma unroll
     for (int nt = 0; nt < 16; ++nt) {
       const int d = 128 * xg + nt * 8 + 2 * cq;
       if (p.out_bf16) {
-        __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out) + base;
+        __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out) + obase;
         *reinterpret_cast<__nv_bfloat162*>(out + h0 * kD + d) = __floats2bfloat162_rn(o[nt][0] * f0, o[nt][1] * f0);
         *reinterpret_cast<__nv_bfloat162*>(out + h1 * kD + d) = __floats2bfloat162_rn(o[nt][2] * f1, o[nt][3] * f1);
       } else {
-        float* out = static_cast<float*>(p.out) + base;
+        float* out = static_cast<float*>(p.out) + obase;
         *reinterpret_cast<float2*>(out + h0 * kD + d) = make_float2(o[nt][0] * f0, o[nt][1] * f0);
         *reinterpret_cast<float2*>(out + h1 * kD + d) = make_float2(o[nt][2] * f1, o[nt][3] * f1);
       }
@@ -398,96 +481,123 @@ __global__ void __launch_bounds__(512, 1) sparse_attn_kernel(const __grid_consta
       p.lse[static_cast<long long>(t) * kH + h0] = (M0 + log2f(d0)) * kLn2;
       p.lse[static_cast<long long>(t) * kH + h1] = (M1 + log2f(d1)) * kLn2;
     }
-  } else {
-    const long long ps = static_cast<long long>(t) * p.nsplit + split;
-    float* wo = p.ws_o + ps * kH * kD;
+    return;
+  }
+
+  // ---- merge over the cluster.  Head h belongs to CTA h % ns.  The CTAs
+  // exchange their (max, sum) per head, each scales its O rows by its weight
+  // exp2(max_r - M) / denominator and stores them as bf16, bulk copies push each
+  // 1-KB head row to the owner, and the owner sums its heads' rows.
+  const int ns = p.nsplit;
+  const int rows_pr = recv_rows_per_rank(ns);                 // receive rows per source rank
+  const int my_heads = (kH - static_cast<int>(rank) + ns - 1) / ns;
+  __nv_bfloat16* sendO = reinterpret_cast<__nv_bfloat16*>(sm + AttnSmem::kOffSend);  // [64][kQStride]
+  __nv_bfloat16* recvO = reinterpret_cast<__nv_bfloat16*>(sm + AttnSmem::kOffRecv);  // [ns][rows_pr][512]
+  cluster_sync();  // (max, sum) of every CTA final; q, K and the staging area no longer read
+  float* sF = sA;  // this CTA's weight per head
+  if (tid < kH) {
+    const int h = tid;
+    float mr[kMaxCluster], lr[kMaxCluster];
+#pragma unroll
+    for (int r = 0; r < kMaxCluster; ++r) {
+      mr[r] = -INFINITY;
+      lr[r] = 0.f;
+      if (r < ns) {
+        mr[r] = ld_cluster_f32(map_rank(smem_u32(&sM[h]), r));
+        lr[r] = ld_cluster_f32(map_rank(smem_u32(&sL[h]), r));
+      }
+    }
+    const float sk = __ldg(p.sink + h) * kLog2e;
+    float M = sk;
+#pragma unroll
+    for (int r = 0; r < kMaxCluster; ++r) M = fmaxf(M, mr[r]);
+    float dsum = exp2f(sk - M);
+#pragma unroll
+    for (int r = 0; r < kMaxCluster; ++r)
+      if (mr[r] != -INFINITY) dsum += exp2f(mr[r] - M) * lr[r];
+    const float mine = sM[h];
+    sF[h] = (mine == -INFINITY) ? 0.f : exp2f(mine - M) / dsum;
+    if (p.lse && static_cast<uint32_t>(h % ns) == rank)
+      p.lse[static_cast<long long>(t) * kH + h] = (M + log2f(dsum)) * kLn2;
+  }
+  if (tid == 0) mbar_arrive_expect_tx(bar_recv, static_cast<uint32_t>(ns * my_heads * kD * 2));
+  __syncthreads();
+  {
+    const float f0 = sF[h0], f1 = sF[h1];
 #pragma unroll
     for (int nt = 0; nt < 16; ++nt) {
       const int d = 128 * xg + nt * 8 + 2 * cq;
-      *reinterpret_cast<float2*>(wo + h0 * kD + d) = make_float2(o[nt][0], o[nt][1]);
-      *reinterpret_cast<float2*>(wo + h1 * kD + d) = make_float2(o[nt][2], o[nt][3]);
-    }
-    if (tid < kH) {
-      p.ws_ml[(ps * kH + tid) * 2] = sM[tid];
-      p.ws_ml[(ps * kH + tid) * 2 + 1] = sL[tid];
+      *reinterpret_cast<__nv_bfloat162*>(sendO + h0 * kQStride + d) = __floats2bfloat162_rn(o[nt][0] * f0, o[nt][1] * f0);
+      *reinterpret_cast<__nv_bfloat162*>(sendO + h1 * kQStride + d) = __floats2bfloat162_rn(o[nt][2] * f1, o[nt][3] * f1);
     }
   }
-}
-
-// Merge of the per-split (max, sum, O) of one (row, head): one warp turns the
-// split statistics into normalised weights, then every thread sums its four
-// dims over the splits with independent loads.
-constexpr int kMaxSplits = 32;
-
-__global__ void __launch_bounds__(128) attn_combine_kernel(const __grid_constant__ AttnParams p) {
-  const int t = blockIdx.x, h = blockIdx.y;
-  __shared__ float s_wt[kMaxSplits];
-  pdl_trigger();
-  pdl_wait();
-  const int ns = p.nsplit;
-  const long long base = static_cast<long long>(t) * ns;
-  if (threadIdx.x < 32) {
-    const int s = threadIdx.x;
-    float m = -INFINITY, l = 0.f;
-    if (s < ns) {
-      m = p.ws_ml[((base + s) * kH + h) * 2];
-      l = p.ws_ml[((base + s) * kH + h) * 2 + 1];
-    }
-    const float sk = __ldg(p.sink + h) * kLog2e;
-    float M = fmaxf(m, sk);
+  fence_proxy_async_smem();  // the rows are read next by the bulk-copy engine
+  cluster_sync();            // every send row written, every receive barrier armed
+  if (tid < kH) {
+    const int h = tid;
+    const uint32_t owner = static_cast<uint32_t>(h % ns);
+    const uint32_t dst = map_rank(smem_u32(recvO + (static_cast<int>(rank) * rows_pr + h / ns) * kD), owner);
+    bulk_copy_to_peer(dst, sendO + h * kQStride, kD * 2, map_rank(smem_u32(bar_recv), owner));
+  }
+  if (!mbar_wait(bar_recv, 0u, nullptr)) set_error(p.err, kErrTimeout);
+  {
+    constexpr int kPerHead = kD / 8;  // 8 bf16 per thread and step
+    for (int i = tid; i < my_heads * kPerHead; i += blockDim.x) {
+      const int li = i / kPerHead;
+      const int h = static_cast<int>(rank) + li * ns;
+      const int d = (i % kPerHead) * 8;
+      float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      for (int r = 0; r < ns; ++r) {
+        const uint4 v = *reinterpret_cast<const uint4*>(recvO + (r * rows_pr + li) * kD + d);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-    const float w = (s < ns && m != -INFINITY) ? exp2f(m - M) : 0.f;
-    float den = w * l;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
-    den += exp2f(sk - M);
-    s_wt[s] = w / den;
-    if (s == 0 && p.lse) p.lse[static_cast<long long>(t) * kH + h] = (M + log2f(den)) * kLn2;
+        for (int j = 0; j < 4; ++j) {
+          const float2 f2 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[j]));
+          acc[2 * j] += f2.x;
+          acc[2 * j + 1] += f2.y;
+        }
+      }
+      const long long oo = obase + static_cast<long long>(h) * kD + d;
+      if (p.out_bf16) {
+        *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + oo) =
+            make_uint4(pack_bf16(acc[0], acc[1]), pack_bf16(acc[2], acc[3]), pack_bf16(acc[4], acc[5]),
+                       pack_bf16(acc[6], acc[7]));
+      } else {
+        float4* out = reinterpret_cast<float4*>(static_cast<float*>(p.out) + oo);
+        out[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+        out[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+      }
+    }
   }
-  __syncthreads();
-  const int d = threadIdx.x * 4;
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 8
-  for (int s = 0; s < ns; ++s) {
-    const float w = s_wt[s];
-    const float4 v = *reinterpret_cast<const float4*>(p.ws_o + ((base + s) * kH + h) * kD + d);
-    acc.x = fmaf(w, v.x, acc.x);
-    acc.y = fmaf(w, v.y, acc.y);
-    acc.z = fmaf(w, v.z, acc.z);
-    acc.w = fmaf(w, v.w, acc.w);
-  }
-  const long long o = (static_cast<long long>(t) * kH + h) * kD + d;
-  if (p.out_bf16) {
-    __nv_bfloat162* out = reinterpret_cast<__nv_bfloat162*>(static_cast<__nv_bfloat16*>(p.out) + o);
-    out[0] = __floats2bfloat162_rn(acc.x, acc.y);
-    out[1] = __floats2bfloat162_rn(acc.z, acc.w);
-  } else {
-    *reinterpret_cast<float4*>(static_cast<float*>(p.out) + o) = acc;
-  }
+  cluster_sync();  // no CTA leaves while its rows may still be copied out of its shared memory
 }
 
 }  // namespace
 
+// CTAs per row: one per 64-key chunk while the rows of the launch still fit the
+// SMs with one CTA each, at most 16 (the cluster limit); the chunks are then
+// spread evenly over that many CTAs.
 int attn_num_splits(int T, int n_keys, int num_sms) {
   const int nchunks = (n_keys + kCK - 1) / kCK;
   if (nchunks <= 1) return 1;
-  int s = (2 * num_sms + T - 1) / T;
+  int s = num_sms / (T > 0 ? T : 1);
   if (s < 1) s = 1;
   if (s > nchunks) s = nchunks;
-  if (s > kMaxSplits) s = kMaxSplits;
-  // equalise the chunk count per split
+  if (s > kMaxCluster) s = kMaxCluster;
   const int cps = (nchunks + s - 1) / s;
   return (nchunks + cps - 1) / cps;
 }
 
 size_t attn_workspace_bytes(int T, int nsplit) {
-  if (nsplit <= 1) return 0;
-  return static_cast<size_t>(T) * nsplit * kH * (kD + 2) * sizeof(float) + 256;
+  (void)T;
+  (void)nsplit;
+  return 0;  // the split results are merged on chip
 }
 
 cudaError_t launch_sparse_attn(const AttnLaunch& a, void* ws, size_t ws_bytes, const DeviceCtx& ctx,
                                cudaStream_t st) {
+  (void)ws;
+  (void)ws_bytes;
   AttnParams p;
   p.q = reinterpret_cast<const __nv_bfloat16*>(a.q);
   p.main_kv = a.main_kv;
@@ -510,21 +620,29 @@ cudaError_t launch_sparse_attn(const AttnLaunch& a, void* ws, size_t ws_bytes, c
   const int L = a.n_swa + a.k;
   const int nchunks = (L + kCK - 1) / kCK;
   const int nsplit = attn_num_splits(a.T, L, ctx.num_sms);
-  p.nsplit = nsplit;
-  p.chunks_per_split = nsplit > 1 ? (nchunks + nsplit - 1) / nsplit : (nchunks > 0 ? nchunks : 1);
-  p.ws_o = nullptr;
-  p.ws_ml = nullptr;
-  if (nsplit > 1) {
-    p.ws_o = static_cast<float*>(ws);
-    p.ws_ml = p.ws_o + static_cast<size_t>(a.T) * nsplit * kH * kD;
-  }
   cudaError_t e = prefer_max_smem(sparse_attn_kernel, AttnSmem::kBytes);
   if (e != cudaSuccess) return e;
-  if ((e = prefer_max_smem(attn_combine_kernel, 0)) != cudaSuccess) return e;
-  e = launch_pdl(sparse_attn_kernel, dim3(nsplit, a.T), dim3(512), AttnSmem::kBytes, st, p);
-  if (e != cudaSuccess) return e;
-  if (nsplit > 1) e = launch_pdl(attn_combine_kernel, dim3(a.T, kH), dim3(128), 0, st, p);
-  return e;
+  if (nsplit > 8) {
+    e = cudaFuncSetAttribute(sparse_attn_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return e;
+  }
+  p.nsplit = nsplit;
+  p.chunks_per_split = nsplit > 1 ? (nchunks + nsplit - 1) / nsplit : (nchunks > 0 ? nchunks : 1);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(nsplit, a.T);
+  cfg.blockDim = dim3(512);
+  cfg.dynamicSmemBytes = AttnSmem::kBytes;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = nsplit;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, sparse_attn_kernel, p);
 }
 
 }  // namespace csa2
