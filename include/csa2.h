@@ -132,8 +132,8 @@ typedef struct {
   float* block_max; int64_t ld_block_max;     /* optional [T, ld_block_max] */
   /* optional [2, T, 2048] uint32, decode path only (else must be NULL): receives
    * 2048-bin histograms of the top 11 bits of the order-preserving key of every
-   * visible score (rows 0..T-1) and of every block maximum (rows T..2T-1, the
-   * newest block counted as +inf; zero when block_max is NULL).  Passing it on
+   * finite visible score (rows 0..T-1) and of every finite block maximum (rows
+   * T..2T-1, the newest block counted as +inf; zero when block_max is NULL).  Passing it on
    * to csa2_topk_with_candidates saves that call a pass over the scores. */
   uint32_t* hist;
 } csa2_index_score_args;
@@ -188,7 +188,10 @@ CSA2_API int csa2_topk_with_candidates_noalloc(const csa2_topk_args* args, void*
  * is -inf otherwise (CSA2 page, "Hierarchical Sparse Indexer" item 2: a
  * Reindex layer scores only the pool).  Then the top-k of those scores, as in
  * csa2_topk_with_candidates, reported as positions and slots.
- * pool_scores (optional, [T, 8*pool_n]) receives the candidate scores. */
+ * pool_scores (optional, [T, 8*pool_n]) receives the candidate scores.
+ * Workspace: csa2_workspace_size(CSA2_CALL_REINDEX, args, &bytes): the
+ * candidate scores (unless pool_scores is given) and a T x 2048 key histogram
+ * of them that the scoring kernel builds for the selection. */
 typedef struct {
   const uint8_t* q_fp8; const float* q_scale; const float* w;  /* as in index_score */
   const uint8_t* index_k; int64_t index_k_pages;

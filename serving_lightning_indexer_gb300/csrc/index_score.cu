@@ -339,7 +339,7 @@ __global__ void __launch_bounds__(kThreads, IdxCfg<NQ>::kCtasPerSm)
       const int quad = warp & 3;
       const int r = quad * 32 + lane;  // key row of this thread within the tile
       float* s_wg = s_w + grp * NQ * 32;
-      constexpr bool kHist = (NQ == 1 && MODE == kModeScan);
+      constexpr bool kHist = (NQ == 1);  // decode scan and Reindex gather
       const bool hist_on = kHist && p.hist != nullptr;
       uint32_t* hs = reinterpret_cast<uint32_t*>(smem + Cfg::kOffHist) + grp * Cfg::kHistWords;
       uint32_t* hb = hs + kHistBins;
@@ -350,11 +350,14 @@ __global__ void __launch_bounds__(kThreads, IdxCfg<NQ>::kCtasPerSm)
         uint32_t* gs = p.hist + static_cast<long long>(t) * kHistBins;
         uint32_t* gb = p.hist + (static_cast<long long>(T) + t) * kHistBins;
         for (int i = gtid; i < kHistBins; i += 128) {
-          const uint32_t a = hs[i], c = hb[i];
+          const uint32_t a = hs[i];
           if (a) atomicAdd(gs + i, a);
-          if (c) atomicAdd(gb + i, c);
           hs[i] = 0u;
-          hb[i] = 0u;
+          if (MODE == kModeScan) {
+            const uint32_t c = hb[i];
+            if (c) atomicAdd(gb + i, c);
+            hb[i] = 0u;
+          }
         }
       };
       int qb = find_qb(s_prefix, nqb, g_begin);
@@ -423,7 +426,7 @@ __global__ void __launch_bounds__(kThreads, IdxCfg<NQ>::kCtasPerSm)
           const float sc = valid ? (acc0 + acc1) * ks : -INFINITY;
           if (MODE == kModeScan) {
             if (t < T && pos < p.ld_out) p.out[static_cast<long long>(t) * p.ld_out + pos] = sc;
-            if (hist_on && valid) atomicAdd(&hs[ord_key(sc) >> 21], 1u);
+            if (hist_on && valid && selectable(sc)) atomicAdd(&hs[ord_key(sc) >> 21], 1u);
             if (p.block_max != nullptr) {
               float m = sc;
               m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
@@ -434,11 +437,13 @@ __global__ void __launch_bounds__(kThreads, IdxCfg<NQ>::kCtasPerSm)
               if ((lane & 7) == 0 && t < T && blk < nblk && blk < p.ld_bm) {
                 p.block_max[static_cast<long long>(t) * p.ld_bm + blk] = m;
                 // the newest block is always kept by the pool: it counts as +inf
-                if (hist_on) atomicAdd(&hb[(blk == nblk - 1 ? 0xFFFFFFFFu : ord_key(m)) >> 21], 1u);
+                if (hist_on && (blk == nblk - 1 || selectable(m)))
+                  atomicAdd(&hb[(blk == nblk - 1 ? 0xFFFFFFFFu : ord_key(m)) >> 21], 1u);
               }
             }
           } else {
             if (ci < static_cast<long long>(p.pool_n) * 8) p.out[static_cast<long long>(t) * p.pool_n * 8 + ci] = sc;
+            if (hist_on && valid && selectable(sc)) atomicAdd(&hs[ord_key(sc) >> 21], 1u);
           }
         }
         tc_fence_before();
@@ -502,11 +507,13 @@ cudaError_t launch_variant(const IndexLaunch& a, const DeviceCtx& ctx, cudaStrea
   p.pool_n = a.pool_n;
   p.err = ctx.err;
   if (a.hist) {
-    if (!(NQ == 1 && MODE == kModeScan)) {
-      *why = "score histograms are produced on the decode path only";
+    if (NQ != 1) {
+      *why = "score histograms are produced on the decode and Reindex paths only";
       return cudaErrorInvalidValue;
     }
-    cudaError_t e0 = cudaMemsetAsync(a.hist, 0, static_cast<size_t>(2) * a.rows.T * kHistBins * 4, st);
+    // scan: [2][T][2048] (scores, block maxima); gather: [T][2048] (candidate scores)
+    const size_t words = static_cast<size_t>(MODE == kModeScan ? 2 : 1) * a.rows.T * kHistBins;
+    cudaError_t e0 = cudaMemsetAsync(a.hist, 0, words * 4, st);
     if (e0 != cudaSuccess) return e0;
   }
   const size_t smem = Cfg::smem_bytes(nqb);

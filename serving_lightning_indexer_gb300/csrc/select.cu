@@ -35,6 +35,8 @@ constexpr int kDirect = 16384;   // rows up to this length are selected in share
 constexpr int kChunk = 16384;    // elements per CTA in the streaming passes
 constexpr int kMaxK = 2048;
 constexpr int kStreamThreads = 256;
+constexpr int kFilterPer = 16;                             // elements per thread in the filter pass
+constexpr int kFilterChunk = kStreamThreads * kFilterPer;  // elements per filter CTA
 constexpr int kFinalThreads = 1024;
 
 struct SelParams {
@@ -55,6 +57,7 @@ struct SelParams {
   const int* pool_in;
   int pool_in_n;
   const uint32_t* hist;  // [V][kBins]: given, or built by the hist pass in `hist_ws`
+  int hist_full;         // hist covers every row (given by the caller), not only the long ones
   uint32_t* hist_ws;
   uint32_t* cnt;         // [V]
   uint32_t* cord;        // [V][kCap]
@@ -212,11 +215,32 @@ __global__ void __launch_bounds__(kStreamThreads) sel_filter_kernel(const __grid
   const int v = blockIdx.y;
   const VRow r = vrow_of(P, v);
   if (r.n <= kDirect) return;
-  const int i0 = blockIdx.x * kChunk;
+  const int i0 = blockIdx.x * kFilterChunk;
   if (i0 >= r.n) return;
   __shared__ __align__(16) uint32_t h[kBins];
   __shared__ int res[4];
   __shared__ uint32_t wsum[8];
+  // this thread's kFilterPer consecutive elements, loaded before the histogram
+  // is searched so that the two latencies overlap
+  const int i = i0 + threadIdx.x * kFilterPer;
+  const int i1 = min(i0 + kFilterChunk, r.n);
+  float vals[kFilterPer];
+#pragma unroll
+  for (int q = 0; q < kFilterPer / 4; ++q) {
+    const int e = i + 4 * q;
+    float4 v4 = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+    if (e + 3 < i1) {
+      v4 = *reinterpret_cast<const float4*>(r.src + e);
+    } else if (e < i1) {
+      v4.x = r.src[e];
+      if (e + 1 < i1) v4.y = r.src[e + 1];
+      if (e + 2 < i1) v4.z = r.src[e + 2];
+    }
+    vals[4 * q] = v4.x;
+    vals[4 * q + 1] = v4.y;
+    vals[4 * q + 2] = v4.z;
+    vals[4 * q + 3] = v4.w;
+  }
   stage_hist(h, P.hist + static_cast<long long>(v) * kBins);
   if (threadIdx.x == 0) res[0] = -1;
   __syncthreads();
@@ -224,88 +248,157 @@ __global__ void __launch_bounds__(kStreamThreads) sel_filter_kernel(const __grid
   const int b1 = res[0];
   const uint32_t thr = b1 < 0 ? 0u : static_cast<uint32_t>(b1);
   const int lane = threadIdx.x & 31;
+  uint32_t keys[kFilterPer];
+  uint32_t mine = 0;
+#pragma unroll
+  for (int j = 0; j < kFilterPer; ++j) {
+    const uint32_t key = (i + j < i1) ? elem_key(r, vals[j], i + j) : 0u;
+    keys[j] = (key && (key >> 21) >= thr) ? key : 0u;
+    mine += keys[j] ? 1u : 0u;
+  }
+  const uint32_t incl = warp_incl_scan(mine);
+  const uint32_t wtot = __shfl_sync(0xffffffffu, incl, 31);
+  if (wtot == 0) return;
+  uint32_t wbase = 0;
+  if (lane == 31) wbase = atomicAdd(P.cnt + v, wtot);
+  wbase = __shfl_sync(0xffffffffu, wbase, 31);
+  uint32_t slot = wbase + incl - mine;
   uint32_t* cord = P.cord + static_cast<long long>(v) * kCap;
   uint32_t* cidx = P.cidx + static_cast<long long>(v) * kCap;
-  const int i1 = min(i0 + kChunk, r.n);
-  // loop bounds are uniform across the block so that every lane takes part in the warp scans
-  for (int base = i0; base < i1; base += blockDim.x * 4) {
-    const int i = base + threadIdx.x * 4;
-    float4 v4 = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-    if (i + 3 < i1) {
-      v4 = __ldg(reinterpret_cast<const float4*>(r.src + i));
-    } else if (i < i1) {
-      v4.x = r.src[i];
-      if (i + 1 < i1) v4.y = r.src[i + 1];
-      if (i + 2 < i1) v4.z = r.src[i + 2];
-    }
-    const float vals[4] = {v4.x, v4.y, v4.z, v4.w};
-    uint32_t keys[4];
-    uint32_t mine = 0;
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const uint32_t key = (i + j < i1) ? elem_key(r, vals[j], i + j) : 0u;
-      keys[j] = (key && (key >> 21) >= thr) ? key : 0u;
-      mine += keys[j] ? 1u : 0u;
+  for (int j = 0; j < kFilterPer; ++j) {
+    if (!keys[j]) continue;
+    if (slot < static_cast<uint32_t>(kCap)) {
+      cord[slot] = keys[j];
+      cidx[slot] = static_cast<uint32_t>(i + j);
     }
-    const uint32_t incl = warp_incl_scan(mine);
-    const uint32_t wtot = __shfl_sync(0xffffffffu, incl, 31);
-    if (wtot == 0) continue;
-    uint32_t wbase = 0;
-    if (lane == 31) wbase = atomicAdd(P.cnt + v, wtot);
-    wbase = __shfl_sync(0xffffffffu, wbase, 31);
-    uint32_t slot = wbase + incl - mine;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      if (!keys[j]) continue;
-      if (slot < static_cast<uint32_t>(kCap)) {
-        cord[slot] = keys[j];
-        cidx[slot] = static_cast<uint32_t>(i + j);
-      }
-      ++slot;
-    }
+    ++slot;
   }
 }
 
 // ---------------------------------------------------------------- final select
+constexpr int kPerThread = kDirect / kFinalThreads;  // direct-row values held in registers per thread
+constexpr int kBitmapWords = 2 * kDirect;            // pool-order bitmap (over the candidates): 2^20 blocks
+
 struct FinalSmem {
-  uint32_t* ord;   // [kDirect]
-  uint32_t* idx;   // [kDirect]
-  uint64_t* sel;   // [kMaxK]
-  uint32_t* hist;  // [256]
-  int* res;        // [8]
-  uint32_t* wsum;  // [32]
+  uint32_t* ord;      // [kDirect] candidate keys (score part)
+  uint32_t* idx;      // [kDirect] candidate element indices
+  uint32_t* bitmap;   // [kBitmapWords], over ord and idx once the survivors are collected
+  uint64_t* sel;      // [kMaxK] survivors
+  uint64_t* xchg;     // [kMaxK] second buffer of the merge sort
+  uint32_t* hist;     // [kBins]
+  int* res;           // [8]
+  uint32_t* wsum;     // [32]
+  uint32_t* counters; // [4]: [0] candidates, [1] survivors
 };
+
+__device__ __forceinline__ FinalSmem final_smem(uint8_t* base) {
+  FinalSmem sm;
+  sm.ord = reinterpret_cast<uint32_t*>(base);
+  sm.idx = sm.ord + kDirect;
+  sm.bitmap = sm.ord;
+  sm.sel = reinterpret_cast<uint64_t*>(sm.ord + kBitmapWords);
+  sm.xchg = sm.sel + kMaxK;
+  sm.hist = reinterpret_cast<uint32_t*>(sm.xchg + kMaxK);
+  sm.res = reinterpret_cast<int*>(sm.hist + kBins);
+  sm.wsum = reinterpret_cast<uint32_t*>(sm.res + 8);
+  sm.counters = sm.wsum + 32;
+  return sm;
+}
 
 __device__ __forceinline__ uint64_t key64(uint32_t ord, uint32_t idx) {
   return (static_cast<uint64_t>(ord) << 32) | static_cast<uint64_t>(~idx);
 }
 
-// Exact radix select of the `need` largest 64-bit keys, 8 bits per pass, ending
-// as soon as the remaining need equals a whole digit bin.  GLOBAL: elements are
-// streamed from the row each pass; else they are the n entries of sm.ord/idx.
-template <bool GLOBAL>
-__device__ void radix_select(const VRow& r, const FinalSmem& sm, int n, int need, uint64_t* prefix_out,
-                             int* pbits_out) {
+__device__ __forceinline__ void hist_add(uint32_t* h, bool on, uint32_t bin) {
+  if (on) atomicAdd(h + bin, 1u);
+}
+
+// Block-wide compaction helper: this thread's slot for `take`, the block's
+// takes counted in *counter (a shared word).  Every lane of the warp must call.
+__device__ __forceinline__ uint32_t block_append(bool take, uint32_t* counter) {
+  const int lane = threadIdx.x & 31;
+  const unsigned m = __ballot_sync(0xffffffffu, take);
+  uint32_t b0 = 0;
+  if (m && lane == __ffs(m) - 1) b0 = atomicAdd(counter, __popc(m));
+  b0 = __shfl_sync(0xffffffffu, b0, m ? __ffs(m) - 1 : 0);
+  return b0 + __popc(m & ((1u << lane) - 1u));
+}
+
+// Exclusive block-wide prefix sum of x (every thread calls); *total gets the sum.
+__device__ __forceinline__ uint32_t block_excl_scan(uint32_t x, uint32_t* wsum, uint32_t* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nwarps = blockDim.x >> 5;
+  const uint32_t incl = warp_incl_scan(x);
+  if (lane == 31) wsum[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    const uint32_t w = (lane < nwarps) ? wsum[lane] : 0u;
+    const uint32_t ws = warp_incl_scan(w);
+    __syncwarp();
+    wsum[lane] = ws;
+  }
+  __syncthreads();
+  const uint32_t base = warp ? wsum[warp - 1] : 0u;
+  *total = wsum[nwarps - 1];
+  __syncthreads();  // wsum is reused by the next scan
+  return base + incl - x;
+}
+
+// Radix refinement below a known prefix: the candidates sm.ord/idx[0..n) whose
+// key starts with *prefix (of *pbits bits) are narrowed digit by digit (11, 10,
+// 11, 11, 10 bits: the rest of the score, then ~index) until the threshold
+// digit's bin is needed whole.  On return the keys whose top *pbits bits are
+// >= *prefix are exactly the `need` best plus those above the entry prefix.
+__device__ void radix_refine(const FinalSmem& sm, int n, int need, uint64_t* prefix_io, int* pbits_io) {
+  uint64_t prefix = *prefix_io;
+  int pbits = *pbits_io;
+  const int nr = (n + blockDim.x - 1) / blockDim.x * blockDim.x;
+  while (pbits < 64) {
+    const int width = (pbits == 22 || pbits == 54) ? 10 : 11;
+    const int shift = 64 - pbits - width;
+    for (int i = threadIdx.x; i < kBins; i += blockDim.x) sm.hist[i] = 0;
+    __syncthreads();
+    for (int i = threadIdx.x; i < nr; i += blockDim.x) {
+      bool on = false;
+      uint32_t bin = 0;
+      if (i < n) {
+        const uint64_t kk = key64(sm.ord[i], sm.idx[i]);
+        on = (kk >> (64 - pbits)) == prefix;
+        bin = static_cast<uint32_t>(kk >> shift) & ((1u << width) - 1u);
+      }
+      hist_add(sm.hist, on, bin);
+    }
+    __syncthreads();
+    block_find_bin(sm.hist, static_cast<uint32_t>(need), sm.res, sm.wsum);
+    const int d = sm.res[0];
+    const int above = sm.res[1];
+    const int cnt = static_cast<int>(sm.hist[d]);
+    __syncthreads();  // res and hist are rewritten by the next digit
+    need -= above;
+    prefix = (prefix << width) | static_cast<uint32_t>(d);
+    pbits += width;
+    if (cnt == need) break;
+  }
+  *prefix_io = prefix;
+  *pbits_io = pbits;
+}
+
+// Exact radix select streaming the row from global memory each pass (rows
+// whose candidate list overflowed), 8-bit digits of the 64-bit keys.
+__device__ void radix_select_stream(const VRow& r, const FinalSmem& sm, int need, uint64_t* prefix_out,
+                                    int* pbits_out) {
   uint64_t prefix = 0;
   int pbits = 0;
   const int lane = threadIdx.x & 31;
-  const int nloop = GLOBAL ? r.n : n;
   for (int pass = 0; pass < 8; ++pass) {
     const int shift = 56 - 8 * pass;
     for (int i = threadIdx.x; i < 256; i += blockDim.x) sm.hist[i] = 0;
     __syncthreads();
-    for (int i = threadIdx.x; i < nloop; i += blockDim.x) {
-      uint64_t kk;
-      bool valid;
-      if (GLOBAL) {
-        const uint32_t o = elem_key(r, r.src[i], i);
-        valid = o != 0u;
-        kk = key64(o, static_cast<uint32_t>(i));
-      } else {
-        valid = true;
-        kk = key64(sm.ord[i], sm.idx[i]);
-      }
-      if (valid && (pbits == 0 || (kk >> (64 - pbits)) == prefix))
+    for (int i = threadIdx.x; i < r.n; i += blockDim.x) {
+      const uint32_t o = elem_key(r, r.src[i], i);
+      const uint64_t kk = key64(o, static_cast<uint32_t>(i));
+      if (o != 0u && (pbits == 0 || (kk >> (64 - pbits)) == prefix))
         atomicAdd(&sm.hist[static_cast<uint32_t>((kk >> shift) & 0xFFu)], 1u);
     }
     __syncthreads();
@@ -347,145 +440,291 @@ __device__ void radix_select(const VRow& r, const FinalSmem& sm, int n, int need
   *pbits_out = pbits;
 }
 
-__device__ __forceinline__ void bitonic_sort(uint64_t* a, int P, bool descending) {
-  for (int size = 2; size <= P; size <<= 1) {
-    for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      for (int i = threadIdx.x; i < P / 2; i += blockDim.x) {
-        const int lo = 2 * i - (i & (stride - 1));
-        const int hi = lo + stride;
-        const bool up = ((lo & size) == 0) != descending;
-        const uint64_t x = a[lo], y = a[hi];
-        if ((x > y) == up) {
-          a[lo] = y;
-          a[hi] = x;
-        }
+// Descending sort of sel[0..got), got <= kMaxK: warps sort runs of 32 keys with
+// shuffles, then runs are merged pairwise, each key placed by a binary search in
+// the partner run (ties keep the left run first, so equal padding keys stay a
+// permutation).  The result is back in sel.
+__device__ void sort_desc(const FinalSmem& sm, int got) {
+  int P2 = 32, lgP = 5;
+  while (P2 < got) {
+    P2 <<= 1;
+    ++lgP;
+  }
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int nwarps = blockDim.x >> 5;
+  uint64_t* A = sm.sel;
+  uint64_t* B = sm.xchg;
+  for (int run = warp; run < (P2 >> 5); run += nwarps) {
+    const int e = (run << 5) + lane;
+    uint64_t x = e < got ? A[e] : 0ull;
+#pragma unroll
+    for (int size = 2; size <= 32; size <<= 1) {
+#pragma unroll
+      for (int stride = size >> 1; stride > 0; stride >>= 1) {
+        const uint64_t y = __shfl_xor_sync(0xffffffffu, x, stride);
+        const bool lower = (lane & stride) == 0;
+        const bool asc = (lane & size) != 0;
+        x = (lower == asc) ? (x < y ? x : y) : (x > y ? x : y);
       }
-      __syncthreads();
     }
+    A[e] = x;
+  }
+  __syncthreads();
+  for (int lg = 5; lg < lgP; ++lg) {
+    const int L = 1 << lg;
+    for (int i = tid; i < P2; i += blockDim.x) {
+      const uint64_t key = A[i];
+      const int run = i >> lg, off = i & (L - 1);
+      const bool left = (run & 1) == 0;
+      const uint64_t* pr = A + ((run ^ 1) << lg);
+      // number of partner keys placed before this one: a prefix of the run
+      int pos = 0;
+      for (int step = L >> 1; step > 0; step >>= 1) {
+        const uint64_t m = pr[pos + step - 1];
+        if (left ? (m > key) : (m >= key)) pos += step;
+      }
+      {
+        const uint64_t m = pr[pos];
+        if (left ? (m > key) : (m >= key)) ++pos;
+      }
+      B[((run & ~1) << lg) + off + pos] = key;
+    }
+    __syncthreads();
+    uint64_t* t = A;
+    A = B;
+    B = t;
+  }
+  if (A != sm.sel) {
+    for (int i = tid; i < got; i += blockDim.x) sm.sel[i] = A[i];
+    __syncthreads();
   }
 }
 
-// Block-wide compaction helper: this thread's slot for `take`, the block's
-// takes counted in *counter (a shared word).  Every lane of the warp must call.
-__device__ __forceinline__ uint32_t block_append(bool take, uint32_t* counter) {
-  const int lane = threadIdx.x & 31;
-  const unsigned m = __ballot_sync(0xffffffffu, take);
-  uint32_t b0 = 0;
-  if (m && lane == __ffs(m) - 1) b0 = atomicAdd(counter, __popc(m));
-  b0 = __shfl_sync(0xffffffffu, b0, m ? __ffs(m) - 1 : 0);
-  return b0 + __popc(m & ((1u << lane) - 1u));
+// Pool output in ascending block order: the survivors' block ids set bits of a
+// bitmap; a block-wide prefix count of the bits gives each id its position.
+__device__ void pool_order_bitmap(const FinalSmem& sm, int got, int nblocks, int* out, int pool_n) {
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  const int nw = (nblocks + 31) / 32;
+  for (int i = t; i < nw; i += blockDim.x) sm.bitmap[i] = 0u;
+  __syncthreads();
+  for (int i = t; i < got; i += blockDim.x) {
+    const uint32_t id = static_cast<uint32_t>(sm.sel[i]);
+    atomicOr(&sm.bitmap[id >> 5], 1u << (id & 31u));
+  }
+  __syncthreads();
+  const int per = (nw + blockDim.x - 1) / blockDim.x;
+  const int w0 = min(t * per, nw), w1 = min(w0 + per, nw);
+  uint32_t cnt = 0;
+  for (int w = w0; w < w1; ++w) cnt += __popc(sm.bitmap[w]);
+  const uint32_t incl = warp_incl_scan(cnt);
+  if (lane == 31) sm.wsum[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    const uint32_t x = (lane < static_cast<int>(blockDim.x >> 5)) ? sm.wsum[lane] : 0u;
+    const uint32_t xs = warp_incl_scan(x);
+    __syncwarp();
+    sm.wsum[lane] = xs;
+  }
+  __syncthreads();
+  uint32_t rank = incl - cnt + (warp ? sm.wsum[warp - 1] : 0u);
+  for (int w = w0; w < w1; ++w) {
+    uint32_t bits = sm.bitmap[w];
+    while (bits) {
+      const int b = __ffs(bits) - 1;
+      bits &= bits - 1u;
+      if (rank < static_cast<uint32_t>(pool_n)) out[rank] = w * 32 + b;
+      ++rank;
+    }
+  }
+  for (int i = got + t; i < pool_n; i += blockDim.x) out[i] = -1;
 }
 
 __global__ void __launch_bounds__(kFinalThreads, 1) sel_final_kernel(const __grid_constant__ SelParams P) {
   extern __shared__ __align__(16) uint8_t fsm_raw[];
-  FinalSmem sm;
-  sm.ord = reinterpret_cast<uint32_t*>(fsm_raw);
-  sm.idx = sm.ord + kDirect;
-  sm.sel = reinterpret_cast<uint64_t*>(sm.idx + kDirect);
-  sm.hist = reinterpret_cast<uint32_t*>(sm.sel + kMaxK);
-  sm.res = reinterpret_cast<int*>(sm.hist + 256);
-  sm.wsum = reinterpret_cast<uint32_t*>(sm.res + 8);
-  uint32_t* counters = sm.wsum + 32;  // [0]: gathered, [1]: selected
+  const FinalSmem sm = final_smem(fsm_raw);
   pdl_trigger();
   pdl_wait();
   const int v = blockIdx.x;
   const VRow r = vrow_of(P, v);
-  if (threadIdx.x < 2) counters[threadIdx.x] = 0;
+  const int tid = threadIdx.x;
+  if (tid < 4) sm.counters[tid] = 0;
+
+  // 1. the 2048-bin histogram of the top 11 key bits: the caller's (scan or
+  //    gather epilogue) or the hist pass's, else built here from the values of
+  //    a short row (kept in registers)
+  int mode;  // 0: short row, 1: candidate list, 2: overflowed candidate list (stream the row)
+  uint32_t c = 0;
+  uint32_t ord[kPerThread];
+  const int nj = (r.n + kFinalThreads - 1) / kFinalThreads;
+  if (r.n <= kDirect) {
+    mode = 0;
+    float val[kPerThread];
+#pragma unroll
+    for (int j = 0; j < kPerThread; ++j) {
+      const int i = j * kFinalThreads + tid;
+      val[j] = (i < r.n) ? r.src[i] : -INFINITY;
+    }
+    if (P.hist_full) {
+      stage_hist(sm.hist, P.hist + static_cast<long long>(v) * kBins);
+    } else {
+      for (int i = tid; i < kBins; i += blockDim.x) sm.hist[i] = 0;
+    }
+#pragma unroll
+    for (int j = 0; j < kPerThread; ++j) {
+      const int i = j * kFinalThreads + tid;
+      ord[j] = (i < r.n) ? elem_key(r, val[j], i) : 0u;
+    }
+    if (!P.hist_full) {
+      __syncthreads();
+#pragma unroll
+      for (int j = 0; j < kPerThread; ++j)
+        if (j < nj) hist_add(sm.hist, ord[j] != 0u, ord[j] >> 21);
+    }
+  } else {
+    c = P.cnt[v];
+    mode = (c <= static_cast<uint32_t>(kCap)) ? 1 : 2;
+    stage_hist(sm.hist, P.hist + static_cast<long long>(v) * kBins);
+#pragma unroll
+    for (int j = 0; j < kPerThread; ++j) ord[j] = 0u;
+  }
+  __syncthreads();
+  block_find_bin(sm.hist, static_cast<uint32_t>(r.k), sm.res, sm.wsum);
+  const int b1 = sm.res[0];
+  const int above1 = sm.res[1];
+  const int total = sm.res[2];
+  const int cnt1 = b1 >= 0 ? static_cast<int>(sm.hist[b1]) : 0;
+  const uint32_t thr = b1 >= 0 ? static_cast<uint32_t>(b1) : 0u;
+  const bool take_all = total <= r.k;
   __syncthreads();
 
-  // 1. gather the candidates into shared memory, or decide to stream the row
-  int mode = 0;  // 0: shared memory, 1: stream the row from global memory
+  // 2. the candidates in shared memory: keys whose top 11 bits reach the threshold bin
   int n = 0;
-  if (r.n <= kDirect) {
-    const int nr = (r.n + blockDim.x - 1) / blockDim.x * blockDim.x;
-    for (int i = threadIdx.x; i < nr; i += blockDim.x) {
-      const uint32_t key = (i < r.n) ? elem_key(r, r.src[i], i) : 0u;
-      const uint32_t slot = block_append(key != 0u, &counters[0]);
-      if (key) {
-        sm.ord[slot] = key;
-        sm.idx[slot] = static_cast<uint32_t>(i);
+  if (mode == 0) {
+    uint32_t tmask = 0, mine = 0;
+#pragma unroll
+    for (int j = 0; j < kPerThread; ++j) {
+      if (j < nj && ord[j] != 0u && (ord[j] >> 21) >= thr) {
+        tmask |= 1u << j;
+        ++mine;
       }
     }
+    uint32_t total_c;
+    uint32_t slot = block_excl_scan(mine, sm.wsum, &total_c);
+#pragma unroll
+    for (int j = 0; j < kPerThread; ++j) {
+      if ((tmask >> j) & 1u) {
+        sm.ord[slot] = ord[j];
+        sm.idx[slot] = static_cast<uint32_t>(j * kFinalThreads + tid);
+        ++slot;
+      }
+    }
+    n = static_cast<int>(total_c);
     __syncthreads();
-    n = static_cast<int>(counters[0]);
-  } else {
-    const uint32_t c = P.cnt[v];
-    if (c <= static_cast<uint32_t>(kCap)) {
-      const uint32_t* cord = P.cord + static_cast<long long>(v) * kCap;
-      const uint32_t* cidx = P.cidx + static_cast<long long>(v) * kCap;
-      for (int i = threadIdx.x; i < static_cast<int>(c); i += blockDim.x) {
-        sm.ord[i] = cord[i];
-        sm.idx[i] = cidx[i];
+  } else if (mode == 1) {
+    const uint32_t* cord = P.cord + static_cast<long long>(v) * kCap;
+    const uint32_t* cidx = P.cidx + static_cast<long long>(v) * kCap;
+    for (int i0 = 0; i0 < static_cast<int>(c); i0 += 4 * kFinalThreads) {
+      uint32_t o4[4], x4[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int i = i0 + u * kFinalThreads + tid;
+        o4[u] = (i < static_cast<int>(c)) ? cord[i] : 0u;
+        x4[u] = (i < static_cast<int>(c)) ? cidx[i] : 0u;
       }
-      n = static_cast<int>(c);
-    } else {  // overflow: count the selectable elements from the histogram
-      stage_hist(sm.ord, P.hist + static_cast<long long>(v) * kBins);
-      __syncthreads();
-      block_find_bin(sm.ord, 1u, sm.res, sm.wsum);
-      n = sm.res[2];
-      mode = 1;
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int i = i0 + u * kFinalThreads + tid;
+        if (i < static_cast<int>(c)) {
+          sm.ord[i] = o4[u];
+          sm.idx[i] = x4[u];
+        }
+      }
     }
+    n = static_cast<int>(c);
     __syncthreads();
   }
-  const int need = min(r.k, n);
 
-  // 2. exact threshold over 64-bit keys, 3. collect exactly `need` survivors
-  uint64_t prefix = 0;
-  int pbits = 0;
-  const bool take_all = (need == n);
+  // 3. the exact threshold over the 64-bit keys
+  uint64_t prefix = thr;
+  int pbits = 11;
   if (!take_all) {
-    if (mode == 0) radix_select<false>(r, sm, n, need, &prefix, &pbits);
-    else radix_select<true>(r, sm, n, need, &prefix, &pbits);
+    if (mode == 2) {
+      radix_select_stream(r, sm, r.k, &prefix, &pbits);
+    } else if (cnt1 != r.k - above1) {
+      radix_refine(sm, n, r.k - above1, &prefix, &pbits);
+    }
   }
-  const int nloop = (mode == 0) ? n : r.n;
-  const int nr = (nloop + blockDim.x - 1) / blockDim.x * blockDim.x;
-  for (int i = threadIdx.x; i < nr; i += blockDim.x) {
-    uint64_t kk = 0;
-    bool valid = false;
-    if (i < nloop) {
-      if (mode == 0) {
-        valid = true;
-        kk = key64(sm.ord[i], sm.idx[i]);
-      } else {
+
+  // 4. collect the survivors (exactly min(k, selectable) of them)
+  const bool bitmap = r.pool && r.n <= kBitmapWords * 32;
+  if (mode != 2) {
+    const int nper = (n + blockDim.x - 1) / blockDim.x;  // <= kPerThread
+    uint32_t tmask = 0, mine = 0;
+    for (int j = 0; j < nper; ++j) {
+      const int i = j * blockDim.x + tid;
+      if (i < n && (take_all || (key64(sm.ord[i], sm.idx[i]) >> (64 - pbits)) >= prefix)) {
+        tmask |= 1u << j;
+        ++mine;
+      }
+    }
+    uint32_t total_s;
+    uint32_t slot = block_excl_scan(mine, sm.wsum, &total_s);
+    for (int j = 0; j < nper; ++j) {
+      if ((tmask >> j) & 1u) {
+        const int i = j * blockDim.x + tid;
+        const uint32_t id = sm.idx[i];
+        if (slot < static_cast<uint32_t>(kMaxK))
+          sm.sel[slot] = r.pool ? static_cast<uint64_t>(bitmap ? id : ~id) : key64(sm.ord[i], id);
+        ++slot;
+      }
+    }
+    if (tid == 0) sm.counters[1] = total_s;
+  } else {
+    const int nr = (r.n + blockDim.x - 1) / blockDim.x * blockDim.x;
+    for (int i = tid; i < nr; i += blockDim.x) {
+      uint64_t kk = 0;
+      bool valid = false;
+      if (i < r.n) {
         const uint32_t o = elem_key(r, r.src[i], i);
         valid = o != 0u;
         kk = key64(o, static_cast<uint32_t>(i));
       }
+      const bool take = valid && (take_all || (kk >> (64 - pbits)) >= prefix);
+      const uint32_t slot = block_append(take, &sm.counters[1]);
+      const uint32_t id = static_cast<uint32_t>(i);
+      if (take && slot < static_cast<uint32_t>(kMaxK))
+        sm.sel[slot] = r.pool ? static_cast<uint64_t>(bitmap ? id : ~id) : kk;
     }
-    const bool take = valid && (take_all || (kk >> (64 - pbits)) >= prefix);
-    const uint32_t slot = block_append(take, &counters[1]);
-    // pools sort by block id ascending, positions by key descending
-    if (take && slot < static_cast<uint32_t>(kMaxK)) sm.sel[slot] = r.pool ? static_cast<uint64_t>(~kk & 0xFFFFFFFFull) : kk;
   }
   __syncthreads();
-  const int got = min(static_cast<int>(counters[1]), kMaxK);
+  const int got = min(static_cast<int>(sm.counters[1]), kMaxK);
 
-  // 4. sort the survivors
-  int Pw = 1;
-  while (Pw < got) Pw <<= 1;
-  for (int i = got + threadIdx.x; i < Pw; i += blockDim.x) sm.sel[i] = r.pool ? ~0ull : 0ull;
-  __syncthreads();
-  bitonic_sort(sm.sel, Pw, !r.pool);
-
-  // 5. outputs
+  // 5. order and write: pools by block id ascending, positions by key descending
   const int t = r.t;
   const int b = row_seq_of(P.rows, t);
   if (r.pool) {
     int* out = P.pool_out + static_cast<long long>(t) * P.pool_n;
-    for (int i = threadIdx.x; i < P.pool_n; i += blockDim.x) out[i] = (i < got) ? static_cast<int>(sm.sel[i]) : -1;
+    if (bitmap) {
+      pool_order_bitmap(sm, got, r.n, out, P.pool_n);
+    } else {  // ~id descending is id ascending
+      sort_desc(sm, got);
+      for (int i = tid; i < P.pool_n; i += blockDim.x)
+        out[i] = (i < got) ? static_cast<int>(~static_cast<uint32_t>(sm.sel[i])) : -1;
+    }
     return;
   }
+  sort_desc(sm, got);
   int* opos = P.topk_pos + static_cast<long long>(t) * P.ld_topk;
   int* oslot = P.topk_slot ? P.topk_slot + static_cast<long long>(t) * P.ld_topk : nullptr;
-  for (int i = threadIdx.x; i < r.k; i += blockDim.x) {
+  for (int i = tid; i < r.k; i += blockDim.x) {
     int pos = -1;
     if (i < got) {
-      const uint32_t idx = ~static_cast<uint32_t>(sm.sel[i] & 0xFFFFFFFFull);
+      const uint32_t id = ~static_cast<uint32_t>(sm.sel[i] & 0xFFFFFFFFull);
       if (P.kind == 2) {
-        const int blk = P.pool_in[static_cast<long long>(t) * P.pool_in_n + (idx >> 3)];
-        pos = blk * 8 + static_cast<int>(idx & 7);
+        const int blk = P.pool_in[static_cast<long long>(t) * P.pool_in_n + (id >> 3)];
+        pos = blk * 8 + static_cast<int>(id & 7);
       } else {
-        pos = static_cast<int>(idx);
+        pos = static_cast<int>(id);
       }
     }
     opos[i] = pos;
@@ -503,7 +742,7 @@ __global__ void __launch_bounds__(kFinalThreads, 1) sel_final_kernel(const __gri
 }
 
 size_t final_smem_bytes() {
-  return static_cast<size_t>(kDirect) * 8 + kMaxK * 8 + 256 * 4 + 8 * 4 + 64 * 4;
+  return static_cast<size_t>(kBitmapWords) * 4 + 2 * kMaxK * 8 + kBins * 4 + 8 * 4 + 32 * 4 + 4 * 4;
 }
 
 }  // namespace
@@ -537,6 +776,7 @@ cudaError_t launch_select(const SelectLaunch& a, void* ws, size_t ws_bytes, cons
   P.err = ctx.err;
   const int V = a.rows.T * ((a.kind == 0 && a.pool_out) ? 2 : 1);
   P.hist = a.hist;
+  P.hist_full = a.hist != nullptr;
   P.hist_ws = nullptr;
   P.cnt = nullptr;
   P.cord = P.cidx = nullptr;
@@ -562,10 +802,11 @@ cudaError_t launch_select(const SelectLaunch& a, void* ws, size_t ws_bytes, cons
     e = cudaMemsetAsync(a.hist ? static_cast<void*>(P.cnt) : ws, 0, zero_bytes, st);
     if (e != cudaSuccess) return e;
     const dim3 grid(static_cast<unsigned>((maxn + kChunk - 1) / kChunk), static_cast<unsigned>(V));
+    const dim3 fgrid(static_cast<unsigned>((maxn + kFilterChunk - 1) / kFilterChunk), static_cast<unsigned>(V));
     if ((e = prefer_max_smem(sel_hist_kernel, 0)) != cudaSuccess) return e;
     if ((e = prefer_max_smem(sel_filter_kernel, 0)) != cudaSuccess) return e;
     if (!a.hist && (e = launch_pdl(sel_hist_kernel, grid, dim3(kStreamThreads), 0, st, P)) != cudaSuccess) return e;
-    if ((e = launch_pdl(sel_filter_kernel, grid, dim3(kStreamThreads), 0, st, P)) != cudaSuccess) return e;
+    if ((e = launch_pdl(sel_filter_kernel, fgrid, dim3(kStreamThreads), 0, st, P)) != cudaSuccess) return e;
   }
   const size_t smem = final_smem_bytes();
   e = prefer_max_smem(sel_final_kernel, smem);
