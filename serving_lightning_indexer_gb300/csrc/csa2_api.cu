@@ -342,8 +342,7 @@ int csa2_sparse_attn(const csa2_sparse_attn_args* a, void* ws, size_t ws_bytes, 
   DeviceCtx ctx;
   cudaError_t e = csa2::device_ctx(&ctx);
   if (e != cudaSuccess) return cuda_fail(e, "csa2_sparse_attn: device");
-  const int nsplit = csa2::attn_num_splits(a->T, a->n_swa + a->k, ctx.num_sms);
-  const size_t need = csa2::attn_workspace_bytes(a->T, nsplit);
+  const size_t need = csa2::attn_workspace_bytes(a->T, a->n_swa + a->k, ctx.num_sms);
   if (need && (!ws || ws_bytes < need)) return fail(CSA2_ERR_WORKSPACE, "csa2_sparse_attn: workspace of %zu bytes needed", need);
   if (need && !aligned16(ws)) return fail(CSA2_ERR_ALIGN, "csa2_sparse_attn: workspace must be 16-B aligned");
   csa2::AttnLaunch L{};
@@ -430,7 +429,7 @@ int csa2_workspace_size(int which, const void* args, size_t* bytes) {
       DeviceCtx ctx;
       cudaError_t e = csa2::device_ctx(&ctx);
       if (e != cudaSuccess) return cuda_fail(e, "csa2_workspace_size: device");
-      *bytes = csa2::attn_workspace_bytes(a->T, csa2::attn_num_splits(a->T, a->n_swa + a->k, ctx.num_sms));
+      *bytes = csa2::attn_workspace_bytes(a->T, a->n_swa + a->k, ctx.num_sms);
       return CSA2_OK;
     }
     default:

@@ -112,7 +112,7 @@ struct AttnLaunch {
   float* lse;
 };
 int attn_num_splits(int T, int n_keys, int num_sms);
-size_t attn_workspace_bytes(int T, int nsplit);
+size_t attn_workspace_bytes(int T, int n_keys, int num_sms);
 cudaError_t launch_sparse_attn(const AttnLaunch& a, void* ws, size_t ws_bytes, const DeviceCtx& ctx,
                                cudaStream_t st);
 

@@ -130,9 +130,6 @@ __device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst, const void* src,
                "r"(smem_u32(src)), "r"(bytes), "r"(mbar)
                : "memory");
 }
-__device__ __forceinline__ void fence_proxy_async_smem() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
 __device__ __forceinline__ float4 ld_cluster_f32x4(uint32_t addr) {
   float4 v;
   asm volatile("ld.shared::cluster.v4.f32 {%0,%1,%2,%3}, [%4];"
@@ -572,6 +569,438 @@ __global__ void __launch_bounds__(512, 1) sparse_attn_kernel(const __grid_consta
   cluster_sync();  // no CTA leaves while its rows may still be copied out of its shared memory
 }
 
+
+// ================================================================ tensor-core path
+// One CTA per 64-key chunk of a row; the row's CTAs form a cluster.  Per CTA:
+//   * the row's q (64 heads x 512, bf16) and the chunk's records are staged in
+//     shared memory; the records are dequantised to bf16 key rows.  Both tiles
+//     use the 128-byte swizzled layout of the tensor cores: 8 atoms of 64
+//     dims, each [64 rows x 128 B], rows of an atom 1024 B per group of 8.
+//   * S = q K^T on tcgen05 (M = 128: heads 0-63, rows 64-127 read the next 8 KB
+//     of shared memory and are discarded; N = 64 keys; K = 512) into TMEM.
+//   * one thread per head reads its S row, masks absent keys, and forms
+//     P = exp2(S*scale - max) (bf16, swizzled) with its max and sum.
+//   * O = P V on tcgen05 (M = 128 as above, N = 256 dims twice, K = 64 keys; V
+//     is the key tile read MN-major) into TMEM.
+//   * O / sum is written as bf16 to a per-row scratch in global memory with
+//     (max, sum); after a cluster barrier the CTA of rank r combines the heads
+//     h = r (mod CTAs) over the row's chunks with the sink and writes them.
+struct TcSmem {
+  static constexpr int kAtom = 8192;                            // 64 rows x 128 B
+  static constexpr int kOffQ = 0;                               // 8 atoms
+  static constexpr int kOffK = kOffQ + 8 * kAtom;               // 8 atoms
+  static constexpr int kOffP = kOffK + 8 * kAtom;               // 1 atom
+  static constexpr int kOffRaw = kOffP + kAtom;                 // [64][kRawStride]
+  static constexpr int kOffKind = kOffRaw + kCK * kRawStride;   // int[64]
+  static constexpr int kOffStat = kOffKind + kCK * 4;           // float m[64], l[64]
+  static constexpr int kOffW = kOffStat + 2 * kH * 4;           // float [ceil(64/ns)][16] combine weights
+  static constexpr int kOffBar = kOffW + 64 * 16 * 4;           // raw, S done, O halves done
+  static constexpr int kOffTmem = kOffBar + 4 * 8;
+  static constexpr int kBytes = kOffTmem + 8;
+  static constexpr int kAlloc = kBytes + 1024;                  // the base is rounded up to 1024 B
+  // the MMAs read 64 rows past the q tile and past the P tile
+  static_assert(kOffK == kOffQ + 8 * kAtom && kOffRaw >= kOffP + kAtom + 0, "operand padding rows stay in bounds");
+  static_assert(kCK * kRawStride >= kAtom, "rows past P stay inside the staging area");
+};
+constexpr int kTcThreads = 512;
+constexpr int kStageStride = kD * 2 + 16;  // bytes per staged O row (conflict-free 16-B stores)
+constexpr uint32_t kTmemCols = 512;  // O: 2 x 256 columns; S (64 columns) shares the second half
+
+struct TcParams {
+  const __nv_bfloat16* q;
+  const uint8_t* main_kv;
+  long long main_slots;
+  const int* topk_slot;
+  int k;
+  long long ld_topk;
+  const uint8_t* swa_kv;
+  long long swa_slots;
+  const int* swa_slot;
+  int n_swa;
+  long long ld_swa;
+  const float* sink;
+  float scale_log2;
+  int T;          // rows of this launch
+  int t_base;     // first row
+  int out_bf16;
+  void* out;
+  float* lse;
+  int nsplit;     // CTAs (64-key chunks) per row = cluster size
+  __nv_bfloat16* part;  // [T][nsplit][64][512] O / sum of each chunk
+  float2* stat;         // [T][nsplit][64] (max, sum), log2 units
+  uint32_t* err;
+};
+
+__device__ __forceinline__ int key_slot_tc(const TcParams& p, int t, int j, int* kind) {
+  int slot = -1;
+  *kind = 0;
+  if (j < p.n_swa) {
+    slot = __ldg(p.swa_slot + static_cast<long long>(t) * p.ld_swa + j);
+    if (slot >= p.swa_slots) {
+      set_error(p.err, kErrBounds);
+      slot = -1;
+    }
+    if (slot >= 0) *kind = 1;
+  } else if (j < p.n_swa + p.k) {
+    slot = __ldg(p.topk_slot + static_cast<long long>(t) * p.ld_topk + (j - p.n_swa));
+    if (slot >= p.main_slots) {
+      set_error(p.err, kErrBounds);
+      slot = -1;
+    }
+    if (slot >= 0) *kind = 2;
+  }
+  return slot;
+}
+
+// 32 dims (block b) of one staged record -> 32 bf16 in o[0..3] (8 each).
+__device__ __forceinline__ void dequant_block32(const uint8_t* raw, int kind, int b, uint4 (&o)[4]) {
+  if (kind == 2) {  // main KV: e2m1 codes, one ue8m0 scale per 32 dims
+    const uint4 w = *reinterpret_cast<const uint4*>(raw + 16 * b);
+    const uint32_t u = raw[256 + b];
+    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+    if (u >= 2u && u <= 252u) {
+      const E2m1Tables tb = e2m1_tables(u);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        e2m1x4_bf16(ws[j] & 0xFFFFu, tb, o[j].x, o[j].y);
+        e2m1x4_bf16(ws[j] >> 16, tb, o[j].z, o[j].w);
+      }
+    } else {
+      const float sc = ue8m0_value(u);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        uint32_t pk[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const uint32_t byte = (ws[j] >> (8 * e)) & 0xFFu;
+          pk[e] = pack_bf16(e2m1_scaled(byte & 0xFu, sc), e2m1_scaled(byte >> 4, sc));
+        }
+        o[j] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+      }
+    }
+  } else if (kind == 1) {  // SWA: e4m3 codes, one fp32 scale per 128 dims
+    const uint4 w0 = *reinterpret_cast<const uint4*>(raw + 32 * b);
+    const uint4 w1 = *reinterpret_cast<const uint4*>(raw + 32 * b + 16);
+    const float sc = *reinterpret_cast<const float*>(raw + 512 + (b >> 2) * 4);
+    const uint32_t ws[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+    uint32_t pk[16];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const float2 a = e4m3x2_to_float2(ws[j] & 0xFFFFu), c = e4m3x2_to_float2(ws[j] >> 16);
+      pk[2 * j] = pack_bf16(a.x * sc, a.y * sc);
+      pk[2 * j + 1] = pack_bf16(c.x * sc, c.y * sc);
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) o[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+  } else {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) o[j] = make_uint4(0u, 0u, 0u, 0u);
+  }
+}
+
+// Loads through L2 only (data written earlier in this grid by other CTAs, or
+// by the previous kernel); not volatile, so independent loads can be batched.
+__device__ __forceinline__ uint4 ld_cg_v4(const void* p) {
+  uint4 v;
+  asm("ld.global.cg.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+  return v;
+}
+__device__ __forceinline__ float2 ld_cg_f2(const float2* p) {
+  float2 v;
+  asm("ld.global.cg.v2.f32 {%0,%1}, [%2];" : "=f"(v.x), "=f"(v.y) : "l"(p));
+  return v;
+}
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+// Bulk copy shared -> global, tracked by this thread's bulk async-group.
+__device__ __forceinline__ void bulk_store(void* gdst, const void* ssrc, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst), "r"(smem_u32(ssrc)),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_store_commit_wait() {
+  asm volatile("cp.async.bulk.commit_group;\n\tcp.async.bulk.wait_group 0;" ::: "memory");
+}
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+__global__ void __launch_bounds__(kTcThreads, 1) sparse_attn_tc_kernel(const __grid_constant__ TcParams p) {
+  extern __shared__ uint8_t tc_smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(tc_smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sQ = sm + TcSmem::kOffQ;
+  uint8_t* sK = sm + TcSmem::kOffK;
+  uint8_t* sP = sm + TcSmem::kOffP;
+  uint8_t* sRaw = sm + TcSmem::kOffRaw;
+  int* sKind = reinterpret_cast<int*>(sm + TcSmem::kOffKind);
+  float* sM = reinterpret_cast<float*>(sm + TcSmem::kOffStat);
+  float* sL = sM + kH;
+  float* sW = reinterpret_cast<float*>(sm + TcSmem::kOffW);
+  uint64_t* bar_raw = reinterpret_cast<uint64_t*>(sm + TcSmem::kOffBar);
+  uint64_t* bar_s = bar_raw + 1;
+  uint64_t* bar_o = bar_raw + 2;  // [2]
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(sm + TcSmem::kOffTmem);
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5, lane = tid & 31;
+  const int rank = blockIdx.x;  // the cluster spans gridDim.x
+  const int ns = p.nsplit;
+  const int tl = blockIdx.y;    // row within this launch
+  const int t = p.t_base + tl;
+
+  if (tid == 0) {
+    mbar_init(bar_raw, kCK);
+    mbar_init(bar_s, 1);
+    mbar_init(bar_o, 1);
+    mbar_init(bar_o + 1, 1);
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(s_tmem, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *s_tmem;
+  pdl_trigger();
+  pdl_wait();
+
+  // ---- records of this chunk (one bulk copy per key) and the row's q
+  if (tid < kCK) {
+    int kind;
+    const int slot = key_slot_tc(p, t, rank * kCK + tid, &kind);
+    sKind[tid] = kind;
+    if (kind == 0) {
+      mbar_arrive(bar_raw);
+    } else {
+      const uint32_t bytes = kind == 1 ? 528u : 288u;
+      const uint8_t* src = (kind == 1 ? p.swa_kv : p.main_kv) + static_cast<long long>(slot) * bytes;
+      mbar_arrive_expect_tx(bar_raw, bytes);
+      bulk_load(sRaw + tid * kRawStride, src, bytes, bar_raw, l2_policy_evict_first());
+    }
+  }
+  {
+    // 4096 chunks of 16 B (8 dims): chunk c -> head c / 64, dims 8 * (c % 64)
+    const uint4* qg = reinterpret_cast<const uint4*>(p.q + static_cast<long long>(t) * kH * kD);
+    uint4 v[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) v[j] = ld_cg_v4(qg + tid + j * kTcThreads);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int c = tid + j * kTcThreads;
+      const int h = c >> 6, c64 = c & 63;
+      *reinterpret_cast<uint4*>(sQ + (c64 >> 3) * TcSmem::kAtom + h * 128 + (((c64 & 7) ^ (h & 7)) << 4)) = v[j];
+    }
+  }
+
+  // ---- dequantise in two waves of 4 atoms (256 dims); thread -> key tid % 64,
+  // 32-dim block tid / 64 of the wave.  The S MMAs of the first wave's atoms
+  // run while the second wave is dequantised.
+  //   S = q K^T  -> TMEM columns 256..319
+  bool ok = mbar_wait(bar_raw, 0u, nullptr);
+  if (!ok) set_error(p.err, kErrTimeout);
+  const unsigned kmask_lo = __ballot_sync(0xffffffffu, ok && sKind[lane] != 0);
+  const unsigned kmask_hi = __ballot_sync(0xffffffffu, ok && sKind[32 + lane] != 0);
+#pragma unroll 1
+  for (int wave = 0; wave < 2; ++wave) {
+    const int key = tid & (kCK - 1);
+    const int b = (tid >> 6) + 8 * wave;
+    uint4 o[4];
+    dequant_block32(sRaw + key * kRawStride, ok ? sKind[key] : 0, b, o);
+    uint8_t* row = sK + (b >> 1) * TcSmem::kAtom + key * 128;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int c = ((b & 1) << 2) + j;
+      *reinterpret_cast<uint4*>(row + ((c ^ (key & 7)) << 4)) = o[j];
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    if (tid == 0) {
+      tc_fence_after();
+      constexpr uint32_t idesc = idesc_bf16_f32(128, 64, 0, 0);
+#pragma unroll
+      for (int a = 4 * wave; a < 4 * wave + 4; ++a) {
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          umma_bf16(tmem + 256, smem_desc_sw128(sQ + a * TcSmem::kAtom + kk * 32),
+                    smem_desc_sw128(sK + a * TcSmem::kAtom + kk * 32), idesc, (a | kk) != 0 ? 1u : 0u);
+        }
+      }
+      if (wave == 1) mma_commit(bar_s);
+    }
+  }
+
+  // ---- softmax of the chunk: warps 0-1 (keys 0-31) and 4-5 (keys 32-63) read
+  // TMEM lanes 0-63, one head per thread; the two halves exchange max and sum
+  float* sMx = sW;           // [2][64] half maxima (the combine weights reuse it later)
+  float* sSx = sW + 2 * kH;  // [2][64] half sums
+  if ((warp & 3) < 2 && warp < 8) {
+    const int half = warp >> 2;  // 0: keys 0-31, 1: keys 32-63
+    const int h = (warp & 3) * 32 + lane;
+    bool oks = mbar_wait(bar_s, 0u, nullptr);
+    if (!oks) set_error(p.err, kErrTimeout);
+    tc_fence_after();
+    float v[32];
+    tmem_ld32(tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + 256 + 32 * half, v);
+    const unsigned km = (half ? kmask_hi : kmask_lo);
+    float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      v[j] = ((km >> j) & 1u) && oks ? v[j] * p.scale_log2 : -INFINITY;
+      mx[j & 3] = fmaxf(mx[j & 3], v[j]);
+    }
+    sMx[half * kH + h] = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+    named_bar_sync(1, 128);
+    const float m = fmaxf(sMx[h], sMx[kH + h]);
+    float sum[4] = {0.f, 0.f, 0.f, 0.f};
+    uint32_t pk[16];
+#pragma unroll
+    for (int j = 0; j < 32; j += 2) {
+      const float e0 = (m == -INFINITY) ? 0.f : ex2_approx(v[j] - m);
+      const float e1 = (m == -INFINITY) ? 0.f : ex2_approx(v[j + 1] - m);
+      sum[(j >> 1) & 3] += e0 + e1;
+      pk[j / 2] = pack_bf16(e0, e1);
+    }
+    sSx[half * kH + h] = (sum[0] + sum[1]) + (sum[2] + sum[3]);
+    uint8_t* prow = sP + h * 128;
+#pragma unroll
+    for (int c4 = 0; c4 < 4; ++c4) {
+      const int c = 4 * half + c4;
+      *reinterpret_cast<uint4*>(prow + ((c ^ (h & 7)) << 4)) =
+          make_uint4(pk[4 * c4], pk[4 * c4 + 1], pk[4 * c4 + 2], pk[4 * c4 + 3]);
+    }
+    named_bar_sync(1, 128);
+    if (half == 0) {
+      sM[h] = m;
+      sL[h] = sSx[h] + sSx[kH + h];
+    }
+    fence_proxy_async_smem();
+  }
+  tc_fence_before();
+  __syncthreads();
+
+  // ---- O = P V  (dims 0-255 -> columns 0..255, dims 256-511 -> columns 256..511)
+  if (tid == 0) {
+    tc_fence_after();
+    constexpr uint32_t idesc = idesc_bf16_f32(128, 256, 0, 1);
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {
+        umma_bf16(tmem + 256 * hh, smem_desc_sw128(sP + kk * 32),
+                  smem_desc_sw128_mn(sK + 4 * hh * TcSmem::kAtom + kk * 2048, TcSmem::kAtom, 1024), idesc,
+                  kk != 0 ? 1u : 0u);
+      }
+      mma_commit(bar_o + hh);  // dims 0-255 done: bar_o[0]; dims 256-511: bar_o[1]
+    }
+  }
+
+  // ---- O / sum (bf16) -> shared staging rows (over the q and key tiles, free
+  // once O is complete) -> one bulk copy per head row into the scratch; the
+  // (max, sum) pairs are stored directly.  Warps of TMEM lane quadrants 0-1,
+  // four column groups of 128.
+  const long long rowbase = static_cast<long long>(tl) * ns;
+  uint8_t* sStage = sm + TcSmem::kOffQ;  // [64][kStageStride]
+  if ((warp & 3) < 2) {
+    const int qd = warp & 3, g = warp >> 2;
+    const int h = qd * 32 + lane;
+    bool oko = mbar_wait(bar_o + (g >> 1), 0u, nullptr);  // column groups 0-1: dims 0-255
+    if (!oko) set_error(p.err, kErrTimeout);
+    tc_fence_after();
+    const float l = sL[h];
+    const float inv = (l > 0.f && oko) ? 1.f / l : 0.f;
+    uint8_t* srow = sStage + h * kStageStride + 256 * g;
+#pragma unroll 1
+    for (int cc = 0; cc < 4; ++cc) {
+      float v[32];
+      tmem_ld32(tmem + (static_cast<uint32_t>(qd * 32) << 16) + 128 * g + 32 * cc, v);
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        *reinterpret_cast<uint4*>(srow + 64 * cc + 16 * j) =
+            make_uint4(pack_bf16(v[8 * j] * inv, v[8 * j + 1] * inv), pack_bf16(v[8 * j + 2] * inv, v[8 * j + 3] * inv),
+                       pack_bf16(v[8 * j + 4] * inv, v[8 * j + 5] * inv),
+                       pack_bf16(v[8 * j + 6] * inv, v[8 * j + 7] * inv));
+    }
+    if (g == 0) p.stat[(rowbase + rank) * kH + h] = make_float2(oko ? sM[h] : -INFINITY, oko ? l : 0.f);
+    fence_proxy_async_smem();
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+  if (tid < kH) {
+    bulk_store(p.part + ((rowbase + rank) * kH + tid) * kD, sStage + tid * kStageStride, kD * 2);
+    bulk_store_commit_wait();
+    fence_proxy_async_global();
+  }
+  cluster_sync();  // every chunk's partial of this row is in the scratch
+
+  // ---- combine: this CTA owns heads h = rank (mod ns)
+  const int my_heads = (kH - rank + ns - 1) / ns;
+  float2* sML = reinterpret_cast<float2*>(sStage);  // [my_heads][16] (max, sum) of each chunk
+  if (tid < my_heads * ns) {
+    const int li = tid / ns, r = tid % ns;
+    sML[li * 16 + r] = ld_cg_f2(p.stat + (rowbase + r) * kH + rank + li * ns);
+  }
+  __syncthreads();
+  if (tid < my_heads) {
+    const int h = rank + tid * ns;
+    const float sk = __ldg(p.sink + h) * kLog2e;
+    float M = sk;
+    for (int r = 0; r < ns; ++r) M = fmaxf(M, sML[tid * 16 + r].x);
+    float D = exp2f(sk - M);
+    for (int r = 0; r < ns; ++r) {
+      const float2 ml = sML[tid * 16 + r];
+      const float w = (ml.x == -INFINITY) ? 0.f : exp2f(ml.x - M) * ml.y;
+      sW[tid * 16 + r] = w;
+      D += w;
+    }
+    const float invD = 1.f / D;
+    for (int r = 0; r < ns; ++r) sW[tid * 16 + r] *= invD;
+    if (p.lse) p.lse[static_cast<long long>(t) * kH + h] = (M + log2f(D)) * kLn2;
+  }
+  __syncthreads();
+  for (int task = tid; task < my_heads * (kD / 8); task += kTcThreads) {
+    const int li = task / (kD / 8), c = task % (kD / 8);
+    const int h = rank + li * ns;
+    uint4 pv[kMaxCluster];
+#pragma unroll
+    for (int r = 0; r < kMaxCluster; ++r)
+      if (r < ns) pv[r] = ld_cg_v4(p.part + ((rowbase + r) * kH + h) * kD + 8 * c);
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int r = 0; r < kMaxCluster; ++r) {
+      if (r < ns) {
+        const float w = sW[li * 16 + r];
+        const uint32_t wv[4] = {pv[r].x, pv[r].y, pv[r].z, pv[r].w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float2 f2 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wv[j]));
+          acc[2 * j] = fmaf(w, f2.x, acc[2 * j]);
+          acc[2 * j + 1] = fmaf(w, f2.y, acc[2 * j + 1]);
+        }
+      }
+    }
+    const long long oo = (static_cast<long long>(t) * kH + h) * kD + 8 * c;
+    if (p.out_bf16) {
+      *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + oo) =
+          make_uint4(pack_bf16(acc[0], acc[1]), pack_bf16(acc[2], acc[3]), pack_bf16(acc[4], acc[5]),
+                     pack_bf16(acc[6], acc[7]));
+    } else {
+      float4* out = reinterpret_cast<float4*>(static_cast<float*>(p.out) + oo);
+      out[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+      out[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+    }
+  }
+}
+
 }  // namespace
 
 // CTAs per row: one per 64-key chunk while the rows of the launch still fit the
@@ -588,16 +1017,83 @@ int attn_num_splits(int T, int n_keys, int num_sms) {
   return (nchunks + cps - 1) / cps;
 }
 
-size_t attn_workspace_bytes(int T, int nsplit) {
-  (void)T;
-  (void)nsplit;
-  return 0;  // the split results are merged on chip
+// The tensor-core path takes rows of 1..16 chunks (up to 1024 keys), one CTA
+// per chunk, in launches of at most kTcRowsPerLaunch rows sharing one scratch.
+constexpr int kTcRowsPerLaunch = 256;
+static bool use_tc_path(int n_keys) {
+  const int nchunks = (n_keys + kCK - 1) / kCK;
+  return nchunks >= 1 && nchunks <= kMaxCluster;
+}
+static size_t tc_part_bytes(int rows, int nchunks) {
+  return (static_cast<size_t>(rows) * nchunks * kH * kD * 2 + 255) & ~size_t(255);
+}
+
+size_t attn_workspace_bytes(int T, int n_keys, int num_sms) {
+  (void)num_sms;
+  if (!use_tc_path(n_keys)) return 0;  // the split-K kernel merges on chip
+  const int nchunks = (n_keys + kCK - 1) / kCK;
+  const int rows = T < kTcRowsPerLaunch ? T : kTcRowsPerLaunch;
+  return tc_part_bytes(rows, nchunks) + static_cast<size_t>(rows) * nchunks * kH * sizeof(float2);
+}
+
+static cudaError_t launch_sparse_attn_tc(const AttnLaunch& a, void* ws, const DeviceCtx& ctx, cudaStream_t st) {
+  const int L = a.n_swa + a.k;
+  const int nchunks = (L + kCK - 1) / kCK;
+  TcParams p;
+  p.q = reinterpret_cast<const __nv_bfloat16*>(a.q);
+  p.main_kv = a.main_kv;
+  p.main_slots = a.main_slots;
+  p.topk_slot = a.topk_slot;
+  p.k = a.k;
+  p.ld_topk = a.ld_topk;
+  p.swa_kv = a.swa_kv;
+  p.swa_slots = a.swa_slots;
+  p.swa_slot = a.swa_slot;
+  p.n_swa = a.n_swa;
+  p.ld_swa = a.ld_swa;
+  p.sink = a.sink;
+  p.scale_log2 = a.scale * kLog2e;
+  p.out_bf16 = a.out_bf16;
+  p.out = a.out;
+  p.lse = a.lse;
+  p.nsplit = nchunks;
+  p.err = ctx.err;
+  const int rows_max = a.T < kTcRowsPerLaunch ? a.T : kTcRowsPerLaunch;
+  p.part = static_cast<__nv_bfloat16*>(ws);
+  p.stat = reinterpret_cast<float2*>(static_cast<uint8_t*>(ws) + tc_part_bytes(rows_max, nchunks));
+  cudaError_t e = prefer_max_smem(sparse_attn_tc_kernel, TcSmem::kAlloc);
+  if (e != cudaSuccess) return e;
+  if (nchunks > 8) {
+    e = cudaFuncSetAttribute(sparse_attn_tc_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return e;
+  }
+  for (int t0 = 0; t0 < a.T; t0 += kTcRowsPerLaunch) {
+    p.t_base = t0;
+    p.T = (a.T - t0) < kTcRowsPerLaunch ? (a.T - t0) : kTcRowsPerLaunch;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(nchunks, p.T);
+    cfg.blockDim = dim3(kTcThreads);
+    cfg.dynamicSmemBytes = TcSmem::kAlloc;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = nchunks;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    e = cudaLaunchKernelEx(&cfg, sparse_attn_tc_kernel, p);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 cudaError_t launch_sparse_attn(const AttnLaunch& a, void* ws, size_t ws_bytes, const DeviceCtx& ctx,
                                cudaStream_t st) {
-  (void)ws;
   (void)ws_bytes;
+  if (use_tc_path(a.n_swa + a.k)) return launch_sparse_attn_tc(a, ws, ctx, st);
   AttnParams p;
   p.q = reinterpret_cast<const __nv_bfloat16*>(a.q);
   p.main_kv = a.main_kv;
