@@ -585,6 +585,8 @@ __global__ void __launch_bounds__(512, 1) sparse_attn_kernel(const __grid_consta
 //   * O / sum is written as bf16 to a per-row scratch in global memory with
 //     (max, sum); after a cluster barrier the CTA of rank r combines the heads
 //     h = r (mod CTAs) over the row's chunks with the sink and writes them.
+// A partial row of the merge: 512 bf16 of O / sum, then (max, sum) and 8 pad bytes.
+constexpr int kPartRow = kD * 2 + 16;
 struct TcSmem {
   static constexpr int kAtom = 8192;                            // 64 rows x 128 B
   static constexpr int kOffQ = 0;                               // 8 atoms
@@ -593,17 +595,21 @@ struct TcSmem {
   static constexpr int kOffRaw = kOffP + kAtom;                 // [64][kRawStride]
   static constexpr int kOffKind = kOffRaw + kCK * kRawStride;   // int[64]
   static constexpr int kOffStat = kOffKind + kCK * 4;           // float m[64], l[64]
-  static constexpr int kOffW = kOffStat + 2 * kH * 4;           // float [ceil(64/ns)][16] combine weights
-  static constexpr int kOffBar = kOffW + 64 * 16 * 4;           // raw, S done, O halves done
-  static constexpr int kOffTmem = kOffBar + 4 * 8;
+  static constexpr int kOffW = kOffStat + 3 * kH * 4;           // float [ceil(64/ns)][16] combine weights
+  static constexpr int kOffBar = kOffW + 64 * 16 * 4;           // raw, S done, O halves done, merge rows
+  static constexpr int kOffTmem = kOffBar + 5 * 8;
+  // merge: the staged partial rows ([64][kPartRow]) and later the received rows
+  // ([ns][heads of this CTA][kPartRow]) use the q and key tiles
+  static_assert(75 * kPartRow <= 2 * 8 * kAtom, "received rows (at most 75 for 1..16 chunks) fit the q and key tiles");
   static constexpr int kBytes = kOffTmem + 8;
   static constexpr int kAlloc = kBytes + 1024;                  // the base is rounded up to 1024 B
   // the MMAs read 64 rows past the q tile and past the P tile
   static_assert(kOffK == kOffQ + 8 * kAtom && kOffRaw >= kOffP + kAtom + 0, "operand padding rows stay in bounds");
   static_assert(kCK * kRawStride >= kAtom, "rows past P stay inside the staging area");
 };
-constexpr int kTcThreads = 512;
-constexpr int kStageStride = kD * 2 + 16;  // bytes per staged O row (conflict-free 16-B stores)
+constexpr int kTcWorkers = 512;              // dequantisation, softmax, readout, combine
+constexpr int kTcThreads = kTcWorkers + 32;  // + one warp that issues the MMAs
+constexpr int kTcMmaThread = kTcWorkers;
 constexpr uint32_t kTmemCols = 512;  // O: 2 x 256 columns; S (64 columns) shares the second half
 
 struct TcParams {
@@ -626,8 +632,7 @@ struct TcParams {
   void* out;
   float* lse;
   int nsplit;     // CTAs (64-key chunks) per row = cluster size
-  __nv_bfloat16* part;  // [T][nsplit][64][512] O / sum of each chunk
-  float2* stat;         // [T][nsplit][64] (max, sum), log2 units
+  uint8_t* part;  // [T][nsplit][64][kPartRow]: O / sum of each chunk and (max, sum), log2 units
   uint32_t* err;
 };
 
@@ -710,23 +715,25 @@ __device__ __forceinline__ float2 ld_cg_f2(const float2* p) {
   asm("ld.global.cg.v2.f32 {%0,%1}, [%2];" : "=f"(v.x), "=f"(v.y) : "l"(p));
   return v;
 }
-__device__ __forceinline__ float ex2_approx(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
 // Bulk copy shared -> global, tracked by this thread's bulk async-group.
 __device__ __forceinline__ void bulk_store(void* gdst, const void* ssrc, uint32_t bytes) {
   asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst), "r"(smem_u32(ssrc)),
                "r"(bytes)
                : "memory");
 }
+// Waits until this thread's bulk stores have been performed.
 __device__ __forceinline__ void bulk_store_commit_wait() {
   asm volatile("cp.async.bulk.commit_group;\n\tcp.async.bulk.wait_group 0;" ::: "memory");
 }
 __device__ __forceinline__ void fence_proxy_async_global() {
   asm volatile("fence.proxy.async.global;" ::: "memory");
 }
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 
 __global__ void __launch_bounds__(kTcThreads, 1) sparse_attn_tc_kernel(const __grid_constant__ TcParams p) {
   extern __shared__ uint8_t tc_smem_raw[];
@@ -738,10 +745,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) sparse_attn_tc_kernel(const __g
   int* sKind = reinterpret_cast<int*>(sm + TcSmem::kOffKind);
   float* sM = reinterpret_cast<float*>(sm + TcSmem::kOffStat);
   float* sL = sM + kH;
+  float* sSink = sL + kH;
   float* sW = reinterpret_cast<float*>(sm + TcSmem::kOffW);
   uint64_t* bar_raw = reinterpret_cast<uint64_t*>(sm + TcSmem::kOffBar);
   uint64_t* bar_s = bar_raw + 1;
   uint64_t* bar_o = bar_raw + 2;  // [2]
+  uint64_t* bar_m = bar_raw + 4;  // merge rows received
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(sm + TcSmem::kOffTmem);
 
   const int tid = threadIdx.x;
@@ -756,6 +765,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) sparse_attn_tc_kernel(const __g
     mbar_init(bar_s, 1);
     mbar_init(bar_o, 1);
     mbar_init(bar_o + 1, 1);
+    mbar_init(bar_m, 1);
     fence_mbar_init();
   }
   if (warp == 0) {
@@ -783,15 +793,16 @@ __global__ void __launch_bounds__(kTcThreads, 1) sparse_attn_tc_kernel(const __g
       bulk_load(sRaw + tid * kRawStride, src, bytes, bar_raw, l2_policy_evict_first());
     }
   }
-  {
+  if (tid < kH) sSink[tid] = __ldg(p.sink + tid) * kLog2e;
+  if (tid < kTcWorkers) {
     // 4096 chunks of 16 B (8 dims): chunk c -> head c / 64, dims 8 * (c % 64)
     const uint4* qg = reinterpret_cast<const uint4*>(p.q + static_cast<long long>(t) * kH * kD);
     uint4 v[8];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) v[j] = ld_cg_v4(qg + tid + j * kTcThreads);
+    for (int j = 0; j < 8; ++j) v[j] = ld_cg_v4(qg + tid + j * kTcWorkers);
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-      const int c = tid + j * kTcThreads;
+      const int c = tid + j * kTcWorkers;
       const int h = c >> 6, c64 = c & 63;
       *reinterpret_cast<uint4*>(sQ + (c64 >> 3) * TcSmem::kAtom + h * 128 + (((c64 & 7) ^ (h & 7)) << 4)) = v[j];
     }
@@ -807,20 +818,22 @@ __global__ void __launch_bounds__(kTcThreads, 1) sparse_attn_tc_kernel(const __g
   const unsigned kmask_hi = __ballot_sync(0xffffffffu, ok && sKind[32 + lane] != 0);
 #pragma unroll 1
   for (int wave = 0; wave < 2; ++wave) {
-    const int key = tid & (kCK - 1);
-    const int b = (tid >> 6) + 8 * wave;
-    uint4 o[4];
-    dequant_block32(sRaw + key * kRawStride, ok ? sKind[key] : 0, b, o);
-    uint8_t* row = sK + (b >> 1) * TcSmem::kAtom + key * 128;
+    if (tid < kTcWorkers) {
+      const int key = tid & (kCK - 1);
+      const int b = (tid >> 6) + 8 * wave;
+      uint4 o[4];
+      dequant_block32(sRaw + key * kRawStride, ok ? sKind[key] : 0, b, o);
+      uint8_t* row = sK + (b >> 1) * TcSmem::kAtom + key * 128;
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int c = ((b & 1) << 2) + j;
-      *reinterpret_cast<uint4*>(row + ((c ^ (key & 7)) << 4)) = o[j];
+      for (int j = 0; j < 4; ++j) {
+        const int c = ((b & 1) << 2) + j;
+        *reinterpret_cast<uint4*>(row + ((c ^ (key & 7)) << 4)) = o[j];
+      }
+      fence_proxy_async_smem();
     }
-    fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
-    if (tid == 0) {
+    if (tid == kTcMmaThread) {
       tc_fence_after();
       constexpr uint32_t idesc = idesc_bf16_f32(128, 64, 0, 0);
 #pragma unroll
@@ -884,8 +897,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) sparse_attn_tc_kernel(const __g
   tc_fence_before();
   __syncthreads();
 
-  // ---- O = P V  (dims 0-255 -> columns 0..255, dims 256-511 -> columns 256..511)
-  if (tid == 0) {
+  // ---- O = P V  (dims 0-255 -> columns 0..255, committed to bar_o[0]; dims
+  // 256-511 -> columns 256..511, bar_o[1])
+  if (tid == kTcMmaThread) {
     tc_fence_after();
     constexpr uint32_t idesc = idesc_bf16_f32(128, 256, 0, 1);
 #pragma unroll
@@ -900,13 +914,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) sparse_attn_tc_kernel(const __g
     }
   }
 
-  // ---- O / sum (bf16) -> shared staging rows (over the q and key tiles, free
-  // once O is complete) -> one bulk copy per head row into the scratch; the
-  // (max, sum) pairs are stored directly.  Warps of TMEM lane quadrants 0-1,
-  // four column groups of 128.
+  // ---- partial rows: O / sum (bf16) and (max, sum) per head, staged over the
+  // q and key tiles (free once O is complete), then bulk stores into the
+  // scratch.  Warps of TMEM lane quadrants 0-1, four column groups of 128.
   const long long rowbase = static_cast<long long>(tl) * ns;
-  uint8_t* sStage = sm + TcSmem::kOffQ;  // [64][kStageStride]
-  if ((warp & 3) < 2) {
+  uint8_t* sStage = sm + TcSmem::kOffQ;  // [64][kPartRow]
+  if ((warp & 3) < 2 && tid < kTcWorkers) {
     const int qd = warp & 3, g = warp >> 2;
     const int h = qd * 32 + lane;
     bool oko = mbar_wait(bar_o + (g >> 1), 0u, nullptr);  // column groups 0-1: dims 0-255
@@ -914,19 +927,21 @@ __global__ void __launch_bounds__(kTcThreads, 1) sparse_attn_tc_kernel(const __g
     tc_fence_after();
     const float l = sL[h];
     const float inv = (l > 0.f && oko) ? 1.f / l : 0.f;
-    uint8_t* srow = sStage + h * kStageStride + 256 * g;
+    uint8_t* srow = sStage + h * kPartRow;
 #pragma unroll 1
     for (int cc = 0; cc < 4; ++cc) {
       float v[32];
       tmem_ld32(tmem + (static_cast<uint32_t>(qd * 32) << 16) + 128 * g + 32 * cc, v);
 #pragma unroll
       for (int j = 0; j < 4; ++j)
-        *reinterpret_cast<uint4*>(srow + 64 * cc + 16 * j) =
+        *reinterpret_cast<uint4*>(srow + 256 * g + 64 * cc + 16 * j) =
             make_uint4(pack_bf16(v[8 * j] * inv, v[8 * j + 1] * inv), pack_bf16(v[8 * j + 2] * inv, v[8 * j + 3] * inv),
                        pack_bf16(v[8 * j + 4] * inv, v[8 * j + 5] * inv),
                        pack_bf16(v[8 * j + 6] * inv, v[8 * j + 7] * inv));
     }
-    if (g == 0) p.stat[(rowbase + rank) * kH + h] = make_float2(oko ? sM[h] : -INFINITY, oko ? l : 0.f);
+    if (g == 0)
+      *reinterpret_cast<float4*>(srow + kD * 2) =
+          make_float4(oko ? sM[h] : -INFINITY, oko ? l : 0.f, 0.f, 0.f);
     fence_proxy_async_smem();
   }
   tc_fence_before();
@@ -935,45 +950,58 @@ __global__ void __launch_bounds__(kTcThreads, 1) sparse_attn_tc_kernel(const __g
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
-  if (tid < kH) {
-    bulk_store(p.part + ((rowbase + rank) * kH + tid) * kD, sStage + tid * kStageStride, kD * 2);
+  if (tid < 4) {
+    bulk_store(p.part + ((rowbase + rank) * kH + 16 * tid) * kPartRow, sStage + tid * 16 * kPartRow, 16 * kPartRow);
     bulk_store_commit_wait();
     fence_proxy_async_global();
   }
   cluster_sync();  // every chunk's partial of this row is in the scratch
 
-  // ---- combine: this CTA owns heads h = rank (mod ns)
-  const int my_heads = (kH - rank + ns - 1) / ns;
-  float2* sML = reinterpret_cast<float2*>(sStage);  // [my_heads][16] (max, sum) of each chunk
-  if (tid < my_heads * ns) {
-    const int li = tid / ns, r = tid % ns;
-    sML[li * 16 + r] = ld_cg_f2(p.stat + (rowbase + r) * kH + rank + li * ns);
+  // ---- combine: this CTA owns heads [hb, hb + nh); it fetches those rows of
+  // every chunk with one bulk copy per chunk and weighs them with the sink
+  const int hb = (kH * rank) / ns;
+  const int nh = (kH * (rank + 1)) / ns - hb;
+  uint8_t* sRecv = sm + TcSmem::kOffQ;  // [ns][nh][kPartRow]
+  if (tid == kTcMmaThread) {
+    fence_proxy_async_global();
+    mbar_arrive_expect_tx(bar_m, static_cast<uint32_t>(ns * nh * kPartRow));
+    for (int r = 0; r < ns; ++r)
+      bulk_load(sRecv + r * nh * kPartRow, p.part + ((rowbase + r) * kH + hb) * kPartRow, nh * kPartRow, bar_m,
+                l2_policy_evict_first());
   }
-  __syncthreads();
-  if (tid < my_heads) {
-    const int h = rank + tid * ns;
-    const float sk = __ldg(p.sink + h) * kLog2e;
-    float M = sk;
-    for (int r = 0; r < ns; ++r) M = fmaxf(M, sML[tid * 16 + r].x);
-    float D = exp2f(sk - M);
-    for (int r = 0; r < ns; ++r) {
-      const float2 ml = sML[tid * 16 + r];
-      const float w = (ml.x == -INFINITY) ? 0.f : exp2f(ml.x - M) * ml.y;
-      sW[tid * 16 + r] = w;
-      D += w;
+  const bool okm = mbar_wait(bar_m, 0u, nullptr);
+  if (!okm) set_error(p.err, kErrTimeout);
+  // weights: lane group of 16 per head, lane r of the group = chunk r
+  // (whole warps take part in the shuffles: the loop runs over warp-aligned bases)
+  for (int i0 = tid - lane; i0 < ((nh * 16 + 31) & ~31); i0 += kTcThreads) {
+    const int i = i0 + lane;
+    const bool valid = i < nh * 16;
+    const int li = valid ? (i >> 4) : 0, r = i & 15;
+    const int h = hb + li;
+    float2 ml = make_float2(-INFINITY, 0.f);
+    if (valid && r < ns && okm) ml = *reinterpret_cast<const float2*>(sRecv + (r * nh + li) * kPartRow + kD * 2);
+    const float sk = sSink[h];
+    float M = fmaxf(sk, ml.x);
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    const float w = (ml.x == -INFINITY) ? 0.f : ex2_approx(ml.x - M) * ml.y;
+    float D = w;
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) D += __shfl_xor_sync(0xffffffffu, D, o);
+    D += ex2_approx(sk - M);
+    if (valid) {
+      sW[li * 16 + r] = w / D;
+      if (r == 0 && p.lse) p.lse[static_cast<long long>(t) * kH + h] = (M + log2f(D)) * kLn2;
     }
-    const float invD = 1.f / D;
-    for (int r = 0; r < ns; ++r) sW[tid * 16 + r] *= invD;
-    if (p.lse) p.lse[static_cast<long long>(t) * kH + h] = (M + log2f(D)) * kLn2;
   }
   __syncthreads();
-  for (int task = tid; task < my_heads * (kD / 8); task += kTcThreads) {
-    const int li = task / (kD / 8), c = task % (kD / 8);
-    const int h = rank + li * ns;
+  for (int task = tid; task < nh * (kD / 8); task += kTcThreads) {
+    const int li = task >> 6, c = task & 63;
+    const int h = hb + li;
     uint4 pv[kMaxCluster];
 #pragma unroll
     for (int r = 0; r < kMaxCluster; ++r)
-      if (r < ns) pv[r] = ld_cg_v4(p.part + ((rowbase + r) * kH + h) * kD + 8 * c);
+      if (r < ns) pv[r] = *reinterpret_cast<const uint4*>(sRecv + (r * nh + li) * kPartRow + 16 * c);
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int r = 0; r < kMaxCluster; ++r) {
@@ -1025,7 +1053,7 @@ static bool use_tc_path(int n_keys) {
   return nchunks >= 1 && nchunks <= kMaxCluster;
 }
 static size_t tc_part_bytes(int rows, int nchunks) {
-  return (static_cast<size_t>(rows) * nchunks * kH * kD * 2 + 255) & ~size_t(255);
+  return static_cast<size_t>(rows) * nchunks * kH * kPartRow;
 }
 
 size_t attn_workspace_bytes(int T, int n_keys, int num_sms) {
@@ -1033,7 +1061,7 @@ size_t attn_workspace_bytes(int T, int n_keys, int num_sms) {
   if (!use_tc_path(n_keys)) return 0;  // the split-K kernel merges on chip
   const int nchunks = (n_keys + kCK - 1) / kCK;
   const int rows = T < kTcRowsPerLaunch ? T : kTcRowsPerLaunch;
-  return tc_part_bytes(rows, nchunks) + static_cast<size_t>(rows) * nchunks * kH * sizeof(float2);
+  return tc_part_bytes(rows, nchunks);
 }
 
 static cudaError_t launch_sparse_attn_tc(const AttnLaunch& a, void* ws, const DeviceCtx& ctx, cudaStream_t st) {
@@ -1059,8 +1087,8 @@ static cudaError_t launch_sparse_attn_tc(const AttnLaunch& a, void* ws, const De
   p.nsplit = nchunks;
   p.err = ctx.err;
   const int rows_max = a.T < kTcRowsPerLaunch ? a.T : kTcRowsPerLaunch;
-  p.part = static_cast<__nv_bfloat16*>(ws);
-  p.stat = reinterpret_cast<float2*>(static_cast<uint8_t*>(ws) + tc_part_bytes(rows_max, nchunks));
+  (void)rows_max;
+  p.part = static_cast<uint8_t*>(ws);
   cudaError_t e = prefer_max_smem(sparse_attn_tc_kernel, TcSmem::kAlloc);
   if (e != cudaSuccess) return e;
   if (nchunks > 8) {
