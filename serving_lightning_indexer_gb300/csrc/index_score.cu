@@ -246,6 +246,12 @@ __global__ void __launch_bounds__(kThreads, IdxCfg<NQ>::kCtasPerSm)
           s_lookup[lane] = rid;
         }
         __syncwarp();
+        // lane 0 switches q when the row changes, reserves a stage per tile of
+        // the group and announces its bytes; the copies are then issued by lane
+        // 0 (scan: 2 pages per tile) or by one lane per copy source (gather: 16
+        // candidate blocks per tile, whose serial issue would dominate)
+        const long long it0 = it;  // tile j of the group uses stage (it0 + j) % S
+        int ntile = 0;
         if (lane == 0) {
           int qb = find_qb(s_prefix, nqb, g0);
           for (int j = 0; j < GT && g0 + j < g_end && ok; ++j, ++it) {
@@ -262,28 +268,45 @@ __global__ void __launch_bounds__(kThreads, IdxCfg<NQ>::kCtasPerSm)
             }
             const int s = static_cast<int>(it % S);
             if (!(ok = mbar_wait(&empty[s], static_cast<uint32_t>((it / S) & 1) ^ 1u, s_abort))) break;
-            uint8_t* kdst = s_keys + s * Cfg::kKeyBytes;
-            float* sdst = s_scales + s * kTileKeys;
             constexpr int kRows = (MODE == kModeScan) ? 64 : 8;  // key rows per copy
             uint32_t bytes = 0;
 #pragma unroll
             for (int c = 0; c < SLOTS; ++c)
               if (s_lookup[j * SLOTS + c] >= 0) bytes += kRows * (kRowBytes + 4);
             mbar_arrive_expect_tx(&full[s], bytes);
+            ntile = j + 1;
+            if (MODE == kModeScan) {
+              uint8_t* kdst = s_keys + s * Cfg::kKeyBytes;
+              float* sdst = s_scales + s * kTileKeys;
 #pragma unroll
-            for (int c = 0; c < SLOTS; ++c) {
-              const int rid = s_lookup[j * SLOTS + c];
-              if (rid < 0) continue;
-              const int phys = rid / kPageRows;
-              const int r = rid - phys * kPageRows;
-              tma_load_2d(kdst + c * kRows * kRowBytes, &map_kv, 0, rid, &full[s], pol_keys);
-              bulk_load(sdst + c * kRows, p.index_k + static_cast<long long>(phys) * 8448 + 8192 + r * 4, kRows * 4,
-                        &full[s], pol_keys);
+              for (int c = 0; c < SLOTS; ++c) {
+                const int rid = s_lookup[j * SLOTS + c];
+                if (rid < 0) continue;
+                const int phys = rid / kPageRows;
+                const int r = rid - phys * kPageRows;
+                tma_load_2d(kdst + c * kRows * kRowBytes, &map_kv, 0, rid, &full[s], pol_keys);
+                bulk_load(sdst + c * kRows, p.index_k + static_cast<long long>(phys) * 8448 + 8192 + r * 4,
+                          kRows * 4, &full[s], pol_keys);
+              }
             }
           }
         }
         ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
         it = __shfl_sync(0xffffffffu, it, 0);
+        if (MODE == kModeGather) {
+          ntile = __shfl_sync(0xffffffffu, ntile, 0);
+          const int j = lane / SLOTS, c = lane % SLOTS;
+          const int rid = s_lookup[lane];
+          if (j < ntile && rid >= 0) {
+            constexpr int kRows = 8;
+            const int s = static_cast<int>((it0 + j) % S);
+            const int phys = rid / kPageRows;
+            const int r = rid - phys * kPageRows;
+            tma_load_2d(s_keys + s * Cfg::kKeyBytes + c * kRows * kRowBytes, &map_kv, 0, rid, &full[s], pol_keys);
+            bulk_load(s_scales + s * kTileKeys + c * kRows,
+                      p.index_k + static_cast<long long>(phys) * 8448 + 8192 + r * 4, kRows * 4, &full[s], pol_keys);
+          }
+        }
         if (!ok) break;
         __syncwarp();
       }
