@@ -110,6 +110,19 @@ def index_k_entries(cache: np.ndarray, page_table_row: np.ndarray, n: int) -> np
     return FP8[codes] * scale[:, None]
 
 
+def index_k_at(cache: np.ndarray, page_table_row: np.ndarray, positions: np.ndarray) -> np.ndarray:
+    """Dequantised index keys [len(positions),128] at the given logical positions
+    of one sequence (the page layout of ``index_k_entries``, for a subset)."""
+    cache = np.asarray(cache, dtype=np.uint8).reshape(-1, INDEX_PAGE_BYTES)
+    pos = np.asarray(positions, dtype=np.int64)
+    page = np.asarray(page_table_row, dtype=np.int64)[pos // PAGE]
+    off = pos % PAGE
+    codes = cache[page[:, None], off[:, None] * IDX_DIM + np.arange(IDX_DIM)[None, :]]
+    sbytes = cache[page[:, None], PAGE * IDX_DIM + off[:, None] * 4 + np.arange(4)[None, :]]
+    scale = np.ascontiguousarray(sbytes).view(np.float32).reshape(len(pos)).astype(np.float64)
+    return FP8[codes] * scale[:, None]
+
+
 def main_kv_records(cache: np.ndarray, slots: np.ndarray) -> np.ndarray:
     """Dequantised main-KV vectors [len(slots),512] of the given physical slots.
 

@@ -128,6 +128,7 @@ class DecodeStep:
                      if c is not None}
         self.on_index_score = None   # optional hooks (event recording around the indexer scan)
         self.after_index_score = None
+        self.after_layer = None      # optional hook called with the layer number after its last call
 
     # ---------------------------------------------------------------- per-step work
     def keys_scored_per_step(self) -> int:
@@ -176,3 +177,5 @@ class DecodeStep:
             at = li.attn
             csa2.sparse_attn(at.q, c.pc.main_kv, b.topk_slot[ci], at.swa_kv, at.swa_slot, at.sink, b.out[l],
                              stream=stream)
+            if self.after_layer:
+                self.after_layer(l)

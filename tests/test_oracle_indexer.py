@@ -172,3 +172,15 @@ def test_reindex_result_inside_pool_and_scores_match_full():
 def test_pool_positions_mask_invisible_tail():
     pos = o.pool_positions(np.array([0, 2, -1]), 19)
     assert pos.tolist() == list(range(8)) + [16, 17, 18] + [-1] * 5 + [-1] * 8
+
+
+def test_index_k_at_matches_whole_row_decode():
+    # keys at arbitrary positions are the rows of the whole-sequence decode
+    pc = W.make_paged_cache([300, 1000], seed=11, device="cpu")
+    cache = pc.index_k.numpy()
+    for b, n in enumerate([300, 1000]):
+        pt = pc.page_table[b].numpy()
+        full = o.index_k_entries(cache, pt, n)
+        pos = np.random.default_rng(b).choice(n, size=min(n, 97), replace=False)
+        assert np.array_equal(o.index_k_at(cache, pt, pos), full[pos])
+        assert np.array_equal(o.index_k_at(cache, pt, np.arange(n)), full)
