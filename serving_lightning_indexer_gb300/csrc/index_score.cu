@@ -150,9 +150,9 @@ __global__ void __launch_bounds__(kThreads, IdxCfg<NQ>::kCtasPerSm)
 
   int* s_seq = s_prefix + nqb + 1;
   int* s_emax = s_seq + nqb;
-  pdl_trigger();
-  pdl_wait();  // global memory is touched only after the previous kernel completed
-  for (int i = threadIdx.x; i < nqb; i += blockDim.x) s_prefix[i + 1] = qb_tiles<NQ, MODE>(p, i, &s_seq[i], &s_emax[i]);
+  // barriers and TMEM are set up while the previous kernel may still run; the
+  // next kernel may start only once this CTA holds its TMEM (so that it can
+  // never take the TMEM this CTA waits for)
   if (threadIdx.x == 0) {
     s_prefix[0] = 0;
     *s_abort = 0;
@@ -176,6 +176,9 @@ __global__ void __launch_bounds__(kThreads, IdxCfg<NQ>::kCtasPerSm)
     tmem_alloc(s_tmem, Cfg::kTmemCols);
     tmem_relinquish();
   }
+  pdl_trigger();
+  pdl_wait();  // global memory is touched only after the previous kernel completed
+  for (int i = threadIdx.x; i < nqb; i += blockDim.x) s_prefix[i + 1] = qb_tiles<NQ, MODE>(p, i, &s_seq[i], &s_emax[i]);
   __syncthreads();
   if (warp == 0) {  // inclusive scan of the tile counts by one warp
     const int per = (nqb + 31) / 32;
