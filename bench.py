@@ -328,7 +328,8 @@ def main():
     achieved = scan_bytes_per_step * K / (scan_ms_total / 1e3) / 1e9
     # our kernels launched per step: a Full layer runs compress, the scan and the
     # two select passes (filter, final); a Reindex layer the pool gather and the
-    # final select; every layer one clustered attention launch (memsets are not kernels)
+    # final select; every layer one clustered attention launch (the histogram
+    # memsets are not kernels)
     from serving_lightning_indexer_gb300 import decode_step as ds
     n_full = sum(1 for l in step.layers if ds.role_of(l) == "full")
     n_reidx = sum(1 for l in step.layers if ds.role_of(l) == "reindex")

@@ -242,9 +242,9 @@ int csa2_topk_with_candidates(const csa2_topk_args* a, void* ws, size_t ws_bytes
   int rc = csa2::topk_prepare(a, &S);
   if (rc) return rc;
   const size_t need = csa2::select_workspace_bytes(S);
-  if (!ws || ws_bytes < need)
+  if (need && (!ws || ws_bytes < need))
     return fail(CSA2_ERR_WORKSPACE, "csa2_topk_with_candidates: workspace of %zu bytes needed", need);
-  if (!aligned16(ws)) return fail(CSA2_ERR_ALIGN, "csa2_topk_with_candidates: workspace must be 16-B aligned");
+  if (need && !aligned16(ws)) return fail(CSA2_ERR_ALIGN, "csa2_topk_with_candidates: workspace must be 16-B aligned");
   DeviceCtx ctx;
   cudaError_t e = csa2::device_ctx(&ctx);
   if (e != cudaSuccess) return cuda_fail(e, "csa2_topk_with_candidates: device");

@@ -13,8 +13,9 @@
 // size, newest block forced to +inf).  Rows longer than kDirect go through:
 //   hist   : 2048-bin histogram of the top 11 key bits (skipped when the
 //            indexer scan already produced it)
-//   filter : many CTAs per row append every element whose bin is at or above
-//            the threshold bin to a per-row candidate list (at most kCap)
+//   filter : CTAs of 4096 elements each store every element whose bin is at
+//            or above the threshold bin in their own region (at most kRegion,
+//            with the true count), so nothing shared needs zeroing
 // and a final CTA per row runs an exact radix select over the 64-bit keys in
 // shared memory, sorts the survivors and writes positions, slots or pools.
 // Rows of at most kDirect elements are selected by the final CTA directly; a
@@ -30,7 +31,8 @@ namespace csa2 {
 namespace {
 
 constexpr int kBins = 2048;
-constexpr int kCap = 16384;      // candidate list per row
+constexpr int kCap = 16384;      // candidates of a row the final CTA holds in shared memory
+constexpr int kRegion = 512;     // candidates stored per filter CTA (a larger count flags an overflow)
 constexpr int kDirect = 16384;   // rows up to this length are selected in shared memory directly
 constexpr int kChunk = 16384;    // elements per CTA in the streaming passes
 constexpr int kMaxK = 2048;
@@ -59,9 +61,9 @@ struct SelParams {
   const uint32_t* hist;  // [V][kBins]: given, or built by the hist pass in `hist_ws`
   int hist_full;         // hist covers every row (given by the caller), not only the long ones
   uint32_t* hist_ws;
-  uint32_t* cnt;         // [V]
-  uint32_t* cord;        // [V][kCap]
-  uint32_t* cidx;        // [V][kCap]
+  uint32_t* cnt;         // [V][nchunks]: candidates found by each filter CTA (may exceed kRegion)
+  uint2* cand;           // [V][nchunks][kRegion]: (key, index) of each filter CTA's candidates
+  int nchunks;           // filter CTAs per row
   uint32_t* err;
 };
 
@@ -220,6 +222,7 @@ __global__ void __launch_bounds__(kStreamThreads) sel_filter_kernel(const __grid
   __shared__ __align__(16) uint32_t h[kBins];
   __shared__ int res[4];
   __shared__ uint32_t wsum[8];
+  __shared__ uint32_t s_cnt;
   // this thread's kFilterPer consecutive elements, loaded before the histogram
   // is searched so that the two latencies overlap
   const int i = i0 + threadIdx.x * kFilterPer;
@@ -242,7 +245,10 @@ __global__ void __launch_bounds__(kStreamThreads) sel_filter_kernel(const __grid
     vals[4 * q + 3] = v4.w;
   }
   stage_hist(h, P.hist + static_cast<long long>(v) * kBins);
-  if (threadIdx.x == 0) res[0] = -1;
+  if (threadIdx.x == 0) {
+    res[0] = -1;
+    s_cnt = 0;
+  }
   __syncthreads();
   block_find_bin(h, static_cast<uint32_t>(r.k), res, wsum);
   const int b1 = res[0];
@@ -256,29 +262,28 @@ __global__ void __launch_bounds__(kStreamThreads) sel_filter_kernel(const __grid
     keys[j] = (key && (key >> 21) >= thr) ? key : 0u;
     mine += keys[j] ? 1u : 0u;
   }
+  // this CTA's own region and count: no counter shared across CTAs, nothing to zero
   const uint32_t incl = warp_incl_scan(mine);
   const uint32_t wtot = __shfl_sync(0xffffffffu, incl, 31);
-  if (wtot == 0) return;
   uint32_t wbase = 0;
-  if (lane == 31) wbase = atomicAdd(P.cnt + v, wtot);
+  if (lane == 31 && wtot) wbase = atomicAdd(&s_cnt, wtot);
   wbase = __shfl_sync(0xffffffffu, wbase, 31);
   uint32_t slot = wbase + incl - mine;
-  uint32_t* cord = P.cord + static_cast<long long>(v) * kCap;
-  uint32_t* cidx = P.cidx + static_cast<long long>(v) * kCap;
+  uint2* cand = P.cand + (static_cast<long long>(v) * P.nchunks + blockIdx.x) * kRegion;
 #pragma unroll
   for (int j = 0; j < kFilterPer; ++j) {
     if (!keys[j]) continue;
-    if (slot < static_cast<uint32_t>(kCap)) {
-      cord[slot] = keys[j];
-      cidx[slot] = static_cast<uint32_t>(i + j);
-    }
+    if (slot < static_cast<uint32_t>(kRegion)) cand[slot] = make_uint2(keys[j], static_cast<uint32_t>(i + j));
     ++slot;
   }
+  __syncthreads();
+  if (threadIdx.x == 0) P.cnt[static_cast<long long>(v) * P.nchunks + blockIdx.x] = s_cnt;
 }
 
 // ---------------------------------------------------------------- final select
 constexpr int kPerThread = kDirect / kFinalThreads;  // direct-row values held in registers per thread
 constexpr int kBitmapWords = 2 * kDirect;            // pool-order bitmap (over the candidates): 2^20 blocks
+constexpr int kMaxChunks = kMaxK;                    // filter CTAs per row the final CTA can gather (counts + offsets in sel)
 
 struct FinalSmem {
   uint32_t* ord;      // [kDirect] candidate keys (score part)
@@ -553,7 +558,6 @@ __global__ void __launch_bounds__(kFinalThreads, 1) sel_final_kernel(const __gri
   //    gather epilogue) or the hist pass's, else built here from the values of
   //    a short row (kept in registers)
   int mode;  // 0: short row, 1: candidate list, 2: overflowed candidate list (stream the row)
-  uint32_t c = 0;
   uint32_t ord[kPerThread];
   const int nj = (r.n + kFinalThreads - 1) / kFinalThreads;
   if (r.n <= kDirect) {
@@ -581,8 +585,12 @@ __global__ void __launch_bounds__(kFinalThreads, 1) sel_final_kernel(const __gri
         if (j < nj) hist_add(sm.hist, ord[j] != 0u, ord[j] >> 21);
     }
   } else {
-    c = P.cnt[v];
-    mode = (c <= static_cast<uint32_t>(kCap)) ? 1 : 2;
+    // the per-CTA candidate counts of the filter pass (over the sel area, free until the collect)
+    const int nch = (r.n + kFilterChunk - 1) / kFilterChunk;
+    uint32_t* scnt = reinterpret_cast<uint32_t*>(sm.sel);  // [kMaxChunks] counts, then offsets
+    mode = (nch <= kMaxChunks) ? 1 : 2;
+    if (mode == 1)
+      for (int i = tid; i < nch; i += blockDim.x) scnt[i] = P.cnt[static_cast<long long>(v) * P.nchunks + i];
     stage_hist(sm.hist, P.hist + static_cast<long long>(v) * kBins);
 #pragma unroll
     for (int j = 0; j < kPerThread; ++j) ord[j] = 0u;
@@ -621,26 +629,35 @@ __global__ void __launch_bounds__(kFinalThreads, 1) sel_final_kernel(const __gri
     n = static_cast<int>(total_c);
     __syncthreads();
   } else if (mode == 1) {
-    const uint32_t* cord = P.cord + static_cast<long long>(v) * kCap;
-    const uint32_t* cidx = P.cidx + static_cast<long long>(v) * kCap;
-    for (int i0 = 0; i0 < static_cast<int>(c); i0 += 4 * kFinalThreads) {
-      uint32_t o4[4], x4[4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int i = i0 + u * kFinalThreads + tid;
-        o4[u] = (i < static_cast<int>(c)) ? cord[i] : 0u;
-        x4[u] = (i < static_cast<int>(c)) ? cidx[i] : 0u;
-      }
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int i = i0 + u * kFinalThreads + tid;
-        if (i < static_cast<int>(c)) {
-          sm.ord[i] = o4[u];
-          sm.idx[i] = x4[u];
+    // concatenate the filter CTAs' regions: offsets by a block prefix sum (two
+    // chunks per thread); an overflowed region or list falls back to streaming
+    const int nch = (r.n + kFilterChunk - 1) / kFilterChunk;
+    uint32_t* scnt = reinterpret_cast<uint32_t*>(sm.sel);
+    uint32_t* soff = scnt + kMaxChunks;
+    const int c0 = 2 * tid;
+    const uint32_t x0 = (c0 < nch) ? scnt[c0] : 0u, x1 = (c0 + 1 < nch) ? scnt[c0 + 1] : 0u;
+    const bool over = x0 > static_cast<uint32_t>(kRegion) || x1 > static_cast<uint32_t>(kRegion);
+    uint32_t total_c;
+    const uint32_t off = block_excl_scan(x0 + x1, sm.wsum, &total_c);
+    if (c0 < nch) soff[c0] = off;
+    if (c0 + 1 < nch) soff[c0 + 1] = off + x0;
+    const bool any_over = __syncthreads_or(over) != 0;
+    if (any_over || total_c > static_cast<uint32_t>(kCap)) {
+      mode = 2;
+    } else {
+      const int lane = tid & 31, warp = tid >> 5;
+      for (int ch = warp; ch < nch; ch += blockDim.x >> 5) {
+        const int nc = static_cast<int>(scnt[ch]);
+        const int o0 = static_cast<int>(soff[ch]);
+        const uint2* src = P.cand + (static_cast<long long>(v) * P.nchunks + ch) * kRegion;
+        for (int i = lane; i < nc; i += 32) {
+          const uint2 e = src[i];
+          sm.ord[o0 + i] = e.x;
+          sm.idx[o0 + i] = e.y;
         }
       }
+      n = static_cast<int>(total_c);
     }
-    n = static_cast<int>(c);
     __syncthreads();
   }
 
@@ -747,11 +764,25 @@ size_t final_smem_bytes() {
 
 }  // namespace
 
-size_t select_workspace_bytes(const SelectLaunch& a) {
+// Workspace of rows longer than kDirect: [histograms, unless given][per-CTA
+// candidate counts][per-CTA candidate regions]
+static long long select_maxn(const SelectLaunch& a) {
   if (a.kind != 0) return 0;  // Reindex rows are short enough for the direct path
+  long long maxn = a.ld_scores;
+  if (a.pool_out) maxn = maxn > a.ld_bm ? maxn : a.ld_bm;
+  return maxn;
+}
+static size_t select_cnt_bytes(long long V, long long nch) {
+  return (static_cast<size_t>(V) * nch * 4 + 255) & ~size_t(255);
+}
+
+size_t select_workspace_bytes(const SelectLaunch& a) {
+  const long long maxn = select_maxn(a);
+  if (maxn <= kDirect) return 0;
   const long long V = static_cast<long long>(a.rows.T) * (a.pool_out ? 2 : 1);
+  const long long nch = (maxn + kFilterChunk - 1) / kFilterChunk;
   const size_t hist = a.hist ? 0 : static_cast<size_t>(V) * kBins * 4;
-  return hist + ((static_cast<size_t>(V) * 4 + 255) & ~size_t(255)) + static_cast<size_t>(V) * kCap * 8 + 256;
+  return hist + select_cnt_bytes(V, nch) + static_cast<size_t>(V) * nch * kRegion * 8;
 }
 
 cudaError_t launch_select(const SelectLaunch& a, void* ws, size_t ws_bytes, const DeviceCtx& ctx, cudaStream_t st) {
@@ -779,30 +810,26 @@ cudaError_t launch_select(const SelectLaunch& a, void* ws, size_t ws_bytes, cons
   P.hist_full = a.hist != nullptr;
   P.hist_ws = nullptr;
   P.cnt = nullptr;
-  P.cord = P.cidx = nullptr;
+  P.cand = nullptr;
+  P.nchunks = 0;
   cudaError_t e;
-  long long maxn = 0;
-  if (a.kind == 0) {
-    maxn = a.ld_scores;
-    if (a.pool_out) maxn = maxn > a.ld_bm ? maxn : a.ld_bm;
-  }
+  const long long maxn = select_maxn(a);
   if (maxn > kDirect) {
+    const long long nch = (maxn + kFilterChunk - 1) / kFilterChunk;
     uint8_t* w = static_cast<uint8_t*>(ws);
     if (!a.hist) {
       P.hist_ws = reinterpret_cast<uint32_t*>(w);
       P.hist = P.hist_ws;
       w += static_cast<size_t>(V) * kBins * 4;
+      // the histogram pass accumulates: zero it (the only memset; given histograms need none)
+      e = cudaMemsetAsync(P.hist_ws, 0, static_cast<size_t>(V) * kBins * 4, st);
+      if (e != cudaSuccess) return e;
     }
     P.cnt = reinterpret_cast<uint32_t*>(w);
-    const size_t cnt_bytes = (static_cast<size_t>(V) * 4 + 255) & ~size_t(255);
-    P.cord = reinterpret_cast<uint32_t*>(w + cnt_bytes);
-    P.cidx = P.cord + static_cast<size_t>(V) * kCap;
-    // zero the histogram being built (if any) and the candidate counters: one contiguous range
-    const size_t zero_bytes = (a.hist ? 0 : static_cast<size_t>(V) * kBins * 4) + cnt_bytes;
-    e = cudaMemsetAsync(a.hist ? static_cast<void*>(P.cnt) : ws, 0, zero_bytes, st);
-    if (e != cudaSuccess) return e;
+    P.cand = reinterpret_cast<uint2*>(w + select_cnt_bytes(V, nch));
+    P.nchunks = static_cast<int>(nch);
     const dim3 grid(static_cast<unsigned>((maxn + kChunk - 1) / kChunk), static_cast<unsigned>(V));
-    const dim3 fgrid(static_cast<unsigned>((maxn + kFilterChunk - 1) / kFilterChunk), static_cast<unsigned>(V));
+    const dim3 fgrid(static_cast<unsigned>(nch), static_cast<unsigned>(V));
     if ((e = prefer_max_smem(sel_hist_kernel, 0)) != cudaSuccess) return e;
     if ((e = prefer_max_smem(sel_filter_kernel, 0)) != cudaSuccess) return e;
     if (!a.hist && (e = launch_pdl(sel_hist_kernel, grid, dim3(kStreamThreads), 0, st, P)) != cudaSuccess) return e;

@@ -102,6 +102,8 @@ def test_validation_returns_codes_without_launch(lib):
     assert lib.csa2_topk_with_candidates(C.byref(t), None, 0, None) == 1         # pool needs block_max
     t.block_max, t.ld_block_max = FAKE, 16
     n = C.c_size_t(0)
+    assert lib.csa2_workspace_size(2, C.cast(C.byref(t), C.c_void_p), C.byref(n)) == 0 and n.value == 0
+    t.ld_scores, t.ld_block_max = 32768, 4096                                    # rows past the direct path
     assert lib.csa2_workspace_size(2, C.cast(C.byref(t), C.c_void_p), C.byref(n)) == 0 and n.value > 0
     assert lib.csa2_topk_with_candidates(C.byref(t), None, 0, None) == 7         # workspace missing
 

@@ -61,14 +61,14 @@ def test_noalloc_topk_matches_workspace_topk_on_two_calls_in_a_row():
 def test_noalloc_topk_rejects_rows_beyond_the_static_scratch():
     dev = need_gpu()
     lib = csa2.load()
-    T = 80                                   # 160 long rows with pools: more than the static scratch
-    scores = torch.zeros(T, 20_000, dtype=torch.float32, device=dev)
-    bm = torch.zeros(T, 2_500, dtype=torch.float32, device=dev)
-    pt = torch.zeros(T, 320, dtype=torch.int32, device=dev)
-    nvis = torch.full((T,), 20_000, dtype=torch.int32, device=dev)
+    T = 80                                   # 160 rows of 100,000 with pools: ~17 MB, more than the static scratch
+    scores = torch.zeros(T, 100_000, dtype=torch.float32, device=dev)
+    bm = torch.zeros(T, 12_500, dtype=torch.float32, device=dev)
+    pt = torch.zeros(T, 1_563, dtype=torch.int32, device=dev)
+    nvis = torch.full((T,), 100_000, dtype=torch.int32, device=dev)
     out = torch.empty(T, 512, dtype=torch.int32, device=dev)
     pool = torch.empty(T, 2048, dtype=torch.int32, device=dev)
-    a = csa2.TopkArgs(scores.data_ptr(), 20_000, bm.data_ptr(), 2_500, pt.data_ptr(), 320,
+    a = csa2.TopkArgs(scores.data_ptr(), 100_000, bm.data_ptr(), 12_500, pt.data_ptr(), 1_563,
                       csa2.rows(T, T, n_visible=nvis), 512, out.data_ptr(), None, 512, pool.data_ptr(), 2048, None)
     assert lib.csa2_topk_with_candidates_noalloc(C.byref(a), torch.cuda.current_stream().cuda_stream) == 7
     assert b"static scratch" in lib.csa2_last_error_detail()
