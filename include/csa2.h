@@ -140,10 +140,9 @@ typedef struct {
 CSA2_API int csa2_index_score(const csa2_index_score_args* args, void* workspace, size_t ws_bytes, void* stream);
 
 /* ---- 2. top-k with slot translation and the candidate pool ------------------
- * Per row: the k (<= 2048) positions s < E_t with the largest finite scores,
- * ordered by score descending then position ascending (ties go to the lower
- * position), -1 filled when fewer than k are finite (DSA page, "Top-k：选的是
- * token，不是 block").  topk_slot[t][i] = slot of topk_pos[t][i] (-1 kept).
+ * Per row: the k (<= 2048) positions s < E_t with the largest finite scores
+ * (ties go to the lower position), in ascending position order, -1 filled
+ * when fewer than k are finite (DSA page, "Top-k：选的是 token，不是 block").  topk_slot[t][i] = slot of topk_pos[t][i] (-1 kept).
  * Pool (pool_blocks not NULL; CSA2 page, "Hierarchical Sparse Indexer",
  * "attention 计算的落点" select_candidate_blocks): block scores are
  * block_max[t][0..ceil(E_t/8)); the newest block ceil(E_t/8)-1 is always kept

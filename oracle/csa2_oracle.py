@@ -192,17 +192,18 @@ def visible_entries(pos: int, ratio_m: int) -> int:
 # ---------------------------------------------------------------------------
 
 def topk_positions(scores: np.ndarray, k: int) -> np.ndarray:
-    """Positions of the k best finite scores, best first, -1 filled.
+    """Positions of the k best finite scores in ascending position order, -1 filled.
 
     DSA page, "Top-k：选的是 token，不是 block": token-level selection, -1 in
-    empty slots.  Ties (left open by the pages) go to the lower position, and
-    the output is ordered by score descending then position ascending.  -inf
-    marks an excluded position and is never selected.
+    empty slots.  Ties (left open by the pages) go to the lower position.  The
+    pages leave the order of the reported positions open; they are reported in
+    ascending position order.  -inf marks an excluded position and is never
+    selected.
     """
     s = np.asarray(scores)
     cand = np.flatnonzero(np.isfinite(s))
     order = np.lexsort((cand, -s[cand]))
-    sel = cand[order[:k]]
+    sel = np.sort(cand[order[:k]])
     out = np.full(k, -1, dtype=np.int64)
     out[: len(sel)] = sel
     return out

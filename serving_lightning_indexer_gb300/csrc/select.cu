@@ -2,7 +2,8 @@
 //
 // Semantics (DSA page, "Top-k：选的是 token，不是 block"; CSA2 page,
 // "Hierarchical Sparse Indexer", "池里的 16384 个位置是哪些", "attention 计算的
-// 落点"): per row keep the k largest finite scores, ties to the lower index;
+// 落点"): per row keep the k largest finite scores, ties to the lower index,
+// reported in ascending position order;
 // positions become physical slots page_table[p / 64] * 64 + p % 64, -1 filled;
 // the pool keeps the newest block plus the blocks with the highest block
 // maxima, reported in ascending block order.
@@ -17,7 +18,8 @@
 //            or above the threshold bin in their own region (at most kRegion,
 //            with the true count), so nothing shared needs zeroing
 // and a final CTA per row runs an exact radix select over the 64-bit keys in
-// shared memory, sorts the survivors and writes positions, slots or pools.
+// shared memory and writes the survivors' positions, slots or pool blocks in
+// ascending order (the compactions keep element order, so no sort is needed).
 // Rows of at most kDirect elements are selected by the final CTA directly; a
 // row whose candidate list overflowed (massive ties near the threshold) is
 // selected by the final CTA streaming the row from global memory, still exact.
@@ -176,6 +178,26 @@ __device__ __forceinline__ void stage_hist(uint32_t* dst, const uint32_t* src) {
   for (int i = threadIdx.x; i < kBins / 4; i += blockDim.x) d4[i] = s4[i];
 }
 
+// Exclusive block-wide prefix sum of x (every thread calls); *total gets the sum.
+__device__ __forceinline__ uint32_t block_excl_scan(uint32_t x, uint32_t* wsum, uint32_t* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nwarps = blockDim.x >> 5;
+  const uint32_t incl = warp_incl_scan(x);
+  if (lane == 31) wsum[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    const uint32_t w = (lane < nwarps) ? wsum[lane] : 0u;
+    const uint32_t ws = warp_incl_scan(w);
+    __syncwarp();
+    wsum[lane] = ws;
+  }
+  __syncthreads();
+  const uint32_t base = warp ? wsum[warp - 1] : 0u;
+  *total = wsum[nwarps - 1];
+  __syncthreads();  // wsum is reused by the next scan
+  return base + incl - x;
+}
+
 // ---------------------------------------------------------------- streaming passes
 __global__ void __launch_bounds__(kStreamThreads) sel_hist_kernel(const __grid_constant__ SelParams P) {
   pdl_trigger();
@@ -221,8 +243,7 @@ __global__ void __launch_bounds__(kStreamThreads) sel_filter_kernel(const __grid
   if (i0 >= r.n) return;
   __shared__ __align__(16) uint32_t h[kBins];
   __shared__ int res[4];
-  __shared__ uint32_t wsum[8];
-  __shared__ uint32_t s_cnt;
+  __shared__ uint32_t wsum[32];
   // this thread's kFilterPer consecutive elements, loaded before the histogram
   // is searched so that the two latencies overlap
   const int i = i0 + threadIdx.x * kFilterPer;
@@ -245,15 +266,11 @@ __global__ void __launch_bounds__(kStreamThreads) sel_filter_kernel(const __grid
     vals[4 * q + 3] = v4.w;
   }
   stage_hist(h, P.hist + static_cast<long long>(v) * kBins);
-  if (threadIdx.x == 0) {
-    res[0] = -1;
-    s_cnt = 0;
-  }
+  if (threadIdx.x == 0) res[0] = -1;
   __syncthreads();
   block_find_bin(h, static_cast<uint32_t>(r.k), res, wsum);
   const int b1 = res[0];
   const uint32_t thr = b1 < 0 ? 0u : static_cast<uint32_t>(b1);
-  const int lane = threadIdx.x & 31;
   uint32_t keys[kFilterPer];
   uint32_t mine = 0;
 #pragma unroll
@@ -262,13 +279,11 @@ __global__ void __launch_bounds__(kStreamThreads) sel_filter_kernel(const __grid
     keys[j] = (key && (key >> 21) >= thr) ? key : 0u;
     mine += keys[j] ? 1u : 0u;
   }
-  // this CTA's own region and count: no counter shared across CTAs, nothing to zero
-  const uint32_t incl = warp_incl_scan(mine);
-  const uint32_t wtot = __shfl_sync(0xffffffffu, incl, 31);
-  uint32_t wbase = 0;
-  if (lane == 31 && wtot) wbase = atomicAdd(&s_cnt, wtot);
-  wbase = __shfl_sync(0xffffffffu, wbase, 31);
-  uint32_t slot = wbase + incl - mine;
+  // this CTA's own region, in element order (each thread holds consecutive
+  // elements; a block prefix sum places them), and its true count: no counter
+  // shared across CTAs, nothing to zero
+  uint32_t total;
+  uint32_t slot = block_excl_scan(mine, wsum, &total);
   uint2* cand = P.cand + (static_cast<long long>(v) * P.nchunks + blockIdx.x) * kRegion;
 #pragma unroll
   for (int j = 0; j < kFilterPer; ++j) {
@@ -276,19 +291,16 @@ __global__ void __launch_bounds__(kStreamThreads) sel_filter_kernel(const __grid
     if (slot < static_cast<uint32_t>(kRegion)) cand[slot] = make_uint2(keys[j], static_cast<uint32_t>(i + j));
     ++slot;
   }
-  __syncthreads();
-  if (threadIdx.x == 0) P.cnt[static_cast<long long>(v) * P.nchunks + blockIdx.x] = s_cnt;
+  if (threadIdx.x == 0) P.cnt[static_cast<long long>(v) * P.nchunks + blockIdx.x] = total;
 }
 
 // ---------------------------------------------------------------- final select
 constexpr int kPerThread = kDirect / kFinalThreads;  // direct-row values held in registers per thread
-constexpr int kBitmapWords = 2 * kDirect;            // pool-order bitmap (over the candidates): 2^20 blocks
 constexpr int kMaxChunks = kMaxK;                    // filter CTAs per row the final CTA can gather (counts + offsets in sel)
 
 struct FinalSmem {
   uint32_t* ord;      // [kDirect] candidate keys (score part)
   uint32_t* idx;      // [kDirect] candidate element indices
-  uint32_t* bitmap;   // [kBitmapWords], over ord and idx once the survivors are collected
   uint64_t* sel;      // [kMaxK] survivors
   uint64_t* xchg;     // [kMaxK] second buffer of the merge sort
   uint32_t* hist;     // [kBins]
@@ -301,8 +313,7 @@ __device__ __forceinline__ FinalSmem final_smem(uint8_t* base) {
   FinalSmem sm;
   sm.ord = reinterpret_cast<uint32_t*>(base);
   sm.idx = sm.ord + kDirect;
-  sm.bitmap = sm.ord;
-  sm.sel = reinterpret_cast<uint64_t*>(sm.ord + kBitmapWords);
+  sm.sel = reinterpret_cast<uint64_t*>(sm.idx + kDirect);
   sm.xchg = sm.sel + kMaxK;
   sm.hist = reinterpret_cast<uint32_t*>(sm.xchg + kMaxK);
   sm.res = reinterpret_cast<int*>(sm.hist + kBins);
@@ -328,26 +339,6 @@ __device__ __forceinline__ uint32_t block_append(bool take, uint32_t* counter) {
   if (m && lane == __ffs(m) - 1) b0 = atomicAdd(counter, __popc(m));
   b0 = __shfl_sync(0xffffffffu, b0, m ? __ffs(m) - 1 : 0);
   return b0 + __popc(m & ((1u << lane) - 1u));
-}
-
-// Exclusive block-wide prefix sum of x (every thread calls); *total gets the sum.
-__device__ __forceinline__ uint32_t block_excl_scan(uint32_t x, uint32_t* wsum, uint32_t* total) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int nwarps = blockDim.x >> 5;
-  const uint32_t incl = warp_incl_scan(x);
-  if (lane == 31) wsum[warp] = incl;
-  __syncthreads();
-  if (warp == 0) {
-    const uint32_t w = (lane < nwarps) ? wsum[lane] : 0u;
-    const uint32_t ws = warp_incl_scan(w);
-    __syncwarp();
-    wsum[lane] = ws;
-  }
-  __syncthreads();
-  const uint32_t base = warp ? wsum[warp - 1] : 0u;
-  *total = wsum[nwarps - 1];
-  __syncthreads();  // wsum is reused by the next scan
-  return base + incl - x;
 }
 
 // Radix refinement below a known prefix: the candidates sm.ord/idx[0..n) whose
@@ -505,45 +496,6 @@ __device__ void sort_desc(const FinalSmem& sm, int got) {
   }
 }
 
-// Pool output in ascending block order: the survivors' block ids set bits of a
-// bitmap; a block-wide prefix count of the bits gives each id its position.
-__device__ void pool_order_bitmap(const FinalSmem& sm, int got, int nblocks, int* out, int pool_n) {
-  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
-  const int nw = (nblocks + 31) / 32;
-  for (int i = t; i < nw; i += blockDim.x) sm.bitmap[i] = 0u;
-  __syncthreads();
-  for (int i = t; i < got; i += blockDim.x) {
-    const uint32_t id = static_cast<uint32_t>(sm.sel[i]);
-    atomicOr(&sm.bitmap[id >> 5], 1u << (id & 31u));
-  }
-  __syncthreads();
-  const int per = (nw + blockDim.x - 1) / blockDim.x;
-  const int w0 = min(t * per, nw), w1 = min(w0 + per, nw);
-  uint32_t cnt = 0;
-  for (int w = w0; w < w1; ++w) cnt += __popc(sm.bitmap[w]);
-  const uint32_t incl = warp_incl_scan(cnt);
-  if (lane == 31) sm.wsum[warp] = incl;
-  __syncthreads();
-  if (warp == 0) {
-    const uint32_t x = (lane < static_cast<int>(blockDim.x >> 5)) ? sm.wsum[lane] : 0u;
-    const uint32_t xs = warp_incl_scan(x);
-    __syncwarp();
-    sm.wsum[lane] = xs;
-  }
-  __syncthreads();
-  uint32_t rank = incl - cnt + (warp ? sm.wsum[warp - 1] : 0u);
-  for (int w = w0; w < w1; ++w) {
-    uint32_t bits = sm.bitmap[w];
-    while (bits) {
-      const int b = __ffs(bits) - 1;
-      bits &= bits - 1u;
-      if (rank < static_cast<uint32_t>(pool_n)) out[rank] = w * 32 + b;
-      ++rank;
-    }
-  }
-  for (int i = got + t; i < pool_n; i += blockDim.x) out[i] = -1;
-}
-
 __global__ void __launch_bounds__(kFinalThreads, 1) sel_final_kernel(const __grid_constant__ SelParams P) {
   extern __shared__ __align__(16) uint8_t fsm_raw[];
   const FinalSmem sm = final_smem(fsm_raw);
@@ -558,15 +510,26 @@ __global__ void __launch_bounds__(kFinalThreads, 1) sel_final_kernel(const __gri
   //    gather epilogue) or the hist pass's, else built here from the values of
   //    a short row (kept in registers)
   int mode;  // 0: short row, 1: candidate list, 2: overflowed candidate list (stream the row)
-  uint32_t ord[kPerThread];
-  const int nj = (r.n + kFinalThreads - 1) / kFinalThreads;
+  uint32_t ord[kPerThread];  // direct rows: elements e0 .. e0 + kPerThread - 1 of this thread
+  const int e0 = tid * kPerThread;
   if (r.n <= kDirect) {
     mode = 0;
     float val[kPerThread];
 #pragma unroll
-    for (int j = 0; j < kPerThread; ++j) {
-      const int i = j * kFinalThreads + tid;
-      val[j] = (i < r.n) ? r.src[i] : -INFINITY;
+    for (int q = 0; q < kPerThread / 4; ++q) {
+      const int e = e0 + 4 * q;
+      float4 v4 = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+      if (e + 3 < r.n) {
+        v4 = *reinterpret_cast<const float4*>(r.src + e);
+      } else if (e < r.n) {
+        v4.x = r.src[e];
+        if (e + 1 < r.n) v4.y = r.src[e + 1];
+        if (e + 2 < r.n) v4.z = r.src[e + 2];
+      }
+      val[4 * q] = v4.x;
+      val[4 * q + 1] = v4.y;
+      val[4 * q + 2] = v4.z;
+      val[4 * q + 3] = v4.w;
     }
     if (P.hist_full) {
       stage_hist(sm.hist, P.hist + static_cast<long long>(v) * kBins);
@@ -574,15 +537,11 @@ __global__ void __launch_bounds__(kFinalThreads, 1) sel_final_kernel(const __gri
       for (int i = tid; i < kBins; i += blockDim.x) sm.hist[i] = 0;
     }
 #pragma unroll
-    for (int j = 0; j < kPerThread; ++j) {
-      const int i = j * kFinalThreads + tid;
-      ord[j] = (i < r.n) ? elem_key(r, val[j], i) : 0u;
-    }
+    for (int j = 0; j < kPerThread; ++j) ord[j] = (e0 + j < r.n) ? elem_key(r, val[j], e0 + j) : 0u;
     if (!P.hist_full) {
       __syncthreads();
 #pragma unroll
-      for (int j = 0; j < kPerThread; ++j)
-        if (j < nj) hist_add(sm.hist, ord[j] != 0u, ord[j] >> 21);
+      for (int j = 0; j < kPerThread; ++j) hist_add(sm.hist, ord[j] != 0u, ord[j] >> 21);
     }
   } else {
     // the per-CTA candidate counts of the filter pass (over the sel area, free until the collect)
@@ -611,18 +570,18 @@ __global__ void __launch_bounds__(kFinalThreads, 1) sel_final_kernel(const __gri
     uint32_t tmask = 0, mine = 0;
 #pragma unroll
     for (int j = 0; j < kPerThread; ++j) {
-      if (j < nj && ord[j] != 0u && (ord[j] >> 21) >= thr) {
+      if (ord[j] != 0u && (ord[j] >> 21) >= thr) {
         tmask |= 1u << j;
         ++mine;
       }
     }
     uint32_t total_c;
-    uint32_t slot = block_excl_scan(mine, sm.wsum, &total_c);
+    uint32_t slot = block_excl_scan(mine, sm.wsum, &total_c);  // candidates stay in element order
 #pragma unroll
     for (int j = 0; j < kPerThread; ++j) {
       if ((tmask >> j) & 1u) {
         sm.ord[slot] = ord[j];
-        sm.idx[slot] = static_cast<uint32_t>(j * kFinalThreads + tid);
+        sm.idx[slot] = static_cast<uint32_t>(e0 + j);
         ++slot;
       }
     }
@@ -672,30 +631,54 @@ __global__ void __launch_bounds__(kFinalThreads, 1) sel_final_kernel(const __gri
     }
   }
 
-  // 4. collect the survivors (exactly min(k, selectable) of them)
-  const bool bitmap = r.pool && r.n <= kBitmapWords * 32;
+  // 4. collect the survivors (exactly min(k, selectable) of them) in element
+  //    order.  Candidates i = j * blockDim + tid form rounds j; a survivor's
+  //    place is the count of survivors in earlier rounds plus earlier warps of
+  //    its round (one prefix over [round][warp]) plus earlier lanes (ballot).
   if (mode != 2) {
     const int nper = (n + blockDim.x - 1) / blockDim.x;  // <= kPerThread
-    uint32_t tmask = 0, mine = 0;
+    const int lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
+    uint32_t* wcnt = sm.hist;  // [kPerThread][32] survivors per round and warp, then their prefix
+    uint32_t tmask = 0;
     for (int j = 0; j < nper; ++j) {
       const int i = j * blockDim.x + tid;
-      if (i < n && (take_all || (key64(sm.ord[i], sm.idx[i]) >> (64 - pbits)) >= prefix)) {
-        tmask |= 1u << j;
-        ++mine;
-      }
+      const bool take = i < n && (take_all || (key64(sm.ord[i], sm.idx[i]) >> (64 - pbits)) >= prefix);
+      const unsigned m = __ballot_sync(0xffffffffu, take);
+      if (take) tmask |= 1u << j;
+      if (lane == 0) wcnt[j * 32 + warp] = __popc(m);
     }
-    uint32_t total_s;
-    uint32_t slot = block_excl_scan(mine, sm.wsum, &total_s);
+    __syncthreads();
+    if (warp == 0) {  // exclusive prefix over the nper x nwarps counts, 16 per lane
+      const int cells = nper * 32;
+      const int per = (cells + 31) / 32;
+      uint32_t loc[16];
+      uint32_t sum = 0;
+#pragma unroll
+      for (int u = 0; u < 16; ++u) {
+        const int cidx = lane * per + u;
+        loc[u] = (u < per && cidx < cells && (cidx & 31) < nwarps) ? wcnt[cidx] : 0u;
+        sum += loc[u];
+      }
+      const uint32_t incl = warp_incl_scan(sum);
+      uint32_t run = incl - sum;
+      __syncwarp();
+#pragma unroll
+      for (int u = 0; u < 16; ++u) {
+        const int cidx = lane * per + u;
+        if (u < per && cidx < cells) wcnt[cidx] = run;
+        run += loc[u];
+      }
+      if (lane == 31) sm.counters[1] = incl;
+    }
+    __syncthreads();
     for (int j = 0; j < nper; ++j) {
-      if ((tmask >> j) & 1u) {
-        const int i = j * blockDim.x + tid;
-        const uint32_t id = sm.idx[i];
-        if (slot < static_cast<uint32_t>(kMaxK))
-          sm.sel[slot] = r.pool ? static_cast<uint64_t>(bitmap ? id : ~id) : key64(sm.ord[i], id);
-        ++slot;
+      const bool take = (tmask >> j) & 1u;
+      const unsigned m = __ballot_sync(0xffffffffu, take);
+      if (take) {
+        const uint32_t place = wcnt[j * 32 + warp] + __popc(m & ((1u << lane) - 1u));
+        if (place < static_cast<uint32_t>(kMaxK)) sm.sel[place] = sm.idx[j * blockDim.x + tid];
       }
     }
-    if (tid == 0) sm.counters[1] = total_s;
   } else {
     const int nr = (r.n + blockDim.x - 1) / blockDim.x * blockDim.x;
     for (int i = tid; i < nr; i += blockDim.x) {
@@ -708,35 +691,32 @@ __global__ void __launch_bounds__(kFinalThreads, 1) sel_final_kernel(const __gri
       }
       const bool take = valid && (take_all || (kk >> (64 - pbits)) >= prefix);
       const uint32_t slot = block_append(take, &sm.counters[1]);
-      const uint32_t id = static_cast<uint32_t>(i);
-      if (take && slot < static_cast<uint32_t>(kMaxK))
-        sm.sel[slot] = r.pool ? static_cast<uint64_t>(bitmap ? id : ~id) : kk;
+      // ~index: the descending sort below then leaves ascending indices
+      if (take && slot < static_cast<uint32_t>(kMaxK)) sm.sel[slot] = static_cast<uint64_t>(~static_cast<uint32_t>(i));
     }
   }
   __syncthreads();
   const int got = min(static_cast<int>(sm.counters[1]), kMaxK);
+  if (mode == 2) {  // streamed survivors arrive in no particular order
+    sort_desc(sm, got);
+    for (int i = tid; i < got; i += blockDim.x) sm.sel[i] = ~static_cast<uint32_t>(sm.sel[i]);
+    __syncthreads();
+  }
 
-  // 5. order and write: pools by block id ascending, positions by key descending
+  // 5. write: sel holds the survivors' element indices in ascending order
   const int t = r.t;
   const int b = row_seq_of(P.rows, t);
   if (r.pool) {
     int* out = P.pool_out + static_cast<long long>(t) * P.pool_n;
-    if (bitmap) {
-      pool_order_bitmap(sm, got, r.n, out, P.pool_n);
-    } else {  // ~id descending is id ascending
-      sort_desc(sm, got);
-      for (int i = tid; i < P.pool_n; i += blockDim.x)
-        out[i] = (i < got) ? static_cast<int>(~static_cast<uint32_t>(sm.sel[i])) : -1;
-    }
+    for (int i = tid; i < P.pool_n; i += blockDim.x) out[i] = (i < got) ? static_cast<int>(sm.sel[i]) : -1;
     return;
   }
-  sort_desc(sm, got);
   int* opos = P.topk_pos + static_cast<long long>(t) * P.ld_topk;
   int* oslot = P.topk_slot ? P.topk_slot + static_cast<long long>(t) * P.ld_topk : nullptr;
   for (int i = tid; i < r.k; i += blockDim.x) {
     int pos = -1;
     if (i < got) {
-      const uint32_t id = ~static_cast<uint32_t>(sm.sel[i] & 0xFFFFFFFFull);
+      const uint32_t id = static_cast<uint32_t>(sm.sel[i]);
       if (P.kind == 2) {
         const int blk = P.pool_in[static_cast<long long>(t) * P.pool_in_n + (id >> 3)];
         pos = blk * 8 + static_cast<int>(id & 7);
@@ -759,7 +739,7 @@ __global__ void __launch_bounds__(kFinalThreads, 1) sel_final_kernel(const __gri
 }
 
 size_t final_smem_bytes() {
-  return static_cast<size_t>(kBitmapWords) * 4 + 2 * kMaxK * 8 + kBins * 4 + 8 * 4 + 32 * 4 + 4 * 4;
+  return static_cast<size_t>(2 * kDirect) * 4 + 2 * kMaxK * 8 + kBins * 4 + 8 * 4 + 32 * 4 + 4 * 4;
 }
 
 }  // namespace

@@ -88,7 +88,9 @@ def test_exact_massive_ties_fall_back_to_streaming_select():
     s = np.full((2, 100_000), 3.5, dtype=np.float32)
     s[0, 99_000] = 4.0
     pos, slot, pool, bm_np, pt = _run_topk(s, lengths)
-    assert pos[0].tolist() == [99_000] + list(range(511))
+    # the best score and the 511 lowest tied positions, in ascending position order
+    assert pos[0].tolist() == list(range(511)) + [99_000]
+    assert pos[0].tolist() == o.topk_positions(s[0, :100_000].astype(np.float64), 512).tolist()
     assert pos[1].tolist() == list(range(512))
     assert pool[0].tolist() == o.candidate_pool(bm_np[0, :12_500].astype(np.float64), 2048).tolist()
 

@@ -88,7 +88,7 @@ def test_topk_bruteforce_and_fill():
         s[rng.random(n) < 0.2] = -np.inf
         k = 8
         want = sorted([(-s[i], i) for i in range(n) if np.isfinite(s[i])])[:k]
-        want = [i for _, i in want] + [-1] * (k - len(want))
+        want = sorted(i for _, i in want) + [-1] * (k - len(want))
         assert o.topk_positions(s, k).tolist() == want
 
 
