@@ -223,6 +223,14 @@ typedef struct {
   int32_t out_bf16;                            /* 0: fp32 out, 1: bf16 out */
   void* out;                                   /* [T,64,512] */
   float* lse;                                  /* optional [T,64] */
+  /* 1: topk_slot, swa_slot, main_kv and swa_kv were written at least two
+   * launches before this call on the stream (a Reuse layer's slots and caches,
+   * written by its Full or Reindex layer), so the keys may be gathered before
+   * the previous launch completes; q and sink are still read after it.  The two
+   * launches before the call must be ordinary launches or kernels that signal
+   * their dependents only after their own dependency wait (as every kernel of
+   * this library does).  0: everything is read after the previous launch. */
+  int32_t kv_ready;
 } csa2_sparse_attn_args;
 CSA2_API int csa2_sparse_attn(const csa2_sparse_attn_args* args, void* workspace, size_t ws_bytes, void* stream);
 

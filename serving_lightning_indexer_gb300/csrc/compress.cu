@@ -64,8 +64,8 @@ __device__ __forceinline__ uint32_t e2m1_code(float v) {
 
 __global__ void __launch_bounds__(256) compress_kernel(const __grid_constant__ CompressParams p) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  pdl_trigger();
   pdl_wait();
+  pdl_trigger();
   const long long e = static_cast<long long>(blockIdx.x) * 8 + warp;
   if (e >= p.n_entries) return;
   const int c0 = lane * 16;

@@ -363,6 +363,7 @@ int csa2_sparse_attn(const csa2_sparse_attn_args* a, void* ws, size_t ws_bytes, 
   L.out_bf16 = a->out_bf16;
   L.out = a->out;
   L.lse = a->lse;
+  L.kv_ready = a->kv_ready != 0;
   e = csa2::launch_sparse_attn(L, ws, ws_bytes, ctx, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "csa2_sparse_attn: launch");
   return CSA2_OK;

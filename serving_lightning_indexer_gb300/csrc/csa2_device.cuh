@@ -220,9 +220,11 @@ __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
 
 // ---------------------------------------------------------------- programmatic dependent launch
 // Every kernel of the library is launched with programmatic stream
-// serialisation: it lets the next kernel's CTAs start (pdl_trigger) as soon as
-// all of its own CTAs are running, and touches global memory only after the
-// previous kernel has completed and flushed (pdl_wait).
+// serialisation.  It touches global memory written by the previous kernel only
+// after that kernel has completed and flushed (pdl_wait), and lets the next
+// kernel's CTAs start (pdl_trigger) once its own CTAs have passed that wait.
+// So when a kernel's CTAs start, every launch before the previous one has
+// completed, and data they wrote may be read before pdl_wait.
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 

@@ -110,6 +110,7 @@ struct AttnLaunch {
   int out_bf16;
   void* out;
   float* lse;
+  int kv_ready;  // slots and caches written at least two launches before: gather before the dependency wait
 };
 int attn_num_splits(int T, int n_keys, int num_sms);
 size_t attn_workspace_bytes(int T, int n_keys, int num_sms);

@@ -176,8 +176,8 @@ __global__ void __launch_bounds__(kThreads, IdxCfg<NQ>::kCtasPerSm)
     tmem_alloc(s_tmem, Cfg::kTmemCols);
     tmem_relinquish();
   }
-  pdl_trigger();
   pdl_wait();  // global memory is touched only after the previous kernel completed
+  pdl_trigger();
   for (int i = threadIdx.x; i < nqb; i += blockDim.x) s_prefix[i + 1] = qb_tiles<NQ, MODE>(p, i, &s_seq[i], &s_emax[i]);
   __syncthreads();
   if (warp == 0) {  // inclusive scan of the tile counts by one warp

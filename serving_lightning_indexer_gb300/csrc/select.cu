@@ -200,8 +200,8 @@ __device__ __forceinline__ uint32_t block_excl_scan(uint32_t x, uint32_t* wsum, 
 
 // ---------------------------------------------------------------- streaming passes
 __global__ void __launch_bounds__(kStreamThreads) sel_hist_kernel(const __grid_constant__ SelParams P) {
-  pdl_trigger();
   pdl_wait();
+  pdl_trigger();
   const int v = blockIdx.y;
   const VRow r = vrow_of(P, v);
   if (r.n <= kDirect) return;
@@ -234,8 +234,8 @@ __global__ void __launch_bounds__(kStreamThreads) sel_hist_kernel(const __grid_c
 }
 
 __global__ void __launch_bounds__(kStreamThreads) sel_filter_kernel(const __grid_constant__ SelParams P) {
-  pdl_trigger();
   pdl_wait();
+  pdl_trigger();
   const int v = blockIdx.y;
   const VRow r = vrow_of(P, v);
   if (r.n <= kDirect) return;
@@ -499,8 +499,8 @@ __device__ void sort_desc(const FinalSmem& sm, int got) {
 __global__ void __launch_bounds__(kFinalThreads, 1) sel_final_kernel(const __grid_constant__ SelParams P) {
   extern __shared__ __align__(16) uint8_t fsm_raw[];
   const FinalSmem sm = final_smem(fsm_raw);
-  pdl_trigger();
   pdl_wait();
+  pdl_trigger();
   const int v = blockIdx.x;
   const VRow r = vrow_of(P, v);
   const int tid = threadIdx.x;

@@ -289,8 +289,8 @@ __global__ void __launch_bounds__(512, 1) sparse_attn_kernel(const __grid_consta
     sL[tid] = 0.f;
   }
   __syncthreads();
-  pdl_trigger();
   pdl_wait();
+  pdl_trigger();
 
   const uint64_t pol = l2_policy_evict_first();
   // q rows and the first chunk's records: bulk copies, one per thread of the first 64
@@ -631,6 +631,7 @@ struct TcParams {
   int out_bf16;
   void* out;
   float* lse;
+  int kv_ready;   // gather the keys before the dependency wait
   int nsplit;     // CTAs (64-key chunks) per row = cluster size
   uint8_t* part;  // [T][nsplit][64][kPartRow]: O / sum of each chunk and (max, sum), log2 units
   uint32_t* err;
@@ -776,23 +777,30 @@ __global__ void __launch_bounds__(kTcThreads, 1) sparse_attn_tc_kernel(const __g
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *s_tmem;
-  pdl_trigger();
-  pdl_wait();
 
-  // ---- records of this chunk (one bulk copy per key) and the row's q
-  if (tid < kCK) {
-    int kind;
-    const int slot = key_slot_tc(p, t, rank * kCK + tid, &kind);
-    sKind[tid] = kind;
-    if (kind == 0) {
-      mbar_arrive(bar_raw);
-    } else {
-      const uint32_t bytes = kind == 1 ? 528u : 288u;
-      const uint8_t* src = (kind == 1 ? p.swa_kv : p.main_kv) + static_cast<long long>(slot) * bytes;
-      mbar_arrive_expect_tx(bar_raw, bytes);
-      bulk_load(sRaw + tid * kRawStride, src, bytes, bar_raw, l2_policy_evict_first());
+  // ---- records of this chunk (one bulk copy per key): before the dependency
+  // wait when the caller marks the slots and caches as written two or more
+  // launches earlier (every launch before the previous one has completed when
+  // this CTA starts), else after it; then the row's q and the sink
+  auto issue_records = [&]() {
+    if (tid < kCK) {
+      int kind;
+      const int slot = key_slot_tc(p, t, rank * kCK + tid, &kind);
+      sKind[tid] = kind;
+      if (kind == 0) {
+        mbar_arrive(bar_raw);
+      } else {
+        const uint32_t bytes = kind == 1 ? 528u : 288u;
+        const uint8_t* src = (kind == 1 ? p.swa_kv : p.main_kv) + static_cast<long long>(slot) * bytes;
+        mbar_arrive_expect_tx(bar_raw, bytes);
+        bulk_load(sRaw + tid * kRawStride, src, bytes, bar_raw, l2_policy_evict_first());
+      }
     }
-  }
+  };
+  if (p.kv_ready) issue_records();
+  pdl_wait();
+  pdl_trigger();
+  if (!p.kv_ready) issue_records();
   if (tid < kH) sSink[tid] = __ldg(p.sink + tid) * kLog2e;
   if (tid < kTcWorkers) {
     // 4096 chunks of 16 B (8 dims): chunk c -> head c / 64, dims 8 * (c % 64)
@@ -1084,6 +1092,7 @@ static cudaError_t launch_sparse_attn_tc(const AttnLaunch& a, void* ws, const De
   p.out_bf16 = a.out_bf16;
   p.out = a.out;
   p.lse = a.lse;
+  p.kv_ready = a.kv_ready;
   p.nsplit = nchunks;
   p.err = ctx.err;
   const int rows_max = a.T < kTcRowsPerLaunch ? a.T : kTcRowsPerLaunch;

@@ -175,7 +175,9 @@ class DecodeStep:
                 csa2.reindex(li.iq.q_fp8, li.iq.q_scale, li.iq.w, c.pc.index_k, c.pc.page_table, self.rows[ci],
                              b.pool, W.TOPK, b.topk_pos, b.topk_slot[ci], stream=stream)
             at = li.attn
+            # a Reuse layer's slots and caches were written by its Full or Reindex
+            # layer's calls, at least two launches back: its keys are gathered early
             csa2.sparse_attn(at.q, c.pc.main_kv, b.topk_slot[ci], at.swa_kv, at.swa_slot, at.sink, b.out[l],
-                             stream=stream)
+                             stream=stream, kv_ready=(role == "reuse"))
             if self.after_layer:
                 self.after_layer(l)

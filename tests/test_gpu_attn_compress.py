@@ -149,3 +149,22 @@ def test_attention_main_kv_with_varied_block_scales():
                                  np_(al.swa_slot[t]), np_(al.sink).astype(np.float64), 1e-3)
         err = np.abs(np_(out[t]).astype(np.float64) - ref).max() / np.abs(ref).max()
         assert err < 1e-2, err
+
+
+def test_attention_keys_gathered_early_give_identical_results():
+    # kv_ready lets the kernel gather slots and records before the dependency
+    # wait; with slots and caches written long before, the result is the same
+    dev = need_gpu()
+    pc = W.make_paged_cache([20000], seed=41, device=dev)
+    al = W.make_attn_layer(8, seed=42, device=dev)
+    rng = np.random.default_rng(43)
+    slots = torch.tensor(np.stack([o.slots_of(rng.choice(20000, size=512, replace=False), np_(pc.page_table[0]))
+                                   for _ in range(8)]), dtype=torch.int32, device=dev)
+    outs = []
+    for ready in (False, True, True):
+        out = torch.empty(8, 64, 512, dtype=torch.bfloat16, device=dev)
+        csa2.sparse_attn(al.q, pc.main_kv, slots, al.swa_kv, al.swa_slot, al.sink, out, kv_ready=ready)
+        outs.append(out)
+    torch.cuda.synchronize()
+    assert csa2.check_device_error() == 0
+    assert torch.equal(outs[0], outs[1]) and torch.equal(outs[0], outs[2])
