@@ -571,45 +571,48 @@ __global__ void __launch_bounds__(512, 1) sparse_attn_kernel(const __grid_consta
 
 
 // ================================================================ tensor-core path
-// One CTA per 64-key chunk of a row; the row's CTAs form a cluster.  Per CTA:
+// One CTA per 80-key chunk of a row; the row's CTAs form a cluster.  Per CTA:
 //   * the row's q (64 heads x 512, bf16) and the chunk's records are staged in
 //     shared memory; the records are dequantised to bf16 key rows.  Both tiles
 //     use the 128-byte swizzled layout of the tensor cores: 8 atoms of 64
 //     dims, each [64 rows x 128 B], rows of an atom 1024 B per group of 8.
 //   * S = q K^T on tcgen05 (M = 128: heads 0-63, rows 64-127 read the next 8 KB
-//     of shared memory and are discarded; N = 64 keys; K = 512) into TMEM.
+//     of shared memory and are discarded; N = 80 keys; K = 512) into TMEM.
 //   * one thread per head reads its S row, masks absent keys, and forms
 //     P = exp2(S*scale - max) (bf16, swizzled) with its max and sum.
-//   * O = P V on tcgen05 (M = 128 as above, N = 256 dims twice, K = 64 keys; V
+//   * O = P V on tcgen05 (M = 128 as above, N = 256 dims twice, K = 80 keys; V
 //     is the key tile read MN-major) into TMEM.
 //   * O / sum is written as bf16 to a per-row scratch in global memory with
 //     (max, sum); after a cluster barrier the CTA of rank r combines the heads
 //     h = r (mod CTAs) over the row's chunks with the sink and writes them.
 // A partial row of the merge: 512 bf16 of O / sum, then (max, sum) and 8 pad bytes.
 constexpr int kPartRow = kD * 2 + 16;
+constexpr int kTcKeys = 80;  // keys per CTA: 640 keys of a decode row in 8 CTAs, so two clusters share a GPC
 struct TcSmem {
-  static constexpr int kAtom = 8192;                            // 64 rows x 128 B
-  static constexpr int kOffQ = 0;                               // 8 atoms
-  static constexpr int kOffK = kOffQ + 8 * kAtom;               // 8 atoms
-  static constexpr int kOffP = kOffK + 8 * kAtom;               // 1 atom
-  static constexpr int kOffRaw = kOffP + kAtom;                 // [64][kRawStride]
-  static constexpr int kOffKind = kOffRaw + kCK * kRawStride;   // int[64]
-  static constexpr int kOffStat = kOffKind + kCK * 4;           // float m[64], l[64]
-  static constexpr int kOffW = kOffStat + 3 * kH * 4;           // float [ceil(64/ns)][16] combine weights
-  static constexpr int kOffBar = kOffW + 64 * 16 * 4;           // raw, S done, O halves done, merge rows
-  static constexpr int kOffTmem = kOffBar + 5 * 8;
-  // merge: the staged partial rows ([64][kPartRow]) and later the received rows
-  // ([ns][heads of this CTA][kPartRow]) use the q and key tiles
-  static_assert(75 * kPartRow <= 2 * 8 * kAtom, "received rows (at most 75 for 1..16 chunks) fit the q and key tiles");
+  static constexpr int kQAtom = 8192;                           // 64 rows x 128 B (q, P)
+  static constexpr int kKAtom = kTcKeys * 128;                  // 80 key rows x 128 B
+  static constexpr int kOffQ = 0;                               // 8 q atoms
+  static constexpr int kOffK = kOffQ + 8 * kQAtom;              // 8 key atoms
+  static constexpr int kOffP = kOffK + 8 * kKAtom;              // 2 P atoms: keys 0-63, keys 64-79
+  static constexpr int kOffRaw = kOffP + 2 * kQAtom;            // [kTcKeys][kRawStride]
+  static constexpr int kOffKind = kOffRaw + kTcKeys * kRawStride;  // int[kTcKeys]
+  static constexpr int kOffStat = kOffKind + kTcKeys * 4;       // float m[64], l[64], sink[64]
+  static constexpr int kOffW = kOffStat + 3 * kH * 4;           // float [64][16]: softmax exchange, combine weights
+  static constexpr int kOffBar = kOffW + 64 * 16 * 4;           // raw, S done, O halves done, merge rows, q
+  static constexpr int kOffTmem = kOffBar + 6 * 8;
   static constexpr int kBytes = kOffTmem + 8;
   static constexpr int kAlloc = kBytes + 1024;                  // the base is rounded up to 1024 B
-  // the MMAs read 64 rows past the q tile and past the P tile
-  static_assert(kOffK == kOffQ + 8 * kAtom && kOffRaw >= kOffP + kAtom + 0, "operand padding rows stay in bounds");
-  static_assert(kCK * kRawStride >= kAtom, "rows past P stay inside the staging area");
+  // merge: the staged partial rows ([64][kPartRow]) and later the received rows
+  // ([ns][heads of this CTA][kPartRow]) use the q and key tiles
+  static_assert(75 * kPartRow <= 8 * kQAtom + 8 * kKAtom, "received rows (at most 75 for 1..16 chunks) fit the q and key tiles");
+  // the M = 128 MMAs read 64 rows past the last q atom (into the keys) and past the last P atom (into the staging)
+  static_assert(8 * kKAtom >= kQAtom && kTcKeys * kRawStride >= kQAtom, "operand padding rows stay in bounds");
+  static_assert(kKAtom % 1024 == 0 && kOffK % 1024 == 0 && kOffP % 1024 == 0, "swizzle atoms are 1024-B aligned");
+  static_assert(kAlloc <= 227 * 1024, "one CTA per SM");
 };
-constexpr int kTcWorkers = 512;              // dequantisation, softmax, readout, combine
-constexpr int kTcThreads = kTcWorkers + 32;  // + one warp that issues the MMAs
-constexpr int kTcMmaThread = kTcWorkers;
+constexpr int kTcWorkers = 640;              // dequantisation (80 keys x 8 blocks per wave), softmax, readout, combine
+constexpr int kTcThreads = kTcWorkers;       // 20 warps: 5 per SM sub-partition, up to 96 registers a thread
+constexpr int kTcMmaThread = 19 * 32;         // issues the copies and MMAs; its warp takes no part in softmax or readout
 constexpr uint32_t kTmemCols = 512;  // O: 2 x 256 columns; S (64 columns) shares the second half
 
 struct TcParams {
@@ -632,7 +635,7 @@ struct TcParams {
   void* out;
   float* lse;
   int kv_ready;   // gather the keys before the dependency wait
-  int nsplit;     // CTAs (64-key chunks) per row = cluster size
+  int nsplit;     // CTAs (80-key chunks) per row = cluster size
   uint8_t* part;  // [T][nsplit][64][kPartRow]: O / sum of each chunk and (max, sum), log2 units
   uint32_t* err;
 };
@@ -736,7 +739,8 @@ __device__ __forceinline__ float ex2_approx(float x) {
 }
 
 
-__global__ void __launch_bounds__(kTcThreads, 1) sparse_attn_tc_kernel(const __grid_constant__ TcParams p) {
+__global__ void __launch_bounds__(kTcThreads, 1)
+    sparse_attn_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ TcParams p) {
   extern __shared__ uint8_t tc_smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(tc_smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = sm + TcSmem::kOffQ;
@@ -752,6 +756,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) sparse_attn_tc_kernel(const __g
   uint64_t* bar_s = bar_raw + 1;
   uint64_t* bar_o = bar_raw + 2;  // [2]
   uint64_t* bar_m = bar_raw + 4;  // merge rows received
+  uint64_t* bar_q = bar_raw + 5;  // the row's q tile
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(sm + TcSmem::kOffTmem);
 
   const int tid = threadIdx.x;
@@ -762,11 +767,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) sparse_attn_tc_kernel(const __g
   const int t = p.t_base + tl;
 
   if (tid == 0) {
-    mbar_init(bar_raw, kCK);
+    mbar_init(bar_raw, kTcKeys);
     mbar_init(bar_s, 1);
     mbar_init(bar_o, 1);
     mbar_init(bar_o + 1, 1);
     mbar_init(bar_m, 1);
+    mbar_init(bar_q, 1);
     fence_mbar_init();
   }
   if (warp == 0) {
@@ -783,9 +789,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) sparse_attn_tc_kernel(const __g
   // launches earlier (every launch before the previous one has completed when
   // this CTA starts), else after it; then the row's q and the sink
   auto issue_records = [&]() {
-    if (tid < kCK) {
+    if (tid < kTcKeys) {
       int kind;
-      const int slot = key_slot_tc(p, t, rank * kCK + tid, &kind);
+      const int slot = key_slot_tc(p, t, rank * kTcKeys + tid, &kind);
       sKind[tid] = kind;
       if (kind == 0) {
         mbar_arrive(bar_raw);
@@ -797,41 +803,24 @@ __global__ void __launch_bounds__(kTcThreads, 1) sparse_attn_tc_kernel(const __g
       }
     }
   };
-  if (p.kv_ready) issue_records();
-  pdl_wait();
-  pdl_trigger();
-  if (!p.kv_ready) issue_records();
-  if (tid < kH) sSink[tid] = __ldg(p.sink + tid) * kLog2e;
-  if (tid < kTcWorkers) {
-    // 4096 chunks of 16 B (8 dims): chunk c -> head c / 64, dims 8 * (c % 64)
-    const uint4* qg = reinterpret_cast<const uint4*>(p.q + static_cast<long long>(t) * kH * kD);
-    uint4 v[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) v[j] = ld_cg_v4(qg + tid + j * kTcWorkers);
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const int c = tid + j * kTcWorkers;
-      const int h = c >> 6, c64 = c & 63;
-      *reinterpret_cast<uint4*>(sQ + (c64 >> 3) * TcSmem::kAtom + h * 128 + (((c64 & 7) ^ (h & 7)) << 4)) = v[j];
-    }
-  }
-
-  // ---- dequantise in two waves of 4 atoms (256 dims); thread -> key tid % 64,
-  // 32-dim block tid / 64 of the wave.  The S MMAs of the first wave's atoms
-  // run while the second wave is dequantised.
-  //   S = q K^T  -> TMEM columns 256..319
-  bool ok = mbar_wait(bar_raw, 0u, nullptr);
-  if (!ok) set_error(p.err, kErrTimeout);
-  const unsigned kmask_lo = __ballot_sync(0xffffffffu, ok && sKind[lane] != 0);
-  const unsigned kmask_hi = __ballot_sync(0xffffffffu, ok && sKind[32 + lane] != 0);
-#pragma unroll 1
-  for (int wave = 0; wave < 2; ++wave) {
+  // ---- dequantisation: two waves of 4 atoms (256 dims); thread -> key tid % 80,
+  // 32-dim block tid / 80 of the wave.  S = q K^T -> TMEM columns 256..335.
+  bool ok = true;
+  unsigned kmask[3] = {0u, 0u, 0u};  // keys 0-31, 32-63, 64-79 present
+  auto wait_records = [&]() {
+    ok = mbar_wait(bar_raw, 0u, nullptr);
+    if (!ok) set_error(p.err, kErrTimeout);
+    kmask[0] = __ballot_sync(0xffffffffu, ok && sKind[lane] != 0);
+    kmask[1] = __ballot_sync(0xffffffffu, ok && sKind[32 + lane] != 0);
+    kmask[2] = __ballot_sync(0xffffffffu, ok && lane < kTcKeys - 64 && sKind[64 + lane] != 0);
+  };
+  auto dequant_wave = [&](int wave) {  // every thread calls (it ends in a barrier)
     if (tid < kTcWorkers) {
-      const int key = tid & (kCK - 1);
-      const int b = (tid >> 6) + 8 * wave;
+      const int key = tid % kTcKeys;
+      const int b = tid / kTcKeys + 8 * wave;
       uint4 o[4];
       dequant_block32(sRaw + key * kRawStride, ok ? sKind[key] : 0, b, o);
-      uint8_t* row = sK + (b >> 1) * TcSmem::kAtom + key * 128;
+      uint8_t* row = sK + (b >> 1) * TcSmem::kKAtom + key * 128;
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const int c = ((b & 1) << 2) + j;
@@ -841,43 +830,81 @@ __global__ void __launch_bounds__(kTcThreads, 1) sparse_attn_tc_kernel(const __g
     }
     tc_fence_before();
     __syncthreads();
-    if (tid == kTcMmaThread) {
-      tc_fence_after();
-      constexpr uint32_t idesc = idesc_bf16_f32(128, 64, 0, 0);
+  };
+  auto issue_s = [&](int wave) {  // the MMA thread, once q and the wave's keys are in place
+    tc_fence_after();
+    constexpr uint32_t idesc = idesc_bf16_f32(128, kTcKeys, 0, 0);
 #pragma unroll
-      for (int a = 4 * wave; a < 4 * wave + 4; ++a) {
+    for (int a = 4 * wave; a < 4 * wave + 4; ++a) {
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          umma_bf16(tmem + 256, smem_desc_sw128(sQ + a * TcSmem::kAtom + kk * 32),
-                    smem_desc_sw128(sK + a * TcSmem::kAtom + kk * 32), idesc, (a | kk) != 0 ? 1u : 0u);
-        }
+      for (int kk = 0; kk < 4; ++kk) {
+        umma_bf16(tmem + 256, smem_desc_sw128(sQ + a * TcSmem::kQAtom + kk * 32),
+                  smem_desc_sw128(sK + a * TcSmem::kKAtom + kk * 32), idesc, (a | kk) != 0 ? 1u : 0u);
       }
-      if (wave == 1) mma_commit(bar_s);
     }
+    if (wave == 1) mma_commit(bar_s);
+  };
+  auto wait_q = [&]() {
+    if (!mbar_wait(bar_q, 0u, nullptr)) set_error(p.err, kErrTimeout);
+  };
+
+  if (p.kv_ready) {  // the keys are ready before the previous launch completes
+    issue_records();
+    wait_records();
+    dequant_wave(0);
+    dequant_wave(1);
+  }
+  pdl_wait();
+  pdl_trigger();
+  // the row's q: eight 64-head x 64-dim atoms, swizzled by the tensor copy
+  if (tid == kTcMmaThread) {
+    mbar_arrive_expect_tx(bar_q, kH * kD * 2);
+#pragma unroll
+    for (int a = 0; a < 8; ++a)
+      tma_load_2d(sQ + a * TcSmem::kQAtom, &map_q, a * 128, t * kH, bar_q, l2_policy_evict_first());
+  }
+  if (tid < kH) sSink[tid] = __ldg(p.sink + tid) * kLog2e;
+  if (p.kv_ready) {
+    if (tid == kTcMmaThread) {
+      wait_q();
+      issue_s(0);
+      issue_s(1);
+    }
+  } else {  // the first wave's S MMAs run while the second wave is dequantised
+    issue_records();
+    wait_records();
+    dequant_wave(0);
+    if (tid == kTcMmaThread) {
+      wait_q();
+      issue_s(0);
+    }
+    dequant_wave(1);
+    if (tid == kTcMmaThread) issue_s(1);
   }
 
-  // ---- softmax of the chunk: warps 0-1 (keys 0-31) and 4-5 (keys 32-63) read
-  // TMEM lanes 0-63, one head per thread; the two halves exchange max and sum
-  float* sMx = sW;           // [2][64] half maxima (the combine weights reuse it later)
-  float* sSx = sW + 2 * kH;  // [2][64] half sums
-  if ((warp & 3) < 2 && warp < 8) {
-    const int half = warp >> 2;  // 0: keys 0-31, 1: keys 32-63
+  // ---- softmax of the chunk: warps 0-1 (keys 0-31), 4-5 (keys 32-63) and 8-9
+  // (keys 64-79) read TMEM lanes 0-63, one head per thread; the three key
+  // groups exchange max and sum through shared memory
+  float* sMx = sW;           // [3][64] group maxima (the combine weights reuse the area later)
+  float* sSx = sW + 3 * kH;  // [3][64] group sums
+  if ((warp & 3) < 2 && warp < 12) {
+    const int grp = warp >> 2;  // keys 32 grp .. 32 grp + 31
     const int h = (warp & 3) * 32 + lane;
     bool oks = mbar_wait(bar_s, 0u, nullptr);
     if (!oks) set_error(p.err, kErrTimeout);
     tc_fence_after();
     float v[32];
-    tmem_ld32(tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + 256 + 32 * half, v);
-    const unsigned km = (half ? kmask_hi : kmask_lo);
+    tmem_ld32(tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + 256 + 32 * grp, v);
+    const unsigned km = kmask[grp];  // keys past 79 are never set
     float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
     for (int j = 0; j < 32; ++j) {
       v[j] = ((km >> j) & 1u) && oks ? v[j] * p.scale_log2 : -INFINITY;
       mx[j & 3] = fmaxf(mx[j & 3], v[j]);
     }
-    sMx[half * kH + h] = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
-    named_bar_sync(1, 128);
-    const float m = fmaxf(sMx[h], sMx[kH + h]);
+    sMx[grp * kH + h] = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+    named_bar_sync(1, 192);
+    const float m = fmaxf(fmaxf(sMx[h], sMx[kH + h]), sMx[2 * kH + h]);
     float sum[4] = {0.f, 0.f, 0.f, 0.f};
     uint32_t pk[16];
 #pragma unroll
@@ -887,18 +914,22 @@ __global__ void __launch_bounds__(kTcThreads, 1) sparse_attn_tc_kernel(const __g
       sum[(j >> 1) & 3] += e0 + e1;
       pk[j / 2] = pack_bf16(e0, e1);
     }
-    sSx[half * kH + h] = (sum[0] + sum[1]) + (sum[2] + sum[3]);
-    uint8_t* prow = sP + h * 128;
+    sSx[grp * kH + h] = (sum[0] + sum[1]) + (sum[2] + sum[3]);
+    // P rows: keys 0-63 in atom 0 (chunks 0-7), keys 64-79 in chunks 0-1 of atom 1
+    uint8_t* prow = sP + (grp >> 1) * TcSmem::kQAtom + h * 128;
+    const int nc = (grp < 2) ? 4 : (kTcKeys - 64) / 8;
 #pragma unroll
     for (int c4 = 0; c4 < 4; ++c4) {
-      const int c = 4 * half + c4;
-      *reinterpret_cast<uint4*>(prow + ((c ^ (h & 7)) << 4)) =
-          make_uint4(pk[4 * c4], pk[4 * c4 + 1], pk[4 * c4 + 2], pk[4 * c4 + 3]);
+      if (c4 < nc) {
+        const int c = 4 * (grp & 1) + c4;
+        *reinterpret_cast<uint4*>(prow + ((c ^ (h & 7)) << 4)) =
+            make_uint4(pk[4 * c4], pk[4 * c4 + 1], pk[4 * c4 + 2], pk[4 * c4 + 3]);
+      }
     }
-    named_bar_sync(1, 128);
-    if (half == 0) {
+    named_bar_sync(1, 192);
+    if (grp == 0) {
       sM[h] = m;
-      sL[h] = sSx[h] + sSx[kH + h];
+      sL[h] = (sSx[h] + sSx[kH + h]) + sSx[2 * kH + h];
     }
     fence_proxy_async_smem();
   }
@@ -913,9 +944,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) sparse_attn_tc_kernel(const __g
 #pragma unroll
     for (int hh = 0; hh < 2; ++hh) {
 #pragma unroll
-      for (int kk = 0; kk < 4; ++kk) {
-        umma_bf16(tmem + 256 * hh, smem_desc_sw128(sP + kk * 32),
-                  smem_desc_sw128_mn(sK + 4 * hh * TcSmem::kAtom + kk * 2048, TcSmem::kAtom, 1024), idesc,
+      for (int kk = 0; kk < kTcKeys / 16; ++kk) {  // 16 keys per step: P atom kk / 4, V rows 16 kk ..
+        umma_bf16(tmem + 256 * hh, smem_desc_sw128(sP + (kk >> 2) * TcSmem::kQAtom + (kk & 3) * 32),
+                  smem_desc_sw128_mn(sK + 4 * hh * TcSmem::kKAtom + kk * 2048, TcSmem::kKAtom, 1024), idesc,
                   kk != 0 ? 1u : 0u);
       }
       mma_commit(bar_o + hh);  // dims 0-255 done: bar_o[0]; dims 256-511: bar_o[1]
@@ -927,7 +958,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) sparse_attn_tc_kernel(const __g
   // scratch.  Warps of TMEM lane quadrants 0-1, four column groups of 128.
   const long long rowbase = static_cast<long long>(tl) * ns;
   uint8_t* sStage = sm + TcSmem::kOffQ;  // [64][kPartRow]
-  if ((warp & 3) < 2 && tid < kTcWorkers) {
+  if ((warp & 3) < 2 && warp < 16) {
     const int qd = warp & 3, g = warp >> 2;
     const int h = qd * 32 + lane;
     bool oko = mbar_wait(bar_o + (g >> 1), 0u, nullptr);  // column groups 0-1: dims 0-255
@@ -1006,22 +1037,17 @@ __global__ void __launch_bounds__(kTcThreads, 1) sparse_attn_tc_kernel(const __g
   for (int task = tid; task < nh * (kD / 8); task += kTcThreads) {
     const int li = task >> 6, c = task & 63;
     const int h = hb + li;
-    uint4 pv[kMaxCluster];
-#pragma unroll
-    for (int r = 0; r < kMaxCluster; ++r)
-      if (r < ns) pv[r] = *reinterpret_cast<const uint4*>(sRecv + (r * nh + li) * kPartRow + 16 * c);
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
+    for (int r = 0; r < ns; ++r) {
+      const uint4 pv = *reinterpret_cast<const uint4*>(sRecv + (r * nh + li) * kPartRow + 16 * c);
+      const float w = sW[li * 16 + r];
+      const uint32_t wv[4] = {pv.x, pv.y, pv.z, pv.w};
 #pragma unroll
-    for (int r = 0; r < kMaxCluster; ++r) {
-      if (r < ns) {
-        const float w = sW[li * 16 + r];
-        const uint32_t wv[4] = {pv[r].x, pv[r].y, pv[r].z, pv[r].w};
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const float2 f2 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wv[j]));
-          acc[2 * j] = fmaf(w, f2.x, acc[2 * j]);
-          acc[2 * j + 1] = fmaf(w, f2.y, acc[2 * j + 1]);
-        }
+      for (int j = 0; j < 4; ++j) {
+        const float2 f2 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wv[j]));
+        acc[2 * j] = fmaf(w, f2.x, acc[2 * j]);
+        acc[2 * j + 1] = fmaf(w, f2.y, acc[2 * j + 1]);
       }
     }
     const long long oo = (static_cast<long long>(t) * kH + h) * kD + 8 * c;
@@ -1053,11 +1079,11 @@ int attn_num_splits(int T, int n_keys, int num_sms) {
   return (nchunks + cps - 1) / cps;
 }
 
-// The tensor-core path takes rows of 1..16 chunks (up to 1024 keys), one CTA
+// The tensor-core path takes rows of 1..16 chunks (up to 1280 keys), one CTA
 // per chunk, in launches of at most kTcRowsPerLaunch rows sharing one scratch.
 constexpr int kTcRowsPerLaunch = 256;
 static bool use_tc_path(int n_keys) {
-  const int nchunks = (n_keys + kCK - 1) / kCK;
+  const int nchunks = (n_keys + kTcKeys - 1) / kTcKeys;
   return nchunks >= 1 && nchunks <= kMaxCluster;
 }
 static size_t tc_part_bytes(int rows, int nchunks) {
@@ -1067,14 +1093,14 @@ static size_t tc_part_bytes(int rows, int nchunks) {
 size_t attn_workspace_bytes(int T, int n_keys, int num_sms) {
   (void)num_sms;
   if (!use_tc_path(n_keys)) return 0;  // the split-K kernel merges on chip
-  const int nchunks = (n_keys + kCK - 1) / kCK;
+  const int nchunks = (n_keys + kTcKeys - 1) / kTcKeys;
   const int rows = T < kTcRowsPerLaunch ? T : kTcRowsPerLaunch;
   return tc_part_bytes(rows, nchunks);
 }
 
 static cudaError_t launch_sparse_attn_tc(const AttnLaunch& a, void* ws, const DeviceCtx& ctx, cudaStream_t st) {
   const int L = a.n_swa + a.k;
-  const int nchunks = (L + kCK - 1) / kCK;
+  const int nchunks = (L + kTcKeys - 1) / kTcKeys;
   TcParams p;
   p.q = reinterpret_cast<const __nv_bfloat16*>(a.q);
   p.main_kv = a.main_kv;
@@ -1095,9 +1121,12 @@ static cudaError_t launch_sparse_attn_tc(const AttnLaunch& a, void* ws, const De
   p.kv_ready = a.kv_ready;
   p.nsplit = nchunks;
   p.err = ctx.err;
-  const int rows_max = a.T < kTcRowsPerLaunch ? a.T : kTcRowsPerLaunch;
-  (void)rows_max;
   p.part = static_cast<uint8_t*>(ws);
+  // q viewed as [T*64 rows of 1024 B]; a 128-B x 64-row box is one swizzled atom
+  CUtensorMap map_q;
+  if (encode_tmap_2d_u8(&map_q, a.q, static_cast<uint64_t>(kD) * 2, static_cast<uint64_t>(a.T) * kH,
+                        static_cast<uint64_t>(kD) * 2, 128, kH) != CUDA_SUCCESS)
+    return cudaErrorInvalidValue;
   cudaError_t e = prefer_max_smem(sparse_attn_tc_kernel, TcSmem::kAlloc);
   if (e != cudaSuccess) return e;
   if (nchunks > 8) {
@@ -1121,7 +1150,7 @@ static cudaError_t launch_sparse_attn_tc(const AttnLaunch& a, void* ws, const De
     attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    e = cudaLaunchKernelEx(&cfg, sparse_attn_tc_kernel, p);
+    e = cudaLaunchKernelEx(&cfg, sparse_attn_tc_kernel, map_q, p);
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;
