@@ -65,6 +65,10 @@ constexpr int kThreads = 64 + kEpiGroups * 128;
 
 template <int NQ>
 struct IdxCfg {
+  // decode: the two epilogue groups take alternate tiles; prefill: both groups
+  // read every accumulator.  Each epilogue warp of a tile releases its stage
+  // once it has read the key scales.
+  static constexpr int kEpiWarpsPerTile = (NQ == 1) ? 4 : 8;
   // decode runs two CTAs per SM (two producers per SM measured ~1.5x the HBM
   // throughput of one CTA with deeper staging); prefill one CTA with 6 stages
   static constexpr int kStages = (NQ == 1) ? 4 : 6;
@@ -158,7 +162,7 @@ __global__ void __launch_bounds__(kThreads, IdxCfg<NQ>::kCtasPerSm)
     *s_abort = 0;
     for (int i = 0; i < S; ++i) {
       mbar_init(&full[i], 1);
-      mbar_init(&empty[i], 1 + 4);  // MMA commit + one arrival per epilogue warp
+      mbar_init(&empty[i], 1 + Cfg::kEpiWarpsPerTile);  // MMA commit + one arrival per epilogue warp of the tile
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&qfull[i], 1);
@@ -166,7 +170,7 @@ __global__ void __launch_bounds__(kThreads, IdxCfg<NQ>::kCtasPerSm)
     }
     for (int i = 0; i < NA; ++i) {
       mbar_init(&tfull[i], 1);
-      mbar_init(&tempty[i], 4);   // the four warps of the epilogue group owning this accumulator
+      mbar_init(&tempty[i], Cfg::kEpiWarpsPerTile);  // the epilogue warps reading this accumulator
     }
     fence_mbar_init();
     prefetch_tmap(&map_q);
@@ -249,15 +253,18 @@ __global__ void __launch_bounds__(kThreads, IdxCfg<NQ>::kCtasPerSm)
           s_lookup[lane] = rid;
         }
         __syncwarp();
-        // lane 0 switches q when the row changes, reserves a stage per tile of
-        // the group and announces its bytes; the copies are then issued by lane
-        // 0 (scan: 2 pages per tile) or by one lane per copy source (gather: 16
-        // candidate blocks per tile, whose serial issue would dominate)
+        // The whole warp walks the group's tiles in step (a warp whose lanes
+        // wait at different points measurably slows the epilogue warps sharing
+        // its scheduler): it switches q when the row changes, reserves a stage
+        // per tile and lane 0 announces its bytes.  The copies are issued by
+        // lane 0 (scan: 2 pages per tile; q: one lane per head box in prefill)
+        // or, after the walk, by one lane per copy source (gather: 16
+        // candidate blocks per tile, whose serial issue would dominate).
         const long long it0 = it;  // tile j of the group uses stage (it0 + j) % S
         int ntile = 0;
-        if (lane == 0) {
+        {
           int qb = find_qb(s_prefix, nqb, g0);
-          for (int j = 0; j < GT && g0 + j < g_end && ok; ++j, ++it) {
+          for (int j = 0; j < GT && g0 + j < g_end; ++j, ++it) {
             const long long g = g0 + j;
             while (g >= s_prefix[qb + 1]) ++qb;
             if (qb != cur_qb) {
@@ -265,39 +272,47 @@ __global__ void __launch_bounds__(kThreads, IdxCfg<NQ>::kCtasPerSm)
               const int slot = qcount & 1;
               if (!(ok = mbar_wait(&qempty[slot], ((qcount >> 1) & 1) ^ 1, s_abort))) break;
               const int t0 = (MODE == kModeScan) ? qb * NQ : qb;
-              mbar_arrive_expect_tx(&qfull[slot], Cfg::kQBytes);
-              tma_load_2d(s_q + slot * Cfg::kQBytes, &map_q, 0, t0 * 32, &qfull[slot], pol_q);
+              if (lane == 0) mbar_arrive_expect_tx(&qfull[slot], Cfg::kQBytes);
+              __syncwarp();
+              if (NQ == 1) {
+                if (lane == 0) tma_load_2d(s_q + slot * Cfg::kQBytes, &map_q, 0, t0 * 32, &qfull[slot], pol_q);
+              } else {
+                // head-major tile: rows h * NQ + j hold head h of query t0 + j
+                tma_load_2d(s_q + slot * Cfg::kQBytes + lane * NQ * kRowBytes, &map_q, lane * kRowBytes, t0,
+                            &qfull[slot], pol_q);
+              }
               ++qcount;
             }
             const int s = static_cast<int>(it % S);
             if (!(ok = mbar_wait(&empty[s], static_cast<uint32_t>((it / S) & 1) ^ 1u, s_abort))) break;
             constexpr int kRows = (MODE == kModeScan) ? 64 : 8;  // key rows per copy
-            uint32_t bytes = 0;
-#pragma unroll
-            for (int c = 0; c < SLOTS; ++c)
-              if (s_lookup[j * SLOTS + c] >= 0) bytes += kRows * (kRowBytes + 4);
-            mbar_arrive_expect_tx(&full[s], bytes);
             ntile = j + 1;
-            if (MODE == kModeScan) {
-              uint8_t* kdst = s_keys + s * Cfg::kKeyBytes;
-              float* sdst = s_scales + s * kTileKeys;
+            if (lane == 0) {
+              uint32_t bytes = 0;
 #pragma unroll
-              for (int c = 0; c < SLOTS; ++c) {
-                const int rid = s_lookup[j * SLOTS + c];
-                if (rid < 0) continue;
-                const int phys = rid / kPageRows;
-                const int r = rid - phys * kPageRows;
-                tma_load_2d(kdst + c * kRows * kRowBytes, &map_kv, 0, rid, &full[s], pol_keys);
-                bulk_load(sdst + c * kRows, p.index_k + static_cast<long long>(phys) * 8448 + 8192 + r * 4,
-                          kRows * 4, &full[s], pol_keys);
+              for (int c = 0; c < SLOTS; ++c)
+                if (s_lookup[j * SLOTS + c] >= 0) bytes += kRows * (kRowBytes + 4);
+              mbar_arrive_expect_tx(&full[s], bytes);
+              if (MODE == kModeScan) {
+                uint8_t* kdst = s_keys + s * Cfg::kKeyBytes;
+                float* sdst = s_scales + s * kTileKeys;
+#pragma unroll
+                for (int c = 0; c < SLOTS; ++c) {
+                  const int rid = s_lookup[j * SLOTS + c];
+                  if (rid < 0) continue;
+                  const int phys = rid / kPageRows;
+                  const int r = rid - phys * kPageRows;
+                  tma_load_2d(kdst + c * kRows * kRowBytes, &map_kv, 0, rid, &full[s], pol_keys);
+                  bulk_load(sdst + c * kRows, p.index_k + static_cast<long long>(phys) * 8448 + 8192 + r * 4,
+                            kRows * 4, &full[s], pol_keys);
+                }
               }
             }
+            __syncwarp();
           }
         }
         ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-        it = __shfl_sync(0xffffffffu, it, 0);
         if (MODE == kModeGather) {
-          ntile = __shfl_sync(0xffffffffu, ntile, 0);
           const int j = lane / SLOTS, c = lane % SLOTS;
           const int rid = s_lookup[lane];
           if (j < ntile && rid >= 0) {
@@ -351,6 +366,140 @@ __global__ void __launch_bounds__(kThreads, IdxCfg<NQ>::kCtasPerSm)
           mma_e4m3(d, adesc + 2 * k, bdesc + 2 * k, idesc, k > 0 ? 1u : 0u);
         mma_commit(&tfull[a]);
         mma_commit(&empty[s]);
+      }
+      if (!ok) {
+        *s_abort = 1;
+        set_error(p.err, kErrTimeout);
+      }
+    } else if (warp >= 2 && NQ == 8) {
+      // ------------------------------------------------------------ prefill epilogue
+      // The accumulator's columns are head-major (column 8 h + j: head h of
+      // query t0 + j).  Both groups read every accumulator: group g reads the
+      // 16-lane half g of its warp's lane quadrant, as eight 16x256b.x4 loads
+      // of 32 columns (heads 4c .. 4c+3), each issued before the previous one
+      // is consumed.  Lane l gets rows ra = 16 g + l/4 and ra + 8 of the
+      // quadrant for queries qa = t0 + 2 (l % 4) and qa + 1, so its 64 head
+      // weights stay in registers and a key's head sum needs no exchange
+      // between threads.  The accumulator is released as soon as it has been
+      // read; the key scales, the stores and the block maxima follow.
+      const int grp = (warp - 2) >> 2;
+      const int quad = warp & 3;
+      const int pc = lane & 3, prr = lane >> 2;
+      const int ra = quad * 32 + grp * 16 + prr;
+      const uint32_t lane_addr = static_cast<uint32_t>(quad * 32 + grp * 16) << 16;
+      uint64_t wq[32];  // wq[h] = (w'[qa][h], w'[qa + 1][h])
+      int Ea = 0, Eb = 0, ta = 0;
+      int qb = find_qb(s_prefix, nqb, g_begin);
+      int cur_qb = -1;
+      uint32_t a = 0, aph = 0;  // accumulator ring position and phase
+      uint32_t st = 0, sph = 0;  // key stage and its phase
+      bool ok = true;
+      for (long long g = g_begin; g < g_end; ++g) {
+        while (g >= s_prefix[qb + 1]) ++qb;
+        const int kb = static_cast<int>(g - s_prefix[qb]);
+        if (qb != cur_qb) {
+          cur_qb = qb;
+          const int t0 = qb * NQ;
+          const int b = s_seq[qb];
+          ta = t0 + 2 * pc;
+          const int tb = ta + 1;
+          const float* wa = p.w + static_cast<long long>(ta) * 32;
+          const float* sa = p.q_scale + static_cast<long long>(ta) * 32;
+#pragma unroll
+          for (int h = 0; h < 32; ++h)
+            wq[h] = pack_f32x2(ta < T ? __ldg(wa + h) * __ldg(sa + h) : 0.f,
+                               tb < T ? __ldg(wa + 32 + h) * __ldg(sa + 32 + h) : 0.f);
+          Ea = (ta < T) ? visible_of(p.rows, ta, b) : 0;
+          Eb = (tb < T) ? visible_of(p.rows, tb, b) : 0;
+        }
+        const uint32_t ca = a, cph = aph, cs = st, csph = sph;
+        if (++a == static_cast<uint32_t>(NA)) {
+          a = 0;
+          aph ^= 1u;
+        }
+        if (++st == static_cast<uint32_t>(S)) {
+          st = 0;
+          sph ^= 1u;
+        }
+        // on a timeout the warp keeps walking the tiles without waiting
+        if (ok) ok = mbar_wait(&tfull[ca], cph, s_abort);
+        if (!ok) continue;
+        tc_fence_after();
+        const uint32_t tbase = tmem_base + ca * Cfg::kAccCols + lane_addr;
+        uint64_t accA0 = 0, accA1 = 0, accB0 = 0, accB1 = 0;  // (qa, qa + 1) of rows ra / ra + 8
+        uint32_t v0[16], v1[16];
+        tmem_ld16x256_x4(tbase, v0);
+        tmem_wait_ld16(v0);
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          uint32_t(&cur)[16] = (c & 1) ? v1 : v0;
+          uint32_t(&nxt)[16] = (c & 1) ? v0 : v1;
+          if (c + 1 < 8) tmem_ld16x256_x4(tbase + (c + 1) * 32, nxt);
+#pragma unroll
+          for (int n = 0; n < 4; ++n) {
+            const uint64_t xa = pack_f32x2(fmaxf(__uint_as_float(cur[4 * n + 0]), 0.f),
+                                           fmaxf(__uint_as_float(cur[4 * n + 1]), 0.f));
+            const uint64_t xb = pack_f32x2(fmaxf(__uint_as_float(cur[4 * n + 2]), 0.f),
+                                           fmaxf(__uint_as_float(cur[4 * n + 3]), 0.f));
+            if (n & 1) {
+              accA1 = fma_f32x2(xa, wq[4 * c + n], accA1);
+              accB1 = fma_f32x2(xb, wq[4 * c + n], accB1);
+            } else {
+              accA0 = fma_f32x2(xa, wq[4 * c + n], accA0);
+              accB0 = fma_f32x2(xb, wq[4 * c + n], accB0);
+            }
+          }
+          if (c + 1 < 8) tmem_wait_ld16(nxt);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tempty[ca]);
+        // The accumulator is free again.  The stage's key scales are read only
+        // now, off the path from one MMA to the next; the stage is released
+        // after that read.
+        if (ok) ok = mbar_wait(&full[cs], csph, s_abort);
+        if (!ok) continue;
+        const float ksA = s_scales[cs * kTileKeys + ra], ksB = s_scales[cs * kTileKeys + ra + 8];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[cs]);
+        const float2 a0 = unpack_f32x2(accA0), a1 = unpack_f32x2(accA1);
+        const float2 b0 = unpack_f32x2(accB0), b1 = unpack_f32x2(accB1);
+        const int posA = kb * kTileKeys + ra, posB = posA + 8;
+        const int tb = ta + 1;
+        // scores (row, query): [0] (ra, qa), [1] (ra, qa+1), [2] (ra+8, qa), [3] (ra+8, qa+1)
+        float sc[4];
+        sc[0] = posA < Ea ? (a0.x + a1.x) * ksA : -INFINITY;
+        sc[1] = posA < Eb ? (a0.y + a1.y) * ksA : -INFINITY;
+        sc[2] = posB < Ea ? (b0.x + b1.x) * ksB : -INFINITY;
+        sc[3] = posB < Eb ? (b0.y + b1.y) * ksB : -INFINITY;
+        if (ta < T) {
+          if (posA < p.ld_out) p.out[static_cast<long long>(ta) * p.ld_out + posA] = sc[0];
+          if (posB < p.ld_out) p.out[static_cast<long long>(ta) * p.ld_out + posB] = sc[2];
+        }
+        if (tb < T) {
+          if (posA < p.ld_out) p.out[static_cast<long long>(tb) * p.ld_out + posA] = sc[1];
+          if (posB < p.ld_out) p.out[static_cast<long long>(tb) * p.ld_out + posB] = sc[3];
+        }
+        if (p.block_max != nullptr) {
+          // rows ra of the 8 lanes sharing lane % 4 are one block of 8 entries
+          // (posA is a multiple of 8 on lane / 4 == 0), rows ra + 8 the next
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            sc[e] = fmaxf(sc[e], __shfl_xor_sync(0xffffffffu, sc[e], 4));
+            sc[e] = fmaxf(sc[e], __shfl_xor_sync(0xffffffffu, sc[e], 8));
+            sc[e] = fmaxf(sc[e], __shfl_xor_sync(0xffffffffu, sc[e], 16));
+          }
+          if (prr == 0) {
+            const int blk = posA >> 3;
+            const int na = (Ea + 7) / 8, nb = (Eb + 7) / 8;
+            float* bma = p.block_max + static_cast<long long>(ta) * p.ld_bm;
+            float* bmb = p.block_max + static_cast<long long>(tb) * p.ld_bm;
+            if (ta < T && blk < na && blk < p.ld_bm) bma[blk] = sc[0];
+            if (tb < T && blk < nb && blk < p.ld_bm) bmb[blk] = sc[1];
+            if (ta < T && blk + 1 < na && blk + 1 < p.ld_bm) bma[blk + 1] = sc[2];
+            if (tb < T && blk + 1 < nb && blk + 1 < p.ld_bm) bmb[blk + 1] = sc[3];
+          }
+        }
       }
       if (!ok) {
         *s_abort = 1;
@@ -432,7 +581,11 @@ __global__ void __launch_bounds__(kThreads, IdxCfg<NQ>::kCtasPerSm)
         if (ok) ok = mbar_wait(&full[s], static_cast<uint32_t>((it / S) & 1), s_abort);  // acquire the scales
         if (!ok) continue;
         tc_fence_after();
+        // the key scale is read first, so the stage goes back to the producer
+        // while the accumulator is still being read
         const float ks = s_scales[s * kTileKeys + r];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
 #pragma unroll 1
         for (int j = 0; j < NQ; ++j) {
           float v[32];
@@ -474,10 +627,7 @@ __global__ void __launch_bounds__(kThreads, IdxCfg<NQ>::kCtasPerSm)
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(&tempty[a]);
-          mbar_arrive(&empty[s]);
-        }
+        if (lane == 0) mbar_arrive(&tempty[a]);
       }
       if (hist_on && cur_qb >= 0) {
         named_bar_sync(1 + grp, 128);
@@ -506,8 +656,13 @@ cudaError_t launch_variant(const IndexLaunch& a, const DeviceCtx& ctx, cudaStrea
     return cudaErrorInvalidValue;
   }
   CUtensorMap map_q, map_kv;
-  if (encode_tmap_2d_u8(&map_q, a.q_fp8, kRowBytes, static_cast<uint64_t>(a.rows.T) * 32, kRowBytes, kRowBytes,
-                        NQ * 32) != CUDA_SUCCESS) {
+  // decode: q as [T * 32 rows of 128 B], one 32-row box per query; prefill: q
+  // as [T rows of 32 * 128 B], boxes of one head (128 B) x NQ queries
+  const CUresult qe = (NQ == 1) ? encode_tmap_2d_u8(&map_q, a.q_fp8, kRowBytes, static_cast<uint64_t>(a.rows.T) * 32,
+                                                    kRowBytes, kRowBytes, 32)
+                                : encode_tmap_2d_u8(&map_q, a.q_fp8, 32 * kRowBytes, static_cast<uint64_t>(a.rows.T),
+                                                    32 * kRowBytes, kRowBytes, NQ);
+  if (qe != CUDA_SUCCESS) {
     *why = "tensor map of q could not be encoded";
     return cudaErrorInvalidValue;
   }

@@ -78,10 +78,9 @@ def test_bad_page_id_is_reported_not_faulted():
     assert csa2.check_device_error() == 0     # the record is cleared
 
 
-@pytest.mark.parametrize("T,ratio", [(64, 2), (100, 1)])
-def test_prefill_query_blocked_path(T, ratio):
+@pytest.mark.parametrize("T,ratio,n_entries", [(64, 2, 3000), (100, 1, 3000), (203, 2, 20000)])
+def test_prefill_query_blocked_path(T, ratio, n_entries):
     dev = need_gpu()
-    n_entries = 3000
     pc = W.make_paged_cache([n_entries], seed=9, device=dev, with_main=False)
     iq = W.make_indexer_query(T, seed=10, device=dev)
     # queries at the end of the context, causal visibility (pos + 1) // m
@@ -102,3 +101,12 @@ def test_prefill_query_blocked_path(T, ratio):
         got = np_(scores[t])
         assert_scores_close(got[:e], ref, f"row {t}")
         assert np.all(np.isneginf(got[e:min(ld, (e + 127) // 128 * 128)]))
+    # block maxima: exactly the max of the kernel's own scores over each block of
+    # 8 visible entries; blocks past the visible ones are not written
+    s_all, bm_all = np_(scores), np_(bm)
+    for t in range(T):
+        e = o.visible_entries(first + t, ratio)
+        nb = (e + 7) // 8
+        want = np.maximum.reduceat(np.where(np.arange(nb * 8) < e, s_all[t, :nb * 8], -np.inf), np.arange(0, nb * 8, 8))
+        assert np.array_equal(bm_all[t, :nb], want.astype(np.float32)), f"block maxima of row {t}"
+        assert np.all(bm_all[t, nb:] == 7.0), f"row {t}: block maxima written past the visible blocks"
