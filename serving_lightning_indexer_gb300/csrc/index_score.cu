@@ -15,15 +15,23 @@
 // The contraction D[key, (query, head)] = K8 . Q8^T (K = 128) runs as
 // tcgen05.mma kind::f8f6f4 with keys on M = 128 and (query, head) on N,
 // both operands TMA-staged in the 128-byte swizzle layout, the fp32
-// accumulator in TMEM (double-buffered).  The epilogue reads one key row per
-// thread (tcgen05.ld 32x32b), applies ReLU, the head weights, the per-key
-// scale, the visibility mask, and emits the 8-entry block maxima used by the
-// candidate pool.
+// accumulator in TMEM (a ring of 4 in decode, 2 in prefill).  The epilogue
+// applies ReLU, the head weights, the per-key scale and the visibility mask,
+// and emits the 8-entry block maxima used by the candidate pool:
+//   * decode / Reindex: one key row per thread (tcgen05.ld 32x32b), head
+//     weights broadcast from shared memory, score and block-max histograms
+//     for the selection kernels;
+//   * prefill: q is staged head-major (row 8 h + j = head h of query j), so a
+//     16x256b load gives each thread two queries of a key pair and all 64 of
+//     its head weights stay in registers (packed fp32x2 FMA, ReLU split
+//     between the ALU and FMA pipes).
 //
-// Roles (320 threads): warp 0 = TMA producer, warp 1 = TMEM owner + MMA
-// issuer, warps 2..9 = two epilogue groups taking alternate tiles (warp w
-// reads TMEM lanes 32*(w%4)...).  The accumulator ring (4 buffers in decode,
-// 2 in prefill) lets the MMA run ahead of both groups.
+// Roles (320 threads): warp 0 = TMA producer (the whole warp walks the stage
+// loop), warp 1 = TMEM owner + MMA issuer, warps 2..9 = two epilogue groups
+// (warp w reads TMEM lanes 32*(w%4)...).  In decode the groups take alternate
+// tiles; in prefill both read every accumulator (group g the 16-lane half g
+// of each lane quadrant) and release it before the key scales, stores and
+// block maxima, so the next MMA starts as early as possible.
 #include <math.h>
 
 #include "csa2_device.cuh"
@@ -70,8 +78,8 @@ struct IdxCfg {
   // once it has read the key scales.
   static constexpr int kEpiWarpsPerTile = (NQ == 1) ? 4 : 8;
   // decode runs two CTAs per SM (two producers per SM measured ~1.5x the HBM
-  // throughput of one CTA with deeper staging); prefill one CTA with 6 stages
-  static constexpr int kStages = (NQ == 1) ? 4 : 6;
+  // throughput of one CTA with deeper staging); prefill one CTA with 8 stages
+  static constexpr int kStages = (NQ == 1) ? 4 : 8;
   static constexpr int kCtasPerSm = (NQ == 1) ? 2 : 1;
   static constexpr int kNumAcc = (NQ == 1) ? 4 : 2;  // TMEM accumulator ring
   static constexpr int kQBytes = NQ * 32 * kRowBytes;
@@ -111,6 +119,23 @@ __device__ __forceinline__ int qb_tiles(const IdxParams& p, int qb, int* seq, in
   *emax_out = emax;
   if (MODE == kModeGather) return (p.pool_n * 8 + kTileKeys - 1) / kTileKeys;
   return (emax + kTileKeys - 1) / kTileKeys;
+}
+
+// ReLU on two pipes (prefill epilogue).  A dot product of two FP8 e4m3 vectors
+// of 128 elements is below 128 * 448^2 < 2^25 in magnitude, so a saturating
+// multiply by 2^-25 (clamp to [0, 1], on the FMA pipe) returns ReLU(x) * 2^-25
+// exactly; the head weight of such a head is stored times 2^25, so the product
+// w' * ReLU(x) and every rounding step are those of the max-based form (on
+// the ALU pipe).  One head in four takes the multiply, which balances the two
+// pipes.
+constexpr float kSatUp = 33554432.f;  // 2^25
+__host__ __device__ constexpr bool kSatHead(int h) { return (h & 3) == 3; }
+__device__ __forceinline__ float relu_mixed(uint32_t bits, bool sat) {
+  const float x = __uint_as_float(bits);
+  if (!sat) return fmaxf(x, 0.f);
+  float y;
+  asm("mul.rn.sat.f32 %0, %1, 0f33000000;" : "=f"(y) : "f"(x));  // x * 2^-25 clamped to [0, 1]
+  return y;
 }
 
 __device__ __forceinline__ int find_qb(const int* prefix, int nqb, long long g) {
@@ -406,9 +431,11 @@ __global__ void __launch_bounds__(kThreads, IdxCfg<NQ>::kCtasPerSm)
           const float* wa = p.w + static_cast<long long>(ta) * 32;
           const float* sa = p.q_scale + static_cast<long long>(ta) * 32;
 #pragma unroll
-          for (int h = 0; h < 32; ++h)
-            wq[h] = pack_f32x2(ta < T ? __ldg(wa + h) * __ldg(sa + h) : 0.f,
-                               tb < T ? __ldg(wa + 32 + h) * __ldg(sa + 32 + h) : 0.f);
+          for (int h = 0; h < 32; ++h) {
+            const float k = kSatHead(h) ? kSatUp : 1.f;
+            wq[h] = pack_f32x2(ta < T ? __ldg(wa + h) * __ldg(sa + h) * k : 0.f,
+                               tb < T ? __ldg(wa + 32 + h) * __ldg(sa + 32 + h) * k : 0.f);
+          }
           Ea = (ta < T) ? visible_of(p.rows, ta, b) : 0;
           Eb = (tb < T) ? visible_of(p.rows, tb, b) : 0;
         }
@@ -437,10 +464,9 @@ __global__ void __launch_bounds__(kThreads, IdxCfg<NQ>::kCtasPerSm)
           if (c + 1 < 8) tmem_ld16x256_x4(tbase + (c + 1) * 32, nxt);
 #pragma unroll
           for (int n = 0; n < 4; ++n) {
-            const uint64_t xa = pack_f32x2(fmaxf(__uint_as_float(cur[4 * n + 0]), 0.f),
-                                           fmaxf(__uint_as_float(cur[4 * n + 1]), 0.f));
-            const uint64_t xb = pack_f32x2(fmaxf(__uint_as_float(cur[4 * n + 2]), 0.f),
-                                           fmaxf(__uint_as_float(cur[4 * n + 3]), 0.f));
+            const bool sat = kSatHead(4 * c + n);
+            const uint64_t xa = pack_f32x2(relu_mixed(cur[4 * n + 0], sat), relu_mixed(cur[4 * n + 1], sat));
+            const uint64_t xb = pack_f32x2(relu_mixed(cur[4 * n + 2], sat), relu_mixed(cur[4 * n + 3], sat));
             if (n & 1) {
               accA1 = fma_f32x2(xa, wq[4 * c + n], accA1);
               accB1 = fma_f32x2(xb, wq[4 * c + n], accB1);
