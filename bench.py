@@ -282,8 +282,12 @@ def main():
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         ms_total = float(t.item())
 
-    # ---- end to end: pinned host inputs -> device, step, outputs -> pinned host
-    host_in, dev_in = [], []
+    # ---- end to end: pinned host inputs -> device, step, outputs -> pinned host.
+    # Every step copies all of its query-side inputs in and all 38 attention
+    # outputs out.  The copies run on two copy streams: layer l waits only for
+    # its own inputs, and its output is read back while later layers compute;
+    # the next step starts after the last read-back.
+    in_by_layer, h2d, host_out = {}, 0, {}
     for l in step.layers:
         li = step.inputs[l]
         ts = [li.attn.q]
@@ -291,21 +295,43 @@ def main():
             ts += [li.iq.q_fp8, li.iq.q_scale, li.iq.w]
         if li.C is not None:
             ts += [li.C] + ([li.Z] if li.Z is not None else [])
-        for t in ts:
-            host_in.append(t.detach().cpu().pin_memory())
-            dev_in.append(t)
-    host_out = [step.buf.out[l].detach().cpu().pin_memory() for l in step.layers]
-    h2d = sum(t.numel() * t.element_size() for t in host_in)
-    d2h = sum(t.numel() * t.element_size() for t in host_out)
+        in_by_layer[l] = [(t.detach().cpu().pin_memory(), t) for t in ts]
+        h2d += sum(t.numel() * t.element_size() for t in ts)
+        host_out[l] = step.buf.out[l].detach().cpu().pin_memory()
+    d2h = sum(t.numel() * t.element_size() for t in host_out.values())
+    cp_in = torch.cuda.Stream(device=dev)
+    cp_out = torch.cuda.Stream(device=dev)
     Ke = max(1, min(K, 20))
     g2 = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g2, stream=stream):
         for _ in range(Ke):
-            for h, d in zip(host_in, dev_in):
-                d.copy_(h, non_blocking=True)
+            begin = torch.cuda.Event()
+            begin.record(stream)
+            cp_in.wait_event(begin)
+            ready = {}
+            with torch.cuda.stream(cp_in):
+                for l in step.layers:
+                    for h, d in in_by_layer[l]:
+                        d.copy_(h, non_blocking=True)
+                    ready[l] = torch.cuda.Event()
+                    ready[l].record(cp_in)
+
+            def before(l, ready=ready):
+                stream.wait_event(ready[l])
+
+            def after(l):
+                done = torch.cuda.Event()
+                done.record(stream)
+                cp_out.wait_event(done)
+                with torch.cuda.stream(cp_out):
+                    host_out[l].copy_(step.buf.out[l], non_blocking=True)
+
+            step.before_layer, step.after_layer = before, after
             step.run(stream)
-            for h, l in zip(host_out, step.layers):
-                h.copy_(step.buf.out[l], non_blocking=True)
+            finished = torch.cuda.Event()
+            finished.record(cp_out)
+            stream.wait_event(finished)
+        step.before_layer = step.after_layer = None
     with torch.cuda.stream(stream):
         g2.replay()
     stream.synchronize()

@@ -128,6 +128,7 @@ class DecodeStep:
                      if c is not None}
         self.on_index_score = None   # optional hooks (event recording around the indexer scan)
         self.after_index_score = None
+        self.before_layer = None     # optional hook called with the layer number before its first call
         self.after_layer = None      # optional hook called with the layer number after its last call
 
     # ---------------------------------------------------------------- per-step work
@@ -150,6 +151,8 @@ class DecodeStep:
     def run(self, stream=None):
         b = self.buf
         for l in self.layers:
+            if self.before_layer:
+                self.before_layer(l)
             li = self.inputs[l]
             ci = cache_of(l)
             c = self.caches[ci]
