@@ -40,6 +40,10 @@ METRIC = "indexer keys scored/s + sparse-attn queries/s at 1M ctx; % of GB300 ro
 LENGTHS = [32768, 262144, 1 << 20, 1 << 20] * 2
 WORKLOAD = "csa2-decode-38layer-b8-ctx{32K,256K,1M,1M}x2"
 INDEX_KEY_BYTES = 132   # 128 e4m3 codes + one fp32 scale per key
+# one attention row (query-layer): q 64 x 512 bf16, 128 SWA records of 528 B,
+# 512 main-KV entries of 272 B (256 B codes + 16 scales), bf16 output, slots
+ATTN_ROW_BYTES = 65536 + 128 * 528 + 512 * 272 + 65536 + 640 * 4
+ATTN_ROW_FLOP = 2 * 2 * 64 * 640 * 512   # S = q K^T and O = P V
 
 
 def _scan_traffic_per_key():
@@ -69,6 +73,14 @@ def _peaks():
         return float(d["hbm_gbs"]), "measured"
     except Exception:
         return 6800.0, "fallback"
+
+
+def _bf16_peak():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops_sustained"])
+    except Exception:
+        return 1700.0
 
 
 class ClockSampler:
@@ -234,8 +246,17 @@ def main():
     def after_scan(layer):
         ev_pairs[-1][2] = side_event()
 
+    attn_pairs = []
+
+    def on_attn(layer):
+        attn_pairs.append([side_event(), None])
+
+    def after_attn(layer):
+        attn_pairs[-1][1] = side_event()
+
     g = torch.cuda.CUDAGraph()
     step.on_index_score, step.after_index_score = on_scan, after_scan
+    step.on_attn, step.after_attn = on_attn, after_attn
     with torch.cuda.graph(g, stream=stream):
         for _ in range(K):
             step.run(stream)
@@ -243,6 +264,7 @@ def main():
         join.record(side)
         stream.wait_event(join)
     step.on_index_score = step.after_index_score = None
+    step.on_attn = step.after_attn = None
     with torch.cuda.stream(stream):
         g.replay()                   # untimed: first replay of the instantiated graph
     stream.synchronize()
@@ -277,6 +299,7 @@ def main():
     for (l, _, _), ms in zip(ev_pairs, scan_ms):
         per_layer.setdefault(l, []).append(ms)
     scan_ms_total = sum(scan_ms)
+    attn_ms = [a.elapsed_time(b) for a, b in attn_pairs]
     if world > 1:
         t = torch.tensor([ms_total], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
@@ -354,6 +377,7 @@ def main():
         return
 
     peak, peak_kind = _peaks()
+    bf16_peak = _bf16_peak()
     traffic_per_key = _scan_traffic_per_key()
     ms_per_step = ms_total / K
     value = keys_per_step * K * world / (ms_total / 1e3)
@@ -391,6 +415,17 @@ def main():
                      "algorithmic_bytes_per_launch": scan_bytes_per_launch,
                      "avg_launch_ms": scan_ms_total / scan_launches, "launches_timed": scan_launches,
                      "per_layer_ms": {str(l): statistics.mean(v) for l, v in per_layer.items()}},
+        # the sparse attention, the step's largest time share: latency-bound at
+        # 8 rows a launch, reported beside the scan against both rooflines
+        "roofline_attention": {
+            "bound": "latency", "kernel": "sparse_attn_tc_kernel (8 rows x 64 heads x 640 keys)",
+            "avg_launch_ms": statistics.mean(attn_ms), "launches_timed": len(attn_ms),
+            "share_of_step": sum(attn_ms) / ms_total,
+            "algorithmic_bytes_per_launch": ATTN_ROW_BYTES * len(LENGTHS),
+            "hbm_frac": ATTN_ROW_BYTES * len(LENGTHS) / (statistics.mean(attn_ms) / 1e3) / 1e9 / peak,
+            "flop_per_launch": ATTN_ROW_FLOP * len(LENGTHS),
+            "bf16_tensor_frac": ATTN_ROW_FLOP * len(LENGTHS) / (statistics.mean(attn_ms) / 1e3) / 1e12 / bf16_peak,
+            "peaks": {"hbm_gbs": peak, "bf16_tflops": bf16_peak, "source": peak_kind}},
         "cpu_baseline": cpu,
         "e2e": {"value": keys_per_step * Ke * world / (e2e_ms / 1e3), "unit": "keys/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": Ke},

@@ -128,6 +128,8 @@ class DecodeStep:
                      if c is not None}
         self.on_index_score = None   # optional hooks (event recording around the indexer scan)
         self.after_index_score = None
+        self.on_attn = None          # optional hooks around the sparse attention call
+        self.after_attn = None
         self.before_layer = None     # optional hook called with the layer number before its first call
         self.after_layer = None      # optional hook called with the layer number after its last call
 
@@ -180,7 +182,11 @@ class DecodeStep:
             at = li.attn
             # a Reuse layer's slots and caches were written by its Full or Reindex
             # layer's calls, at least two launches back: its keys are gathered early
+            if self.on_attn:
+                self.on_attn(l)
             csa2.sparse_attn(at.q, c.pc.main_kv, b.topk_slot[ci], at.swa_kv, at.swa_slot, at.sink, b.out[l],
                              stream=stream, kv_ready=(role == "reuse"))
+            if self.after_attn:
+                self.after_attn(l)
             if self.after_layer:
                 self.after_layer(l)
