@@ -34,6 +34,7 @@ ATT_DIM = 512
 ROPE_DIMS = 64
 PAGE = 64                      # entries per page (DSA page, "KV pool")
 INDEX_PAGE_BYTES = PAGE * (IDX_DIM + 4)   # 64 x 128 B FP8 keys, then 64 x 4 B fp32 scales
+INDEX_FP4_PAGE_BYTES = PAGE * (IDX_DIM // 2 + 4)   # 64 x 64 B FP4 keys, then 64 x 4 ue8m0 scales
 MAIN_RECORD_BYTES = 288        # 256 B e2m1 codes + 16 B ue8m0 scales + 16 B pad
 SWA_RECORD_BYTES = 528         # 512 B e4m3 codes + 4 x fp32 scales (one per 128 channels)
 POOL_BLOCK = 8                 # candidate-pool block size (CSA2 page, "Hierarchical Sparse Indexer")
@@ -123,6 +124,34 @@ def index_k_at(cache: np.ndarray, page_table_row: np.ndarray, positions: np.ndar
     return FP8[codes] * scale[:, None]
 
 
+def index_k_fp4_at(cache: np.ndarray, page_table_row: np.ndarray, positions: np.ndarray) -> np.ndarray:
+    """Dequantised FP4 index keys [len(positions),128] at the given logical
+    positions of one sequence.
+
+    The CSA2 page and the V4.1 Q&A page store the index K in FP4 (68 B per
+    entry by the per-token byte count of the report reading: 890 B = 2.5 x
+    (288 + 68)).  Reading taken: 128 e2m1 codes in 64 bytes (element 2i in the
+    low nibble of byte i) and 4 ue8m0 scales, one per 32 dims (the MX block
+    format of the main-KV records).  A page holds 64 keys: first their 64 x 64
+    code bytes in order, then their 64 x 4 scale bytes.
+    """
+    cache = np.asarray(cache, dtype=np.uint8).reshape(-1, INDEX_FP4_PAGE_BYTES)
+    pos = np.asarray(positions, dtype=np.int64)
+    page = np.asarray(page_table_row, dtype=np.int64)[pos // PAGE]
+    off = pos % PAGE
+    data = cache[page[:, None], off[:, None] * (IDX_DIM // 2) + np.arange(IDX_DIM // 2)[None, :]]
+    codes = np.empty((len(pos), IDX_DIM), dtype=np.int64)
+    codes[:, 0::2] = data & 0xF
+    codes[:, 1::2] = data >> 4
+    u = cache[page[:, None], PAGE * (IDX_DIM // 2) + off[:, None] * 4 + np.arange(4)[None, :]]
+    return FP4[codes] * np.repeat(ue8m0(u), 32, axis=1)
+
+
+def index_k_fp4_entries(cache: np.ndarray, page_table_row: np.ndarray, n: int) -> np.ndarray:
+    """Dequantised FP4 index keys [n,128] of logical positions 0..n-1."""
+    return index_k_fp4_at(cache, page_table_row, np.arange(n))
+
+
 def main_kv_records(cache: np.ndarray, slots: np.ndarray) -> np.ndarray:
     """Dequantised main-KV vectors [len(slots),512] of the given physical slots.
 
@@ -172,9 +201,10 @@ def dequant_q(q8: np.ndarray, q_scale: np.ndarray) -> np.ndarray:
     return FP8[np.asarray(q8, dtype=np.int64)] * np.asarray(q_scale, dtype=np.float64)[:, None]
 
 
-def index_scores_row(q8, q_scale, w, cache, page_table_row, n_visible) -> np.ndarray:
-    """Scores of one query row over its n_visible entries (Full layer)."""
-    keys = index_k_entries(cache, page_table_row, n_visible)
+def index_scores_row(q8, q_scale, w, cache, page_table_row, n_visible, fp4=False) -> np.ndarray:
+    """Scores of one query row over its n_visible entries (Full layer); fp4
+    selects the FP4 index-K page format."""
+    keys = (index_k_fp4_entries if fp4 else index_k_entries)(cache, page_table_row, n_visible)
     return index_score_values(dequant_q(q8, q_scale), w, keys)
 
 
@@ -269,7 +299,7 @@ def pool_positions(pool_blocks: np.ndarray, n_visible: int, block: int = POOL_BL
     return np.where(valid, pos, -1)
 
 
-def reindex_scores(q8, q_scale, w, cache, page_table_row, n_visible, pool_blocks) -> np.ndarray:
+def reindex_scores(q8, q_scale, w, cache, page_table_row, n_visible, pool_blocks, fp4=False) -> np.ndarray:
     """Scores over the candidate list of a Reindex layer: [8*len(pool)], -inf for
     padding and invisible positions.
 
@@ -281,17 +311,17 @@ def reindex_scores(q8, q_scale, w, cache, page_table_row, n_visible, pool_blocks
     out = np.full(len(pos), -np.inf)
     ok = pos >= 0
     if ok.any():
-        keys_all = index_k_entries(cache, page_table_row, n_visible)
-        out[ok] = index_score_values(dequant_q(q8, q_scale), w, keys_all[pos[ok]])
+        keys = (index_k_fp4_at if fp4 else index_k_at)(cache, page_table_row, pos[ok])
+        out[ok] = index_score_values(dequant_q(q8, q_scale), w, keys)
     return out
 
 
-def reindex_topk(q8, q_scale, w, cache, page_table_row, n_visible, pool_blocks, k=512):
+def reindex_topk(q8, q_scale, w, cache, page_table_row, n_visible, pool_blocks, k=512, fp4=False):
     """Top-k positions of a Reindex layer: full-length score row with -inf outside
     the pool, then the ordinary top-k."""
     full = np.full(int(n_visible), -np.inf)
     pos = pool_positions(pool_blocks, n_visible)
-    sc = reindex_scores(q8, q_scale, w, cache, page_table_row, n_visible, pool_blocks)
+    sc = reindex_scores(q8, q_scale, w, cache, page_table_row, n_visible, pool_blocks, fp4=fp4)
     ok = pos >= 0
     full[pos[ok]] = sc[ok]
     return topk_positions(full, k)

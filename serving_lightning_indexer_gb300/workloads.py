@@ -22,6 +22,7 @@ PAGE = 64
 IDX_HEADS, IDX_DIM = 32, 128
 ATT_HEADS, ATT_DIM = 64, 512
 INDEX_PAGE_BYTES = PAGE * (IDX_DIM + 4)
+INDEX_FP4_PAGE_BYTES = PAGE * (IDX_DIM // 2 + 4)   # 64 x 64 B e2m1 codes, then 64 x 4 ue8m0 scales
 MAIN_RECORD_BYTES = 288
 SWA_RECORD_BYTES = 528
 SWA_WINDOW = 128
@@ -50,13 +51,14 @@ def fp8_encode(x: torch.Tensor):
 _FP4_MIDS = (0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0)
 
 
-def fp4_encode_records(x: torch.Tensor) -> torch.Tensor:
-    """288-byte main-KV records of x [n,512]: 512 e2m1 codes (element 2i in the
-    low nibble of byte i), 16 ue8m0 scales (one per 32 elements: the smallest
-    power of two 2^k with 6 * 2^k >= amax), 16 zero bytes."""
-    x = x.float().reshape(-1, ATT_DIM)
-    n = x.shape[0]
-    g = x.reshape(n, 16, 32)
+def fp4_encode_blocks(x: torch.Tensor):
+    """e2m1 codes of x [n,d] (d a multiple of 32) with one ue8m0 scale per 32
+    elements: the smallest power of two 2^k with 6 * 2^k >= amax, 127 for an
+    all-zero block.  Returns (codes uint8 [n,d//2], element 2i in the low nibble
+    of byte i; scales uint8 [n,d//32])."""
+    x = x.float()
+    n, d = x.shape
+    g = x.reshape(n, d // 32, 32)
     amax = g.abs().amax(dim=-1)
     safe = torch.where(amax > 0, amax, torch.full_like(amax, 6.0))
     k = torch.ceil(torch.log2(safe / 6.0))
@@ -70,10 +72,19 @@ def fp4_encode_records(x: torch.Tensor) -> torch.Tensor:
     for i, m in enumerate(_FP4_MIDS):
         code += (mag > m).int() if i % 2 == 0 else (mag >= m).int()
     code = code.clamp(max=7) | ((y < 0).int() << 3)
-    code = code.reshape(n, ATT_DIM)
-    rec = torch.zeros(n, MAIN_RECORD_BYTES, dtype=torch.uint8, device=x.device)
-    rec[:, :256] = (code[:, 0::2] | (code[:, 1::2] << 4)).to(torch.uint8)
-    rec[:, 256:272] = u.to(torch.uint8)
+    code = code.reshape(n, d)
+    return (code[:, 0::2] | (code[:, 1::2] << 4)).to(torch.uint8), u.to(torch.uint8)
+
+
+def fp4_encode_records(x: torch.Tensor) -> torch.Tensor:
+    """288-byte main-KV records of x [n,512]: 512 e2m1 codes (element 2i in the
+    low nibble of byte i), 16 ue8m0 scales (one per 32 elements), 16 zero
+    bytes."""
+    x = x.float().reshape(-1, ATT_DIM)
+    codes, u = fp4_encode_blocks(x)
+    rec = torch.zeros(x.shape[0], MAIN_RECORD_BYTES, dtype=torch.uint8, device=x.device)
+    rec[:, :256] = codes
+    rec[:, 256:272] = u
     return rec
 
 
@@ -98,7 +109,7 @@ class PagedCache:
     """One shared cache pair of a Full layer: the index-K pages and the main-KV
     records, addressed through the same page table (entry e of sequence b is
     slot page_table[b, e // 64] * 64 + e % 64 in both)."""
-    index_k: torch.Tensor          # uint8 [n_pages, 8448]
+    index_k: torch.Tensor          # uint8 [n_pages, 8448] (FP8 keys) or [n_pages, 4352] (FP4 keys)
     main_kv: torch.Tensor          # uint8 [n_pages * 64, 288]
     page_table: torch.Tensor       # int32 [B, pt_stride], -1 past the sequence
     n_entries: torch.Tensor        # int32 [B]
@@ -113,10 +124,12 @@ def _gen(seed: int, device) -> torch.Generator:
 
 def make_paged_cache(entries: list[int], seed: int, device="cpu", permute=True,
                      plant_dirs: torch.Tensor | None = None, plant_frac: float = 0.0,
-                     plant_shift: float = 3.0, with_main=True, chunk_pages=4096) -> PagedCache:
-    """Index-K pages (keys ~ N(0,1) -> e4m3 + fp32 scale per key) and main-KV
-    records (~ N(0,1) -> e2m1 + ue8m0/32) for sequences with the given entry
-    counts, pages of 64 in a random physical permutation.
+                     plant_shift: float = 3.0, with_main=True, chunk_pages=4096,
+                     index_fp4=False) -> PagedCache:
+    """Index-K pages (keys ~ N(0,1) -> e4m3 + fp32 scale per key, or with
+    index_fp4 e2m1 + one ue8m0 scale per 32 dims) and main-KV records (~ N(0,1)
+    -> e2m1 + ue8m0/32) for sequences with the given entry counts, pages of 64
+    in a random physical permutation.
 
     plant_dirs [B,128] (optional): for a random plant_frac of the 8-entry blocks
     of sequence b, plant_shift * unit(plant_dirs[b]) is added to the key before
@@ -153,7 +166,8 @@ def make_paged_cache(entries: list[int], seed: int, device="cpu", permute=True,
             pos = pos[pos < entries[b]]
             pp = page_table[b, (pos // PAGE)].long()
             mask[pp, pos % PAGE] = True
-    index_k = torch.empty(P, INDEX_PAGE_BYTES, dtype=torch.uint8, device=device)
+    index_k = torch.empty(P, INDEX_FP4_PAGE_BYTES if index_fp4 else INDEX_PAGE_BYTES, dtype=torch.uint8,
+                          device=device)
     main_kv = torch.empty(P * PAGE, MAIN_RECORD_BYTES, dtype=torch.uint8, device=device) if with_main else None
     for p0 in range(0, P, chunk_pages):
         p1 = min(P, p0 + chunk_pages)
@@ -161,9 +175,14 @@ def make_paged_cache(entries: list[int], seed: int, device="cpu", permute=True,
         if planted is not None:
             shift = units[owner[p0:p1]][:, None, :] * plant_shift           # [n,1,128]
             k = k + shift * mask[p0:p1, :, None].float()
-        codes, scale = fp8_encode(k)
-        index_k[p0:p1, :PAGE * IDX_DIM] = codes.reshape(p1 - p0, -1)
-        index_k[p0:p1, PAGE * IDX_DIM:] = scale.contiguous().view(torch.uint8).reshape(p1 - p0, -1)
+        if index_fp4:
+            codes, u = fp4_encode_blocks(k.reshape(-1, IDX_DIM))
+            index_k[p0:p1, :PAGE * IDX_DIM // 2] = codes.reshape(p1 - p0, -1)
+            index_k[p0:p1, PAGE * IDX_DIM // 2:] = u.reshape(p1 - p0, -1)
+        else:
+            codes, scale = fp8_encode(k)
+            index_k[p0:p1, :PAGE * IDX_DIM] = codes.reshape(p1 - p0, -1)
+            index_k[p0:p1, PAGE * IDX_DIM:] = scale.contiguous().view(torch.uint8).reshape(p1 - p0, -1)
         if with_main:
             x = torch.randn((p1 - p0) * PAGE, ATT_DIM, generator=g, device=device)
             main_kv[p0 * PAGE:p1 * PAGE] = fp4_encode_records(x)

@@ -111,3 +111,70 @@ def test_index_page_layout_roundtrip():
     codes = pc.index_k[page, row * 128:(row + 1) * 128].numpy()
     scale = pc.index_k[page, 8192 + row * 4:8192 + row * 4 + 4].numpy().view(np.float32)[0]
     assert np.array_equal(e1[69], o.FP8[codes.astype(np.int64)] * np.float64(scale))
+
+
+def _fp4_page_by_hand(codes, u):
+    """One FP4 index-K page [4352] from codes [64,128] (0..15) and scales [64,4]."""
+    codes = np.asarray(codes, dtype=np.uint8)
+    page = np.zeros(4352, dtype=np.uint8)
+    page[:4096] = (codes[:, 0::2] | (codes[:, 1::2] << 4)).reshape(-1)
+    page[4096:] = np.asarray(u, dtype=np.uint8).reshape(-1)
+    return page
+
+
+def test_fp4_index_page_hand_values():
+    # key 5: dims 0..31 scale 2^0, 32..63 scale 2^-1, 64..95 scale 2^2, 96..127 scale 2^-3;
+    # codes: dim 0 -> +6 (0x7), dim 1 -> -0.5 (0x9), dim 32 -> +3 (0x5), dim 127 -> -4 (0xE)
+    codes = np.zeros((64, 128), dtype=np.uint8)
+    u = np.full((64, 4), 127, dtype=np.uint8)
+    codes[5, 0], codes[5, 1], codes[5, 32], codes[5, 127] = 0x7, 0x9, 0x5, 0xE
+    u[5] = [127, 126, 129, 124]
+    page = _fp4_page_by_hand(codes, u)
+    # byte-level layout: byte 5*64 holds dims 0 (low nibble) and 1 (high nibble)
+    assert page[5 * 64] == 0x97 and page[4096 + 5 * 4 + 2] == 129
+    k = o.index_k_fp4_at(page, np.array([0]), np.array([5]))[0]
+    want = np.zeros(128)
+    want[0], want[1], want[32], want[127] = 6.0, -0.5, 3.0 * 0.5, -4.0 * 0.125
+    assert np.array_equal(k, want)
+    assert o.INDEX_FP4_PAGE_BYTES == 4352 == 64 * 68   # 68 B per entry (report reading: 890 = 2.5 x (288 + 68))
+
+
+def test_fp4_index_keys_equal_fp8_index_keys_for_common_values():
+    # keys whose values are exact in both formats, written once as an FP4 page and
+    # once as an FP8 page (e4m3 codes times an fp32 scale of 2^-2): both decoders
+    # (the FP8 one pinned against torch) must return the same keys
+    rng = np.random.default_rng(7)
+    codes = rng.integers(0, 16, size=(64, 128)).astype(np.uint8)
+    u = rng.integers(124, 130, size=(64, 4)).astype(np.uint8)          # 2^-3 .. 2^2
+    fp4_page = _fp4_page_by_hand(codes, u)
+    vals = o.FP4[codes.astype(np.int64)] * np.repeat(o.ue8m0(u), 32, axis=1)   # in [-24, 24]
+    fp8_scale = np.float32(0.25)
+    e4m3 = torch.tensor(vals / 0.25, dtype=torch.float64).to(torch.float8_e4m3fn)
+    assert np.array_equal(e4m3.double().numpy() * 0.25, vals)           # exact in e4m3 too
+    fp8_page = np.zeros(8448, dtype=np.uint8)
+    fp8_page[:8192] = e4m3.view(torch.uint8).numpy().reshape(-1)
+    fp8_page[8192:] = np.full(64, fp8_scale, dtype=np.float32).view(np.uint8)
+    pt = np.array([0])
+    assert np.array_equal(o.index_k_fp4_entries(fp4_page, pt, 64), o.index_k_entries(fp8_page, pt, 64))
+    # and so the scores of both formats agree
+    q8 = rng.integers(0, 0x7E, size=(32, 128))
+    qs = rng.random(32) + 0.5
+    w = rng.standard_normal(32)
+    assert np.array_equal(o.index_scores_row(q8, qs, w, fp4_page, pt, 64, fp4=True),
+                          o.index_scores_row(q8, qs, w, fp8_page, pt, 64))
+
+
+def test_generator_fp4_index_pages_decode_near_the_fp8_keys():
+    # the same seeded keys written in both formats: the FP4 decode is within half
+    # an e2m1 grid step (x block scale) of the finer FP8 decode
+    pc8 = W.make_paged_cache([300], seed=5, with_main=False)
+    pc4 = W.make_paged_cache([300], seed=5, with_main=False, index_fp4=True)
+    assert pc4.index_k.shape[1] == 4352
+    assert torch.equal(pc8.page_table, pc4.page_table)
+    k8 = o.index_k_entries(pc8.index_k.numpy(), pc8.page_table[0].numpy(), 300)
+    k4 = o.index_k_fp4_entries(pc4.index_k.numpy(), pc4.page_table[0].numpy(), 300)
+    pages = pc4.index_k.numpy()[pc4.page_table[0].numpy()[np.arange(300) // 64]]
+    u = pages[np.arange(300)[:, None], 4096 + (np.arange(300) % 64)[:, None] * 4 + np.arange(4)[None, :]]
+    step = np.repeat(o.ue8m0(u), 32, axis=1)          # the widest e2m1 gap (4 -> 6) is 2 x scale
+    assert np.all(np.abs(k4 - k8) <= step + np.abs(k8) * 2.0 ** -4 + 1e-9)
+    assert np.abs(k4 - k8).mean() < 0.2
