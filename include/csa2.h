@@ -40,6 +40,10 @@
  *   index-K page : 8448 B = 64 keys x 128 e4m3 codes, then 64 fp32 scales
  *                  (DSA page, "KV pool").  Key s of a sequence is in physical
  *                  page page_table[b][s / 64], row s % 64.
+ *   FP4 index-K page: 4352 B = 64 keys x 64 B of 128 e2m1 codes (element 2i
+ *                  in the low nibble of byte i), then 64 x 4 ue8m0 scales (one
+ *                  per 32 dims); 68 B per entry (CSA2 page and V4.1 Q&A page:
+ *                  the index K is FP4; 890 B per token = 2.5 x (288 + 68)).
  *   main-KV record: 288 B at slot*288 = 256 B of 512 e2m1 codes (element 2i
  *                  in the low nibble of byte i), 16 ue8m0 scales (one per 32
  *                  elements, value 2^(u-127)), 16 B padding (CSA2 page,
@@ -81,10 +85,13 @@ typedef enum {
 enum {
   CSA2_IDX_HEADS = 32, CSA2_IDX_DIM = 128,
   CSA2_ATT_HEADS = 64, CSA2_ATT_DIM = 512, CSA2_ROPE_DIMS = 64,
-  CSA2_PAGE = 64, CSA2_INDEX_PAGE_BYTES = 8448,
+  CSA2_PAGE = 64, CSA2_INDEX_PAGE_BYTES = 8448, CSA2_INDEX_FP4_PAGE_BYTES = 4352,
   CSA2_MAIN_RECORD_BYTES = 288, CSA2_SWA_RECORD_BYTES = 528,
   CSA2_MAX_TOPK = 2048, CSA2_POOL_BLOCK = 8, CSA2_MAX_SWA = 128
 };
+
+/* Index-K page formats (the index_k_format field of the scoring calls). */
+enum { CSA2_INDEX_FP8 = 0, CSA2_INDEX_FP4 = 1 };
 
 /* Static description of a status code. */
 CSA2_API const char* csa2_status_string(int status);
@@ -116,14 +123,17 @@ typedef struct {
  * Written: scores[t][s] for s < round_up(E_t, 128) clipped to ld_scores
  * (s >= E_t holds -inf); block_max[t][j] = max over the visible positions of
  * block j (8 positions) for j < ceil(E_t / 8), if block_max is not NULL.
- * Alignment: q_fp8, index_k 16 B; ld_scores and ld_block_max multiples of 4.
+ * Alignment: q_fp8, index_k 16 B (32 B for FP4 pages); ld_scores and
+ * ld_block_max multiples of 4.
  * Prefill (row_pos given, B == 1, T >= 64) runs the query-blocked tensor-core
- * path (8 queries x 32 heads per MMA); everything else the per-row scan. */
+ * path (8 queries x 32 heads per MMA); everything else the per-row scan.
+ * FP4 index-K pages are scored on the per-row scan (CSA2_ERR_UNSUPPORTED on
+ * the prefill path): k = sum over its 4 blocks of 2^(u_b-127) * e2m1 codes. */
 typedef struct {
   const uint8_t* q_fp8;       /* [T,32,128] e4m3 codes */
   const float* q_scale;       /* [T,32] >= 0 */
   const float* w;             /* [T,32] head weights */
-  const uint8_t* index_k;     /* pages of 8448 B */
+  const uint8_t* index_k;     /* pages of 8448 B (FP8) or 4352 B (FP4) */
   int64_t index_k_pages;      /* number of pages in index_k */
   const int32_t* page_table;  /* [B, pt_stride] logical page -> physical page */
   int32_t pt_stride;
@@ -136,6 +146,7 @@ typedef struct {
    * T..2T-1, the newest block counted as +inf; zero when block_max is NULL).  Passing it on
    * to csa2_topk_with_candidates saves that call a pass over the scores. */
   uint32_t* hist;
+  int32_t index_k_format;     /* CSA2_INDEX_FP8 (0) or CSA2_INDEX_FP4 */
 } csa2_index_score_args;
 CSA2_API int csa2_index_score(const csa2_index_score_args* args, void* workspace, size_t ws_bytes, void* stream);
 
@@ -200,6 +211,7 @@ typedef struct {
   int32_t k;                                   /* 1..2048 */
   int32_t* topk_pos; int32_t* topk_slot; int64_t ld_topk;
   float* pool_scores;                          /* optional [T, 8*pool_n] */
+  int32_t index_k_format;                      /* CSA2_INDEX_FP8 (0) or CSA2_INDEX_FP4 */
 } csa2_reindex_args;
 CSA2_API int csa2_reindex(const csa2_reindex_args* args, void* workspace, size_t ws_bytes, void* stream);
 

@@ -33,7 +33,7 @@ class Rows(C.Structure):
 class IndexScoreArgs(C.Structure):
     _fields_ = [("q_fp8", _P), ("q_scale", _P), ("w", _P), ("index_k", _P), ("index_k_pages", _I64),
                 ("page_table", _P), ("pt_stride", _I32), ("rows", Rows), ("scores", _P), ("ld_scores", _I64),
-                ("block_max", _P), ("ld_block_max", _I64), ("hist", _P)]
+                ("block_max", _P), ("ld_block_max", _I64), ("hist", _P), ("index_k_format", _I32)]
 
 
 class TopkArgs(C.Structure):
@@ -45,7 +45,8 @@ class TopkArgs(C.Structure):
 class ReindexArgs(C.Structure):
     _fields_ = [("q_fp8", _P), ("q_scale", _P), ("w", _P), ("index_k", _P), ("index_k_pages", _I64),
                 ("page_table", _P), ("pt_stride", _I32), ("rows", Rows), ("pool_blocks", _P), ("pool_n", _I32),
-                ("k", _I32), ("topk_pos", _P), ("topk_slot", _P), ("ld_topk", _I64), ("pool_scores", _P)]
+                ("k", _I32), ("topk_pos", _P), ("topk_slot", _P), ("ld_topk", _I64), ("pool_scores", _P),
+                ("index_k_format", _I32)]
 
 
 class SparseAttnArgs(C.Structure):
@@ -146,6 +147,18 @@ def workspace(nbytes: int, device, tag: str = "main") -> torch.Tensor | None:
     return buf
 
 
+INDEX_FP8, INDEX_FP4 = 0, 1
+INDEX_PAGE_BYTES = {8448: INDEX_FP8, 4352: INDEX_FP4}
+
+
+def index_format(index_k) -> int:
+    """Page format of an index-K cache [n_pages, page bytes]: FP8 (8448 B) or FP4 (4352 B)."""
+    fmt = INDEX_PAGE_BYTES.get(int(index_k.shape[-1]))
+    if fmt is None:
+        raise ValueError(f"index-K pages of {index_k.shape[-1]} B: expected 8448 (FP8) or 4352 (FP4)")
+    return fmt
+
+
 def rows(T, B, row_seq=None, row_pos=None, n_visible=None, ratio_m=1) -> Rows:
     return Rows(T, B, _ptr(row_seq), _ptr(row_pos), _ptr(n_visible), ratio_m)
 
@@ -157,7 +170,7 @@ def index_score(q_fp8, q_scale, w, index_k, page_table, r: Rows, scores, block_m
     lib = load()
     a = IndexScoreArgs(_ptr(q_fp8), _ptr(q_scale), _ptr(w), _ptr(index_k), index_k.shape[0], _ptr(page_table),
                        page_table.shape[-1], r, _ptr(scores), scores.shape[-1], _ptr(block_max),
-                       block_max.shape[-1] if block_max is not None else 0, _ptr(hist))
+                       block_max.shape[-1] if block_max is not None else 0, _ptr(hist), index_format(index_k))
     _check(lib.csa2_index_score(C.byref(a), None, 0, _stream(stream)), "csa2_index_score")
 
 
@@ -195,7 +208,7 @@ def reindex(q_fp8, q_scale, w, index_k, page_table, r: Rows, pool_blocks, k, top
     lib = load()
     a = ReindexArgs(_ptr(q_fp8), _ptr(q_scale), _ptr(w), _ptr(index_k), index_k.shape[0], _ptr(page_table),
                     page_table.shape[-1], r, _ptr(pool_blocks), pool_blocks.shape[-1], k, _ptr(topk_pos),
-                    _ptr(topk_slot), topk_pos.shape[-1], _ptr(pool_scores))
+                    _ptr(topk_slot), topk_pos.shape[-1], _ptr(pool_scores), index_format(index_k))
     need = C.c_size_t(0)
     _check(lib.csa2_workspace_size(CALL_REINDEX, C.cast(C.byref(a), _P), C.byref(need)), "csa2_workspace_size")
     buf = ws if ws is not None else workspace(need.value, q_fp8.device, "reindex")

@@ -94,8 +94,7 @@ cudaError_t device_ctx(DeviceCtx* out) {
   return cudaSuccess;
 }
 
-CUresult encode_tmap_2d_u8(CUtensorMap* map, const void* base, uint64_t inner_bytes, uint64_t rows,
-                           uint64_t row_stride, uint32_t box_inner, uint32_t box_rows) {
+static PFN_cuTensorMapEncodeTiled_v12000 tmap_encoder() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   static std::once_flag once;
   std::call_once(once, [] {
@@ -106,6 +105,24 @@ CUresult encode_tmap_2d_u8(CUtensorMap* map, const void* base, uint64_t inner_by
         q == cudaDriverEntryPointSuccess)
       fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
   });
+  return fn;
+}
+
+CUresult encode_tmap_2d_fp4(CUtensorMap* map, const void* base, uint64_t rows, uint32_t box_rows) {
+  PFN_cuTensorMapEncodeTiled_v12000 fn = tmap_encoder();
+  if (!fn) return CUDA_ERROR_NOT_FOUND;
+  const cuuint64_t dims[2] = {128, rows};   // 4-bit elements per row, rows
+  const cuuint64_t strides[1] = {64};       // bytes
+  const cuuint32_t box[2] = {128, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
+CUresult encode_tmap_2d_u8(CUtensorMap* map, const void* base, uint64_t inner_bytes, uint64_t rows,
+                           uint64_t row_stride, uint32_t box_inner, uint32_t box_rows) {
+  PFN_cuTensorMapEncodeTiled_v12000 fn = tmap_encoder();
   if (!fn) return CUDA_ERROR_NOT_FOUND;
   const cuuint64_t dims[2] = {inner_bytes, rows};
   const cuuint64_t strides[1] = {row_stride};
@@ -143,10 +160,14 @@ const char* csa2_last_error_detail(void) { return g_detail.c_str(); }
 
 static int check_index_common(const uint8_t* q_fp8, const float* q_scale, const float* w, const uint8_t* index_k,
                               int64_t pages, const int32_t* pt, int32_t pt_stride, const csa2_rows& rows,
-                              const char* who) {
+                              int32_t format, const char* who) {
   if (!q_fp8 || !q_scale || !w || !index_k || !pt) return fail(CSA2_ERR_NULL, "%s: null input pointer", who);
+  if (format != CSA2_INDEX_FP8 && format != CSA2_INDEX_FP4)
+    return fail(CSA2_ERR_UNSUPPORTED, "%s: index_k_format=%d is neither FP8 (0) nor FP4 (1)", who, format);
   if (!aligned16(q_fp8) || !aligned16(index_k)) return fail(CSA2_ERR_ALIGN, "%s: q_fp8 and index_k must be 16-B aligned", who);
-  if (pages < 1 || pages * 66 > 0x7FFFFFFFLL) return fail(CSA2_ERR_SHAPE, "%s: index_k_pages=%lld out of range", who, (long long)pages);
+  if (format == CSA2_INDEX_FP4 && (reinterpret_cast<uintptr_t>(index_k) & 31))
+    return fail(CSA2_ERR_ALIGN, "%s: FP4 index_k pages must be 32-B aligned", who);
+  if (pages < 1 || pages * 68 > 0x7FFFFFFFLL) return fail(CSA2_ERR_SHAPE, "%s: index_k_pages=%lld out of range", who, (long long)pages);
   if (pt_stride < 1) return fail(CSA2_ERR_SHAPE, "%s: pt_stride must be >= 1", who);
   return rows_check(rows, who);
 }
@@ -156,7 +177,7 @@ int csa2_index_score(const csa2_index_score_args* a, void* ws, size_t ws_bytes, 
   (void)ws_bytes;
   if (!a) return fail(CSA2_ERR_NULL, "csa2_index_score: args is NULL");
   int rc = check_index_common(a->q_fp8, a->q_scale, a->w, a->index_k, a->index_k_pages, a->page_table, a->pt_stride,
-                              a->rows, "csa2_index_score");
+                              a->rows, a->index_k_format, "csa2_index_score");
   if (rc) return rc;
   if (!a->scores) return fail(CSA2_ERR_NULL, "csa2_index_score: scores is NULL");
   if (a->ld_scores < 1) return fail(CSA2_ERR_SHAPE, "csa2_index_score: ld_scores must be >= 1");
@@ -170,6 +191,8 @@ int csa2_index_score(const csa2_index_score_args* a, void* ws, size_t ws_bytes, 
     return fail(CSA2_ERR_SHAPE, "csa2_index_score: at most %d rows per call on this path", 2048 * nq);
   if (a->hist && prefill)
     return fail(CSA2_ERR_UNSUPPORTED, "csa2_index_score: hist is produced on the decode path only (pass NULL)");
+  if (prefill && a->index_k_format == CSA2_INDEX_FP4)
+    return fail(CSA2_ERR_UNSUPPORTED, "csa2_index_score: FP4 index-K pages are scored on the decode path only");
   if (a->hist && !aligned16(a->hist)) return fail(CSA2_ERR_ALIGN, "csa2_index_score: hist must be 16-B aligned");
   DeviceCtx ctx;
   cudaError_t e = csa2::device_ctx(&ctx);
@@ -180,6 +203,7 @@ int csa2_index_score(const csa2_index_score_args* a, void* ws, size_t ws_bytes, 
   L.w = a->w;
   L.index_k = a->index_k;
   L.n_pages = a->index_k_pages;
+  L.fp4 = a->index_k_format == CSA2_INDEX_FP4;
   L.page_table = a->page_table;
   L.pt_stride = a->pt_stride;
   L.rows = rows_host(a->rows);
@@ -265,7 +289,7 @@ static size_t reindex_ws(const csa2_reindex_args* a) {
 int csa2_reindex(const csa2_reindex_args* a, void* ws, size_t ws_bytes, void* stream) {
   if (!a) return fail(CSA2_ERR_NULL, "csa2_reindex: args is NULL");
   int rc = check_index_common(a->q_fp8, a->q_scale, a->w, a->index_k, a->index_k_pages, a->page_table, a->pt_stride,
-                              a->rows, "csa2_reindex");
+                              a->rows, a->index_k_format, "csa2_reindex");
   if (rc) return rc;
   if (a->rows.T > 2048) return fail(CSA2_ERR_SHAPE, "csa2_reindex: at most 2048 rows per call");
   if (!a->pool_blocks || !a->topk_pos) return fail(CSA2_ERR_NULL, "csa2_reindex: pool_blocks/topk_pos is NULL");
@@ -287,6 +311,7 @@ int csa2_reindex(const csa2_reindex_args* a, void* ws, size_t ws_bytes, void* st
   L.w = a->w;
   L.index_k = a->index_k;
   L.n_pages = a->index_k_pages;
+  L.fp4 = a->index_k_format == CSA2_INDEX_FP4;
   L.page_table = a->page_table;
   L.pt_stride = a->pt_stride;
   L.rows = rows_host(a->rows);

@@ -63,6 +63,7 @@ struct IndexLaunch {
   uint32_t* hist;
   const int* pool_blocks;
   int pool_n;
+  int fp4;  // index-K pages: 0 FP8 (8448 B), 1 FP4 (4352 B)
 };
 cudaError_t launch_index_tiles(const IndexLaunch& a, int mode, int nq, const DeviceCtx& ctx, cudaStream_t st,
                                const char** why);
@@ -161,6 +162,10 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
 }
 
 // Tensor-map encoder from the driver (fetched once through the runtime).
+// 2-D tensor map over rows of 128 packed e2m1 codes (64 B, row stride 64 B),
+// unpacked to 16-byte chunks in shared memory, 128-byte swizzle, boxes of
+// box_rows rows; base must be 32-byte aligned.
+CUresult encode_tmap_2d_fp4(CUtensorMap* map, const void* base, uint64_t rows, uint32_t box_rows);
 CUresult encode_tmap_2d_u8(CUtensorMap* map, const void* base, uint64_t inner_bytes, uint64_t rows,
                            uint64_t row_stride, uint32_t box_inner, uint32_t box_rows);
 

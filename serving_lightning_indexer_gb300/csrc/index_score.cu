@@ -45,7 +45,6 @@ constexpr int kModeScan = 0;
 constexpr int kModeGather = 1;
 constexpr int kTileKeys = 128;
 constexpr int kRowBytes = 128;                       // one FP8 key / one head of q
-constexpr int kPageRows = 66;                        // an 8448-B page seen as 66 rows of 128 B
 constexpr int kMaxQB = 2048;                         // query blocks per launch
 
 struct IdxParams {
@@ -71,7 +70,17 @@ constexpr int kHistBins = 2048;  // top 11 bits of the order-preserving key
 constexpr int kEpiGroups = 2;                        // epilogue groups of 4 warps, alternating tiles
 constexpr int kThreads = 64 + kEpiGroups * 128;
 
-template <int NQ>
+// Index-K page formats: FP8 (8448 B = 64 x 128 e4m3 codes + 64 fp32 scales,
+// seen as 66 rows of 128 B) and FP4 (4352 B = 64 x 64 B of e2m1 codes + 64 x
+// 4 ue8m0 scales, one per 32 dims, seen as 68 rows of 64 B).
+template <bool F4>
+struct PageFmt {
+  static constexpr int kBytes = F4 ? 4352 : 8448;
+  static constexpr int kRows = F4 ? 68 : 66;        // rows of the 2-D tensor view per page
+  static constexpr int kScaleOff = F4 ? 4096 : 8192;
+};
+
+template <int NQ, bool F4 = false>
 struct IdxCfg {
   // decode: the two epilogue groups take alternate tiles; prefill: both groups
   // read every accumulator.  Each epilogue warp of a tile releases its stage
@@ -81,9 +90,12 @@ struct IdxCfg {
   // throughput of one CTA with deeper staging); prefill one CTA with 8 stages
   static constexpr int kStages = (NQ == 1) ? 4 : 8;
   static constexpr int kCtasPerSm = (NQ == 1) ? 2 : 1;
-  static constexpr int kNumAcc = (NQ == 1) ? 4 : 2;  // TMEM accumulator ring
+  // TMEM accumulator ring.  FP4 keys: one 32-column accumulator per 32-dim
+  // block of the key (the MMA has no per-block scale here; the epilogue
+  // applies the ue8m0 block scales), 128 columns a tile.
+  static constexpr int kNumAcc = F4 ? 2 : ((NQ == 1) ? 4 : 2);
   static constexpr int kQBytes = NQ * 32 * kRowBytes;
-  static constexpr int kAccCols = NQ * 32;
+  static constexpr int kAccCols = F4 ? 4 * NQ * 32 : NQ * 32;
   static constexpr int kTmemCols = kNumAcc * kAccCols;
   static constexpr int kKeyBytes = kTileKeys * kRowBytes;
   static constexpr int kOffKeys = 0;
@@ -103,6 +115,7 @@ struct IdxCfg {
 };
 static_assert(128 == IdxCfg<1>::kTmemCols, "decode accumulators: 4 x 32 columns");
 static_assert(512 == IdxCfg<8>::kTmemCols, "prefill accumulators: 2 x 256 columns");
+static_assert(256 == IdxCfg<1, true>::kTmemCols, "FP4 decode accumulators: 2 x 128 columns");
 static_assert(kEpiGroups == 2 && IdxCfg<1>::kNumAcc % kEpiGroups == 0 && IdxCfg<8>::kNumAcc % kEpiGroups == 0,
               "each epilogue group owns the accumulators of its tiles");
 
@@ -138,6 +151,11 @@ __device__ __forceinline__ float relu_mixed(uint32_t bits, bool sat) {
   return y;
 }
 
+// Value 2^(u-127) of a ue8m0 scale byte (u = 0: 2^-127; u = 255: NaN).
+__device__ __forceinline__ float ue8m0_to_float(uint32_t u) {
+  return u == 0u ? __uint_as_float(0x00400000u) : (u == 255u ? __uint_as_float(0x7FC00000u) : __uint_as_float(u << 23));
+}
+
 __device__ __forceinline__ int find_qb(const int* prefix, int nqb, long long g) {
   int lo = 0, hi = nqb - 1;  // largest qb with prefix[qb] <= g
   while (lo < hi) {
@@ -147,11 +165,13 @@ __device__ __forceinline__ int find_qb(const int* prefix, int nqb, long long g) 
   return lo;
 }
 
-template <int NQ, int MODE>
-__global__ void __launch_bounds__(kThreads, IdxCfg<NQ>::kCtasPerSm)
+template <int NQ, int MODE, bool F4>
+__global__ void __launch_bounds__(kThreads, IdxCfg<NQ, F4>::kCtasPerSm)
     index_tiles_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_kv,
                        const __grid_constant__ IdxParams p) {
-  using Cfg = IdxCfg<NQ>;
+  using Cfg = IdxCfg<NQ, F4>;
+  using Fmt = PageFmt<F4>;
+  static_assert(!F4 || NQ == 1, "FP4 index keys on the decode scan and the Reindex gather");
   constexpr int S = Cfg::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -262,7 +282,7 @@ __global__ void __launch_bounds__(kThreads, IdxCfg<NQ>::kCtasPerSm)
               const int lp = kb * 2 + sl;
               if (lp * 64 < emax) {
                 const int phys = (lp < p.pt_stride) ? __ldg(ptab + lp) : -1;
-                if (phys >= 0 && phys < p.n_pages) rid = phys * kPageRows;
+                if (phys >= 0 && phys < p.n_pages) rid = phys * Fmt::kRows;
                 else set_error(p.err, kErrBounds);
               }
             } else {
@@ -270,7 +290,7 @@ __global__ void __launch_bounds__(kThreads, IdxCfg<NQ>::kCtasPerSm)
               const int blk = (cb < p.pool_n) ? __ldg(p.pool_blocks + static_cast<long long>(qbl) * p.pool_n + cb) : -1;
               if (blk >= 0 && blk * 8 < emax) {
                 const int phys = ((blk >> 3) < p.pt_stride) ? __ldg(ptab + (blk >> 3)) : -1;
-                if (phys >= 0 && phys < p.n_pages) rid = phys * kPageRows + (blk & 7) * 8;
+                if (phys >= 0 && phys < p.n_pages) rid = phys * Fmt::kRows + (blk & 7) * 8;
                 else set_error(p.err, kErrBounds);
               }
             }
@@ -311,12 +331,16 @@ __global__ void __launch_bounds__(kThreads, IdxCfg<NQ>::kCtasPerSm)
             const int s = static_cast<int>(it % S);
             if (!(ok = mbar_wait(&empty[s], static_cast<uint32_t>((it / S) & 1) ^ 1u, s_abort))) break;
             constexpr int kRows = (MODE == kModeScan) ? 64 : 8;  // key rows per copy
+            // bytes a key row adds to the stage's transaction count: the 128 B
+            // of an FP8 key; the 64 B of packed codes of an FP4 key (unpacked
+            // into 128 B of shared memory by the copy)
+            constexpr uint32_t kKeyTxBytes = F4 ? 64 : kRowBytes;
             ntile = j + 1;
             if (lane == 0) {
               uint32_t bytes = 0;
 #pragma unroll
               for (int c = 0; c < SLOTS; ++c)
-                if (s_lookup[j * SLOTS + c] >= 0) bytes += kRows * (kRowBytes + 4);
+                if (s_lookup[j * SLOTS + c] >= 0) bytes += kRows * (kKeyTxBytes + 4);
               mbar_arrive_expect_tx(&full[s], bytes);
               if (MODE == kModeScan) {
                 uint8_t* kdst = s_keys + s * Cfg::kKeyBytes;
@@ -325,10 +349,10 @@ __global__ void __launch_bounds__(kThreads, IdxCfg<NQ>::kCtasPerSm)
                 for (int c = 0; c < SLOTS; ++c) {
                   const int rid = s_lookup[j * SLOTS + c];
                   if (rid < 0) continue;
-                  const int phys = rid / kPageRows;
-                  const int r = rid - phys * kPageRows;
+                  const int phys = rid / Fmt::kRows;
+                  const int r = rid - phys * Fmt::kRows;
                   tma_load_2d(kdst + c * kRows * kRowBytes, &map_kv, 0, rid, &full[s], pol_keys);
-                  bulk_load(sdst + c * kRows, p.index_k + static_cast<long long>(phys) * 8448 + 8192 + r * 4,
+                  bulk_load(sdst + c * kRows, p.index_k + static_cast<long long>(phys) * Fmt::kBytes + Fmt::kScaleOff + r * 4,
                             kRows * 4, &full[s], pol_keys);
                 }
               }
@@ -343,11 +367,12 @@ __global__ void __launch_bounds__(kThreads, IdxCfg<NQ>::kCtasPerSm)
           if (j < ntile && rid >= 0) {
             constexpr int kRows = 8;
             const int s = static_cast<int>((it0 + j) % S);
-            const int phys = rid / kPageRows;
-            const int r = rid - phys * kPageRows;
+            const int phys = rid / Fmt::kRows;
+            const int r = rid - phys * Fmt::kRows;
             tma_load_2d(s_keys + s * Cfg::kKeyBytes + c * kRows * kRowBytes, &map_kv, 0, rid, &full[s], pol_keys);
             bulk_load(s_scales + s * kTileKeys + c * kRows,
-                      p.index_k + static_cast<long long>(phys) * 8448 + 8192 + r * 4, kRows * 4, &full[s], pol_keys);
+                      p.index_k + static_cast<long long>(phys) * Fmt::kBytes + Fmt::kScaleOff + r * 4, kRows * 4, &full[s],
+                      pol_keys);
           }
         }
         if (!ok) break;
@@ -364,7 +389,9 @@ __global__ void __launch_bounds__(kThreads, IdxCfg<NQ>::kCtasPerSm)
       }
     } else if (warp == 1 && lane == 0) {
       // ------------------------------------------------------------ MMA issuer
-      constexpr uint32_t idesc = idesc_e4m3_f32(128, NQ * 32);
+      // FP4 keys: A is e2m1 (format 5 of kind::f8f6f4), in the 16-byte chunks
+      // the tensor copy unpacks them to (8 bytes of codes, 8 bytes of gap)
+      constexpr uint32_t idesc = idesc_e4m3_f32(128, NQ * 32) | (F4 ? (5u << 7) : 0u);
       int qb = find_qb(s_prefix, nqb, g_begin);
       int cur_qb = -1, qcount = 0, slot = 0;
       long long it = 0;
@@ -387,8 +414,12 @@ __global__ void __launch_bounds__(kThreads, IdxCfg<NQ>::kCtasPerSm)
         const uint64_t bdesc = smem_desc_sw128(s_q + slot * Cfg::kQBytes);
         const uint32_t d = tmem_base + a * Cfg::kAccCols;
 #pragma unroll
-        for (int k = 0; k < 4; ++k)  // K = 128 bytes = 4 x 32 e4m3
-          mma_e4m3(d, adesc + 2 * k, bdesc + 2 * k, idesc, k > 0 ? 1u : 0u);
+        for (int k = 0; k < 4; ++k) {  // K = 128 = 4 steps of 32 elements (32 B of the swizzled rows)
+          if (F4)  // one accumulator per 32-dim block: the block scales differ
+            mma_e4m3(d + k * NQ * 32, adesc + 2 * k, bdesc + 2 * k, idesc, 0u);
+          else
+            mma_e4m3(d, adesc + 2 * k, bdesc + 2 * k, idesc, k > 0 ? 1u : 0u);
+        }
         mma_commit(&tfull[a]);
         mma_commit(&empty[s]);
       }
@@ -609,22 +640,55 @@ __global__ void __launch_bounds__(kThreads, IdxCfg<NQ>::kCtasPerSm)
         tc_fence_after();
         // the key scale is read first, so the stage goes back to the producer
         // while the accumulator is still being read
-        const float ks = s_scales[s * kTileKeys + r];
+        // FP8 keys: one fp32 scale per key; FP4 keys: four ue8m0 block scales
+        const float ks = F4 ? 1.f : s_scales[s * kTileKeys + r];
+        const uint32_t ub = F4 ? reinterpret_cast<const uint32_t*>(s_scales)[s * kTileKeys + r] : 0u;
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);
 #pragma unroll 1
         for (int j = 0; j < NQ; ++j) {
-          float v[32];
-          tmem_ld32(tmem_base + a * Cfg::kAccCols + j * 32 + (static_cast<uint32_t>(quad * 32) << 16), v);
+          const uint32_t tq = tmem_base + a * Cfg::kAccCols + (static_cast<uint32_t>(quad * 32) << 16);
           const float4* w4 = reinterpret_cast<const float4*>(s_wg + j * 32);
           float acc0 = 0.f, acc1 = 0.f;
+          if constexpr (F4) {
+            // q . k = sum over the 4 blocks of 2^(u_b - 127) * (q . e2m1 codes of
+            // block b); 16 heads at a time
+            float sb[4];
 #pragma unroll
-          for (int h4 = 0; h4 < 8; ++h4) {
-            const float4 ww = w4[h4];
-            acc0 = fmaf(ww.x, fmaxf(v[4 * h4 + 0], 0.f), acc0);
-            acc1 = fmaf(ww.y, fmaxf(v[4 * h4 + 1], 0.f), acc1);
-            acc0 = fmaf(ww.z, fmaxf(v[4 * h4 + 2], 0.f), acc0);
-            acc1 = fmaf(ww.w, fmaxf(v[4 * h4 + 3], 0.f), acc1);
+            for (int b = 0; b < 4; ++b) sb[b] = ue8m0_to_float((ub >> (8 * b)) & 0xFFu);
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+              float v[16];
+              tmem_ld32x16(tq + hh * 16, v);
+#pragma unroll
+              for (int i = 0; i < 16; ++i) v[i] *= sb[0];
+#pragma unroll
+              for (int b = 1; b < 4; ++b) {
+                float d[16];
+                tmem_ld32x16(tq + b * 32 + hh * 16, d);
+#pragma unroll
+                for (int i = 0; i < 16; ++i) v[i] = fmaf(d[i], sb[b], v[i]);
+              }
+#pragma unroll
+              for (int h4 = 0; h4 < 4; ++h4) {
+                const float4 ww = w4[4 * hh + h4];
+                acc0 = fmaf(ww.x, fmaxf(v[4 * h4 + 0], 0.f), acc0);
+                acc1 = fmaf(ww.y, fmaxf(v[4 * h4 + 1], 0.f), acc1);
+                acc0 = fmaf(ww.z, fmaxf(v[4 * h4 + 2], 0.f), acc0);
+                acc1 = fmaf(ww.w, fmaxf(v[4 * h4 + 3], 0.f), acc1);
+              }
+            }
+          } else {
+            float v[32];
+            tmem_ld32(tq + j * 32, v);
+#pragma unroll
+            for (int h4 = 0; h4 < 8; ++h4) {
+              const float4 ww = w4[h4];
+              acc0 = fmaf(ww.x, fmaxf(v[4 * h4 + 0], 0.f), acc0);
+              acc1 = fmaf(ww.y, fmaxf(v[4 * h4 + 1], 0.f), acc1);
+              acc0 = fmaf(ww.z, fmaxf(v[4 * h4 + 2], 0.f), acc0);
+              acc1 = fmaf(ww.w, fmaxf(v[4 * h4 + 3], 0.f), acc1);
+            }
           }
           const int t = t0 + j;
           const bool valid = pos >= 0 && pos < E[j];
@@ -673,9 +737,10 @@ __global__ void __launch_bounds__(kThreads, IdxCfg<NQ>::kCtasPerSm)
   }
 }
 
-template <int NQ, int MODE>
+template <int NQ, int MODE, bool F4>
 cudaError_t launch_variant(const IndexLaunch& a, const DeviceCtx& ctx, cudaStream_t st, const char** why) {
-  using Cfg = IdxCfg<NQ>;
+  using Cfg = IdxCfg<NQ, F4>;
+  using Fmt = PageFmt<F4>;
   const int nqb = (MODE == kModeScan) ? (a.rows.T + NQ - 1) / NQ : a.rows.T;
   if (nqb > kMaxQB) {
     *why = "too many query rows for one launch";
@@ -692,8 +757,14 @@ cudaError_t launch_variant(const IndexLaunch& a, const DeviceCtx& ctx, cudaStrea
     *why = "tensor map of q could not be encoded";
     return cudaErrorInvalidValue;
   }
-  if (encode_tmap_2d_u8(&map_kv, a.index_k, kRowBytes, static_cast<uint64_t>(a.n_pages) * kPageRows, kRowBytes,
-                        kRowBytes, MODE == kModeScan ? 64 : 8) != CUDA_SUCCESS) {
+  // FP8 pages as rows of 128 B; FP4 pages as rows of 128 e2m1 codes (64 B),
+  // unpacked by the tensor copy into 16-byte chunks of 8 code bytes + 8 gap
+  // bytes (128 B of shared memory per key, the layout of a 4-bit MMA operand)
+  const uint64_t kv_rows = static_cast<uint64_t>(a.n_pages) * Fmt::kRows;
+  const CUresult ke = F4 ? encode_tmap_2d_fp4(&map_kv, a.index_k, kv_rows, MODE == kModeScan ? 64 : 8)
+                         : encode_tmap_2d_u8(&map_kv, a.index_k, kRowBytes, kv_rows, kRowBytes, kRowBytes,
+                                             MODE == kModeScan ? 64 : 8);
+  if (ke != CUDA_SUCCESS) {
     *why = "tensor map of the index-K cache could not be encoded";
     return cudaErrorInvalidValue;
   }
@@ -724,14 +795,16 @@ cudaError_t launch_variant(const IndexLaunch& a, const DeviceCtx& ctx, cudaStrea
     if (e0 != cudaSuccess) return e0;
   }
   const size_t smem = Cfg::smem_bytes(nqb);
-  auto kern = index_tiles_kernel<NQ, MODE>;
+  auto kern = index_tiles_kernel<NQ, MODE, F4>;
   cudaError_t e = prefer_max_smem(kern, smem);
   if (e != cudaSuccess) return e;
   // CTAs per SM: bounded by shared memory, the register budget of the launch
   // bounds and the TMEM columns (kTmemCols per CTA, 512 per SM)
   int occ = ctas_per_sm_by_smem(ctx, smem);
   occ = occ > Cfg::kCtasPerSm ? Cfg::kCtasPerSm : occ;
-  static_assert(IdxCfg<1>::kTmemCols * IdxCfg<1>::kCtasPerSm <= 512, "TMEM of the CTAs sharing an SM");
+  static_assert(IdxCfg<1>::kTmemCols * IdxCfg<1>::kCtasPerSm <= 512 &&
+                    IdxCfg<1, true>::kTmemCols * IdxCfg<1, true>::kCtasPerSm <= 512,
+                "TMEM of the CTAs sharing an SM");
   return launch_pdl(kern, dim3(ctx.num_sms * occ), dim3(kThreads), smem, st, map_q, map_kv, p);
 }
 
@@ -739,9 +812,15 @@ cudaError_t launch_variant(const IndexLaunch& a, const DeviceCtx& ctx, cudaStrea
 
 cudaError_t launch_index_tiles(const IndexLaunch& a, int mode, int nq, const DeviceCtx& ctx, cudaStream_t st,
                                const char** why) {
-  if (mode == kModeScan && nq == 1) return launch_variant<1, kModeScan>(a, ctx, st, why);
-  if (mode == kModeScan && nq == 8) return launch_variant<8, kModeScan>(a, ctx, st, why);
-  if (mode == kModeGather && nq == 1) return launch_variant<1, kModeGather>(a, ctx, st, why);
+  if (a.fp4) {
+    if (mode == kModeScan && nq == 1) return launch_variant<1, kModeScan, true>(a, ctx, st, why);
+    if (mode == kModeGather && nq == 1) return launch_variant<1, kModeGather, true>(a, ctx, st, why);
+    *why = "FP4 index keys are scored on the decode scan and the Reindex gather only";
+    return cudaErrorInvalidValue;
+  }
+  if (mode == kModeScan && nq == 1) return launch_variant<1, kModeScan, false>(a, ctx, st, why);
+  if (mode == kModeScan && nq == 8) return launch_variant<8, kModeScan, false>(a, ctx, st, why);
+  if (mode == kModeGather && nq == 1) return launch_variant<1, kModeGather, false>(a, ctx, st, why);
   *why = "unsupported index tiling";
   return cudaErrorInvalidValue;
 }

@@ -6,6 +6,8 @@
   python -m serving_lightning_indexer_gb300.profile_case --case attn
   python -m serving_lightning_indexer_gb300.profile_case --case prefill
 
+--fp4 stores the index keys of the scan / topk / reindex cases as FP4 pages.
+
 Each case holds well under 2 GB on the device, reads more than the 129 MB L2
 per launch where the call is HBM-bound, runs a few warm-up launches and then
 `--iters` timed launches (CUDA events), and prints one line per case.
@@ -40,6 +42,7 @@ def main():
     ap.add_argument("--iters", type=int, default=3)
     ap.add_argument("--batch", type=int, default=8)
     ap.add_argument("--entries", type=int, default=262144)
+    ap.add_argument("--fp4", action="store_true", help="FP4 index-K pages (68 B per key)")
     a = ap.parse_args()
     csa2.load(build_if_missing=True)
     dev = torch.device("cuda:0")
@@ -48,7 +51,8 @@ def main():
     res = {"case": a.case}
     if a.case in ("scan", "topk", "reindex"):
         lengths = [n] * B
-        pc = W.make_paged_cache(lengths, seed=1, device=dev, with_main=False)
+        pc = W.make_paged_cache(lengths, seed=1, device=dev, with_main=False, index_fp4=a.fp4)
+        kb = 68 if a.fp4 else 132  # index-K bytes per key
         iq = W.make_indexer_query(B, seed=2, device=dev)
         r = csa2.rows(B, B, n_visible=pc.n_entries)
         ld = (n + 127) // 128 * 128
@@ -57,7 +61,7 @@ def main():
         if a.case == "scan":
             ms = _time(lambda: csa2.index_score(iq.q_fp8, iq.q_scale, iq.w, pc.index_k, pc.page_table, r, scores, bm),
                        a.iters, st)
-            res.update(ms=ms, keys=B * n, GBps=B * n * 132 / ms / 1e6)
+            res.update(ms=ms, keys=B * n, GBps=B * n * kb / ms / 1e6, fp4=a.fp4)
         elif a.case == "topk":
             csa2.index_score(iq.q_fp8, iq.q_scale, iq.w, pc.index_k, pc.page_table, r, scores, bm)
             pos = torch.empty(B, 512, dtype=torch.int32, device=dev)
@@ -72,7 +76,7 @@ def main():
             slot = torch.empty_like(pos)
             ms = _time(lambda: csa2.reindex(iq.q_fp8, iq.q_scale, iq.w, pc.index_k, pc.page_table, r, pool, 512, pos,
                                             slot), a.iters, st)
-            res.update(ms=ms, keys=B * 16384, GBps=B * 16384 * 132 / ms / 1e6)
+            res.update(ms=ms, keys=B * 16384, GBps=B * 16384 * kb / ms / 1e6, fp4=a.fp4)
     elif a.case == "attn":
         pc = W.make_paged_cache([n], seed=4, device=dev)
         al = W.make_attn_layer(B, seed=5, device=dev)

@@ -93,6 +93,17 @@ def test_validation_returns_codes_without_launch(lib):
     a.rows = csa2.Rows(2, 2, None, FAKE, None, 3)
     assert lib.csa2_index_score(C.byref(a), None, 0, None) == 4                  # ratio_m = 3
     assert b"ratio_m" in lib.csa2_last_error_detail()
+    a.rows = csa2.Rows(2, 2, None, None, FAKE, 1)
+    a.index_k_format = 2
+    assert lib.csa2_index_score(C.byref(a), None, 0, None) == 4                  # unknown page format
+    a.index_k_format = csa2.INDEX_FP4
+    a.index_k = FAKE + 16
+    assert lib.csa2_index_score(C.byref(a), None, 0, None) == 3                  # FP4 pages need 32-B alignment
+    a.index_k = FAKE
+    a.rows = csa2.Rows(64, 1, FAKE, FAKE, None, 2)
+    assert lib.csa2_index_score(C.byref(a), None, 0, None) == 4                  # FP4 keys: decode path only
+    assert b"FP4" in lib.csa2_last_error_detail()
+    a.index_k_format = csa2.INDEX_FP8
 
     t = csa2.TopkArgs(FAKE, 128, None, 0, None, 0, csa2.Rows(2, 2, None, None, FAKE, 1), 4096, FAKE, None, 4096,
                       None, 0)

@@ -11,17 +11,17 @@ from serving_lightning_indexer_gb300 import workloads as W
 pytestmark = pytest.mark.gpu
 
 
-def _decode(lengths, seed, ld=None, with_bm=True):
+def _decode(lengths, seed, ld=None, with_bm=True, fp4=False, hist=None):
     dev = need_gpu()
     B = len(lengths)
-    pc = W.make_paged_cache(lengths, seed=seed, device=dev, with_main=False)
+    pc = W.make_paged_cache(lengths, seed=seed, device=dev, with_main=False, index_fp4=fp4)
     iq = W.make_indexer_query(B, seed=seed + 1, device=dev)
     nvis = torch.tensor(lengths, dtype=torch.int32, device=dev)
     ld = ld or ((max(lengths) + 127) // 128 * 128)
     scores = torch.full((B, ld), 7.0, dtype=torch.float32, device=dev)
     bm = torch.full((B, (ld + 7) // 8 + 4), 7.0, dtype=torch.float32, device=dev) if with_bm else None
     r = csa2.rows(B, B, n_visible=nvis)
-    csa2.index_score(iq.q_fp8, iq.q_scale, iq.w, pc.index_k, pc.page_table, r, scores, bm)
+    csa2.index_score(iq.q_fp8, iq.q_scale, iq.w, pc.index_k, pc.page_table, r, scores, bm, hist=hist)
     torch.cuda.synchronize()
     assert csa2.check_device_error() == 0
     return pc, iq, scores, bm
@@ -110,3 +110,24 @@ def test_prefill_query_blocked_path(T, ratio, n_entries):
         want = np.maximum.reduceat(np.where(np.arange(nb * 8) < e, s_all[t, :nb * 8], -np.inf), np.arange(0, nb * 8, 8))
         assert np.array_equal(bm_all[t, :nb], want.astype(np.float32)), f"block maxima of row {t}"
         assert np.all(bm_all[t, nb:] == 7.0), f"row {t}: block maxima written past the visible blocks"
+
+
+@pytest.mark.parametrize("lengths", [[1], [127, 128, 129], [4096], [100, 1000, 4133, 64, 65, 8191]])
+def test_decode_fp4_index_keys_match_oracle(lengths):
+    # FP4 index-K pages (e2m1 + ue8m0 per 32 dims): the same scan, the e2m1 keys
+    # fed to the tensor cores as 4-bit operands, one accumulator per 32-dim block
+    dev = need_gpu()
+    hist = torch.zeros(2, len(lengths), 2048, dtype=torch.int32, device=dev)
+    pc, iq, scores, bm = _decode(lengths, seed=20 + len(lengths), fp4=True, hist=hist)
+    assert pc.index_k.shape[1] == 4352
+    cache, pt = np_(pc.index_k), np_(pc.page_table)
+    for b, n in enumerate(lengths):
+        ref = o.index_scores_row(np_(iq.q_fp8[b]), np_(iq.q_scale[b]), np_(iq.w[b]), cache, pt[b], n, fp4=True)
+        got = np_(scores[b])
+        assert_scores_close(got[:n], ref, f"fp4 row {b}")
+        assert np.all(np.isneginf(got[n:(n + 127) // 128 * 128]))
+        nb = (n + 7) // 8
+        want = [got[8 * j:min(8 * j + 8, n)].max() for j in range(nb)]
+        assert np.array_equal(np_(bm[b, :nb]), np.array(want, dtype=np.float32))
+        # the score histogram counts every visible score once
+        assert int(np_(hist[0, b]).sum()) == n

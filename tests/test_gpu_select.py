@@ -219,3 +219,30 @@ def test_fused_histograms_give_identical_selection():
         bmk = np.where(bmk & 0x80000000, ~bmk & 0xFFFFFFFF, bmk | 0x80000000)
         bmk[-1] = 0xFFFFFFFF
         assert np.array_equal(h[1, b_], np.bincount(bmk >> 21, minlength=2048))
+
+
+def test_reindex_fp4_index_keys_match_oracle():
+    dev = need_gpu()
+    lengths = [30000, 16384 * 8 + 5, 700]
+    B = len(lengths)
+    pc = W.make_paged_cache(lengths, seed=23, device=dev, with_main=False, index_fp4=True)
+    iq = W.make_indexer_query(B, seed=24, device=dev)
+    pool = W.make_pool(lengths, seed=25, device=dev)
+    r = csa2.rows(B, B, n_visible=torch.tensor(lengths, dtype=torch.int32, device=dev))
+    pos = torch.empty(B, 512, dtype=torch.int32, device=dev)
+    slot = torch.empty(B, 512, dtype=torch.int32, device=dev)
+    ps = torch.empty(B, 2048 * 8, dtype=torch.float32, device=dev)
+    csa2.reindex(iq.q_fp8, iq.q_scale, iq.w, pc.index_k, pc.page_table, r, pool, 512, pos, slot, ps)
+    torch.cuda.synchronize()
+    assert csa2.check_device_error() == 0
+    cache, pt = np_(pc.index_k), np_(pc.page_table)
+    for b, n in enumerate(lengths):
+        ref = o.reindex_scores(np_(iq.q_fp8[b]), np_(iq.q_scale[b]), np_(iq.w[b]), cache, pt[b], n,
+                               np_(pool[b]), fp4=True)
+        assert_scores_close(np_(ps[b]), ref, f"fp4 pool scores {b}")
+        full = np.full(n, -np.inf, dtype=np.float32)
+        pp = o.pool_positions(np_(pool[b]), n)
+        full[pp[pp >= 0]] = np_(ps[b])[pp >= 0]
+        want = o.topk_positions(full, 512)
+        assert np_(pos[b]).tolist() == want.tolist()
+        assert np_(slot[b]).tolist() == o.slots_of(want, pt[b]).tolist()
