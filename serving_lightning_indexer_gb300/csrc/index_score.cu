@@ -658,16 +658,19 @@ __global__ void __launch_bounds__(kThreads, IdxCfg<NQ, F4>::kCtasPerSm)
             for (int b = 0; b < 4; ++b) sb[b] = ue8m0_to_float((ub >> (8 * b)) & 0xFFu);
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh) {
+              // the four blocks' loads are issued together, then one wait
+              uint32_t d[4][16];
+#pragma unroll
+              for (int b = 0; b < 4; ++b) tmem_ld32x16_async(tq + b * 32 + hh * 16, d[b]);
+#pragma unroll
+              for (int b = 0; b < 4; ++b) tmem_wait_ld16(d[b]);
               float v[16];
-              tmem_ld32x16(tq + hh * 16, v);
 #pragma unroll
-              for (int i = 0; i < 16; ++i) v[i] *= sb[0];
-#pragma unroll
-              for (int b = 1; b < 4; ++b) {
-                float d[16];
-                tmem_ld32x16(tq + b * 32 + hh * 16, d);
-#pragma unroll
-                for (int i = 0; i < 16; ++i) v[i] = fmaf(d[i], sb[b], v[i]);
+              for (int i = 0; i < 16; ++i) {
+                v[i] = __uint_as_float(d[0][i]) * sb[0];
+                v[i] = fmaf(__uint_as_float(d[1][i]), sb[1], v[i]);
+                v[i] = fmaf(__uint_as_float(d[2][i]), sb[2], v[i]);
+                v[i] = fmaf(__uint_as_float(d[3][i]), sb[3], v[i]);
               }
 #pragma unroll
               for (int h4 = 0; h4 < 4; ++h4) {
