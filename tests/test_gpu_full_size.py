@@ -32,9 +32,9 @@ def _q(iq, t):
     return o.dequant_q(np_(iq.q_fp8[t]), np_(iq.q_scale[t])), np_(iq.w[t])
 
 
-def _scores_at(iq, t, pc, b, positions):
+def _scores_at(iq, t, pc, b, positions, fp4=False):
     """Oracle scores of indexer row t (sequence b) at the given positions,
-    reading only the pages holding them."""
+    reading only the pages holding them (FP8 or, with fp4, FP4 pages)."""
     pos = np.asarray(positions, dtype=np.int64)
     if len(pos) == 0:
         return np.zeros(0)
@@ -44,7 +44,7 @@ def _scores_at(iq, t, pc, b, positions):
     remap = np.full(int(lp.max()) + 1, -1, dtype=np.int64)
     remap[lp] = np.arange(len(lp))
     q, w = _q(iq, t)
-    return o.index_score_values(q, w, o.index_k_at(sub, remap, pos))
+    return o.index_score_values(q, w, (o.index_k_fp4_at if fp4 else o.index_k_at)(sub, remap, pos))
 
 
 def _row_scores(iq, t, pc, b, n):
@@ -72,7 +72,7 @@ def _check_attention(al, out, rows, main_kv, slots):
         assert_attention_close(out[t].double().cpu().numpy(), ref, f"attention row {t}")
 
 
-def _check_topk_sampled(iq, t, pc, b, n, got_pos, k=512, n_sample=4096, seed=0):
+def _check_topk_sampled(iq, t, pc, b, n, got_pos, k=512, n_sample=4096, seed=0, fp4=False):
     """Selection check for rows too long for the oracle's full score row: the
     selected positions against a random sample of the others."""
     sel = got_pos[got_pos >= 0]
@@ -80,7 +80,7 @@ def _check_topk_sampled(iq, t, pc, b, n, got_pos, k=512, n_sample=4096, seed=0):
     assert sel.min() >= 0 and sel.max() < n
     rng = np.random.default_rng(seed)
     oth = np.setdiff1d(rng.choice(n, size=min(n, n_sample), replace=False), sel)
-    s_sel, s_oth = _scores_at(iq, t, pc, b, sel), _scores_at(iq, t, pc, b, oth)
+    s_sel, s_oth = _scores_at(iq, t, pc, b, sel, fp4), _scores_at(iq, t, pc, b, oth, fp4)
     thr = s_sel.min()
     assert s_oth.max() <= thr + NEAR_TIE_RTOL * abs(thr), \
         f"row {t}: an unselected key scores {s_oth.max()} above the selection's minimum {thr}"
@@ -335,3 +335,42 @@ def test_decode_step_38_layers_sampled():
     for l, rows in ((2, [0]), (3, [1]), (20, [2]), (21, [3]), (24, [1]), (25, [6])):
         c = step.caches[ds.cache_of(l)]
         _check_attention(step.inputs[l].attn, b.out[l], rows, c.pc.main_kv, cap[l]["slot"])
+
+
+# ---------------------------------------------------------------- FP4 index keys, 1M context
+def test_decode_fp4_index_keys_batch8_1m():
+    """The decoder Full layer of the 38-layer step (batch 8, {32K, 256K, 1M x2} x 2)
+    with FP4 index-K pages: scan with block maxima and histograms, then top-512
+    and the candidate pool, checked on sampled rows."""
+    dev = need_gpu()
+    lengths = [32768, 262144, 1 << 20, 1 << 20] * 2
+    B = len(lengths)
+    pc = W.make_paged_cache(lengths, seed=31, device=dev, with_main=False, index_fp4=True)
+    iq = W.make_indexer_query(B, seed=32, device=dev)
+    nvis = torch.tensor(lengths, dtype=torch.int32, device=dev)
+    r = csa2.rows(B, B, n_visible=nvis)
+    ld = max(lengths)
+    scores = torch.empty(B, ld, dtype=torch.float32, device=dev)
+    bm = torch.empty(B, ld // 8, dtype=torch.float32, device=dev)
+    hist = torch.empty(2, B, 2048, dtype=torch.int32, device=dev)
+    pos = torch.empty(B, 512, dtype=torch.int32, device=dev)
+    slot = torch.empty(B, 512, dtype=torch.int32, device=dev)
+    pool = torch.empty(B, 2048, dtype=torch.int32, device=dev)
+    csa2.index_score(iq.q_fp8, iq.q_scale, iq.w, pc.index_k, pc.page_table, r, scores, bm, hist=hist)
+    csa2.topk_with_candidates(scores, r, 512, pos, slot, pc.page_table, bm, pool, hist=hist)
+    torch.cuda.synchronize()
+    assert csa2.check_device_error() == 0
+    _all_rows_valid(pos, slot, nvis)
+    rng = np.random.default_rng(33)
+    for b in (0, 3, 6):
+        n = lengths[b]
+        sample = np.sort(rng.choice(n, size=min(n, 8192), replace=False))
+        got = np_(scores[b])[sample]
+        assert_scores_close(got, _scores_at(iq, b, pc, b, sample, fp4=True), f"fp4 row {b}")
+        p = np_(pos[b])
+        _check_topk_sampled(iq, b, pc, b, n, p, seed=b, fp4=True)
+        _check_slots(p, np_(slot[b]), pc.page_table[b])
+        # the pool: 2048 ascending distinct blocks with the newest block, ⊇ the top-k blocks
+        pb = np_(pool[b])
+        assert len(pb) == 2048 and (np.diff(pb) > 0).all() and pb[-1] == (n - 1) // 8
+        assert set((p // 8).tolist()) <= set(pb.tolist())
