@@ -66,6 +66,24 @@ def _scan_traffic_per_key():
     return float(per_key.group(1))
 
 
+def max_over_ranks(value: float, device) -> float:
+    """The largest of a per-rank value over all ranks of the process group
+    (the value itself when there is none or it has one rank)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank_step: float, steps: int, world: int, ms_max: float) -> float:
+    """Units per second of the whole job: every rank processes units_per_rank_step
+    each step (weak scaling), over the slowest rank's time."""
+    return units_per_rank_step * steps * world / (ms_max / 1e3)
+
+
 def _peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -300,10 +318,7 @@ def main():
         per_layer.setdefault(l, []).append(ms)
     scan_ms_total = sum(scan_ms)
     attn_ms = [a.elapsed_time(b) for a, b in attn_pairs]
-    if world > 1:
-        t = torch.tensor([ms_total], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_total = float(t.item())
+    ms_total = max_over_ranks(ms_total, dev)
 
     # ---- end to end: pinned host inputs -> device, step, outputs -> pinned host.
     # Every step copies all of its query-side inputs in and all 38 attention
@@ -366,10 +381,7 @@ def main():
         e1.record(stream)
     stream.synchronize()
     e2e_ms = e0.elapsed_time(e1)
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e2e_ms, dev)
 
     if rank != 0:
         if world > 1:
@@ -380,7 +392,7 @@ def main():
     bf16_peak = _bf16_peak()
     traffic_per_key = _scan_traffic_per_key()
     ms_per_step = ms_total / K
-    value = keys_per_step * K * world / (ms_total / 1e3)
+    value = whole_job_rate(keys_per_step, K, world, ms_total)
     scan_launches = len(scan_ms)
     scan_bytes_per_launch = scan_bytes_per_step * K / scan_launches
     achieved = scan_bytes_per_step * K / (scan_ms_total / 1e3) / 1e9
@@ -404,7 +416,7 @@ def main():
                    "keys_scored_per_step": keys_per_step, "attn_query_layers_per_step": attn_per_step,
                    "timing": "K steps in one CUDA graph; inputs larger than L2 (no flush)",
                    "parallelism": f"replicas x{world}"},
-        "attn_query_layers_per_s": attn_per_step * K * world / (ms_total / 1e3),
+        "attn_query_layers_per_s": whole_job_rate(attn_per_step, K, world, ms_total),
         "roofline": {"bound": "hbm", "kernel": "index_tiles_kernel<1,scan> (decode Lightning-Indexer scan)",
                      "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "peak_source": peak_kind,
@@ -427,7 +439,7 @@ def main():
             "bf16_tensor_frac": ATTN_ROW_FLOP * len(LENGTHS) / (statistics.mean(attn_ms) / 1e3) / 1e12 / bf16_peak,
             "peaks": {"hbm_gbs": peak, "bf16_tflops": bf16_peak, "source": peak_kind}},
         "cpu_baseline": cpu,
-        "e2e": {"value": keys_per_step * Ke * world / (e2e_ms / 1e3), "unit": "keys/s", "h2d_bytes_per_step": h2d,
+        "e2e": {"value": whole_job_rate(keys_per_step, Ke, world, e2e_ms), "unit": "keys/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": Ke},
         "gpu_launches": launches_per_step * K,
         "clocks": sampler.summary(),
