@@ -400,15 +400,15 @@ def compress_latent(C: np.ndarray, Z, ratio_m: int, gamma: np.ndarray, eps: floa
 
 
 def rope_interleaved(y: np.ndarray, positions: np.ndarray, theta: float) -> np.ndarray:
-    """RoPE on the last 64 dims, interleaved pairs (CSA2 page: RoPE only on the
-    last 64 dims; pairing and base are readings)."""
+    """RoPE on the last 64 dims of y [n,d], interleaved pairs (CSA2 page: RoPE
+    only on the last 64 dims; pairing and base are readings)."""
     y = np.array(y, dtype=np.float64, copy=True)
     pos = np.asarray(positions, dtype=np.float64)
     half = ROPE_DIMS // 2
     inv = theta ** (-2.0 * np.arange(half) / ROPE_DIMS)
     ang = pos[:, None] * inv[None, :]
     c, s = np.cos(ang), np.sin(ang)
-    base = ATT_DIM - ROPE_DIMS
+    base = y.shape[1] - ROPE_DIMS
     x0 = y[:, base + 0::2].copy()
     x1 = y[:, base + 1::2].copy()
     y[:, base + 0::2] = x0 * c - x1 * s
@@ -465,3 +465,61 @@ def compress_records(C, Z, ratio_m, gamma, eps, positions, rope_theta, apply_rop
     """Records [n_entries,288] of the main-KV entries built from C (and Z)."""
     lat = compress_latent(C, Z, ratio_m, gamma, eps, positions, rope_theta, apply_rope)
     return fp4_encode_records(lat), lat
+
+
+# ---------------------------------------------------------------------------
+# Index-key build of a Full layer
+# ---------------------------------------------------------------------------
+
+def index_key_latent(y_pre: np.ndarray, w_ik: np.ndarray, k_gamma: np.ndarray, eps: float,
+                     positions: np.ndarray, rope_theta: float) -> np.ndarray:
+    """Index keys [n,128] before quantisation from the main-KV latents before
+    RoPE y_pre [n,512].
+
+    V4.1 Q&A page (indexer K from the main KV): k = RMSNorm(y_pre W^IK) with
+    W^IK of 512 x 128, projected from the latent before its RoPE; the last 64
+    dims of k then get their own RoPE.  CSA2 page item 3: latent -> wk -> k_norm
+    -> RoPE -> quantisation.  Readings: k_norm is RMSNorm with a weight k_gamma
+    and the eps of the main latent; the RoPE is the main latent's (interleaved
+    pairs, base theta, the entry's position).
+    """
+    k = np.asarray(y_pre, dtype=np.float64) @ np.asarray(w_ik, dtype=np.float64)
+    k = k / np.sqrt((k * k).mean(axis=1, keepdims=True) + eps) * np.asarray(k_gamma, dtype=np.float64)[None, :]
+    return rope_interleaved(k, positions, rope_theta)
+
+
+def fp8_e4m3_codes(v) -> np.ndarray:
+    """e4m3 codes of v: the nearest finite e4m3 value, ties to the even code,
+    saturating at +-448."""
+    v = np.asarray(v, dtype=np.float64)
+    mags = FP8[:0x7F]                                     # 0 .. 448 at codes 0 .. 0x7E
+    a = np.minimum(np.abs(v), 448.0)
+    best = np.clip(np.searchsorted(mags, a), 1, 0x7E)     # mags[best-1] < a <= mags[best]
+    lo, hi = best - 1, best
+    dlo, dhi = a - mags[lo], mags[hi] - a
+    code = np.where(dlo < dhi, lo, np.where(dhi < dlo, hi, np.where(lo % 2 == 0, lo, hi)))
+    code = np.where(a == 0, 0, code)
+    return (code | np.where(v < 0, 0x80, 0)).astype(np.int64)
+
+
+def index_key_fp8_bytes(k32: np.ndarray):
+    """FP8 index-K entry of fp32 keys k32 [n,128]: scale = amax / 448 in fp32 (1
+    for an all-zero key), codes = e4m3 of the fp32 quotient k / scale.
+    Returns (codes uint8 [n,128], scale float32 [n])."""
+    k32 = np.asarray(k32, dtype=np.float32)
+    amax = np.abs(k32).max(axis=1)
+    scale = np.where(amax > 0, amax / np.float32(448.0), np.float32(1.0)).astype(np.float32)
+    q = (k32 / scale[:, None]).astype(np.float32)
+    return fp8_e4m3_codes(q).astype(np.uint8), scale
+
+
+def index_key_fp4_bytes(k: np.ndarray):
+    """FP4 index-K entry of keys k [n,128]: e2m1 codes (element 2i in the low
+    nibble of byte i) and one ue8m0 scale per 32 dims, as the main-KV records.
+    Returns (code bytes uint8 [n,64], scales uint8 [n,4])."""
+    k = np.asarray(k, dtype=np.float64)
+    n = k.shape[0]
+    g = k.reshape(n, 4, 32)
+    u = fp4_scale_exponent(np.abs(g).max(axis=2))
+    codes = fp4_codes(g / np.exp2(u - 127)[..., None]).reshape(n, IDX_DIM)
+    return (codes[:, 0::2] | (codes[:, 1::2] << 4)).astype(np.uint8), u.astype(np.uint8)

@@ -76,3 +76,72 @@ def test_records_decode_close_to_latent():
     assert rec.shape == (32, 288) and (rec[:, 272:] == 0).all()
     # the report reading's bound: a unit-RMS 512-vector has |x| <= sqrt(512) << 2688
     assert np.abs(lat).max() < np.sqrt(512) * 1.5
+
+
+# ---------------------------------------------------------------- index-key build
+def _ik_inputs(n, seed):
+    rng = np.random.default_rng(seed)
+    y_pre = rng.standard_normal((n, 512))
+    w_ik = rng.standard_normal((512, 128)) / np.sqrt(512)
+    k_gamma = 1.0 + 0.1 * rng.standard_normal(128)
+    return y_pre, w_ik, k_gamma
+
+
+def test_index_key_is_library_rmsnorm_of_the_projection_at_position_zero():
+    # V4.1 Q&A page: k = RMSNorm(y_pre W^IK); position 0 rotates nothing
+    y_pre, w_ik, k_gamma = _ik_inputs(5, 3)
+    k = o.index_key_latent(y_pre, w_ik, k_gamma, 1e-6, np.zeros(5), 10000.0)
+    proj = torch.tensor(y_pre) @ torch.tensor(w_ik)               # library matmul
+    ref = torch.nn.functional.rms_norm(proj, (128,), torch.tensor(k_gamma), eps=1e-6).numpy()
+    assert np.allclose(k, ref, rtol=1e-10, atol=1e-12)
+    # a selector projection picks input dims: k = RMSNorm of the first 128 latent dims
+    sel = np.zeros((512, 128))
+    sel[np.arange(128), np.arange(128)] = 1.0
+    k2 = o.index_key_latent(y_pre, sel, np.ones(128), 0.0, np.zeros(5), 10000.0)
+    x = y_pre[:, :128]
+    assert np.allclose(k2, x / np.sqrt((x * x).mean(axis=1, keepdims=True)), rtol=1e-12)
+
+
+def test_index_key_rope_turns_only_the_last_64_dims():
+    # V4.1 Q&A page: after the projection the last 64 dims get their own RoPE
+    y_pre, w_ik, k_gamma = _ik_inputs(4, 4)
+    pos = np.array([0, 1, 77, 131071])
+    k0 = o.index_key_latent(y_pre, w_ik, k_gamma, 1e-6, np.zeros(4), 10000.0)
+    k = o.index_key_latent(y_pre, w_ik, k_gamma, 1e-6, pos, 10000.0)
+    assert np.array_equal(k[:, :64], k0[:, :64])
+    assert np.allclose(np.linalg.norm(k, axis=1), np.linalg.norm(k0, axis=1), rtol=1e-12)   # rotation
+    # the same rotation as complex multiplication of the pairs (64+2i, 65+2i)
+    z = torch.complex(torch.tensor(k0[:, 64::2]), torch.tensor(k0[:, 65::2]))
+    ang = torch.tensor(pos, dtype=torch.float64)[:, None] * (10000.0 ** (-2.0 * torch.arange(32, dtype=torch.float64) / 64))
+    zr = z * torch.polar(torch.ones_like(ang), ang)
+    assert np.allclose(k[:, 64::2], zr.real.numpy(), atol=1e-9) and np.allclose(k[:, 65::2], zr.imag.numpy(), atol=1e-9)
+
+
+def test_fp8_e4m3_codes_match_torch_conversion():
+    # library routine: torch's float32 -> float8_e4m3fn conversion (round to nearest even)
+    v = np.concatenate([np.linspace(-447, 447, 40001), o.FP8[:0x7F], -o.FP8[1:0x7F],
+                        (o.FP8[1:0x7F] + o.FP8[:0x7E]) / 2, [448.0, -448.0, 1e-4, -1e-4]])
+    ref = torch.tensor(v, dtype=torch.float32).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(o.fp8_e4m3_codes(v.astype(np.float32)).astype(np.uint8), ref)
+    assert o.fp8_e4m3_codes(np.array([1e9]))[0] == 0x7E and o.fp8_e4m3_codes(np.array([-1e9]))[0] == 0xFE
+
+
+def test_index_key_bytes_decode_through_the_page_readers():
+    y_pre, w_ik, k_gamma = _ik_inputs(64, 5)
+    k = o.index_key_latent(y_pre, w_ik, k_gamma, 1e-6, np.arange(64), 10000.0)
+    k32 = k.astype(np.float32)
+    codes, scale = o.index_key_fp8_bytes(k32)
+    page8 = np.zeros(8448, dtype=np.uint8)
+    page8[:8192] = codes.reshape(-1)
+    page8[8192:] = scale.view(np.uint8)
+    dec8 = o.index_k_entries(page8, np.array([0]), 64)
+    assert np.all(np.abs(dec8 - k32) <= np.abs(k32) * 2.0 ** -4 + scale[:, None] * 2.0 ** -9 + 1e-12)
+    c4, u4 = o.index_key_fp4_bytes(k)
+    page4 = np.zeros(4352, dtype=np.uint8)
+    page4[:4096] = c4.reshape(-1)
+    page4[4096:] = u4.reshape(-1)
+    dec4 = o.index_k_fp4_entries(page4, np.array([0]), 64)
+    assert np.all(np.abs(dec4 - k) <= np.repeat(o.ue8m0(u4), 32, axis=1) + 1e-12)
+    # the generator's independent FP4 encoder writes the same bytes
+    gc, gu = W.fp4_encode_blocks(torch.tensor(k))
+    assert np.array_equal(gc.numpy(), c4) and np.array_equal(gu.numpy(), u4)
