@@ -260,7 +260,16 @@ CSA2_API int csa2_sparse_attn(const csa2_sparse_attn_args* args, void* workspace
  * page_table[(first_entry + e) / 64] * 64 + (first_entry + e) % 64.
  * (CSA2 page item 3 and V4.1 Q&A page; V4.1-Flash report reading, section 六:
  * FP4 after RoPE, no global scale.)  latent_out (optional, fp32 [n_entries,512])
- * receives y after RoPE, before quantisation.  Alignment: C, Z 16 B. */
+ * receives y after RoPE, before quantisation.  Alignment: C, Z 16 B.
+ * Index keys (optional, w_ik not NULL; CSA2 page item 3, V4.1 Q&A page "the
+ * indexer K is projected from the main KV"): from y before RoPE,
+ *   k = RMSNorm(y W^IK) * k_gamma   (W^IK: 512 x 128, the same eps),
+ *   RoPE on k's dims 64..127 (pairs (64+2i, 65+2i), the angles of the main
+ *   latent's pair i), then quantised into the index-K page of the entry's slot
+ *   (page slot/64, row slot%64): FP8: scale = amax/448 (fp32), codes = e4m3
+ *   round-to-nearest-even of k/scale; FP4: e2m1 + ue8m0 per 32 dims as above.
+ * index_latent_out (optional, fp32 [n_entries,128]) receives k before
+ * quantisation. */
 typedef struct {
   const uint16_t* C; const uint16_t* Z;        /* [n_tokens,512] bf16; Z unused for m=1 */
   int64_t n_tokens; int32_t ratio_m;
@@ -272,6 +281,11 @@ typedef struct {
   const int32_t* page_table; int64_t pt_len;   /* [pt_len] of the one sequence, or NULL */
   const int32_t* entry_slot;                   /* optional [n_entries] direct slots */
   float* latent_out;                           /* optional [n_entries,512] */
+  const uint16_t* w_ik;                        /* optional [512,128] bf16 W^IK (row = latent dim) */
+  const float* k_gamma;                        /* [128] k_norm weight (with w_ik) */
+  uint8_t* index_k; int64_t index_k_pages;     /* index-K pages (with w_ik) */
+  int32_t index_k_format;                      /* CSA2_INDEX_FP8 or CSA2_INDEX_FP4 */
+  float* index_latent_out;                     /* optional [n_entries,128] */
 } csa2_compress_args;
 CSA2_API int csa2_compress_m2(const csa2_compress_args* args, void* stream);
 

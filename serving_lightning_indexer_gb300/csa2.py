@@ -60,7 +60,8 @@ class CompressArgs(C.Structure):
     _fields_ = [("C", _P), ("Z", _P), ("n_tokens", _I64), ("ratio_m", _I32), ("gamma", _P), ("eps", C.c_float),
                 ("apply_rope", _I32), ("rope_theta", C.c_float), ("first_entry", _I64), ("entry_pos", _P),
                 ("main_kv", _P), ("main_kv_slots", _I64), ("page_table", _P), ("pt_len", _I64),
-                ("entry_slot", _P), ("latent_out", _P)]
+                ("entry_slot", _P), ("latent_out", _P), ("w_ik", _P), ("k_gamma", _P), ("index_k", _P),
+                ("index_k_pages", _I64), ("index_k_format", _I32), ("index_latent_out", _P)]
 
 
 CALL_INDEX_SCORE, CALL_TOPK, CALL_REINDEX, CALL_SPARSE_ATTN = 1, 2, 3, 4
@@ -236,12 +237,16 @@ def sparse_attn(q, main_kv, topk_slot, swa_kv, swa_slot, sink, out, lse=None, so
 
 
 def compress_m2(Cm, Z, ratio_m, gamma, main_kv, page_table=None, entry_slot=None, eps=1e-6, rope_theta=10000.0,
-                apply_rope=True, first_entry=0, entry_pos=None, latent_out=None, stream=None):
-    """Main-KV entry build: m=2 softmax pooling (or m=1), RMSNorm, RoPE, FP4 (csa2_compress_m2)."""
+                apply_rope=True, first_entry=0, entry_pos=None, latent_out=None, stream=None,
+                w_ik=None, k_gamma=None, index_k=None, index_latent_out=None):
+    """Main-KV entry build: m=2 softmax pooling (or m=1), RMSNorm, RoPE, FP4 (csa2_compress_m2);
+    with w_ik ([512,128] bf16), k_gamma and index_k also the entries' index keys."""
     lib = load()
     a = CompressArgs(_ptr(Cm), _ptr(Z), Cm.shape[0], ratio_m, _ptr(gamma), eps, 1 if apply_rope else 0, rope_theta,
                      first_entry, _ptr(entry_pos), _ptr(main_kv), main_kv.shape[0], _ptr(page_table),
-                     page_table.numel() if page_table is not None else 0, _ptr(entry_slot), _ptr(latent_out))
+                     page_table.numel() if page_table is not None else 0, _ptr(entry_slot), _ptr(latent_out),
+                     _ptr(w_ik), _ptr(k_gamma), _ptr(index_k), index_k.shape[0] if index_k is not None else 0,
+                     index_format(index_k) if index_k is not None else 0, _ptr(index_latent_out))
     _check(lib.csa2_compress_m2(C.byref(a), _stream(stream)), "csa2_compress_m2")
 
 

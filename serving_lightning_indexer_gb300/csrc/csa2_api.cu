@@ -407,6 +407,16 @@ int csa2_compress_m2(const csa2_compress_args* a, void* stream) {
   if (!(a->eps >= 0.f)) return fail(CSA2_ERR_SHAPE, "csa2_compress_m2: eps must be >= 0");
   if (a->apply_rope && !(a->rope_theta > 0.f)) return fail(CSA2_ERR_SHAPE, "csa2_compress_m2: rope_theta must be > 0");
   if (a->first_entry < 0) return fail(CSA2_ERR_SHAPE, "csa2_compress_m2: first_entry < 0");
+  if (a->w_ik) {
+    if (!a->k_gamma || !a->index_k) return fail(CSA2_ERR_NULL, "csa2_compress_m2: w_ik needs k_gamma and index_k");
+    if (a->index_k_format != CSA2_INDEX_FP8 && a->index_k_format != CSA2_INDEX_FP4)
+      return fail(CSA2_ERR_UNSUPPORTED, "csa2_compress_m2: index_k_format=%d is neither FP8 (0) nor FP4 (1)",
+                  a->index_k_format);
+    if (!aligned16(a->w_ik) || !aligned16(a->index_k) ||
+        (a->index_latent_out && !aligned16(a->index_latent_out)))
+      return fail(CSA2_ERR_ALIGN, "csa2_compress_m2: w_ik, index_k, index_latent_out must be 16-B aligned");
+    if (a->index_k_pages < 1) return fail(CSA2_ERR_SHAPE, "csa2_compress_m2: index_k_pages must be >= 1");
+  }
   DeviceCtx ctx;
   cudaError_t e = csa2::device_ctx(&ctx);
   if (e != cudaSuccess) return cuda_fail(e, "csa2_compress_m2: device");
@@ -427,6 +437,12 @@ int csa2_compress_m2(const csa2_compress_args* a, void* stream) {
   L.pt_len = a->pt_len;
   L.entry_slot = a->entry_slot;
   L.latent_out = a->latent_out;
+  L.w_ik = a->w_ik;
+  L.k_gamma = a->k_gamma;
+  L.index_k = a->index_k;
+  L.index_k_pages = a->index_k_pages;
+  L.index_k_fp4 = a->index_k_format == CSA2_INDEX_FP4;
+  L.index_latent_out = a->index_latent_out;
   e = csa2::launch_compress(L, ctx, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "csa2_compress_m2: launch");
   return CSA2_OK;

@@ -136,6 +136,12 @@ struct CompressLaunch {
   long long pt_len;
   const int* entry_slot;
   float* latent_out;
+  const uint16_t* w_ik;  // optional index-key build
+  const float* k_gamma;
+  uint8_t* index_k;
+  long long index_k_pages;
+  int index_k_fp4;
+  float* index_latent_out;
 };
 cudaError_t launch_compress(const CompressLaunch& a, const DeviceCtx& ctx, cudaStream_t st);
 

@@ -273,6 +273,15 @@ def make_compress_inputs(n_tokens: int, seed: int, device="cpu"):
     return C.contiguous(), Z.contiguous(), gamma.contiguous()
 
 
+def make_index_projection(seed: int, device="cpu"):
+    """W^IK [512,128] bf16 ~ N(0,1)/sqrt(512) (a random initialisation: no
+    trained weights) and the k_norm weight k_gamma = 1 + 0.1 N(0,1)."""
+    g = _gen(seed, device)
+    w = (torch.randn(ATT_DIM, IDX_DIM, generator=g, device=device) / math.sqrt(ATT_DIM)).to(torch.bfloat16)
+    k_gamma = 1.0 + 0.1 * torch.randn(IDX_DIM, generator=g, device=device)
+    return w.contiguous(), k_gamma.contiguous()
+
+
 # ---------------------------------------------------------------------------
 # the five workloads
 # ---------------------------------------------------------------------------

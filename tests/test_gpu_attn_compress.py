@@ -169,3 +169,51 @@ def test_attention_keys_gathered_early_give_identical_results():
     torch.cuda.synchronize()
     assert csa2.check_device_error() == 0
     assert torch.equal(outs[0], outs[1]) and torch.equal(outs[0], outs[2])
+
+
+@pytest.mark.parametrize("ratio,fp4", [(2, False), (1, False), (2, True), (1, True)])
+def test_compress_builds_index_keys(ratio, fp4):
+    # Full layer's index key from the main-KV latent before RoPE (V4.1 Q&A page):
+    # k = RMSNorm(y W^IK) * k_gamma, RoPE on dims 64..127, FP8 or FP4 entry
+    dev = need_gpu()
+    n_tok = 1000 * ratio + ratio
+    Cm, Z, gamma = W.make_compress_inputs(n_tok, seed=40 + ratio, device=dev)
+    w_ik, k_gamma = W.make_index_projection(seed=41, device=dev)
+    n_ent = n_tok // ratio
+    first = 300
+    pt = torch.randperm(40, device=dev).to(torch.int32)            # 40 pages hold entries < 2560
+    kv = torch.zeros(40 * 64, 288, dtype=torch.uint8, device=dev)
+    kv_plain = torch.zeros_like(kv)
+    ik = torch.zeros(40, 4352 if fp4 else 8448, dtype=torch.uint8, device=dev)
+    klat = torch.empty(n_ent, 128, dtype=torch.float32, device=dev)
+    csa2.compress_m2(Cm, Z if ratio == 2 else None, ratio, gamma, kv, page_table=pt, first_entry=first,
+                     w_ik=w_ik, k_gamma=k_gamma, index_k=ik, index_latent_out=klat)
+    csa2.compress_m2(Cm, Z if ratio == 2 else None, ratio, gamma, kv_plain, page_table=pt, first_entry=first)
+    torch.cuda.synchronize()
+    assert csa2.check_device_error() == 0
+    assert torch.equal(kv, kv_plain)                                # the main-KV records are unchanged
+    pos = (first + np.arange(n_ent)) * ratio
+    y_pre = o.compress_latent(Cm.float().cpu().numpy().astype(np.float64),
+                              Z.float().cpu().numpy().astype(np.float64) if ratio == 2 else None,
+                              ratio, np_(gamma).astype(np.float64), 1e-6, pos, 10000.0, apply_rope=False)
+    ref = o.index_key_latent(y_pre, w_ik.float().cpu().numpy().astype(np.float64), np_(k_gamma).astype(np.float64),
+                             1e-6, pos, 10000.0)
+    got = np_(klat)
+    assert np.abs(got - ref).max() <= 1e-4 * np.abs(ref).max()
+    # the entry bytes equal the oracle's encoder applied to the kernel's own fp32 key
+    slots = o.slots_of(first + np.arange(n_ent), np_(pt))
+    page, row = slots // 64, slots % 64
+    pages = np_(ik)
+    if fp4:
+        c4, u4 = o.index_key_fp4_bytes(got.astype(np.float64))
+        assert np.array_equal(pages[page[:, None], row[:, None] * 64 + np.arange(64)[None, :]], c4)
+        assert np.array_equal(pages[page[:, None], 4096 + row[:, None] * 4 + np.arange(4)[None, :]], u4)
+        dec = o.index_k_fp4_at(pages, np_(pt), first + np.arange(n_ent))
+        assert np.all(np.abs(dec - ref) <= np.repeat(o.ue8m0(u4), 32, axis=1) + 1e-4 * np.abs(ref).max())
+    else:
+        c8, s8 = o.index_key_fp8_bytes(got)
+        assert np.array_equal(pages[page[:, None], row[:, None] * 128 + np.arange(128)[None, :]], c8)
+        sb = pages[page[:, None], 8192 + row[:, None] * 4 + np.arange(4)[None, :]]
+        assert np.array_equal(np.ascontiguousarray(sb).view(np.float32).reshape(-1), s8)
+        dec = o.index_k_at(pages, np_(pt), first + np.arange(n_ent))
+        assert np.all(np.abs(dec - ref) <= np.abs(ref) * 2.0 ** -4 + s8[:, None] * 2.0 ** -9 + 1e-4 * np.abs(ref).max())
