@@ -9,6 +9,13 @@
 //
 // One warp per entry, lane l owning channels 16l .. 16l+15 (two e2m1 scale
 // groups span a lane pair).  HBM-bound: 2 KB (m=2: 4 KB) read, 288 B written.
+//
+// With W^IK the kernel also writes each entry's index key (V4.1 Q&A page:
+// k = RMSNorm(y W^IK) from the latent before RoPE, RoPE on its last 64 dims;
+// CSA2 page item 3: wk -> k_norm -> RoPE -> quantisation).  The CTA's 8
+// latents go to shared memory and the 8 warps split the 512 x 128 projection
+// by input rows (each warp's 64 rows of W^IK are loaded before the dependency
+// wait), so W^IK is read once per CTA.
 #include <cuda_fp8.h>
 #include <math.h>
 
@@ -44,22 +51,6 @@ struct CompressParams {
   float* index_latent_out;
   uint32_t* err;
 };
-
-// Sum over the warp of 32 values per lane, scattered: lane l returns the total
-// of element l (five butterfly halvings, 31 shuffles).
-__device__ __forceinline__ float reduce_scatter32(float (&v)[32], int lane) {
-#pragma unroll
-  for (int s = 16; s >= 1; s >>= 1) {
-    const bool up = (lane & s) != 0;
-#pragma unroll
-    for (int j = 0; j < s; ++j) {
-      const float send = up ? v[j] : v[j + s];
-      const float keep = up ? v[j + s] : v[j];
-      v[j] = keep + __shfl_xor_sync(0xffffffffu, send, s);
-    }
-  }
-  return v[0];
-}
 
 // sin and cos of pos * inv_freq: the angle reaches ~1e6 rad, so it is formed
 // and reduced modulo 2 pi in double (2 pi split in two parts), then sin/cos
@@ -98,13 +89,34 @@ __device__ __forceinline__ uint32_t e2m1_code(float v) {
   return c | (v < 0.f ? 8u : 0u);
 }
 
+// Shared memory of the index-key phase: the CTA's 8 latents before RoPE,
+// [512 channels][8 entries], then the partial projections [8 warps][8 entries][128].
+template <int EPC>
+constexpr int ik_smem_floats() { return 512 * EPC + 8 * EPC * 128; }
+
+// IK: also the index keys (W^IK given); EPC: entries per CTA (8, or 1 so that
+// few entries spread over more SMs: the other warps then only help project)
+template <bool IK, int EPC>
 __global__ void __launch_bounds__(256) compress_kernel(const __grid_constant__ CompressParams p) {
+  extern __shared__ float s_ik[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // W^IK is a weight (no earlier kernel writes it): this warp's 64 rows, lane
+  // l's 4 columns 4l .. 4l+3, are loaded before the dependency wait
+  uint2 wr[IK ? 64 : 1];
+  if constexpr (IK) {
+#pragma unroll
+    for (int r = 0; r < 64; ++r)
+      wr[r] = __ldg(reinterpret_cast<const uint2*>(p.w_ik + (64 * warp + r) * 128 + 4 * lane));
+  }
   pdl_wait();
   pdl_trigger();
-  const long long e = static_cast<long long>(blockIdx.x) * 8 + warp;
-  if (e >= p.n_entries) return;
+  const long long e_raw = static_cast<long long>(blockIdx.x) * EPC + warp;
+  const bool active = warp < EPC && e_raw < p.n_entries;  // other warps help the index-key phase only
+  const long long e = active ? e_raw : p.n_entries - 1;
   const int c0 = lane * 16;
+  long long pos = 0, slot = -1;
+  bool slot_ok = false;
+  if (warp < EPC) {
   float x[16];
   if (p.ratio_m == 1) {
     load16_bf16(p.C + e * 512 + c0, x);
@@ -132,49 +144,10 @@ __global__ void __launch_bounds__(256) compress_kernel(const __grid_constant__ C
   float y[16];
 #pragma unroll
   for (int i = 0; i < 16; ++i) y[i] = x[i] * inv * __ldg(p.gamma + c0 + i);
-  const long long pos = p.entry_pos ? static_cast<long long>(__ldg(p.entry_pos + e)) : (p.first_entry + e) * p.ratio_m;
-  // index key (V4.1 Q&A page): k = RMSNorm(y W^IK) * k_gamma from the latent
-  // before RoPE, then RoPE on dims 64..127; lane l holds k[32 b + l], b < 4
-  float kk[4] = {0.f, 0.f, 0.f, 0.f};
-  if (p.w_ik) {
+  pos = p.entry_pos ? static_cast<long long>(__ldg(p.entry_pos + e)) : (p.first_entry + e) * p.ratio_m;
+  if constexpr (IK) {  // the latent before RoPE feeds the index key
 #pragma unroll
-    for (int b = 0; b < 4; ++b) {
-      float part[32];
-#pragma unroll
-      for (int j = 0; j < 32; ++j) part[j] = 0.f;
-#pragma unroll 4
-      for (int i = 0; i < 16; ++i) {
-        const uint4* wr = reinterpret_cast<const uint4*>(p.w_ik + (c0 + i) * 128 + 32 * b);
-        const float yi = y[i];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const uint4 r = __ldg(wr + q);
-          const uint32_t w4[4] = {r.x, r.y, r.z, r.w};
-#pragma unroll
-          for (int t2 = 0; t2 < 4; ++t2) {
-            const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w4[t2]));
-            part[8 * q + 2 * t2] = fmaf(yi, f.x, part[8 * q + 2 * t2]);
-            part[8 * q + 2 * t2 + 1] = fmaf(yi, f.y, part[8 * q + 2 * t2 + 1]);
-          }
-        }
-      }
-      kk[b] = reduce_scatter32(part, lane);
-    }
-    float s2 = (kk[0] * kk[0] + kk[1] * kk[1]) + (kk[2] * kk[2] + kk[3] * kk[3]);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) s2 += __shfl_xor_sync(0xffffffffu, s2, o);
-    const float inv2 = 1.0f / sqrtf(s2 / 128.0f + p.eps);
-#pragma unroll
-    for (int b = 0; b < 4; ++b) kk[b] = kk[b] * inv2 * __ldg(p.k_gamma + 32 * b + lane);
-    if (p.apply_rope) {
-#pragma unroll
-      for (int b = 2; b < 4; ++b) {  // dims 64..127: pair i = (dim - 64) / 2 of lanes (2j, 2j+1)
-        float sn, cs;
-        rope_angle(pos, p.inv_freq[16 * (b - 2) + (lane >> 1)], &sn, &cs);
-        const float other = __shfl_xor_sync(0xffffffffu, kk[b], 1);
-        kk[b] = (lane & 1) ? fmaf(other, sn, kk[b] * cs) : fmaf(-other, sn, kk[b] * cs);
-      }
-    }
+    for (int i = 0; i < 16; ++i) s_ik[(c0 + i) * EPC + warp] = y[i];
   }
   // RoPE on dims 448..511: interleaved pairs, angle pos * theta^(-2i/64)
   if (p.apply_rope && lane >= 28) {
@@ -188,7 +161,7 @@ __global__ void __launch_bounds__(256) compress_kernel(const __grid_constant__ C
       y[2 * j + 1] = a * sn + b * cs;
     }
   }
-  if (p.latent_out) {
+  if (p.latent_out && active) {
     float4* lo = reinterpret_cast<float4*>(p.latent_out + e * 512 + c0);
 #pragma unroll
     for (int i = 0; i < 4; ++i) lo[i] = make_float4(y[4 * i], y[4 * i + 1], y[4 * i + 2], y[4 * i + 3]);
@@ -212,7 +185,6 @@ __global__ void __launch_bounds__(256) compress_kernel(const __grid_constant__ C
     packed[i >> 3] |= code << (4 * (i & 7));
   }
   // destination slot
-  long long slot;
   if (p.entry_slot) {
     slot = __ldg(p.entry_slot + e);
   } else {
@@ -220,57 +192,124 @@ __global__ void __launch_bounds__(256) compress_kernel(const __grid_constant__ C
     const long long lp = ent >> 6;
     slot = (lp < p.pt_len) ? static_cast<long long>(__ldg(p.page_table + lp)) * 64 + (ent & 63) : -1;
   }
-  if (slot < 0 || slot >= p.main_slots) {
+  slot_ok = slot >= 0 && slot < p.main_slots;
+  if (active && !slot_ok && lane == 0) set_error(p.err, kErrBounds);
+  if (active && slot_ok) {
+    uint8_t* rec = p.main_kv + slot * 288;
+    *reinterpret_cast<uint2*>(rec + lane * 8) = make_uint2(packed[0], packed[1]);
+    if ((lane & 1) == 0) rec[256 + (lane >> 1)] = static_cast<uint8_t>(u);
+    if (lane < 4) *reinterpret_cast<uint32_t*>(rec + 272 + lane * 4) = 0u;
+  }
+  }  // warp < EPC
+  if constexpr (!IK) return;
+
+  // ---- index keys of the CTA's entries (V4.1 Q&A page): k = RMSNorm(y W^IK) *
+  // k_gamma from the latents before RoPE, RoPE on dims 64..127, then the FP8 or
+  // FP4 entry.  Warp w multiplies channels 64w .. 64w+63 of all 8 latents by
+  // its rows of W^IK (lane l: outputs 4l .. 4l+3); the 8 partial sums of each
+  // entry are then added by the entry's own warp.
+  __syncthreads();
+  float acc[EPC][4];
+#pragma unroll
+  for (int q = 0; q < EPC; ++q)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) acc[q][j] = 0.f;
+#pragma unroll
+  for (int r = 0; r < 64; ++r) {
+    float yv[EPC];
+    if constexpr (EPC == 8) {
+      const float4 ya = *reinterpret_cast<const float4*>(s_ik + (64 * warp + r) * 8);
+      const float4 yb = *reinterpret_cast<const float4*>(s_ik + (64 * warp + r) * 8 + 4);
+      yv[0] = ya.x; yv[1] = ya.y; yv[2] = ya.z; yv[3] = ya.w;
+      yv[4] = yb.x; yv[5] = yb.y; yv[6] = yb.z; yv[7] = yb.w;
+    } else {
+#pragma unroll
+      for (int q = 0; q < EPC; ++q) yv[q] = s_ik[(64 * warp + r) * EPC + q];
+    }
+    const float2 w01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wr[r].x));
+    const float2 w23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wr[r].y));
+#pragma unroll
+    for (int q = 0; q < EPC; ++q) {
+      acc[q][0] = fmaf(yv[q], w01.x, acc[q][0]);
+      acc[q][1] = fmaf(yv[q], w01.y, acc[q][1]);
+      acc[q][2] = fmaf(yv[q], w23.x, acc[q][2]);
+      acc[q][3] = fmaf(yv[q], w23.y, acc[q][3]);
+    }
+  }
+  float* s_part = s_ik + 512 * EPC;  // [warp][entry][128]
+#pragma unroll
+  for (int q = 0; q < EPC; ++q)
+    *reinterpret_cast<float4*>(s_part + (warp * EPC + q) * 128 + 4 * lane) =
+        make_float4(acc[q][0], acc[q][1], acc[q][2], acc[q][3]);
+  __syncthreads();
+  if (warp >= EPC) return;
+  float kk[4] = {0.f, 0.f, 0.f, 0.f};  // k[4 lane + j] of this warp's entry
+#pragma unroll
+  for (int w = 0; w < 8; ++w) {
+    const float4 v = *reinterpret_cast<const float4*>(s_part + (w * EPC + warp) * 128 + 4 * lane);
+    kk[0] += v.x;
+    kk[1] += v.y;
+    kk[2] += v.z;
+    kk[3] += v.w;
+  }
+  float s2 = (kk[0] * kk[0] + kk[1] * kk[1]) + (kk[2] * kk[2] + kk[3] * kk[3]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) s2 += __shfl_xor_sync(0xffffffffu, s2, o);
+  const float inv2 = 1.0f / sqrtf(s2 / 128.0f + p.eps);
+  const float4 kg = __ldg(reinterpret_cast<const float4*>(p.k_gamma) + lane);
+  kk[0] *= inv2 * kg.x;
+  kk[1] *= inv2 * kg.y;
+  kk[2] *= inv2 * kg.z;
+  kk[3] *= inv2 * kg.w;
+  if (p.apply_rope && lane >= 16) {  // dims 64..127: pairs (4l, 4l+1), (4l+2, 4l+3) = pair 2l-32, 2l-31
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      float sn, cs;
+      rope_angle(pos, p.inv_freq[2 * lane - 32 + h], &sn, &cs);
+      const float a = kk[2 * h], b = kk[2 * h + 1];
+      kk[2 * h] = a * cs - b * sn;
+      kk[2 * h + 1] = a * sn + b * cs;
+    }
+  }
+  if (!active) return;
+  if (p.index_latent_out)
+    *reinterpret_cast<float4*>(p.index_latent_out + e * 128 + 4 * lane) = make_float4(kk[0], kk[1], kk[2], kk[3]);
+  if (!slot_ok) return;
+  const long long page = slot >> 6;
+  const int row = static_cast<int>(slot & 63);
+  if (page >= p.index_k_pages) {
     if (lane == 0) set_error(p.err, kErrBounds);
     return;
   }
-  uint8_t* rec = p.main_kv + slot * 288;
-  *reinterpret_cast<uint2*>(rec + lane * 8) = make_uint2(packed[0], packed[1]);
-  if ((lane & 1) == 0) rec[256 + (lane >> 1)] = static_cast<uint8_t>(u);
-  if (lane < 4) *reinterpret_cast<uint32_t*>(rec + 272 + lane * 4) = 0u;
-  if (p.w_ik) {
-    if (p.index_latent_out) {
+  if (!p.index_k_fp4) {  // FP8: one fp32 scale amax / 448, e4m3 codes round-to-nearest-even
+    float am = fmaxf(fmaxf(fabsf(kk[0]), fabsf(kk[1])), fmaxf(fabsf(kk[2]), fabsf(kk[3])));
 #pragma unroll
-      for (int b = 0; b < 4; ++b) p.index_latent_out[e * 128 + 32 * b + lane] = kk[b];
+    for (int o = 16; o > 0; o >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
+    const float sc = am > 0.f ? am / 448.0f : 1.0f;
+    uint8_t* pg = p.index_k + page * 8448;
+    uint32_t word = 0u;
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      word |= static_cast<uint32_t>(__nv_cvt_float_to_fp8(kk[j] / sc, __NV_SATFINITE, __NV_E4M3)) << (8 * j);
+    *reinterpret_cast<uint32_t*>(pg + row * 128 + 4 * lane) = word;
+    if (lane == 0) *reinterpret_cast<float*>(pg + 8192 + row * 4) = sc;
+  } else {  // FP4: e2m1 + one ue8m0 scale per 32 dims (lanes 8b .. 8b+7)
+    float am = fmaxf(fmaxf(fabsf(kk[0]), fabsf(kk[1])), fmaxf(fabsf(kk[2]), fabsf(kk[3])));
+#pragma unroll
+    for (int o = 4; o > 0; o >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
+    int ue = 127;
+    if (am > 0.f) {
+      int ex;
+      const float f = frexpf(am, &ex);
+      const int k = (f <= 0.75f) ? ex - 3 : ex - 2;
+      ue = min(max(k + 127, 0), 254);
     }
-    const long long page = slot >> 6;
-    const int row = static_cast<int>(slot & 63);
-    if (page >= p.index_k_pages) {
-      if (lane == 0) set_error(p.err, kErrBounds);
-      return;
-    }
-    if (!p.index_k_fp4) {  // FP8: one fp32 scale amax / 448, e4m3 codes round-to-nearest-even
-      float am = fmaxf(fmaxf(fabsf(kk[0]), fabsf(kk[1])), fmaxf(fabsf(kk[2]), fabsf(kk[3])));
+    uint32_t half = 0u;
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
-      const float sc = am > 0.f ? am / 448.0f : 1.0f;
-      uint8_t* pg = p.index_k + page * 8448;
-#pragma unroll
-      for (int b = 0; b < 4; ++b)
-        pg[row * 128 + 32 * b + lane] = static_cast<uint8_t>(__nv_cvt_float_to_fp8(kk[b] / sc, __NV_SATFINITE, __NV_E4M3));
-      if (lane == 0) *reinterpret_cast<float*>(pg + 8192 + row * 4) = sc;
-    } else {  // FP4: e2m1 + one ue8m0 scale per 32 dims (a block = one register across the warp)
-      uint8_t* pg = p.index_k + page * 4352;
-      uint32_t ub = 0u;
-#pragma unroll
-      for (int b = 0; b < 4; ++b) {
-        float am = fabsf(kk[b]);
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
-        int ue = 127;
-        if (am > 0.f) {
-          int ex;
-          const float f = frexpf(am, &ex);
-          const int k = (f <= 0.75f) ? ex - 3 : ex - 2;
-          ue = min(max(k + 127, 0), 254);
-        }
-        const uint32_t code = e2m1_code(ldexpf(kk[b], 127 - ue));
-        const uint32_t hi = __shfl_xor_sync(0xffffffffu, code, 1);
-        if ((lane & 1) == 0) pg[row * 64 + 16 * b + (lane >> 1)] = static_cast<uint8_t>(code | (hi << 4));
-        ub |= static_cast<uint32_t>(ue) << (8 * b);
-      }
-      if (lane == 0) *reinterpret_cast<uint32_t*>(pg + 4096 + row * 4) = ub;
-    }
+    for (int j = 0; j < 4; ++j) half |= e2m1_code(ldexpf(kk[j], 127 - ue)) << (4 * j);
+    uint8_t* pg = p.index_k + page * 4352;
+    *reinterpret_cast<uint16_t*>(pg + row * 64 + 2 * lane) = static_cast<uint16_t>(half);
+    if ((lane & 7) == 0) pg[4096 + row * 4 + (lane >> 3)] = static_cast<uint8_t>(ue);
   }
 }
 
@@ -302,10 +341,26 @@ cudaError_t launch_compress(const CompressLaunch& a, const DeviceCtx& ctx, cudaS
   p.index_latent_out = a.index_latent_out;
   p.err = ctx.err;
   if (a.n_entries == 0) return cudaSuccess;
+  if (!a.w_ik) {
+    const long long blocks = (a.n_entries + 7) / 8;
+    cudaError_t e = prefer_max_smem(compress_kernel<false, 8>, 0);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(compress_kernel<false, 8>, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, st, p);
+  }
+  // with index keys: up to one entry per SM, one entry per CTA (the projection
+  // of an entry spread over 8 warps); beyond, 8 entries per CTA (W^IK read
+  // once per 8 entries)
+  if (a.n_entries <= ctx.num_sms) {
+    constexpr size_t smem = ik_smem_floats<1>() * sizeof(float);
+    cudaError_t e = prefer_max_smem(compress_kernel<true, 1>, smem);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(compress_kernel<true, 1>, dim3(static_cast<unsigned>(a.n_entries)), dim3(256), smem, st, p);
+  }
   const long long blocks = (a.n_entries + 7) / 8;
-  cudaError_t e = prefer_max_smem(compress_kernel, 0);
+  constexpr size_t smem = ik_smem_floats<8>() * sizeof(float);
+  cudaError_t e = prefer_max_smem(compress_kernel<true, 8>, smem);
   if (e != cudaSuccess) return e;
-  return launch_pdl(compress_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, st, p);
+  return launch_pdl(compress_kernel<true, 8>, dim3(static_cast<unsigned>(blocks)), dim3(256), smem, st, p);
 }
 
 }  // namespace csa2

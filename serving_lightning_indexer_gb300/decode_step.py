@@ -63,6 +63,8 @@ class LayerInputs:
     C: torch.Tensor | None = None    # bf16 [B*m, 512] tokens of the new entry (Full layers)
     Z: torch.Tensor | None = None
     gamma: torch.Tensor | None = None
+    w_ik: torch.Tensor | None = None  # bf16 [512,128] index-key projection of a Full layer (weights)
+    k_gamma: torch.Tensor | None = None
 
 
 @dataclass
@@ -107,6 +109,7 @@ class DecodeStep:
                 m = self.caches[cache_of(l)].ratio_m
                 Cm, Z, gamma = W.make_compress_inputs(self.B * m, seed=seed * 1000 + 700 + l, device=dev)
                 li.C, li.Z, li.gamma = Cm, (Z if m == 2 else None), gamma
+                li.w_ik, li.k_gamma = W.make_index_projection(seed=seed * 1000 + 800 + l, device=dev)
             self.inputs[l] = li
         ld = max(c.ld for c in self.caches if c is not None)
         self.buf = StepBuffers(
@@ -160,9 +163,11 @@ class DecodeStep:
             c = self.caches[ci]
             role = role_of(l)
             if role == "full":
-                # the Full layer writes its group's newest main-KV entry, then scores and selects
+                # the Full layer writes its group's newest main-KV entry and index key,
+                # then scores and selects
                 csa2.compress_m2(li.C, li.Z, c.ratio_m, li.gamma, c.pc.main_kv, entry_slot=c.entry_slot_new,
-                                 entry_pos=c.entry_pos_new, stream=stream)
+                                 entry_pos=c.entry_pos_new, stream=stream, w_ik=li.w_ik, k_gamma=li.k_gamma,
+                                 index_k=c.pc.index_k)
                 sc = b.scores[:, :c.ld]
                 bm = b.block_max[:, :c.ld // 8]
                 if self.on_index_score:

@@ -171,12 +171,14 @@ def test_attention_keys_gathered_early_give_identical_results():
     assert torch.equal(outs[0], outs[1]) and torch.equal(outs[0], outs[2])
 
 
-@pytest.mark.parametrize("ratio,fp4", [(2, False), (1, False), (2, True), (1, True)])
-def test_compress_builds_index_keys(ratio, fp4):
+@pytest.mark.parametrize("ratio,fp4,n_ent", [(2, False, 1001), (1, False, 1001), (2, True, 1001), (1, True, 1001),
+                                              (2, False, 7), (1, True, 152)])
+def test_compress_builds_index_keys(ratio, fp4, n_ent):
     # Full layer's index key from the main-KV latent before RoPE (V4.1 Q&A page):
-    # k = RMSNorm(y W^IK) * k_gamma, RoPE on dims 64..127, FP8 or FP4 entry
+    # k = RMSNorm(y W^IK) * k_gamma, RoPE on dims 64..127, FP8 or FP4 entry;
+    # up to one entry per SM takes the one-entry-per-CTA launch, beyond it eight
     dev = need_gpu()
-    n_tok = 1000 * ratio + ratio
+    n_tok = n_ent * ratio
     Cm, Z, gamma = W.make_compress_inputs(n_tok, seed=40 + ratio, device=dev)
     w_ik, k_gamma = W.make_index_projection(seed=41, device=dev)
     n_ent = n_tok // ratio
