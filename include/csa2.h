@@ -243,6 +243,24 @@ typedef struct {
    * their dependents only after their own dependency wait (as every kernel of
    * this library does).  0: everything is read after the previous launch. */
   int32_t kv_ready;
+  /* Optional (zero / NULL leaves each off):
+   * q_pos [T]: position of each query row in its sequence.
+   * out_inv_rope = 1: the output is rotated back by its query's RoPE before it
+   *   is stored (CSA2 page, attention section: the output is un-RoPE'd before
+   *   the grouped output projection): pair (448+2p, 449+2p) of out[t,i] turns
+   *   by -q_pos[t] * rope_theta^(-2p/64), p < 32, the inverse of the rotation
+   *   the keys carry.  rope_theta == 0 selects 10000.  lse is not affected.
+   * swa_seg_start [T]: SWA bounded replay (CSA2 page, "Decoder SWA Bounded
+   *   Replay"): swa_slot[t][j] holds the key at position
+   *   q_pos[t] - n_swa + 1 + j, and a key at a position below
+   *   swa_seg_start[t] is skipped, so the row at position i attends to the
+   *   SWA keys of [max(s, i - n_swa + 1), i] only.
+   * Both need q_pos.  q_pos and swa_seg_start are read together with the slots
+   * (under kv_ready = 1 they too must be written two launches before). */
+  const int32_t* q_pos;
+  int32_t out_inv_rope;
+  float rope_theta;
+  const int32_t* swa_seg_start;
 } csa2_sparse_attn_args;
 CSA2_API int csa2_sparse_attn(const csa2_sparse_attn_args* args, void* workspace, size_t ws_bytes, void* stream);
 

@@ -352,18 +352,50 @@ def sparse_attention(q: np.ndarray, kv: np.ndarray, sink: np.ndarray, scale: flo
     return o, m + np.log(denom)
 
 
-def attention_row(q_bf16_values, main_cache, topk_slot_row, swa_cache, swa_slot_row, sink, scale):
+def swa_replay_visible(q_pos: int, seg_start: int, n_swa: int) -> np.ndarray:
+    """Which keys of a query row's SWA window stay visible under Decoder SWA
+    Bounded Replay (CSA2 page, "Decoder SWA Bounded Replay"): the query at
+    position i of a replayed segment that starts at s sees the SWA keys at
+    positions [max(s, i - W + 1), i] only.  Readings: the window W is the
+    row's number of SWA slots, and slot j of the window holds position
+    i - W + 1 + j (oldest first, the query's own key last).  Returns bool [W]."""
+    i, W = int(q_pos), int(n_swa)
+    key_pos = i - W + 1 + np.arange(W)
+    lo = max(int(seg_start), i - W + 1)
+    return (key_pos >= lo) & (key_pos <= i)
+
+
+def output_inverse_rope(o: np.ndarray, q_pos: int, theta: float) -> np.ndarray:
+    """The attention output of a query at position q_pos with its RoPE taken
+    back off the last 64 dims, before the grouped output projection (CSA2 page,
+    attention section: the output is un-RoPE'd first).  The inverse of the
+    rotation by angle q_pos * f is the rotation by -q_pos * f, i.e. the
+    same interleaved RoPE at position -q_pos."""
+    o = np.asarray(o, dtype=np.float64)
+    return rope_interleaved(o, np.full(o.shape[0], -float(q_pos)), theta)
+
+
+def attention_row(q_bf16_values, main_cache, topk_slot_row, swa_cache, swa_slot_row, sink, scale,
+                  q_pos=None, swa_seg_start=None, inv_rope_theta=None):
     """Attention of one query row from the caches: gathers the valid SWA and main
-    slots (slot -1 is empty) and evaluates ``sparse_attention``."""
+    slots (slot -1 is empty) and evaluates ``sparse_attention``.  With
+    ``swa_seg_start`` the SWA window is cut to the replayed segment
+    (``swa_replay_visible``); with ``inv_rope_theta`` the output is
+    un-RoPE'd at ``q_pos`` (``output_inverse_rope``)."""
     ts = np.asarray(topk_slot_row, dtype=np.int64)
     ss = np.asarray(swa_slot_row, dtype=np.int64)
+    if swa_seg_start is not None:
+        ss = np.where(swa_replay_visible(q_pos, swa_seg_start, ss.shape[0]), ss, -1)
     parts = []
     if (ss >= 0).any():
         parts.append(swa_records(swa_cache, ss[ss >= 0]))
     if (ts >= 0).any():
         parts.append(main_kv_records(main_cache, ts[ts >= 0]))
     kv = np.concatenate(parts, axis=0) if parts else np.zeros((0, ATT_DIM))
-    return sparse_attention(q_bf16_values, kv, sink, scale)
+    o, lse = sparse_attention(q_bf16_values, kv, sink, scale)
+    if inv_rope_theta is not None:
+        o = output_inverse_rope(o, q_pos, inv_rope_theta)
+    return o, lse
 
 
 # ---------------------------------------------------------------------------

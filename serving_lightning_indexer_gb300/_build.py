@@ -19,7 +19,7 @@ OBJDIR = os.path.join(PKG, "_build")
 LIB = os.path.join(LIBDIR, "libcsa2.so")
 SOURCES = ["csa2_api.cu", "index_score.cu", "select.cu", "sparse_attn.cu", "compress.cu", "topk_noalloc.cu"]
 HEADERS = [os.path.join(ROOT, "include", "csa2.h")] + [
-    os.path.join(CSRC, f) for f in ("csa2_device.cuh", "csa2_internal.h")]
+    os.path.join(CSRC, f) for f in ("csa2_device.cuh", "csa2_rope.cuh", "csa2_internal.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
          "--expt-relaxed-constexpr"]

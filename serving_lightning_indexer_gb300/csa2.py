@@ -53,7 +53,8 @@ class SparseAttnArgs(C.Structure):
     _fields_ = [("q", _P), ("main_kv", _P), ("main_kv_slots", _I64), ("topk_slot", _P), ("k", _I32),
                 ("ld_topk", _I64), ("swa_kv", _P), ("swa_slots", _I64), ("swa_slot", _P), ("n_swa", _I32),
                 ("ld_swa", _I64), ("sink", _P), ("softmax_scale", C.c_float), ("T", _I32), ("out_bf16", _I32),
-                ("out", _P), ("lse", _P), ("kv_ready", _I32)]
+                ("out", _P), ("lse", _P), ("kv_ready", _I32), ("q_pos", _P), ("out_inv_rope", _I32),
+                ("rope_theta", C.c_float), ("swa_seg_start", _P)]
 
 
 class CompressArgs(C.Structure):
@@ -218,8 +219,11 @@ def reindex(q_fp8, q_scale, w, index_k, page_table, r: Rows, pool_blocks, k, top
 
 
 def sparse_attn(q, main_kv, topk_slot, swa_kv, swa_slot, sink, out, lse=None, softmax_scale=0.0, k=None,
-                n_swa=None, stream=None, ws=None, kv_ready=False):
-    """MQA sparse attention with SWA keys and sink (csa2_sparse_attn)."""
+                n_swa=None, stream=None, ws=None, kv_ready=False, q_pos=None, out_inv_rope=False, rope_theta=0.0,
+                swa_seg_start=None):
+    """MQA sparse attention with SWA keys and sink (csa2_sparse_attn); with q_pos
+    ([T] int32) optionally the output's inverse RoPE and the SWA bounded-replay
+    mask (swa_seg_start, [T] int32)."""
     lib = load()
     T = q.shape[0]
     kk = topk_slot.shape[-1] if (k is None and topk_slot is not None) else (k or 0)
@@ -228,7 +232,8 @@ def sparse_attn(q, main_kv, topk_slot, swa_kv, swa_slot, sink, out, lse=None, so
                        topk_slot.shape[-1] if topk_slot is not None else 0, _ptr(swa_kv),
                        swa_kv.shape[0] if swa_kv is not None else 0, _ptr(swa_slot), ns,
                        swa_slot.shape[-1] if swa_slot is not None else 0, _ptr(sink), float(softmax_scale), T,
-                       1 if out.dtype == torch.bfloat16 else 0, _ptr(out), _ptr(lse), 1 if kv_ready else 0)
+                       1 if out.dtype == torch.bfloat16 else 0, _ptr(out), _ptr(lse), 1 if kv_ready else 0,
+                       _ptr(q_pos), 1 if out_inv_rope else 0, float(rope_theta), _ptr(swa_seg_start))
     need = C.c_size_t(0)
     _check(lib.csa2_workspace_size(CALL_SPARSE_ATTN, C.cast(C.byref(a), _P), C.byref(need)), "csa2_workspace_size")
     buf = ws if ws is not None else workspace(need.value, q.device, "attn")

@@ -20,6 +20,7 @@
 #include <math.h>
 
 #include "csa2_device.cuh"
+#include "csa2_rope.cuh"
 #include "csa2_internal.h"
 
 namespace csa2 {
@@ -51,19 +52,6 @@ struct CompressParams {
   float* index_latent_out;
   uint32_t* err;
 };
-
-// sin and cos of pos * inv_freq: the angle reaches ~1e6 rad, so it is formed
-// and reduced modulo 2 pi in double (2 pi split in two parts), then sin/cos
-// run in fp32 on the reduced angle.
-__device__ __forceinline__ void rope_angle(long long pos, double inv_freq, float* sn, float* cs) {
-  constexpr double kTwoPiHi = 6.283185307179586;
-  constexpr double kTwoPiLo = 2.4492935982947064e-16;
-  constexpr double kInvTwoPi = 0.15915494309189535;
-  const double ang = static_cast<double>(pos) * inv_freq;
-  const double kq = rint(ang * kInvTwoPi);
-  const double red = fma(-kq, kTwoPiLo, fma(-kq, kTwoPiHi, ang));
-  sincosf(static_cast<float>(red), sn, cs);
-}
 
 __device__ __forceinline__ void load16_bf16(const __nv_bfloat16* src, float (&v)[16]) {
   const uint4* s = reinterpret_cast<const uint4*>(src);

@@ -358,6 +358,12 @@ static int attn_check(const csa2_sparse_attn_args* a) {
     return fail(CSA2_ERR_ALIGN, "csa2_sparse_attn: q, out, main_kv, swa_kv must be 16-B aligned");
   if (!(a->softmax_scale >= 0.f) || !isfinite(a->softmax_scale))
     return fail(CSA2_ERR_SHAPE, "csa2_sparse_attn: softmax_scale must be finite and >= 0");
+  if (a->out_inv_rope != 0 && a->out_inv_rope != 1)
+    return fail(CSA2_ERR_SHAPE, "csa2_sparse_attn: out_inv_rope=%d must be 0 or 1", a->out_inv_rope);
+  if ((a->out_inv_rope || a->swa_seg_start) && !a->q_pos)
+    return fail(CSA2_ERR_NULL, "csa2_sparse_attn: out_inv_rope and swa_seg_start need q_pos");
+  if (!(a->rope_theta >= 0.f) || !isfinite(a->rope_theta))
+    return fail(CSA2_ERR_SHAPE, "csa2_sparse_attn: rope_theta must be finite and >= 0");
   return CSA2_OK;
 }
 
@@ -389,6 +395,10 @@ int csa2_sparse_attn(const csa2_sparse_attn_args* a, void* ws, size_t ws_bytes, 
   L.out = a->out;
   L.lse = a->lse;
   L.kv_ready = a->kv_ready != 0;
+  L.q_pos = a->q_pos;
+  L.inv_rope = a->out_inv_rope;
+  L.rope_theta = a->rope_theta > 0.f ? a->rope_theta : 10000.0f;
+  L.swa_seg_start = a->swa_seg_start;
   e = csa2::launch_sparse_attn(L, ws, ws_bytes, ctx, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "csa2_sparse_attn: launch");
   return CSA2_OK;

@@ -112,6 +112,10 @@ struct AttnLaunch {
   void* out;
   float* lse;
   int kv_ready;  // slots and caches written at least two launches before: gather before the dependency wait
+  const int* q_pos;          // [T] query positions (inverse RoPE, bounded replay)
+  int inv_rope;              // rotate the output's last 64 dims back by the query's RoPE
+  float rope_theta;
+  const int* swa_seg_start;  // [T] bounded-replay segment starts, or null
 };
 int attn_num_splits(int T, int n_keys, int num_sms);
 size_t attn_workspace_bytes(int T, int n_keys, int num_sms);

@@ -22,6 +22,7 @@
 #include <math.h>
 
 #include "csa2_device.cuh"
+#include "csa2_rope.cuh"
 #include "csa2_internal.h"
 
 namespace csa2 {
@@ -60,6 +61,10 @@ struct AttnParams {
   float* lse;
   int nsplit;             // CTAs per row = cluster size
   int chunks_per_split;
+  const int* q_pos;          // [T] query positions (inverse RoPE, bounded replay)
+  const int* swa_seg_start;  // [T] bounded-replay segment starts, or null
+  int inv_rope;              // rotate the output's last 64 dims back by the query's RoPE
+  double inv_freq[32];       // theta^(-2p/64)
   uint32_t* err;
 };
 
@@ -238,6 +243,11 @@ __device__ __forceinline__ int key_slot(const AttnParams& p, int t, int j, int* 
   *kind = 0;
   if (j < p.n_swa) {
     slot = __ldg(p.swa_slot + static_cast<long long>(t) * p.ld_swa + j);
+    // bounded replay: slot j holds position q_pos - n_swa + 1 + j; keys before
+    // the segment start are not attended to
+    if (p.swa_seg_start &&
+        static_cast<long long>(__ldg(p.q_pos + t)) - p.n_swa + 1 + j < __ldg(p.swa_seg_start + t))
+      slot = -1;
     if (slot >= p.swa_slots) {
       set_error(p.err, kErrBounds);
       slot = -1;
@@ -464,14 +474,21 @@ __global__ void __launch_bounds__(512, 1) sparse_attn_kernel(const __grid_consta
 #pragma unroll
     for (int nt = 0; nt < 16; ++nt) {
       const int d = 128 * xg + nt * 8 + 2 * cq;
+      float a0 = o[nt][0] * f0, b0 = o[nt][1] * f0, a1 = o[nt][2] * f1, b1 = o[nt][3] * f1;
+      if (p.inv_rope && d >= kD - 64) {  // (d, d + 1) is RoPE pair (d - 448) / 2
+        const long long pos = __ldg(p.q_pos + t);
+        const double fr = p.inv_freq[(d - (kD - 64)) >> 1];
+        inv_rope_pair(a0, b0, pos, fr);
+        inv_rope_pair(a1, b1, pos, fr);
+      }
       if (p.out_bf16) {
         __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out) + obase;
-        *reinterpret_cast<__nv_bfloat162*>(out + h0 * kD + d) = __floats2bfloat162_rn(o[nt][0] * f0, o[nt][1] * f0);
-        *reinterpret_cast<__nv_bfloat162*>(out + h1 * kD + d) = __floats2bfloat162_rn(o[nt][2] * f1, o[nt][3] * f1);
+        *reinterpret_cast<__nv_bfloat162*>(out + h0 * kD + d) = __floats2bfloat162_rn(a0, b0);
+        *reinterpret_cast<__nv_bfloat162*>(out + h1 * kD + d) = __floats2bfloat162_rn(a1, b1);
       } else {
         float* out = static_cast<float*>(p.out) + obase;
-        *reinterpret_cast<float2*>(out + h0 * kD + d) = make_float2(o[nt][0] * f0, o[nt][1] * f0);
-        *reinterpret_cast<float2*>(out + h1 * kD + d) = make_float2(o[nt][2] * f1, o[nt][3] * f1);
+        *reinterpret_cast<float2*>(out + h0 * kD + d) = make_float2(a0, b0);
+        *reinterpret_cast<float2*>(out + h1 * kD + d) = make_float2(a1, b1);
       }
     }
     if (p.lse && xg == 0 && cq == 0) {
@@ -553,6 +570,11 @@ __global__ void __launch_bounds__(512, 1) sparse_attn_kernel(const __grid_consta
           acc[2 * j] += f2.x;
           acc[2 * j + 1] += f2.y;
         }
+      }
+      if (p.inv_rope && d >= kD - 64) {
+        const long long pos = __ldg(p.q_pos + t);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) inv_rope_pair(acc[2 * j], acc[2 * j + 1], pos, p.inv_freq[(d - (kD - 64)) / 2 + j]);
       }
       const long long oo = obase + static_cast<long long>(h) * kD + d;
       if (p.out_bf16) {
@@ -638,6 +660,10 @@ struct TcParams {
   int nsplit;     // CTAs (80-key chunks) per row = cluster size
   uint8_t* part;  // [T][nsplit][64][kPartRow]: O / sum of each chunk and (max, sum), log2 units
   uint32_t* err;
+  const int* q_pos;          // [T] query positions (inverse RoPE, bounded replay)
+  const int* swa_seg_start;  // [T] bounded-replay segment starts, or null
+  int inv_rope;              // rotate the output's last 64 dims back by the query's RoPE
+  double inv_freq[32];       // theta^(-2p/64)
 };
 
 __device__ __forceinline__ int key_slot_tc(const TcParams& p, int t, int j, int* kind) {
@@ -645,6 +671,11 @@ __device__ __forceinline__ int key_slot_tc(const TcParams& p, int t, int j, int*
   *kind = 0;
   if (j < p.n_swa) {
     slot = __ldg(p.swa_slot + static_cast<long long>(t) * p.ld_swa + j);
+    // bounded replay: slot j holds position q_pos - n_swa + 1 + j; keys before
+    // the segment start are not attended to
+    if (p.swa_seg_start &&
+        static_cast<long long>(__ldg(p.q_pos + t)) - p.n_swa + 1 + j < __ldg(p.swa_seg_start + t))
+      slot = -1;
     if (slot >= p.swa_slots) {
       set_error(p.err, kErrBounds);
       slot = -1;
@@ -995,6 +1026,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     fence_proxy_async_global();
   }
   cluster_sync();  // every chunk's partial of this row is in the scratch
+  float* sRope = sM;  // (cos, sin) of the 32 RoPE pairs at the query's position; sM is no longer read
+  if (p.inv_rope && tid < 32) {
+    float sn, cs;
+    rope_angle(__ldg(p.q_pos + t), p.inv_freq[tid], &sn, &cs);
+    sRope[2 * tid] = cs;
+    sRope[2 * tid + 1] = sn;
+  }
 
   // ---- combine: this CTA owns heads [hb, hb + nh); it fetches those rows of
   // every chunk with one bulk copy per chunk and weighs them with the sink
@@ -1048,6 +1086,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const float2 f2 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wv[j]));
         acc[2 * j] = fmaf(w, f2.x, acc[2 * j]);
         acc[2 * j + 1] = fmaf(w, f2.y, acc[2 * j + 1]);
+      }
+    }
+    if (p.inv_rope && c >= (kD - 64) / 8) {  // dims 8c .. 8c+7 are RoPE pairs 4(c - 56) .. +3
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int pp = 4 * (c - (kD - 64) / 8) + j;
+        const float cs = sRope[2 * pp], sn = sRope[2 * pp + 1];
+        const float x = acc[2 * j], y = acc[2 * j + 1];
+        acc[2 * j] = x * cs + y * sn;
+        acc[2 * j + 1] = y * cs - x * sn;
       }
     }
     const long long oo = (static_cast<long long>(t) * kH + h) * kD + 8 * c;
@@ -1122,6 +1170,10 @@ static cudaError_t launch_sparse_attn_tc(const AttnLaunch& a, void* ws, const De
   p.nsplit = nchunks;
   p.err = ctx.err;
   p.part = static_cast<uint8_t*>(ws);
+  p.q_pos = a.q_pos;
+  p.swa_seg_start = a.swa_seg_start;
+  p.inv_rope = a.inv_rope;
+  for (int i = 0; i < 32; ++i) p.inv_freq[i] = pow(static_cast<double>(a.rope_theta), -2.0 * i / 64.0);
   // q viewed as [T*64 rows of 1024 B]; a 128-B x 64-row box is one swizzled atom
   CUtensorMap map_q;
   if (encode_tmap_2d_u8(&map_q, a.q, static_cast<uint64_t>(kD) * 2, static_cast<uint64_t>(a.T) * kH,
@@ -1179,6 +1231,10 @@ cudaError_t launch_sparse_attn(const AttnLaunch& a, void* ws, size_t ws_bytes, c
   p.out = a.out;
   p.lse = a.lse;
   p.err = ctx.err;
+  p.q_pos = a.q_pos;
+  p.swa_seg_start = a.swa_seg_start;
+  p.inv_rope = a.inv_rope;
+  for (int i = 0; i < 32; ++i) p.inv_freq[i] = pow(static_cast<double>(a.rope_theta), -2.0 * i / 64.0);
   const int L = a.n_swa + a.k;
   const int nchunks = (L + kCK - 1) / kCK;
   const int nsplit = attn_num_splits(a.T, L, ctx.num_sms);

@@ -122,6 +122,14 @@ def test_validation_returns_codes_without_launch(lib):
     assert lib.csa2_sparse_attn(C.byref(s), None, 0, None) == 2                  # n_swa > 128
     s.n_swa, s.softmax_scale = 128, -1.0
     assert lib.csa2_sparse_attn(C.byref(s), None, 0, None) == 2                  # negative scale
+    s.softmax_scale, s.out_inv_rope = 0.0, 1
+    assert lib.csa2_sparse_attn(C.byref(s), None, 0, None) == 1                  # inverse RoPE needs q_pos
+    s.out_inv_rope, s.swa_seg_start = 0, FAKE
+    assert lib.csa2_sparse_attn(C.byref(s), None, 0, None) == 1                  # bounded replay needs q_pos
+    s.q_pos, s.out_inv_rope = FAKE, 2
+    assert lib.csa2_sparse_attn(C.byref(s), None, 0, None) == 2                  # flag is 0 or 1
+    s.out_inv_rope, s.rope_theta = 1, -5.0
+    assert lib.csa2_sparse_attn(C.byref(s), None, 0, None) == 2                  # negative theta
 
     ca = csa2.CompressArgs(FAKE, None, 64, 2, FAKE, 1e-6, 1, 10000.0, 0, None, FAKE, 64, FAKE, 1, None, None)
     assert lib.csa2_compress_m2(C.byref(ca), None) == 1                          # m=2 needs Z

@@ -13,7 +13,7 @@ from serving_lightning_indexer_gb300 import workloads as W
 pytestmark = pytest.mark.gpu
 
 
-def _attn_case(T, k, n_swa, seed, holes=0.0, out_bf16=False, n_entries=5000):
+def _attn_case(T, k, n_swa, seed, holes=0.0, out_bf16=False, n_entries=5000, inv_rope=False, replay=False):
     dev = need_gpu()
     pc = W.make_paged_cache([n_entries], seed=seed, device=dev)
     al = W.make_attn_layer(T, seed=seed + 1, device=dev)
@@ -27,9 +27,19 @@ def _attn_case(T, k, n_swa, seed, holes=0.0, out_bf16=False, n_entries=5000):
     if n_swa and holes:
         swa = swa.clone()
         swa[torch.tensor(rng.random(tuple(swa.shape)) < holes, device=dev)] = -1
+    qp_np = sg_np = None
+    qp = sg = None
+    if inv_rope or replay:   # query positions up to 1M: RoPE angles up to 1e6 rad
+        qp_np = rng.integers(n_swa + 1000, 1 << 20, size=T)
+        qp = torch.tensor(qp_np, dtype=torch.int32, device=dev)
+    if replay:               # segment starts from the query itself to before its window
+        sg_np = qp_np - rng.integers(0, n_swa + 20, size=T)
+        sg_np[0] = qp_np[0]
+        sg = torch.tensor(sg_np, dtype=torch.int32, device=dev)
     out = torch.empty(T, 64, 512, dtype=torch.bfloat16 if out_bf16 else torch.float32, device=dev)
     lse = torch.empty(T, 64, dtype=torch.float32, device=dev)
-    csa2.sparse_attn(al.q, pc.main_kv if k else None, tks, al.swa_kv if n_swa else None, swa, al.sink, out, lse)
+    csa2.sparse_attn(al.q, pc.main_kv if k else None, tks, al.swa_kv if n_swa else None, swa, al.sink, out, lse,
+                     q_pos=qp, out_inv_rope=inv_rope, swa_seg_start=sg)
     torch.cuda.synchronize()
     assert csa2.check_device_error() == 0
     main_np, swa_np = np_(pc.main_kv), np_(al.swa_kv)
@@ -37,7 +47,10 @@ def _attn_case(T, k, n_swa, seed, holes=0.0, out_bf16=False, n_entries=5000):
         ref, rl = o.attention_row(al.q[t].float().cpu().numpy().astype(np.float64), main_np,
                                   slots[t] if k else np.zeros(0, dtype=np.int64), swa_np,
                                   np_(swa[t]) if n_swa else np.zeros(0, dtype=np.int64),
-                                  np_(al.sink).astype(np.float64), 1 / math.sqrt(512))
+                                  np_(al.sink).astype(np.float64), 1 / math.sqrt(512),
+                                  q_pos=None if qp_np is None else int(qp_np[t]),
+                                  swa_seg_start=None if sg_np is None else int(sg_np[t]),
+                                  inv_rope_theta=10000.0 if inv_rope else None)
         assert_attention_close(out[t].double().cpu().numpy(), ref, f"row {t}")
         assert np.abs(np_(lse[t]) - rl).max() < 2e-3
 
@@ -51,6 +64,17 @@ def test_attention_matches_oracle(T, k, n_swa):
 
 def test_attention_with_empty_slots_and_bf16_out():
     _attn_case(4, 512, 128, seed=99, holes=0.3, out_bf16=True)
+
+
+@pytest.mark.parametrize("T,k,n_swa,inv_rope,replay,out_bf16", [
+    (3, 512, 128, True, False, False), (8, 512, 128, True, True, False), (16, 512, 128, False, True, True),
+    (2, 2048, 128, True, True, False),      # split-K kernel, merged over the cluster
+    (160, 2048, 128, True, True, True),     # split-K kernel, one CTA per row
+    (4, 100, 37, True, True, False)])
+def test_attention_inverse_rope_and_bounded_replay(T, k, n_swa, inv_rope, replay, out_bf16):
+    # output inverse RoPE at the query position and the SWA window cut to the
+    # replayed segment (CSA2 page: attention section; "Decoder SWA Bounded Replay")
+    _attn_case(T, k, n_swa, seed=300 + T + k, out_bf16=out_bf16, inv_rope=inv_rope, replay=replay)
 
 
 def test_attention_no_keys_at_all_gives_zero():

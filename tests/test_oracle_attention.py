@@ -96,3 +96,116 @@ def test_empty_slots_ignored_and_order_free():
     oa, la = o.attention_row(q, pc.main_kv.numpy(), a, al.swa_kv.numpy(), al.swa_slot[0].numpy(), sink, 0.05)
     ob, lb = o.attention_row(q, pc.main_kv.numpy(), b, al.swa_kv.numpy(), al.swa_slot[0].numpy(), sink, 0.05)
     assert np.allclose(oa, ob, rtol=1e-12) and np.allclose(la, lb, rtol=1e-13)
+
+
+# ---- Decoder SWA Bounded Replay (CSA2 page, "Decoder SWA Bounded Replay") ----
+
+def test_replay_visible_counts_close_the_triangle():
+    # a replayed tail of W tokens: query k of the segment (0-based) sees k + 1 SWA
+    # keys, so the segment holds 1 + 2 + ... + W = W (W + 1) / 2 query-key pairs
+    W, s = 128, 5000
+    counts = [int(o.swa_replay_visible(s + k, s, W).sum()) for k in range(W)]
+    assert counts == list(range(1, W + 1))
+    assert sum(counts) == W * (W + 1) // 2 == 8256
+    # a longer segment: every query after the first W sees the full window
+    L = 300
+    total = sum(int(o.swa_replay_visible(s + k, s, W).sum()) for k in range(L))
+    assert total == W * (W + 1) // 2 + (L - W) * W
+
+
+def test_replay_visible_special_cases():
+    W = 128
+    # the first query of a segment sees only its own key, the newest slot
+    v = o.swa_replay_visible(777, 777, W)
+    assert v.sum() == 1 and v[-1]
+    # a segment start at or before the window's first position cuts nothing
+    for s in (0, 777 - W + 1, 777 - 5000):
+        assert o.swa_replay_visible(777, s, W).all()
+    # one position inside: the oldest slot alone drops out
+    v = o.swa_replay_visible(777, 777 - W + 2, W)
+    assert not v[0] and v[1:].all()
+    # the visible keys are a contiguous run that ends at the query's own key
+    for s in range(700, 778):
+        v = o.swa_replay_visible(777, s, W)
+        first = int(np.argmax(v))
+        assert v[first:].all() and not v[:first].any()
+
+
+def test_replay_row_equals_attention_over_the_segment_keys_only():
+    # brute force: attend over exactly the keys whose positions lie in the
+    # segment and the window, built position by position
+    rng = np.random.default_rng(11)
+    W, s, i = 16, 40, 47
+    kv_by_pos = {p: rng.normal(size=512) for p in range(i - W + 1, i + 1)}
+    q = rng.normal(size=(64, 512))
+    sink = rng.normal(size=64)
+    keys = np.array([kv_by_pos[p] for p in range(i - W + 1, i + 1) if p >= s])
+    ref, _ = o.sparse_attention(q, keys, sink, 0.05)
+    vis = o.swa_replay_visible(i, s, W)
+    window = np.array([kv_by_pos[p] for p in range(i - W + 1, i + 1)])
+    got, _ = o.sparse_attention(q, window[vis], sink, 0.05)
+    assert len(keys) == i - s + 1 == int(vis.sum())
+    assert np.allclose(got, ref, rtol=1e-14, atol=1e-15)
+
+
+# ---- Output inverse RoPE (CSA2 page, attention section) ----
+
+def _rope_rows(x, pos, theta=10000.0):
+    return o.rope_interleaved(x, np.full(x.shape[0], float(pos)), theta)
+
+
+def test_inverse_rope_makes_the_output_relative():
+    # keys carry RoPE at their own positions, the query at its position; after the
+    # output's inverse RoPE only relative positions remain: shifting every
+    # position by the same amount leaves the output unchanged.  Without the
+    # inverse (or with the rotation's sign flipped) the shift shows.
+    rng = np.random.default_rng(12)
+    x = rng.normal(size=(20, 512))
+    kpos = np.sort(rng.choice(5000, size=20, replace=False))
+    qx = rng.normal(size=(64, 512)) * 0.05
+    qpos = 5000
+    sink = rng.normal(size=64)
+
+    def run(shift, inverse=True, sign=1.0):
+        K = o.rope_interleaved(x, kpos + shift, 10000.0)
+        q = _rope_rows(qx, qpos + shift)
+        out, lse = o.sparse_attention(q, K, sink, 1 / math.sqrt(512))
+        if inverse:
+            out = o.output_inverse_rope(out, sign * (qpos + shift), 10000.0)
+        return out, lse
+
+    a, la = run(0)
+    b, lb = run(123457)
+    assert np.allclose(la, lb, rtol=1e-9)             # logits depend on relative positions only
+    assert np.allclose(a, b, rtol=1e-8, atol=1e-10)
+    c, _ = run(123457, inverse=False)
+    assert not np.allclose(a[:, 448:], c[:, 448:], atol=1e-3)
+    d, _ = run(123457, sign=-1.0)
+    assert not np.allclose(a[:, 448:], d[:, 448:], atol=1e-3)
+    assert np.array_equal(b[:, :448], c[:, :448])     # the first 448 dims are not rotated
+
+
+def test_inverse_rope_of_a_single_key_returns_its_latent():
+    # one key at the query's own position and no sink mass: the output is that
+    # key, and its inverse RoPE at the same position is the latent before RoPE
+    rng = np.random.default_rng(13)
+    lat = rng.normal(size=(1, 512))
+    pos = 987654
+    out, _ = o.sparse_attention(rng.normal(size=(64, 512)), _rope_rows(lat, pos), np.full(64, -np.inf), 0.1)
+    back = o.output_inverse_rope(out, pos, 10000.0)
+    assert np.allclose(back, np.repeat(lat, 64, axis=0), rtol=1e-9, atol=1e-12)
+
+
+def test_inverse_rope_is_a_complex_rotation_by_minus_the_angle():
+    # torch complex arithmetic: pair (2p, 2p+1) of the last 64 dims times
+    # exp(-i * pos * theta^(-2p/64)); position 0 is the identity
+    rng = np.random.default_rng(14)
+    y = rng.normal(size=(64, 512))
+    pos, theta = 31337, 10000.0
+    got = o.output_inverse_rope(y, pos, theta)
+    z = torch.view_as_complex(torch.tensor(y[:, 448:]).reshape(64, 32, 2).contiguous())
+    ang = -pos * theta ** (-2.0 * torch.arange(32, dtype=torch.float64) / 64)
+    ref = torch.view_as_real(z * torch.polar(torch.ones(32, dtype=torch.float64), ang)).reshape(64, 64).numpy()
+    assert np.abs(got[:, 448:] - ref).max() <= 1e-10 * np.abs(ref).max()   # angles ~3e4 rad
+    assert np.array_equal(got[:, :448], y[:, :448])
+    assert np.array_equal(o.output_inverse_rope(y, 0, theta), y)
