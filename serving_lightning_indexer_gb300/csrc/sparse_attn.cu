@@ -604,11 +604,17 @@ __global__ void __launch_bounds__(512, 1) sparse_attn_kernel(const __grid_consta
 //     P = exp2(S*scale - max) (bf16, swizzled) with its max and sum.
 //   * O = P V on tcgen05 (M = 128 as above, N = 256 dims twice, K = 80 keys; V
 //     is the key tile read MN-major) into TMEM.
-//   * O / sum is written as bf16 to a per-row scratch in global memory with
-//     (max, sum); after a cluster barrier the CTA of rank r combines the heads
-//     h = r (mod CTAs) over the row's chunks with the sink and writes them.
-// A partial row of the merge: 512 bf16 of O / sum, then (max, sum) and 8 pad bytes.
-constexpr int kPartRow = kD * 2 + 16;
+//   * O / sum is stored as bf16 straight from the accumulator into a per-row
+//     scratch in global memory, with (max, sum) per head; after a cluster
+//     barrier the CTA of rank r fetches its range of heads of every chunk with
+//     one 2-D tensor copy per chunk and combines them with the sink.
+// Scratch of one chunk: O / sum as bf16 in [64 blocks of 8 dims][64 heads][16 B]
+// -- a warp's 32 heads of one block are 512 contiguous bytes, and a head range
+// of every block is one box of a 2-D tensor copy -- plus (max, sum) per head in
+// a separate array [rows][chunks][64] of float2.
+constexpr int kPartBlocks = kD / 8;                     // blocks of 8 dims
+constexpr int kPartBlockBytes = kH * 16;                // one block: 64 heads x 8 bf16
+constexpr int kPartChunkBytes = kPartBlocks * kPartBlockBytes;
 constexpr int kTcKeys = 80;  // keys per CTA: 640 keys of a decode row in 8 CTAs, so two clusters share a GPC
 struct TcSmem {
   static constexpr int kQAtom = 8192;                           // 64 rows x 128 B (q, P)
@@ -619,14 +625,15 @@ struct TcSmem {
   static constexpr int kOffRaw = kOffP + 2 * kQAtom;            // [kTcKeys][kRawStride]
   static constexpr int kOffKind = kOffRaw + kTcKeys * kRawStride;  // int[kTcKeys]
   static constexpr int kOffStat = kOffKind + kTcKeys * 4;       // float m[64], l[64], sink[64]
-  static constexpr int kOffW = kOffStat + 3 * kH * 4;           // float [64][16]: softmax exchange, combine weights
-  static constexpr int kOffBar = kOffW + 64 * 16 * 4;           // raw, S done, O halves done, merge rows, q
-  static constexpr int kOffTmem = kOffBar + 6 * 8;
+  static constexpr int kOffW = kOffStat + 3 * kH * 4;           // float [6][64]: softmax exchange of group maxima, sums
+  static constexpr int kOffBar = kOffW + 6 * kH * 4;            // raw, S done, O halves done, q
+  static constexpr int kOffTmem = kOffBar + 5 * 8;
   static constexpr int kBytes = kOffTmem + 8;
   static constexpr int kAlloc = kBytes + 1024;                  // the base is rounded up to 1024 B
-  // merge: the staged partial rows ([64][kPartRow]) and later the received rows
-  // ([ns][heads of this CTA][kPartRow]) use the q and key tiles
-  static_assert(75 * kPartRow <= 8 * kQAtom + 8 * kKAtom, "received rows (at most 75 for 1..16 chunks) fit the q and key tiles");
+  // merge: the received head ranges ([ns][64 blocks][ceil(64 / ns) heads][16 B])
+  // use the q and key tiles
+  static_assert(75 * kPartBlocks * 16 <= 8 * kQAtom + 8 * kKAtom,
+                "received head ranges (ns * ceil(64 / ns) <= 75 heads for 1..16 chunks) fit the q and key tiles");
   // the M = 128 MMAs read 64 rows past the last q atom (into the keys) and past the last P atom (into the staging)
   static_assert(8 * kKAtom >= kQAtom && kTcKeys * kRawStride >= kQAtom, "operand padding rows stay in bounds");
   static_assert(kKAtom % 1024 == 0 && kOffK % 1024 == 0 && kOffP % 1024 == 0, "swizzle atoms are 1024-B aligned");
@@ -658,7 +665,8 @@ struct TcParams {
   float* lse;
   int kv_ready;   // gather the keys before the dependency wait
   int nsplit;     // CTAs (80-key chunks) per row = cluster size
-  uint8_t* part;  // [T][nsplit][64][kPartRow]: O / sum of each chunk and (max, sum), log2 units
+  uint8_t* part;     // [T][nsplit][64 blocks][64 heads][16 B]: O / sum of each chunk (bf16)
+  float2* part_ml;   // [T][nsplit][64]: (max, sum) of each chunk and head, log2 units
   uint32_t* err;
   const int* q_pos;          // [T] query positions (inverse RoPE, bounded replay)
   const int* swa_seg_start;  // [T] bounded-replay segment starts, or null
@@ -738,31 +746,6 @@ __device__ __forceinline__ void dequant_block32(const uint8_t* raw, int kind, in
   }
 }
 
-// Loads through L2 only (data written earlier in this grid by other CTAs, or
-// by the previous kernel); not volatile, so independent loads can be batched.
-__device__ __forceinline__ uint4 ld_cg_v4(const void* p) {
-  uint4 v;
-  asm("ld.global.cg.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
-  return v;
-}
-__device__ __forceinline__ float2 ld_cg_f2(const float2* p) {
-  float2 v;
-  asm("ld.global.cg.v2.f32 {%0,%1}, [%2];" : "=f"(v.x), "=f"(v.y) : "l"(p));
-  return v;
-}
-// Bulk copy shared -> global, tracked by this thread's bulk async-group.
-__device__ __forceinline__ void bulk_store(void* gdst, const void* ssrc, uint32_t bytes) {
-  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst), "r"(smem_u32(ssrc)),
-               "r"(bytes)
-               : "memory");
-}
-// Waits until this thread's bulk stores have been performed.
-__device__ __forceinline__ void bulk_store_commit_wait() {
-  asm volatile("cp.async.bulk.commit_group;\n\tcp.async.bulk.wait_group 0;" ::: "memory");
-}
-__device__ __forceinline__ void fence_proxy_async_global() {
-  asm volatile("fence.proxy.async.global;" ::: "memory");
-}
 __device__ __forceinline__ float ex2_approx(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -786,8 +769,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   uint64_t* bar_raw = reinterpret_cast<uint64_t*>(sm + TcSmem::kOffBar);
   uint64_t* bar_s = bar_raw + 1;
   uint64_t* bar_o = bar_raw + 2;  // [2]
-  uint64_t* bar_m = bar_raw + 4;  // merge rows received
-  uint64_t* bar_q = bar_raw + 5;  // the row's q tile
+  uint64_t* bar_q = bar_raw + 4;  // the row's q tile
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(sm + TcSmem::kOffTmem);
 
   const int tid = threadIdx.x;
@@ -802,7 +784,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     mbar_init(bar_s, 1);
     mbar_init(bar_o, 1);
     mbar_init(bar_o + 1, 1);
-    mbar_init(bar_m, 1);
     mbar_init(bar_q, 1);
     fence_mbar_init();
   }
@@ -916,7 +897,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   // ---- softmax of the chunk: warps 0-1 (keys 0-31), 4-5 (keys 32-63) and 8-9
   // (keys 64-79) read TMEM lanes 0-63, one head per thread; the three key
   // groups exchange max and sum through shared memory
-  float* sMx = sW;           // [3][64] group maxima (the combine weights reuse the area later)
+  float* sMx = sW;           // [3][64] group maxima
   float* sSx = sW + 3 * kH;  // [3][64] group sums
   if ((warp & 3) < 2 && warp < 12) {
     const int grp = warp >> 2;  // keys 32 grp .. 32 grp + 31
@@ -984,11 +965,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
   }
 
-  // ---- partial rows: O / sum (bf16) and (max, sum) per head, staged over the
-  // q and key tiles (free once O is complete), then bulk stores into the
-  // scratch.  Warps of TMEM lane quadrants 0-1, four column groups of 128.
+  // ---- partial results: O / sum (bf16) and (max, sum) per head, stored from
+  // the accumulator straight into the scratch.  Warps of TMEM lane quadrants
+  // 0-1 (lane = head), four column groups of 128 dims; each 16-B store of a
+  // warp covers one 8-dim block of its 32 heads (512 contiguous bytes).
   const long long rowbase = static_cast<long long>(tl) * ns;
-  uint8_t* sStage = sm + TcSmem::kOffQ;  // [64][kPartRow]
   if ((warp & 3) < 2 && warp < 16) {
     const int qd = warp & 3, g = warp >> 2;
     const int h = qd * 32 + lane;
@@ -997,33 +978,25 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     tc_fence_after();
     const float l = sL[h];
     const float inv = (l > 0.f && oko) ? 1.f / l : 0.f;
-    uint8_t* srow = sStage + h * kPartRow;
+    uint8_t* dst = p.part + (rowbase + rank) * kPartChunkBytes + h * 16;
 #pragma unroll 1
     for (int cc = 0; cc < 4; ++cc) {
       float v[32];
       tmem_ld32(tmem + (static_cast<uint32_t>(qd * 32) << 16) + 128 * g + 32 * cc, v);
 #pragma unroll
-      for (int j = 0; j < 4; ++j)
-        *reinterpret_cast<uint4*>(srow + 256 * g + 64 * cc + 16 * j) =
+      for (int j = 0; j < 4; ++j)  // block 16 g + 4 cc + j
+        *reinterpret_cast<uint4*>(dst + (16 * g + 4 * cc + j) * kPartBlockBytes) =
             make_uint4(pack_bf16(v[8 * j] * inv, v[8 * j + 1] * inv), pack_bf16(v[8 * j + 2] * inv, v[8 * j + 3] * inv),
                        pack_bf16(v[8 * j + 4] * inv, v[8 * j + 5] * inv),
                        pack_bf16(v[8 * j + 6] * inv, v[8 * j + 7] * inv));
     }
-    if (g == 0)
-      *reinterpret_cast<float4*>(srow + kD * 2) =
-          make_float4(oko ? sM[h] : -INFINITY, oko ? l : 0.f, 0.f, 0.f);
-    fence_proxy_async_smem();
+    if (g == 0) p.part_ml[(rowbase + rank) * kH + h] = make_float2(oko ? sM[h] : -INFINITY, oko ? l : 0.f);
   }
   tc_fence_before();
   __syncthreads();
   if (warp == 0) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
-  }
-  if (tid < 4) {
-    bulk_store(p.part + ((rowbase + rank) * kH + 16 * tid) * kPartRow, sStage + tid * 16 * kPartRow, 16 * kPartRow);
-    bulk_store_commit_wait();
-    fence_proxy_async_global();
   }
   cluster_sync();  // every chunk's partial of this row is in the scratch
   float* sRope = sM;  // (cos, sin) of the 32 RoPE pairs at the query's position; sM is no longer read
@@ -1034,58 +1007,56 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     sRope[2 * tid + 1] = sn;
   }
 
-  // ---- combine: this CTA owns heads [hb, hb + nh); it fetches those rows of
-  // every chunk with one bulk copy per chunk and weighs them with the sink
+  // ---- combine: this CTA owns heads [hb, hb + nh).  The cluster barrier
+  // above orders the chunks' stores before these loads (L2, generic proxy
+  // on both sides).  A thread takes one head and 8-dim block: the chunk
+  // weights exp2(max_r - M) sum_r / D (the sink in D) from the (max, sum)
+  // pairs, then the weighted sum of the chunks' O / sum.
   const int hb = (kH * rank) / ns;
   const int nh = (kH * (rank + 1)) / ns - hb;
-  uint8_t* sRecv = sm + TcSmem::kOffQ;  // [ns][nh][kPartRow]
-  if (tid == kTcMmaThread) {
-    fence_proxy_async_global();
-    mbar_arrive_expect_tx(bar_m, static_cast<uint32_t>(ns * nh * kPartRow));
-    for (int r = 0; r < ns; ++r)
-      bulk_load(sRecv + r * nh * kPartRow, p.part + ((rowbase + r) * kH + hb) * kPartRow, nh * kPartRow, bar_m,
-                l2_policy_evict_first());
-  }
-  const bool okm = mbar_wait(bar_m, 0u, nullptr);
-  if (!okm) set_error(p.err, kErrTimeout);
-  // weights: lane group of 16 per head, lane r of the group = chunk r
-  // (whole warps take part in the shuffles: the loop runs over warp-aligned bases)
-  for (int i0 = tid - lane; i0 < ((nh * 16 + 31) & ~31); i0 += kTcThreads) {
-    const int i = i0 + lane;
-    const bool valid = i < nh * 16;
-    const int li = valid ? (i >> 4) : 0, r = i & 15;
+  if (p.inv_rope) __syncthreads();  // sRope written
+  for (int task = tid; task < nh * kPartBlocks; task += kTcThreads) {
+    // consecutive threads: consecutive heads, then blocks (64-B runs of nh
+    // heads per load and store of a warp)
+    const int li = task % nh, c = task / nh;
     const int h = hb + li;
-    float2 ml = make_float2(-INFINITY, 0.f);
-    if (valid && r < ns && okm) ml = *reinterpret_cast<const float2*>(sRecv + (r * nh + li) * kPartRow + kD * 2);
-    const float sk = sSink[h];
-    float M = fmaxf(sk, ml.x);
+    float wr[kMaxCluster], ml_l[kMaxCluster];
+    float M = sSink[h];
 #pragma unroll
-    for (int o = 8; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-    const float w = (ml.x == -INFINITY) ? 0.f : ex2_approx(ml.x - M) * ml.y;
-    float D = w;
-#pragma unroll
-    for (int o = 8; o > 0; o >>= 1) D += __shfl_xor_sync(0xffffffffu, D, o);
-    D += ex2_approx(sk - M);
-    if (valid) {
-      sW[li * 16 + r] = w / D;
-      if (r == 0 && p.lse) p.lse[static_cast<long long>(t) * kH + h] = (M + log2f(D)) * kLn2;
+    for (int r = 0; r < kMaxCluster; ++r) {
+      float2 ml = make_float2(-INFINITY, 0.f);
+      if (r < ns) ml = __ldcg(p.part_ml + (rowbase + r) * kH + h);
+      wr[r] = ml.x;
+      M = fmaxf(M, ml.x);
+      ml_l[r] = ml.y;
     }
-  }
-  __syncthreads();
-  for (int task = tid; task < nh * (kD / 8); task += kTcThreads) {
-    const int li = task >> 6, c = task & 63;
-    const int h = hb + li;
-    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll 4
-    for (int r = 0; r < ns; ++r) {
-      const uint4 pv = *reinterpret_cast<const uint4*>(sRecv + (r * nh + li) * kPartRow + 16 * c);
-      const float w = sW[li * 16 + r];
-      const uint32_t wv[4] = {pv.x, pv.y, pv.z, pv.w};
+    float D = ex2_approx(sSink[h] - M);
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const float2 f2 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wv[j]));
-        acc[2 * j] = fmaf(w, f2.x, acc[2 * j]);
-        acc[2 * j + 1] = fmaf(w, f2.y, acc[2 * j + 1]);
+    for (int r = 0; r < kMaxCluster; ++r) {
+      wr[r] = (wr[r] == -INFINITY) ? 0.f : ex2_approx(wr[r] - M) * ml_l[r];
+      D += wr[r];
+    }
+    const float invD = 1.f / D;
+    if (c == 0 && p.lse) p.lse[static_cast<long long>(t) * kH + h] = (M + log2f(D)) * kLn2;
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    const uint8_t* src = p.part + (rowbase * kPartBlocks + c) * kPartBlockBytes + h * 16;
+#pragma unroll
+    for (int r0 = 0; r0 < kMaxCluster; r0 += 8) {  // 8 chunks' loads in flight at a time
+      uint4 pv[8];
+#pragma unroll
+      for (int r = 0; r < 8; ++r)
+        pv[r] = (r0 + r < ns) ? __ldcg(reinterpret_cast<const uint4*>(src + static_cast<long long>(r0 + r) * kPartChunkBytes))
+                              : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+      for (int r = 0; r < 8; ++r) {
+        const float w = wr[r0 + r] * invD;
+        const uint32_t wv[4] = {pv[r].x, pv[r].y, pv[r].z, pv[r].w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float2 f2 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wv[j]));
+          acc[2 * j] = fmaf(w, f2.x, acc[2 * j]);
+          acc[2 * j + 1] = fmaf(w, f2.y, acc[2 * j + 1]);
+        }
       }
     }
     if (p.inv_rope && c >= (kD - 64) / 8) {  // dims 8c .. 8c+7 are RoPE pairs 4(c - 56) .. +3
@@ -1135,7 +1106,7 @@ static bool use_tc_path(int n_keys) {
   return nchunks >= 1 && nchunks <= kMaxCluster;
 }
 static size_t tc_part_bytes(int rows, int nchunks) {
-  return static_cast<size_t>(rows) * nchunks * kH * kPartRow;
+  return static_cast<size_t>(rows) * nchunks * (kPartChunkBytes + kH * sizeof(float2));
 }
 
 size_t attn_workspace_bytes(int T, int n_keys, int num_sms) {
@@ -1169,7 +1140,11 @@ static cudaError_t launch_sparse_attn_tc(const AttnLaunch& a, void* ws, const De
   p.kv_ready = a.kv_ready;
   p.nsplit = nchunks;
   p.err = ctx.err;
+  // scratch: O / sum of [rows][chunks] as 2-D rows of 64 heads x 16 B (one row
+  // per 8-dim block), then (max, sum) [rows][chunks][64]
+  const int rows_max = a.T < kTcRowsPerLaunch ? a.T : kTcRowsPerLaunch;
   p.part = static_cast<uint8_t*>(ws);
+  p.part_ml = reinterpret_cast<float2*>(p.part + static_cast<size_t>(rows_max) * nchunks * kPartChunkBytes);
   p.q_pos = a.q_pos;
   p.swa_seg_start = a.swa_seg_start;
   p.inv_rope = a.inv_rope;
