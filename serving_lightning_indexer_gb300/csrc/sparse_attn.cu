@@ -598,16 +598,16 @@ __global__ void __launch_bounds__(512, 1) sparse_attn_kernel(const __grid_consta
 //     shared memory; the records are dequantised to bf16 key rows.  Both tiles
 //     use the 128-byte swizzled layout of the tensor cores: 8 atoms of 64
 //     dims, each [64 rows x 128 B], rows of an atom 1024 B per group of 8.
-//   * S = q K^T on tcgen05 (M = 128: heads 0-63, rows 64-127 read the next 8 KB
-//     of shared memory and are discarded; N = 80 keys; K = 512) into TMEM.
+//   * S = q K^T on tcgen05 (M = 64 heads, N = 80 keys, K = 512) into TMEM;
+//     an M = 64 accumulator puts head h in lane 32 (h / 16) + h % 16.
 //   * one thread per head reads its S row, masks absent keys, and forms
 //     P = exp2(S*scale - max) (bf16, swizzled) with its max and sum.
-//   * O = P V on tcgen05 (M = 128 as above, N = 256 dims twice, K = 80 keys; V
+//   * O = P V on tcgen05 (M = 64 heads, N = 256 dims twice, K = 80 keys; V
 //     is the key tile read MN-major) into TMEM.
 //   * O / sum is stored as bf16 straight from the accumulator into a per-row
 //     scratch in global memory, with (max, sum) per head; after a cluster
-//     barrier the CTA of rank r fetches its range of heads of every chunk with
-//     one 2-D tensor copy per chunk and combines them with the sink.
+//     barrier the CTA of rank r loads its range of heads of every chunk from
+//     L2 and combines them with the sink.
 // Scratch of one chunk: O / sum as bf16 in [64 blocks of 8 dims][64 heads][16 B]
 // -- a warp's 32 heads of one block are 512 contiguous bytes, and a head range
 // of every block is one box of a 2-D tensor copy -- plus (max, sum) per head in
@@ -634,8 +634,6 @@ struct TcSmem {
   // use the q and key tiles
   static_assert(75 * kPartBlocks * 16 <= 8 * kQAtom + 8 * kKAtom,
                 "received head ranges (ns * ceil(64 / ns) <= 75 heads for 1..16 chunks) fit the q and key tiles");
-  // the M = 128 MMAs read 64 rows past the last q atom (into the keys) and past the last P atom (into the staging)
-  static_assert(8 * kKAtom >= kQAtom && kTcKeys * kRawStride >= kQAtom, "operand padding rows stay in bounds");
   static_assert(kKAtom % 1024 == 0 && kOffK % 1024 == 0 && kOffP % 1024 == 0, "swizzle atoms are 1024-B aligned");
   static_assert(kAlloc <= 227 * 1024, "one CTA per SM");
 };
@@ -845,7 +843,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   };
   auto issue_s = [&](int wave) {  // the MMA thread, once q and the wave's keys are in place
     tc_fence_after();
-    constexpr uint32_t idesc = idesc_bf16_f32(128, kTcKeys, 0, 0);
+    constexpr uint32_t idesc = idesc_bf16_f32(64, kTcKeys, 0, 0);
 #pragma unroll
     for (int a = 4 * wave; a < 4 * wave + 4; ++a) {
 #pragma unroll
@@ -894,14 +892,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (tid == kTcMmaThread) issue_s(1);
   }
 
-  // ---- softmax of the chunk: warps 0-1 (keys 0-31), 4-5 (keys 32-63) and 8-9
-  // (keys 64-79) read TMEM lanes 0-63, one head per thread; the three key
-  // groups exchange max and sum through shared memory
+  // ---- softmax of the chunk: warps 0-3 (keys 0-31), 4-7 (keys 32-63) and
+  // 8-11 (keys 64-79), one head per thread.  An M = 64 accumulator holds head
+  // h in TMEM lane 32 (h / 16) + h % 16: lanes 0-15 of each warp's quadrant
+  // (lanes 16-31 compute on unused lanes and store nothing).  The three key
+  // groups exchange max and sum through shared memory.
   float* sMx = sW;           // [3][64] group maxima
   float* sSx = sW + 3 * kH;  // [3][64] group sums
-  if ((warp & 3) < 2 && warp < 12) {
+  if (warp < 12) {
     const int grp = warp >> 2;  // keys 32 grp .. 32 grp + 31
-    const int h = (warp & 3) * 32 + lane;
+    const int h = (warp & 3) * 16 + (lane & 15);
+    const bool act = lane < 16;
     bool oks = mbar_wait(bar_s, 0u, nullptr);
     if (!oks) set_error(p.err, kErrTimeout);
     tc_fence_after();
@@ -914,8 +915,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       v[j] = ((km >> j) & 1u) && oks ? v[j] * p.scale_log2 : -INFINITY;
       mx[j & 3] = fmaxf(mx[j & 3], v[j]);
     }
-    sMx[grp * kH + h] = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
-    named_bar_sync(1, 192);
+    if (act) sMx[grp * kH + h] = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+    named_bar_sync(1, 384);
     const float m = fmaxf(fmaxf(sMx[h], sMx[kH + h]), sMx[2 * kH + h]);
     float sum[4] = {0.f, 0.f, 0.f, 0.f};
     uint32_t pk[16];
@@ -926,20 +927,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       sum[(j >> 1) & 3] += e0 + e1;
       pk[j / 2] = pack_bf16(e0, e1);
     }
-    sSx[grp * kH + h] = (sum[0] + sum[1]) + (sum[2] + sum[3]);
+    if (act) sSx[grp * kH + h] = (sum[0] + sum[1]) + (sum[2] + sum[3]);
     // P rows: keys 0-63 in atom 0 (chunks 0-7), keys 64-79 in chunks 0-1 of atom 1
     uint8_t* prow = sP + (grp >> 1) * TcSmem::kQAtom + h * 128;
     const int nc = (grp < 2) ? 4 : (kTcKeys - 64) / 8;
 #pragma unroll
     for (int c4 = 0; c4 < 4; ++c4) {
-      if (c4 < nc) {
+      if (act && c4 < nc) {
         const int c = 4 * (grp & 1) + c4;
         *reinterpret_cast<uint4*>(prow + ((c ^ (h & 7)) << 4)) =
             make_uint4(pk[4 * c4], pk[4 * c4 + 1], pk[4 * c4 + 2], pk[4 * c4 + 3]);
       }
     }
-    named_bar_sync(1, 192);
-    if (grp == 0) {
+    named_bar_sync(1, 384);
+    if (act && grp == 0) {
       sM[h] = m;
       sL[h] = (sSx[h] + sSx[kH + h]) + sSx[2 * kH + h];
     }
@@ -952,7 +953,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   // 256-511 -> columns 256..511, bar_o[1])
   if (tid == kTcMmaThread) {
     tc_fence_after();
-    constexpr uint32_t idesc = idesc_bf16_f32(128, 256, 0, 1);
+    constexpr uint32_t idesc = idesc_bf16_f32(64, 256, 0, 1);
 #pragma unroll
     for (int hh = 0; hh < 2; ++hh) {
 #pragma unroll
@@ -966,13 +967,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   }
 
   // ---- partial results: O / sum (bf16) and (max, sum) per head, stored from
-  // the accumulator straight into the scratch.  Warps of TMEM lane quadrants
-  // 0-1 (lane = head), four column groups of 128 dims; each 16-B store of a
-  // warp covers one 8-dim block of its 32 heads (512 contiguous bytes).
+  // the accumulator straight into the scratch.  Warps 0-15: lane quadrant
+  // warp % 4 (heads 16 q .. 16 q + 15 in its lanes 0-15), column group warp / 4
+  // of 128 dims; each 16-B store of a warp covers one 8-dim block of its 16
+  // heads (256 contiguous bytes).
   const long long rowbase = static_cast<long long>(tl) * ns;
-  if ((warp & 3) < 2 && warp < 16) {
+  if (warp < 16) {
     const int qd = warp & 3, g = warp >> 2;
-    const int h = qd * 32 + lane;
+    const int h = qd * 16 + (lane & 15);
+    const bool act = lane < 16;
     bool oko = mbar_wait(bar_o + (g >> 1), 0u, nullptr);  // column groups 0-1: dims 0-255
     if (!oko) set_error(p.err, kErrTimeout);
     tc_fence_after();
@@ -985,12 +988,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       tmem_ld32(tmem + (static_cast<uint32_t>(qd * 32) << 16) + 128 * g + 32 * cc, v);
 #pragma unroll
       for (int j = 0; j < 4; ++j)  // block 16 g + 4 cc + j
-        *reinterpret_cast<uint4*>(dst + (16 * g + 4 * cc + j) * kPartBlockBytes) =
+        if (act)
+          *reinterpret_cast<uint4*>(dst + (16 * g + 4 * cc + j) * kPartBlockBytes) =
             make_uint4(pack_bf16(v[8 * j] * inv, v[8 * j + 1] * inv), pack_bf16(v[8 * j + 2] * inv, v[8 * j + 3] * inv),
                        pack_bf16(v[8 * j + 4] * inv, v[8 * j + 5] * inv),
                        pack_bf16(v[8 * j + 6] * inv, v[8 * j + 7] * inv));
     }
-    if (g == 0) p.part_ml[(rowbase + rank) * kH + h] = make_float2(oko ? sM[h] : -INFINITY, oko ? l : 0.f);
+    if (act && g == 0) p.part_ml[(rowbase + rank) * kH + h] = make_float2(oko ? sM[h] : -INFINITY, oko ? l : 0.f);
   }
   tc_fence_before();
   __syncthreads();
