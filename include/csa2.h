@@ -184,8 +184,9 @@ CSA2_API int csa2_topk_with_candidates(const csa2_topk_args* args, void* workspa
  * operator interface that passes only inputs and outputs, an engine whose
  * allocator cannot serve extra buffers, a path that must not call cudaMalloc).
  * The scratch is a static device array of CSA2_TOPK_NOALLOC_SCRATCH_BYTES that
- * every GPU loading the library holds until exit; rows needing more (about 60
- * rows when long rows and pools are selected) return CSA2_ERR_WORKSPACE.  The
+ * every GPU loading the library holds until exit.  A row longer than 16,384
+ * elements needs about 2 B of it per element plus 8 KB (a 1M-entry row and its
+ * pool about 2.3 MB); calls needing more return CSA2_ERR_WORKSPACE.  The
  * library allocates nothing during the call.  The first call on each device
  * looks up the array's device address, so make it before any stream capture.
  * All calls share the array: calls that overlap on the GPU race. */

@@ -34,7 +34,11 @@ namespace {
 
 constexpr int kBins = 2048;
 constexpr int kCap = 16384;      // candidates of a row the final CTA holds in shared memory
-constexpr int kRegion = 512;     // candidates stored per filter CTA (a larger count flags an overflow)
+// Candidates stored per filter CTA of 4096 elements (a larger count flags an
+// overflow and sends the row to the streaming path).  A quarter of the chunk:
+// block-maximum rows are narrow, and with 512 the pool rows of 32,768 blocks in
+// the 38-layer decode step overflowed (623 candidates in one chunk).
+constexpr int kRegion = 1024;
 constexpr int kDirect = 16384;   // rows up to this length are selected in shared memory directly
 constexpr int kChunk = 16384;    // elements per CTA in the streaming passes
 constexpr int kMaxK = 2048;
