@@ -625,8 +625,7 @@ struct TcSmem {
   static constexpr int kOffRaw = kOffP + 2 * kQAtom;            // [kTcKeys][kRawStride]
   static constexpr int kOffKind = kOffRaw + kTcKeys * kRawStride;  // int[kTcKeys]
   static constexpr int kOffStat = kOffKind + kTcKeys * 4;       // float m[64], l[64], sink[64]
-  static constexpr int kOffW = kOffStat + 3 * kH * 4;           // float [6][64]: softmax exchange of group maxima, sums
-  static constexpr int kOffBar = kOffW + 6 * kH * 4;            // raw, S done, O halves done, q
+  static constexpr int kOffBar = kOffStat + 3 * kH * 4;             // raw, S done, O halves done, q
   static constexpr int kOffTmem = kOffBar + 5 * 8;
   static constexpr int kBytes = kOffTmem + 8;
   static constexpr int kAlloc = kBytes + 1024;                  // the base is rounded up to 1024 B
@@ -763,7 +762,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   float* sM = reinterpret_cast<float*>(sm + TcSmem::kOffStat);
   float* sL = sM + kH;
   float* sSink = sL + kH;
-  float* sW = reinterpret_cast<float*>(sm + TcSmem::kOffW);
   uint64_t* bar_raw = reinterpret_cast<uint64_t*>(sm + TcSmem::kOffBar);
   uint64_t* bar_s = bar_raw + 1;
   uint64_t* bar_o = bar_raw + 2;  // [2]
@@ -892,57 +890,75 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (tid == kTcMmaThread) issue_s(1);
   }
 
-  // ---- softmax of the chunk: warps 0-3 (keys 0-31), 4-7 (keys 32-63) and
-  // 8-11 (keys 64-79), one head per thread.  An M = 64 accumulator holds head
-  // h in TMEM lane 32 (h / 16) + h % 16: lanes 0-15 of each warp's quadrant
-  // (lanes 16-31 compute on unused lanes and store nothing).  The three key
-  // groups exchange max and sum through shared memory.
-  float* sMx = sW;           // [3][64] group maxima
-  float* sSx = sW + 3 * kH;  // [3][64] group sums
-  if (warp < 12) {
-    const int grp = warp >> 2;  // keys 32 grp .. 32 grp + 31
-    const int h = (warp & 3) * 16 + (lane & 15);
-    const bool act = lane < 16;
+  // ---- softmax of the chunk: warps 0-3, one per TMEM lane quadrant q (an
+  // M = 64 accumulator holds heads 16q .. 16q+15 in lanes 0-15 of quadrant q).
+  // Three 16x256b loads give lane l heads hA = 16q + l/4 and hB = hA + 8, keys
+  // 8g + 2(l%4) and the next of every 8-key group g (keys 80-95 are masked);
+  // the four lanes of a head combine max and sum by shuffles.
+  if (warp < 4) {
+    const int q = warp;
+    const int hA = 16 * q + (lane >> 2), hB = hA + 8;
+    const int kc = 2 * (lane & 3);  // this lane's first key of each 8-key group
     bool oks = mbar_wait(bar_s, 0u, nullptr);
     if (!oks) set_error(p.err, kErrTimeout);
     tc_fence_after();
-    float v[32];
-    tmem_ld32(tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + 256 + 32 * grp, v);
-    const unsigned km = kmask[grp];  // keys past 79 are never set
-    float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+    uint32_t r0[16], r1[16], r2[16];
+    const uint32_t ta = tmem + (static_cast<uint32_t>(32 * q) << 16) + 256;
+    tmem_ld16x256_x4(ta, r0);
+    tmem_ld16x256_x4(ta + 32, r1);
+    tmem_ld16x256_x4(ta + 64, r2);
+    tmem_wait_ld16(r0);
+    tmem_wait_ld16(r1);
+    tmem_wait_ld16(r2);
+    constexpr int kG = kTcKeys / 8;  // 8-key groups of the chunk
+    float xA[2 * kG], xB[2 * kG];
+    float mA = -INFINITY, mB = -INFINITY;
 #pragma unroll
-    for (int j = 0; j < 32; ++j) {
-      v[j] = ((km >> j) & 1u) && oks ? v[j] * p.scale_log2 : -INFINITY;
-      mx[j & 3] = fmaxf(mx[j & 3], v[j]);
-    }
-    if (act) sMx[grp * kH + h] = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
-    named_bar_sync(1, 384);
-    const float m = fmaxf(fmaxf(sMx[h], sMx[kH + h]), sMx[2 * kH + h]);
-    float sum[4] = {0.f, 0.f, 0.f, 0.f};
-    uint32_t pk[16];
+    for (int g = 0; g < kG; ++g) {
+      const uint32_t* rr = (g < 4) ? r0 : (g < 8) ? r1 : r2;
+      const int gi = g & 3;
 #pragma unroll
-    for (int j = 0; j < 32; j += 2) {
-      const float e0 = (m == -INFINITY) ? 0.f : ex2_approx(v[j] - m);
-      const float e1 = (m == -INFINITY) ? 0.f : ex2_approx(v[j + 1] - m);
-      sum[(j >> 1) & 3] += e0 + e1;
-      pk[j / 2] = pack_bf16(e0, e1);
-    }
-    if (act) sSx[grp * kH + h] = (sum[0] + sum[1]) + (sum[2] + sum[3]);
-    // P rows: keys 0-63 in atom 0 (chunks 0-7), keys 64-79 in chunks 0-1 of atom 1
-    uint8_t* prow = sP + (grp >> 1) * TcSmem::kQAtom + h * 128;
-    const int nc = (grp < 2) ? 4 : (kTcKeys - 64) / 8;
-#pragma unroll
-    for (int c4 = 0; c4 < 4; ++c4) {
-      if (act && c4 < nc) {
-        const int c = 4 * (grp & 1) + c4;
-        *reinterpret_cast<uint4*>(prow + ((c ^ (h & 7)) << 4)) =
-            make_uint4(pk[4 * c4], pk[4 * c4 + 1], pk[4 * c4 + 2], pk[4 * c4 + 3]);
+      for (int u = 0; u < 2; ++u) {
+        const int k = 8 * g + kc + u;
+        const bool valid = oks && ((kmask[k >> 5] >> (k & 31)) & 1u);
+        xA[2 * g + u] = valid ? __uint_as_float(rr[4 * gi + u]) * p.scale_log2 : -INFINITY;
+        xB[2 * g + u] = valid ? __uint_as_float(rr[4 * gi + 2 + u]) * p.scale_log2 : -INFINITY;
+        mA = fmaxf(mA, xA[2 * g + u]);
+        mB = fmaxf(mB, xB[2 * g + u]);
       }
     }
-    named_bar_sync(1, 384);
-    if (act && grp == 0) {
-      sM[h] = m;
-      sL[h] = (sSx[h] + sSx[kH + h]) + sSx[2 * kH + h];
+#pragma unroll
+    for (int o = 1; o <= 2; o <<= 1) {
+      mA = fmaxf(mA, __shfl_xor_sync(0xffffffffu, mA, o));
+      mB = fmaxf(mB, __shfl_xor_sync(0xffffffffu, mB, o));
+    }
+    float sA = 0.f, sB = 0.f;
+    uint8_t* prA = sP + hA * 128;
+    uint8_t* prB = sP + hB * 128;
+#pragma unroll
+    for (int g = 0; g < kG; ++g) {
+      const float a0 = (mA == -INFINITY) ? 0.f : ex2_approx(xA[2 * g] - mA);
+      const float a1 = (mA == -INFINITY) ? 0.f : ex2_approx(xA[2 * g + 1] - mA);
+      const float b0 = (mB == -INFINITY) ? 0.f : ex2_approx(xB[2 * g] - mB);
+      const float b1 = (mB == -INFINITY) ? 0.f : ex2_approx(xB[2 * g + 1] - mB);
+      sA += a0 + a1;
+      sB += b0 + b1;
+      // P rows: keys 0-63 in atom 0 (16-B chunks 0-7), keys 64-79 in chunks
+      // 0-1 of atom 1; this lane's key pair is bytes 2 kc .. 2 kc + 3 of chunk g % 8
+      const int off = (g >> 3) * TcSmem::kQAtom + 2 * kc;
+      *reinterpret_cast<uint32_t*>(prA + off + (((g & 7) ^ (hA & 7)) << 4)) = pack_bf16(a0, a1);
+      *reinterpret_cast<uint32_t*>(prB + off + (((g & 7) ^ (hB & 7)) << 4)) = pack_bf16(b0, b1);
+    }
+#pragma unroll
+    for (int o = 1; o <= 2; o <<= 1) {
+      sA += __shfl_xor_sync(0xffffffffu, sA, o);
+      sB += __shfl_xor_sync(0xffffffffu, sB, o);
+    }
+    if ((lane & 3) == 0) {
+      sM[hA] = mA;
+      sL[hA] = sA;
+      sM[hB] = mB;
+      sL[hB] = sB;
     }
     fence_proxy_async_smem();
   }
