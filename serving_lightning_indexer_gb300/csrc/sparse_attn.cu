@@ -998,17 +998,27 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const float l = sL[h];
     const float inv = (l > 0.f && oko) ? 1.f / l : 0.f;
     uint8_t* dst = p.part + (rowbase + rank) * kPartChunkBytes + h * 16;
-#pragma unroll 1
-    for (int cc = 0; cc < 4; ++cc) {
-      float v[32];
-      tmem_ld32(tmem + (static_cast<uint32_t>(qd * 32) << 16) + 128 * g + 32 * cc, v);
+    // eight 16-column loads, each issued before the previous one is consumed
+    const uint32_t tcol = tmem + (static_cast<uint32_t>(qd * 32) << 16) + 128 * g;
+    uint32_t ra[16], rb[16];
+    tmem_ld32x16_async(tcol, ra);
+    tmem_wait_ld16(ra);
 #pragma unroll
-      for (int j = 0; j < 4; ++j)  // block 16 g + 4 cc + j
+    for (int cc = 0; cc < 8; ++cc) {
+      uint32_t(&cur)[16] = (cc & 1) ? rb : ra;
+      uint32_t(&nxt)[16] = (cc & 1) ? ra : rb;
+      if (cc + 1 < 8) tmem_ld32x16_async(tcol + 16 * (cc + 1), nxt);
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {  // block 16 g + 2 cc + j
+        const uint32_t* w = cur + 8 * j;
         if (act)
-          *reinterpret_cast<uint4*>(dst + (16 * g + 4 * cc + j) * kPartBlockBytes) =
-            make_uint4(pack_bf16(v[8 * j] * inv, v[8 * j + 1] * inv), pack_bf16(v[8 * j + 2] * inv, v[8 * j + 3] * inv),
-                       pack_bf16(v[8 * j + 4] * inv, v[8 * j + 5] * inv),
-                       pack_bf16(v[8 * j + 6] * inv, v[8 * j + 7] * inv));
+          *reinterpret_cast<uint4*>(dst + (16 * g + 2 * cc + j) * kPartBlockBytes) = make_uint4(
+              pack_bf16(__uint_as_float(w[0]) * inv, __uint_as_float(w[1]) * inv),
+              pack_bf16(__uint_as_float(w[2]) * inv, __uint_as_float(w[3]) * inv),
+              pack_bf16(__uint_as_float(w[4]) * inv, __uint_as_float(w[5]) * inv),
+              pack_bf16(__uint_as_float(w[6]) * inv, __uint_as_float(w[7]) * inv));
+      }
+      if (cc + 1 < 8) tmem_wait_ld16(nxt);
     }
     if (act && g == 0) p.part_ml[(rowbase + rank) * kH + h] = make_float2(oko ? sM[h] : -INFINITY, oko ? l : 0.f);
   }
