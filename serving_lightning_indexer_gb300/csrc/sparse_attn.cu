@@ -600,8 +600,9 @@ __global__ void __launch_bounds__(512, 1) sparse_attn_kernel(const __grid_consta
 //     dims, each [64 rows x 128 B], rows of an atom 1024 B per group of 8.
 //   * S = q K^T on tcgen05 (M = 64 heads, N = 80 keys, K = 512) into TMEM;
 //     an M = 64 accumulator puts head h in lane 32 (h / 16) + h % 16.
-//   * one thread per head reads its S row, masks absent keys, and forms
-//     P = exp2(S*scale - max) (bf16, swizzled) with its max and sum.
+//   * four lanes per head (4 warps, one per TMEM lane quadrant) read its S
+//     row, mask absent keys, and form P = exp2(S*scale - max) (bf16, swizzled)
+//     with its max and sum, combined across the four lanes by shuffles.
 //   * O = P V on tcgen05 (M = 64 heads, N = 256 dims twice, K = 80 keys; V
 //     is the key tile read MN-major) into TMEM.
 //   * O / sum is stored as bf16 straight from the accumulator into a per-row
@@ -609,9 +610,8 @@ __global__ void __launch_bounds__(512, 1) sparse_attn_kernel(const __grid_consta
 //     barrier the CTA of rank r loads its range of heads of every chunk from
 //     L2 and combines them with the sink.
 // Scratch of one chunk: O / sum as bf16 in [64 blocks of 8 dims][64 heads][16 B]
-// -- a warp's 32 heads of one block are 512 contiguous bytes, and a head range
-// of every block is one box of a 2-D tensor copy -- plus (max, sum) per head in
-// a separate array [rows][chunks][64] of float2.
+// (a readout warp's 16 heads of one block are 256 contiguous bytes), plus
+// (max, sum) per head in a separate array [rows][chunks][64] of float2.
 constexpr int kPartBlocks = kD / 8;                     // blocks of 8 dims
 constexpr int kPartBlockBytes = kH * 16;                // one block: 64 heads x 8 bf16
 constexpr int kPartChunkBytes = kPartBlocks * kPartBlockBytes;
