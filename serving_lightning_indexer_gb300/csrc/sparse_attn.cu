@@ -5,9 +5,11 @@
 // <= k main-KV entries of the row's top-k, with the per-head sink s_i only in
 // the denominator; K = V is one shared 512-vector (MQA, 64 heads).
 //
-// The key list of a row is [SWA slots..., main slots...], cut into chunks of
-// 64 keys.  A thread-block cluster of S CTAs works on one row, CTA r taking a
-// contiguous range of chunks.  Per chunk a CTA
+// The key list of a row is [SWA slots..., main slots...].  Rows of up to 16
+// chunks of 80 keys (decode and prefill: 128 SWA + 512 main keys) take the
+// tcgen05 kernel further below.  Longer rows take this split-K kernel: the
+// list is cut into chunks of 64 keys, and a thread-block cluster of S CTAs
+// works on one row, CTA r taking a contiguous range of chunks.  Per chunk a CTA
 //   * gathers the records with bulk async copies (one per key, completing on an
 //     mbarrier) into a staging area, the row's q arriving the same way,
 //   * dequantises them to bf16 rows in shared memory (FP8 e4m3 x fp32 scale for
