@@ -631,10 +631,6 @@ struct TcSmem {
   static constexpr int kOffTmem = kOffBar + 5 * 8;
   static constexpr int kBytes = kOffTmem + 8;
   static constexpr int kAlloc = kBytes + 1024;                  // the base is rounded up to 1024 B
-  // merge: the received head ranges ([ns][64 blocks][ceil(64 / ns) heads][16 B])
-  // use the q and key tiles
-  static_assert(75 * kPartBlocks * 16 <= 8 * kQAtom + 8 * kKAtom,
-                "received head ranges (ns * ceil(64 / ns) <= 75 heads for 1..16 chunks) fit the q and key tiles");
   static_assert(kKAtom % 1024 == 0 && kOffK % 1024 == 0 && kOffP % 1024 == 0, "swizzle atoms are 1024-B aligned");
   static_assert(kAlloc <= 227 * 1024, "one CTA per SM");
 };
