@@ -38,7 +38,6 @@ constexpr int kQStride = kD + 8;     // bf16 per shared row (1040 B: conflict-fr
 constexpr int kSStride = kCK + 4;    // floats
 constexpr int kPStride = kCK + 8;    // bf16
 constexpr int kRawStride = 528;      // staging bytes per key (largest record)
-constexpr int kOStride = kD + 4;     // floats per row of the O partial in the merge
 constexpr int kMaxCluster = 16;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -136,13 +135,6 @@ __device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst, const void* src,
                    "r"(dst),
                "r"(smem_u32(src)), "r"(bytes), "r"(mbar)
                : "memory");
-}
-__device__ __forceinline__ float4 ld_cluster_f32x4(uint32_t addr) {
-  float4 v;
-  asm volatile("ld.shared::cluster.v4.f32 {%0,%1,%2,%3}, [%4];"
-               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-               : "r"(addr));
-  return v;
 }
 
 // ---------------------------------------------------------------- dequantisation
