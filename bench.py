@@ -174,8 +174,6 @@ def cpu_baseline(step, budget_s: float, device_copy):
     """The oracle, as it stands, on a bounded sample of the same workload:
     decoder Full-layer rows (score every visible entry, top-512, pool) until the
     time budget is spent.  Returns keys/s, threads used and the sample."""
-    import numpy as np
-
     from oracle import csa2_oracle as o
     c = step.caches[3]
     li = step.inputs[20]
@@ -212,7 +210,6 @@ def main():
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
-    import numpy as np
     import torch
 
     if args.impl == "reference":
@@ -455,7 +452,6 @@ def reference_arm(args, rank, world):
     with its top-512 and pool)."""
     if rank != 0:
         return
-    import numpy as np
     import torch
 
     from oracle import csa2_oracle as o

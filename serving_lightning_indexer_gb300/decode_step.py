@@ -17,7 +17,6 @@ kernels; this module only allocates buffers and issues the calls in order.
 """
 from __future__ import annotations
 
-import math
 from dataclasses import dataclass, field
 
 import torch

@@ -4,7 +4,6 @@ brute force and invariants the pages state."""
 import itertools
 
 import numpy as np
-import torch
 
 from conftest import read_golden
 from oracle import csa2_oracle as o
