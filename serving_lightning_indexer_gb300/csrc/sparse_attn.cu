@@ -1040,6 +1040,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // heads per load and store of a warp)
     const int li = task % nh, c = task / nh;
     const int h = hb + li;
+    const uint8_t* src = p.part + (rowbase * kPartBlocks + c) * kPartBlockBytes + h * 16;
+    auto load_batch = [&](int r0, uint4 (&pv)[8]) {
+#pragma unroll
+      for (int r = 0; r < 8; ++r)
+        pv[r] = (r0 + r < ns) ? __ldcg(reinterpret_cast<const uint4*>(src + static_cast<long long>(r0 + r) * kPartChunkBytes))
+                              : make_uint4(0u, 0u, 0u, 0u);
+    };
+    // the first 8 chunks' rows are requested before the (max, sum) pairs, so
+    // both arrive in one round trip to L2
+    uint4 pv[8];
+    load_batch(0, pv);
     float wr[kMaxCluster], ml_l[kMaxCluster];
     float M = sSink[h];
 #pragma unroll
@@ -1059,14 +1070,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const float invD = 1.f / D;
     if (c == 0 && p.lse) p.lse[static_cast<long long>(t) * kH + h] = (M + log2f(D)) * kLn2;
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    const uint8_t* src = p.part + (rowbase * kPartBlocks + c) * kPartBlockBytes + h * 16;
 #pragma unroll
     for (int r0 = 0; r0 < kMaxCluster; r0 += 8) {  // 8 chunks' loads in flight at a time
-      uint4 pv[8];
-#pragma unroll
-      for (int r = 0; r < 8; ++r)
-        pv[r] = (r0 + r < ns) ? __ldcg(reinterpret_cast<const uint4*>(src + static_cast<long long>(r0 + r) * kPartChunkBytes))
-                              : make_uint4(0u, 0u, 0u, 0u);
+      if (r0 > 0) {
+        if (r0 >= ns) break;
+        load_batch(r0, pv);
+      }
 #pragma unroll
       for (int r = 0; r < 8; ++r) {
         const float w = wr[r0 + r] * invD;
