@@ -292,7 +292,7 @@ CSA2_API int csa2_sparse_attn(const csa2_sparse_attn_args* args, void* workspace
 typedef struct {
   const uint16_t* C; const uint16_t* Z;        /* [n_tokens,512] bf16; Z unused for m=1 */
   int64_t n_tokens; int32_t ratio_m;
-  const float* gamma; float eps;               /* [512] */
+  const float* gamma; float eps;               /* [512], 16-B aligned */
   int32_t apply_rope; float rope_theta;
   int64_t first_entry;
   const int32_t* entry_pos;                    /* optional [n_entries] */
@@ -301,7 +301,7 @@ typedef struct {
   const int32_t* entry_slot;                   /* optional [n_entries] direct slots */
   float* latent_out;                           /* optional [n_entries,512] */
   const uint16_t* w_ik;                        /* optional [512,128] bf16 W^IK (row = latent dim) */
-  const float* k_gamma;                        /* [128] k_norm weight (with w_ik) */
+  const float* k_gamma;                        /* [128] k_norm weight (with w_ik), 16-B aligned */
   uint8_t* index_k; int64_t index_k_pages;     /* index-K pages (with w_ik) */
   int32_t index_k_format;                      /* CSA2_INDEX_FP8 or CSA2_INDEX_FP4 */
   float* index_latent_out;                     /* optional [n_entries,128] */

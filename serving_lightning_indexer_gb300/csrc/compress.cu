@@ -91,17 +91,29 @@ __global__ void __launch_bounds__(256) compress_kernel(const __grid_constant__ C
   // W^IK is a weight (no earlier kernel writes it): this warp's 64 rows, lane
   // l's 4 columns 4l .. 4l+3, are loaded before the dependency wait
   uint2 wr[IK ? 64 : 1];
+  float4 kg = make_float4(1.f, 1.f, 1.f, 1.f);  // k_norm weights of outputs 4l .. 4l+3
   if constexpr (IK) {
 #pragma unroll
     for (int r = 0; r < 64; ++r)
       wr[r] = __ldg(reinterpret_cast<const uint2*>(p.w_ik + (64 * warp + r) * 128 + 4 * lane));
+    kg = __ldg(reinterpret_cast<const float4*>(p.k_gamma) + lane);
+  }
+  // the RMSNorm weights of this lane's 16 channels, likewise
+  const int c0 = lane * 16;
+  float gam[16];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float4 g4 = __ldg(reinterpret_cast<const float4*>(p.gamma + c0) + i);
+    gam[4 * i] = g4.x;
+    gam[4 * i + 1] = g4.y;
+    gam[4 * i + 2] = g4.z;
+    gam[4 * i + 3] = g4.w;
   }
   pdl_wait();
   pdl_trigger();
   const long long e_raw = static_cast<long long>(blockIdx.x) * EPC + warp;
   const bool active = warp < EPC && e_raw < p.n_entries;  // other warps help the index-key phase only
   const long long e = active ? e_raw : p.n_entries - 1;
-  const int c0 = lane * 16;
   long long pos = 0, slot = -1;
   bool slot_ok = false;
   if (warp < EPC) {
@@ -131,7 +143,7 @@ __global__ void __launch_bounds__(256) compress_kernel(const __grid_constant__ C
   const float inv = 1.0f / sqrtf(ss / 512.0f + p.eps);
   float y[16];
 #pragma unroll
-  for (int i = 0; i < 16; ++i) y[i] = x[i] * inv * __ldg(p.gamma + c0 + i);
+  for (int i = 0; i < 16; ++i) y[i] = x[i] * inv * gam[i];
   pos = p.entry_pos ? static_cast<long long>(__ldg(p.entry_pos + e)) : (p.first_entry + e) * p.ratio_m;
   if constexpr (IK) {  // the latent before RoPE feeds the index key
 #pragma unroll
@@ -244,7 +256,6 @@ __global__ void __launch_bounds__(256) compress_kernel(const __grid_constant__ C
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) s2 += __shfl_xor_sync(0xffffffffu, s2, o);
   const float inv2 = 1.0f / sqrtf(s2 / 128.0f + p.eps);
-  const float4 kg = __ldg(reinterpret_cast<const float4*>(p.k_gamma) + lane);
   kk[0] *= inv2 * kg.x;
   kk[1] *= inv2 * kg.y;
   kk[2] *= inv2 * kg.z;

@@ -411,9 +411,9 @@ int csa2_compress_m2(const csa2_compress_args* a, void* stream) {
   if (a->ratio_m == 2 && !a->Z) return fail(CSA2_ERR_NULL, "csa2_compress_m2: Z is NULL with ratio_m=2");
   if (a->n_tokens < 0) return fail(CSA2_ERR_SHAPE, "csa2_compress_m2: n_tokens < 0");
   if (!a->entry_slot && !a->page_table) return fail(CSA2_ERR_NULL, "csa2_compress_m2: entry_slot or page_table is required");
-  if (!aligned16(a->C) || (a->Z && !aligned16(a->Z)) || !aligned16(a->main_kv) ||
+  if (!aligned16(a->C) || (a->Z && !aligned16(a->Z)) || !aligned16(a->main_kv) || !aligned16(a->gamma) ||
       (a->latent_out && !aligned16(a->latent_out)))
-    return fail(CSA2_ERR_ALIGN, "csa2_compress_m2: C, Z, main_kv, latent_out must be 16-B aligned");
+    return fail(CSA2_ERR_ALIGN, "csa2_compress_m2: C, Z, gamma, main_kv, latent_out must be 16-B aligned");
   if (!(a->eps >= 0.f)) return fail(CSA2_ERR_SHAPE, "csa2_compress_m2: eps must be >= 0");
   if (a->apply_rope && !(a->rope_theta > 0.f)) return fail(CSA2_ERR_SHAPE, "csa2_compress_m2: rope_theta must be > 0");
   if (a->first_entry < 0) return fail(CSA2_ERR_SHAPE, "csa2_compress_m2: first_entry < 0");
@@ -422,9 +422,9 @@ int csa2_compress_m2(const csa2_compress_args* a, void* stream) {
     if (a->index_k_format != CSA2_INDEX_FP8 && a->index_k_format != CSA2_INDEX_FP4)
       return fail(CSA2_ERR_UNSUPPORTED, "csa2_compress_m2: index_k_format=%d is neither FP8 (0) nor FP4 (1)",
                   a->index_k_format);
-    if (!aligned16(a->w_ik) || !aligned16(a->index_k) ||
+    if (!aligned16(a->w_ik) || !aligned16(a->k_gamma) || !aligned16(a->index_k) ||
         (a->index_latent_out && !aligned16(a->index_latent_out)))
-      return fail(CSA2_ERR_ALIGN, "csa2_compress_m2: w_ik, index_k, index_latent_out must be 16-B aligned");
+      return fail(CSA2_ERR_ALIGN, "csa2_compress_m2: w_ik, k_gamma, index_k, index_latent_out must be 16-B aligned");
     if (a->index_k_pages < 1) return fail(CSA2_ERR_SHAPE, "csa2_compress_m2: index_k_pages must be >= 1");
   }
   DeviceCtx ctx;
