@@ -135,6 +135,11 @@ def test_validation_returns_codes_without_launch(lib):
     assert lib.csa2_compress_m2(C.byref(ca), None) == 1                          # m=2 needs Z
     ca.ratio_m = 4
     assert lib.csa2_compress_m2(C.byref(ca), None) == 4
+    ca.ratio_m = 1
+    ca.gamma = FAKE + 4                                                          # weights read as 16-B vectors
+    assert lib.csa2_compress_m2(C.byref(ca), None) == 3
+    ca.gamma, ca.w_ik, ca.k_gamma, ca.index_k, ca.index_k_pages = FAKE, FAKE, FAKE + 8, FAKE, 1
+    assert lib.csa2_compress_m2(C.byref(ca), None) == 3
     for code in range(9):
         assert lib.csa2_status_string(code)
 
