@@ -43,6 +43,11 @@ def cache_of(layer: int) -> int:
     return (layer - 2) // 6 if layer < 20 else 3
 
 
+def ratio_of(cache: int) -> int:
+    """Compression ratio m of a cache copy: 2 in the encoder, 1 in the decoder."""
+    return 2 if cache < 3 else 1
+
+
 @dataclass
 class CacheCopy:
     ratio_m: int
@@ -88,7 +93,7 @@ class DecodeStep:
         dev = device
         self.caches: list[CacheCopy] = []
         for ci in range(4):
-            m = 2 if ci < 3 else 1
+            m = ratio_of(ci)
             ents = [n // m for n in lengths]
             if not any(cache_of(l) == ci for l in self.layers):
                 self.caches.append(None)
