@@ -48,6 +48,20 @@ def ratio_of(cache: int) -> int:
     return 2 if cache < 3 else 1
 
 
+def keys_scored(lengths, layers=LAYERS) -> int:
+    """Index keys one decode step scores: every visible entry (N // m) of each
+    sequence for a Full layer, the pool positions (at most 2048 blocks of 8)
+    for a Reindex layer, none for a Reuse layer."""
+    n = 0
+    for l in layers:
+        ents = [length // ratio_of(cache_of(l)) for length in lengths]
+        if role_of(l) == "full":
+            n += sum(ents)
+        elif role_of(l) == "reindex":
+            n += sum(min(e, W.POOL_BLOCKS * W.POOL_BLOCK) for e in ents)
+    return n
+
+
 @dataclass
 class CacheCopy:
     ratio_m: int
@@ -142,14 +156,7 @@ class DecodeStep:
 
     # ---------------------------------------------------------------- per-step work
     def keys_scored_per_step(self) -> int:
-        n = 0
-        for l in self.layers:
-            c = self.caches[cache_of(l)]
-            if role_of(l) == "full":
-                n += sum(c.entries)
-            elif role_of(l) == "reindex":
-                n += sum(min(e, W.POOL_BLOCKS * W.POOL_BLOCK) for e in c.entries)
-        return n
+        return keys_scored(self.lengths, self.layers)
 
     def attn_query_layers_per_step(self) -> int:
         return len(self.layers) * self.B

@@ -38,3 +38,16 @@ def test_every_layer_reads_the_nearest_preceding_kv_source():
 def test_compressed_entries_per_token():
     assert [ds.ratio_of(ds.cache_of(s)) for s in KV_SOURCE] == [2, 2, 2, 1]
     assert sum(1.0 / ds.ratio_of(ds.cache_of(s)) for s in KV_SOURCE) == 2.5
+
+
+def test_keys_scored_per_step_of_the_benchmark_step():
+    # batch 8 at {32K, 256K, 1M, 1M} x 2: three encoder Full layers score N/2
+    # entries a sequence, the decoder Full layer N, four Reindex layers the
+    # 2048 x 8 pool positions of each sequence
+    lengths = [32768, 262144, 1 << 20, 1 << 20] * 2
+    encoder = sum(n // 2 for n in lengths)
+    decoder = sum(lengths)
+    reindex = 8 * 2048 * 8
+    assert ds.keys_scored(lengths) == 3 * encoder + decoder + 4 * reindex == 12_484_608
+    # short sequences: the pool covers every entry
+    assert ds.keys_scored([1000], layers=(24,)) == 1000
