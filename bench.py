@@ -1,34 +1,45 @@
-"""Benchmark of the CSA2 global-attention decode step on GB300.
+"""Benchmark of the CSA2 global-attention step on GB300.
 
-Workload: one 38-layer CSA2 decode step (encoder layers 2..19 at m=2 with Full
-layers 2/8/14, decoder layers 20..39 at m=1 with Full layer 20 and Reindex
-layers 24/28/32/36), batch 8 with context lengths {32K, 256K, 1M, 1M} x 2, four
-resident main-KV / index-K cache copies, per-layer q, w, SWA and sink drawn
-independently.  A step = the Full layers' entry build, Lightning-Indexer scan,
-top-512 (+ candidate pool at layer 20), the Reindex layers' pool rescoring and
-top-512, and sparse attention in all 38 layers.
+Headline workload: one 38-layer CSA2 decode step (encoder layers 2..19 at m=2
+with Full layers 2/8/14, decoder layers 20..39 at m=1 with Full layer 20 and
+Reindex layers 24/28/32/36), batch 8 with context lengths {32K, 256K, 1M, 1M}
+x 2, four resident main-KV / index-K cache copies, per-layer q, w, SWA and sink
+drawn independently.  A step = the Full layers' entry build, Lightning-Indexer
+scan, top-512 (+ candidate pool at layer 20), the Reindex layers' pool
+rescoring and top-512, and sparse attention in all 38 layers.
 
 Metric: indexer keys scored per second (every visible entry of the Full layers
 plus the 16,384 pool candidates of each Reindex row); sparse-attention
-query-layers per second is reported beside it.
+query-layers per second is reported beside it.  The same run also measures
+  * the 4096-query prefill chunk after a 256K-token prefix (m = 2): entry
+    build, the prefill indexer GEMM (roofline against the FP8 tensor peak),
+    top-512 of every query and sparse attention of the 4096 queries;
+  * the decode Reindex at 1M context (batch 16, 16,384 pool candidates per
+    row, 10 % planted blocks) and the attention of its four layers.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+  python bench.py --case scan|topk|reindex|attn|prefill [--iters N]   (one call, for profilers)
 
-Timing: W eager warm-up steps, then K steps captured in one CUDA graph and
-replayed once between two device synchronisations (max over ranks).  Every
-step streams ~1.6 GB of index-K cache, far above the 129 MB L2, so no L2
-flush is inserted.  CUDA events recorded inside the graph (on a side branch,
-so that the kernels keep their programmatic-launch overlap) around each
-indexer-scan launch give the dominant kernel's duration for the roofline.
+Timing: W eager warm-up steps, then K steps captured in one CUDA graph; the
+graph is replayed (each replay timed with CUDA events between two device
+synchronisations) until at least --min-seconds have passed, and the median
+replay gives the step time (max over ranks).  Every step streams ~1.6 GB of
+index-K cache, far above the 129 MB L2, so no L2 flush is inserted.  CUDA
+events recorded inside the graph (on a side branch, so that the kernels keep
+their programmatic-launch overlap) around each indexer scan and attention
+launch give those kernels' durations for the rooflines.
 """
 from __future__ import annotations
 
 import argparse
 import json
+import math
 import os
+import platform
 import statistics
 import subprocess
 import sys
+import tempfile
 import threading
 import time
 
@@ -44,6 +55,11 @@ INDEX_KEY_BYTES = 132   # 128 e4m3 codes + one fp32 scale per key
 # 512 main-KV entries of 272 B (256 B codes + 16 scales), bf16 output, slots
 ATTN_ROW_BYTES = 65536 + 128 * 528 + 512 * 272 + 65536 + 640 * 4
 ATTN_ROW_FLOP = 2 * 2 * 64 * 640 * 512   # S = q K^T and O = P V
+INDEX_PAIR_FLOP = 2 * 32 * 128           # one (query, entry) pair of the indexer: 32 heads x 128 dims
+# prefill chunk: 4096 new tokens after a 256K-token prefix, m = 2
+PREFILL_PREFIX, PREFILL_T, PREFILL_M = 1 << 18, 4096, 2
+# decode Reindex: batch 16 at 1M context, 2048-block x 8 pools
+REINDEX_B, REINDEX_N = 16, 1 << 20
 
 
 def _scan_traffic_per_key():
@@ -85,20 +101,13 @@ def whole_job_rate(units_per_rank_step: float, steps: int, world: int, ms_max: f
 
 
 def _peaks():
+    """(HBM GB/s, bf16 burst TFLOP/s, bf16 sustained TFLOP/s, source)."""
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
             d = json.load(f)
-        return float(d["hbm_gbs"]), "measured"
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), float(d["bf16_tflops_sustained"]), "measured"
     except Exception:
-        return 6800.0, "fallback"
-
-
-def _bf16_peak():
-    try:
-        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
-            return float(json.load(f)["bf16_tflops_sustained"])
-    except Exception:
-        return 1700.0
+        return 6800.0, 1900.0, 1700.0, "fallback"
 
 
 class ClockSampler:
@@ -155,7 +164,7 @@ class ClockSampler:
             except ValueError:
                 continue
         if not rows:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"]}
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"], "samples": 0}
         inside = [r for r in rows if self.t0 and self.t1 and self.t0 <= r[0] <= self.t1]
         if not inside:   # region shorter than the sampling period: nearest samples
             mid = (self.t0 + self.t1) / 2 if self.t0 and self.t1 else rows[-1][0]
@@ -170,42 +179,355 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(inside)}
 
 
-def cpu_baseline(step, budget_s: float, device_copy):
-    """The oracle, as it stands, on a bounded sample of the same workload:
-    decoder Full-layer rows (score every visible entry, top-512, pool) until the
-    time budget is spent.  Returns keys/s, threads used and the sample."""
+# ---------------------------------------------------------------------------
+# CPU baseline: the oracle on the host cores, in worker processes whose BLAS
+# thread count is set before numpy loads
+# ---------------------------------------------------------------------------
+
+def cpu_model() -> str:
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    return platform.processor() or platform.machine()
+
+
+def _cpu_worker(path: str, budget: float) -> dict:
+    """Runs in a child process: the oracle on the saved sample until the time
+    budget is spent; reports the rates, wall time and CPU time of the process."""
+    import numpy as np
+
     from oracle import csa2_oracle as o
-    c = step.caches[3]
-    li = step.inputs[20]
-    cache, pt = device_copy(c.pc.index_k), device_copy(c.pc.page_table)
-    q8, qs, w = device_copy(li.iq.q_fp8), device_copy(li.iq.q_scale), device_copy(li.iq.w)
-    keys = 0
+    d = np.load(path)
+    n = int(d["n"])
+    res = {}
+    # indexer: score every visible entry of a row prefix, top-512 and the pool
+    t0, c0 = time.perf_counter(), time.process_time()
     rows = 0
-    t0 = time.perf_counter()
-    chunk = 131072
-    b = 0
-    while time.perf_counter() - t0 < budget_s and rows < 64:
-        n = min(c.entries[b], chunk)
-        s = o.index_scores_row(q8[b], qs[b], w[b], cache, pt[b], n)
+    while rows < 1 or (time.perf_counter() - t0 < 0.6 * budget and rows < 64):
+        s = o.index_scores_row(d["q8"], d["qs"], d["w"], d["cache"], d["pt"], n)
         o.topk_positions(s, 512)
         o.candidate_pool(o.block_maxima(s, n), 2048)
-        keys += n
         rows += 1
-        b = (b + 1) % len(c.entries)
-    dt = time.perf_counter() - t0
-    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
-    return keys / dt, cores, f"{rows} decoder Full-layer row prefixes of {chunk} entries: score + top-512 + pool"
+    wall, cpu = time.perf_counter() - t0, time.process_time() - c0
+    res.update(keys_per_s=n * rows / wall, index_rows=rows, index_wall_s=wall, index_cpu_s=cpu)
+    # attention: one query-layer (64 heads over 128 SWA + 512 main entries, sink)
+    t0, c0 = time.perf_counter(), time.process_time()
+    qa = 0
+    while qa < 1 or (time.perf_counter() - t0 < 0.4 * budget and qa < 400):
+        o.attention_row(d["aq"], d["main"], d["mslot"], d["swa"], d["sslot"], d["sink"], 1 / math.sqrt(512))
+        qa += 1
+    awall, acpu = time.perf_counter() - t0, time.process_time() - c0
+    res.update(attn_query_layers_per_s=qa / awall, attn_rows=qa, attn_wall_s=awall, attn_cpu_s=acpu)
+    res["threads_busy"] = (cpu + acpu) / (wall + awall)
+    return res
 
+
+def _save_cpu_sample(step, device_copy, n=131072) -> str:
+    """One decoder Full-layer row prefix of n entries (its pages remapped to
+    0..n/64-1) and one attention query-layer of layer 21, saved for the CPU
+    workers."""
+    import numpy as np
+    import torch
+    c = step.caches[3]
+    li = step.inputs[20]
+    b = 2                                   # a 1M-entry sequence
+    cache = device_copy(c.pc.index_k[c.pc.page_table[b, : n // 64].long()])
+    al = step.inputs[21].attn
+    slots = device_copy(step.buf.topk_slot[3][b]).astype(np.int64)
+    ok = slots >= 0
+    mslot = np.full(slots.shape, -1, dtype=np.int64)
+    mslot[ok] = np.arange(ok.sum())
+    main = device_copy(c.pc.main_kv[step.buf.topk_slot[3][b][torch.as_tensor(ok, device=c.pc.main_kv.device)].long()])
+    ss = device_copy(al.swa_slot[b]).astype(np.int64)
+    sok = ss >= 0
+    sslot = np.full(ss.shape, -1, dtype=np.int64)
+    sslot[sok] = np.arange(sok.sum())
+    swa = device_copy(al.swa_kv[al.swa_slot[b][torch.as_tensor(sok, device=al.swa_kv.device)].long()])
+    fd, path = tempfile.mkstemp(suffix=".npz", prefix="csa2_cpu_sample_")
+    os.close(fd)
+    np.savez(path, n=n, q8=device_copy(li.iq.q_fp8[b]), qs=device_copy(li.iq.q_scale[b]), w=device_copy(li.iq.w[b]),
+             cache=cache, pt=np.arange(n // 64, dtype=np.int64),
+             aq=al.q[b].float().cpu().numpy().astype(np.float64), main=main, mslot=mslot, swa=swa, sslot=sslot,
+             sink=device_copy(al.sink).astype(np.float64))
+    return path
+
+
+def _run_cpu_worker(path: str, threads: int, budget: float) -> dict:
+    env = dict(os.environ)
+    for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "BLIS_NUM_THREADS",
+              "NUMEXPR_NUM_THREADS", "VECLIB_MAXIMUM_THREADS"):
+        env[k] = str(threads)
+    env["CUDA_VISIBLE_DEVICES"] = ""
+    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-worker", path, "--cpu-budget", str(budget)],
+                       capture_output=True, text=True, env=env, timeout=600)
+    if r.returncode != 0:
+        raise RuntimeError(f"CPU worker failed: {r.stderr[-2000:]}")
+    return json.loads(r.stdout.strip().splitlines()[-1])
+
+
+def cpu_baseline(path: str, budget: float) -> dict:
+    """The oracle, as it stands, on the host cores: once with its BLAS on every
+    core the process may use, once on one thread."""
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    multi = _run_cpu_worker(path, cores, budget)
+    one = _run_cpu_worker(path, 1, budget * 0.5)
+    return {
+        "value": multi["keys_per_s"], "unit": "keys/s", "cores": cores, "kind": "oracle",
+        "threads": round(multi["threads_busy"], 2),
+        "threads_note": "process CPU time / wall time of the worker, BLAS threads set to `cores`",
+        "model": cpu_model(), "value_1thread": one["keys_per_s"],
+        "attn_query_layers_per_s": multi["attn_query_layers_per_s"],
+        "attn_query_layers_per_s_1thread": one["attn_query_layers_per_s"],
+        "sample": (f"{multi['index_rows']} x one decoder Full-layer row prefix of 131072 entries (score + top-512 + "
+                   f"pool) and {multi['attn_rows']} x one attention query-layer (64 heads, 128 SWA + 512 main keys, "
+                   f"sink), float64 numpy oracle"),
+    }
+
+
+# ---------------------------------------------------------------------------
+# GPU measurement helpers
+# ---------------------------------------------------------------------------
+
+def _time_calls(fn, iters: int, stream, warm: int = 2) -> float:
+    """Average ms of fn() over iters back-to-back calls on the stream (CUDA events)."""
+    import torch
+    with torch.cuda.stream(stream):
+        for _ in range(warm):
+            fn()
+    stream.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(iters):
+            fn()
+        e1.record(stream)
+    stream.synchronize()
+    return e0.elapsed_time(e1) / iters
+
+
+def prefill_case(dev, seed=300):
+    """The 4096-query prefill chunk after a 256K-token prefix (m = 2): inputs
+    and the calls of one chunk, in step order."""
+    import torch
+
+    from serving_lightning_indexer_gb300 import csa2
+    from serving_lightning_indexer_gb300 import workloads as W
+    m, prefix, T = PREFILL_M, PREFILL_PREFIX, PREFILL_T
+    n_tok = prefix + T
+    n_ent = n_tok // m
+    pc = W.make_paged_cache([n_ent], seed=seed, device=dev)
+    Cm, Z, gamma = W.make_compress_inputs(n_tok, seed=seed + 1, device=dev)
+    iq = W.make_indexer_query(T, seed=seed + 2, device=dev)
+    row_pos = torch.arange(prefix, n_tok, dtype=torch.int32, device=dev)
+    r = csa2.rows(T, 1, row_seq=torch.zeros(T, dtype=torch.int32, device=dev), row_pos=row_pos, ratio_m=m)
+    ld = (n_ent + 127) // 128 * 128
+    scores = torch.empty(T, ld, dtype=torch.float32, device=dev)
+    pos = torch.empty(T, 512, dtype=torch.int32, device=dev)
+    slot = torch.empty_like(pos)
+    al = W.make_attn_layer(T, seed=seed + 3, device=dev, swa_positions=[(t, 128) for t in range(T)],
+                           n_swa_records=T + 127)
+    out = torch.empty(T, 64, 512, dtype=torch.bfloat16, device=dev)
+    pt0 = pc.page_table[0].contiguous()
+    calls = {
+        "compress": lambda: csa2.compress_m2(Cm, Z, m, gamma, pc.main_kv, page_table=pt0, first_entry=0),
+        "index_score": lambda: csa2.index_score(iq.q_fp8, iq.q_scale, iq.w, pc.index_k, pc.page_table, r, scores),
+        "topk": lambda: csa2.topk_with_candidates(scores, r, 512, pos, slot, pc.page_table),
+        "attn": lambda: csa2.sparse_attn(al.q, pc.main_kv, slot, al.swa_kv, al.swa_slot, al.sink, out),
+    }
+    flop = float(sum((p + 1) // m for p in range(prefix, n_tok))) * INDEX_PAIR_FLOP
+    return calls, dict(n_entries=n_ent, tokens=n_tok, queries=T, flop=flop)
+
+
+def reindex_case(dev, seed=200):
+    """The decode Reindex at 1M context: batch 16, a given 2048-block pool per
+    row, 10 % of the blocks shifted by +3 sigma along the Reindex query's
+    weighted direction, then the attention of the Reindex layer and 3 Reuse
+    layers."""
+    import torch
+
+    from serving_lightning_indexer_gb300 import csa2
+    from serving_lightning_indexer_gb300 import workloads as W
+    B, n = REINDEX_B, REINDEX_N
+    lengths = [n] * B
+    iq = W.make_indexer_query(B, seed=seed + 1, device=dev)
+    dirs = (iq.w[:, :, None] * iq.q_float).sum(dim=1)
+    pc = W.make_paged_cache(lengths, seed=seed, device=dev, plant_dirs=dirs, plant_frac=0.1, plant_shift=3.0)
+    pool = W.make_pool(lengths, seed=seed + 2, device=dev)
+    layers = [W.make_attn_layer(B, seed=seed + 10 + i, device=dev) for i in range(4)]
+    r = csa2.rows(B, B, n_visible=pc.n_entries)
+    pos = torch.empty(B, 512, dtype=torch.int32, device=dev)
+    slot = torch.empty_like(pos)
+    outs = [torch.empty(B, 64, 512, dtype=torch.bfloat16, device=dev) for _ in layers]
+    calls = {"reindex": lambda: csa2.reindex(iq.q_fp8, iq.q_scale, iq.w, pc.index_k, pc.page_table, r, pool, 512,
+                                             pos, slot)}
+    for i, (al, o_) in enumerate(zip(layers, outs)):
+        calls[f"attn{i}"] = (lambda al=al, o_=o_, i=i: csa2.sparse_attn(al.q, pc.main_kv, slot, al.swa_kv,
+                                                                       al.swa_slot, al.sink, o_, kv_ready=i > 0))
+    keys = int(sum(min(n, W.POOL_BLOCKS * W.POOL_BLOCK) for _ in range(B)))
+    return calls, dict(rows=B, keys=keys)
+
+
+def measure_prefill(dev, stream, iters: int, peak_fp8: float, peak_fp8_sust: float) -> dict:
+    """Per-call times of the prefill chunk and the prefill indexer's roofline."""
+    import torch
+    calls, info = prefill_case(dev)
+    for name in ("compress", "index_score", "topk", "attn"):   # one pass in order: inputs of each call
+        with torch.cuda.stream(stream):
+            calls[name]()
+    stream.synchronize()
+    ms = {name: _time_calls(calls[name], iters if name == "index_score" else max(3, iters // 4), stream)
+          for name in ("compress", "index_score", "topk", "attn")}
+    achieved = info["flop"] / (ms["index_score"] / 1e3) / 1e12
+    del calls
+    torch.cuda.empty_cache()
+    return {
+        "roofline_prefill": {
+            "bound": "tensor", "kernel": "index_tiles_kernel (prefill: 8 queries x 32 heads per MMA tile)",
+            "workload": f"4096 queries at positions 262144..266239, m=2, {info['n_entries']} entries (causal)",
+            "achieved": achieved, "peak": peak_fp8, "unit": "TFLOP/s", "frac": achieved / peak_fp8,
+            "frac_vs_sustained": achieved / peak_fp8_sust,
+            "peak_source": "FP8 dense = 2 x the measured bf16 burst (nominal FP8:BF16 ratio); sustained likewise",
+            "flop_per_launch": info["flop"], "avg_launch_ms": ms["index_score"], "launches_timed": iters,
+            "traffic": None},
+        "prefill_chunk": {
+            "workload": "prefill chunk: 4096 queries after a 256K-token prefix, m=2",
+            "call_ms": ms, "chunk_ms": sum(ms.values()),
+            "attn_query_layers_per_s": PREFILL_T / (ms["attn"] / 1e3),
+            "entries_built_per_s": info["n_entries"] / (ms["compress"] / 1e3),
+            "topk_rows_per_s": PREFILL_T / (ms["topk"] / 1e3)},
+    }
+
+
+def measure_reindex(dev, stream, iters: int, hbm_peak: float) -> dict:
+    """Reindex at 1M context, batch 16: the call (gather + selection) and the
+    attention of its four layers."""
+    import torch
+    calls, info = reindex_case(dev)
+    with torch.cuda.stream(stream):
+        for fn in calls.values():
+            fn()
+    stream.synchronize()
+    ms = {name: _time_calls(fn, iters, stream) for name, fn in calls.items()}
+    attn = statistics.mean(ms[f"attn{i}"] for i in range(4))
+    del calls
+    torch.cuda.empty_cache()
+    gbs = info["keys"] * INDEX_KEY_BYTES / (ms["reindex"] / 1e3) / 1e9
+    return {"roofline_reindex": {
+        "bound": "hbm", "kernel": "index_tiles_kernel<gather> + sel_final_kernel (csa2_reindex)",
+        "workload": "decode Reindex at 1M context, batch 16 x 16384 pool candidates, 10% planted blocks",
+        "keys_per_s": info["keys"] / (ms["reindex"] / 1e3), "achieved": gbs, "peak": hbm_peak, "unit": "GB/s",
+        "frac": gbs / hbm_peak, "algorithmic_bytes_per_launch": info["keys"] * INDEX_KEY_BYTES,
+        "avg_launch_ms": ms["reindex"], "launches_timed": iters, "traffic": None,
+        "attn_avg_launch_ms": attn, "attn_query_layers_per_s": REINDEX_B / (attn / 1e3),
+        "attn_hbm_frac": ATTN_ROW_BYTES * REINDEX_B / (attn / 1e3) / 1e9 / hbm_peak}}
+
+
+# ---------------------------------------------------------------------------
+# single-call cases for profilers
+# ---------------------------------------------------------------------------
+
+def run_case(args):
+    """One call of the library on a small input, timed with CUDA events (for
+    ncu captures: a few GB on the device at most)."""
+    import torch
+
+    import __graft_entry__
+    __graft_entry__.build()
+    from serving_lightning_indexer_gb300 import csa2
+    from serving_lightning_indexer_gb300 import workloads as W
+    dev = torch.device("cuda:0")
+    st = torch.cuda.current_stream()
+    B, n = args.batch, args.entries
+    res = {"case": args.case}
+    if args.case in ("scan", "topk", "reindex"):
+        lengths = [n] * B
+        pc = W.make_paged_cache(lengths, seed=1, device=dev, with_main=False, index_fp4=args.fp4)
+        kb = 68 if args.fp4 else INDEX_KEY_BYTES
+        iq = W.make_indexer_query(B, seed=2, device=dev)
+        r = csa2.rows(B, B, n_visible=pc.n_entries)
+        ld = (n + 127) // 128 * 128
+        scores = torch.empty(B, ld, dtype=torch.float32, device=dev)
+        bm = torch.empty(B, ld // 8, dtype=torch.float32, device=dev)
+        hist = torch.empty(2, B, 2048, dtype=torch.int32, device=dev)
+        if args.case == "scan":
+            ms = _time_calls(lambda: csa2.index_score(iq.q_fp8, iq.q_scale, iq.w, pc.index_k, pc.page_table, r, scores,
+                                                      bm, hist=hist), args.iters, st)
+            res.update(ms=ms, keys=B * n, GBps=B * n * kb / ms / 1e6, fp4=args.fp4)
+        elif args.case == "topk":
+            pos = torch.empty(B, 512, dtype=torch.int32, device=dev)
+            slot = torch.empty_like(pos)
+            pool = torch.empty(B, 2048, dtype=torch.int32, device=dev)
+
+            def both():
+                csa2.index_score(iq.q_fp8, iq.q_scale, iq.w, pc.index_k, pc.page_table, r, scores, bm, hist=hist)
+                csa2.topk_with_candidates(scores, r, 512, pos, slot, pc.page_table, bm, pool, hist=hist)
+            ms = _time_calls(both, args.iters, st)
+            res.update(ms_scan_and_select=ms, rows=B, entries=n)
+        else:
+            pool = W.make_pool(lengths, seed=3, device=dev)
+            pos = torch.empty(B, 512, dtype=torch.int32, device=dev)
+            slot = torch.empty_like(pos)
+            ms = _time_calls(lambda: csa2.reindex(iq.q_fp8, iq.q_scale, iq.w, pc.index_k, pc.page_table, r, pool, 512,
+                                                  pos, slot), args.iters, st)
+            res.update(ms=ms, keys=B * 16384, GBps=B * 16384 * kb / ms / 1e6, fp4=args.fp4)
+    elif args.case == "attn":
+        pc = W.make_paged_cache([n], seed=4, device=dev)
+        al = W.make_attn_layer(B, seed=5, device=dev)
+        slot = torch.randint(0, n, (B, 512), dtype=torch.int32, device=dev)
+        out = torch.empty(B, 64, 512, dtype=torch.bfloat16, device=dev)
+        ms = _time_calls(lambda: csa2.sparse_attn(al.q, pc.main_kv, slot, al.swa_kv, al.swa_slot, al.sink, out),
+                         args.iters, st)
+        res.update(ms=ms, query_layers=B)
+    else:  # prefill: the query-blocked indexer over one sequence, m = 2, T queries at the end of n entries
+        T = args.queries
+        pc = W.make_paged_cache([n], seed=6, device=dev, with_main=False)
+        iq = W.make_indexer_query(T, seed=7, device=dev)
+        row_pos = torch.arange(2 * n - T, 2 * n, dtype=torch.int32, device=dev)
+        r = csa2.rows(T, 1, row_seq=torch.zeros(T, dtype=torch.int32, device=dev), row_pos=row_pos, ratio_m=2)
+        ld = (n + 127) // 128 * 128
+        scores = torch.empty(T, ld, dtype=torch.float32, device=dev)
+        ms = _time_calls(lambda: csa2.index_score(iq.q_fp8, iq.q_scale, iq.w, pc.index_k, pc.page_table, r, scores),
+                         args.iters, st)
+        flop = float(sum((p + 1) // 2 for p in range(2 * n - T, 2 * n))) * INDEX_PAIR_FLOP
+        res.update(ms=ms, queries=T, entries=n, TFLOPs=flop / ms / 1e9)
+    rc = csa2.check_device_error()
+    if rc != 0:
+        raise RuntimeError(f"device error status {rc}")
+    print(json.dumps(res), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# the benchmark
+# ---------------------------------------------------------------------------
 
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--min-seconds", type=float, default=0.6, help="replay the K-step graph at least this long")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-workloads", action="store_true", help="skip the prefill and Reindex workloads")
+    ap.add_argument("--case", choices=["scan", "topk", "reindex", "attn", "prefill"])
+    ap.add_argument("--iters", type=int, default=3)
+    ap.add_argument("--batch", type=int, default=8)
+    ap.add_argument("--entries", type=int, default=262144)
+    ap.add_argument("--queries", type=int, default=1024)
+    ap.add_argument("--fp4", action="store_true", help="FP4 index-K pages in --case scan/topk/reindex")
+    ap.add_argument("--cpu-worker", help=argparse.SUPPRESS)
     args = ap.parse_args()
+
+    if args.cpu_worker:
+        print(json.dumps(_cpu_worker(args.cpu_worker, args.cpu_budget)), flush=True)
+        return
+    if args.case:
+        return run_case(args)
 
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -218,6 +540,7 @@ def main():
     import __graft_entry__
     __graft_entry__.build()
     from serving_lightning_indexer_gb300 import csa2
+    from serving_lightning_indexer_gb300 import decode_step as ds
     from serving_lightning_indexer_gb300.decode_step import DecodeStep
 
     dev = torch.device("cuda", local)
@@ -239,12 +562,12 @@ def main():
     if rc != 0:
         raise RuntimeError(f"device error status {rc} during warm-up")
 
-    # ---- K steps in one graph, events around every indexer scan.  The timing
-    # events are recorded on a side stream that forks from the step's stream,
-    # so they hang off the kernel chain instead of sitting between two kernels
-    # (a node between them would cut the programmatic-launch overlap).
+    # ---- K steps in one graph, events around every indexer scan and attention.
+    # The timing events are recorded on a side stream that forks from the
+    # step's stream, so they hang off the kernel chain instead of sitting
+    # between two kernels (a node between them would cut the programmatic-launch
+    # overlap).
     K = args.steps
-    ev_pairs = []
     side = torch.cuda.Stream(device=dev)
 
     def side_event():
@@ -255,67 +578,58 @@ def main():
         e.record(side)
         return e
 
-    def on_scan(layer):
-        ev_pairs.append([layer, side_event(), None])
-
-    def after_scan(layer):
-        ev_pairs[-1][2] = side_event()
-
-    attn_pairs = []
-
-    def on_attn(layer):
-        attn_pairs.append([side_event(), None])
-
-    def after_attn(layer):
-        attn_pairs[-1][1] = side_event()
-
+    ev_pairs, attn_pairs = [], []
+    step.on_index_score = lambda l: ev_pairs.append([l, side_event(), None])
+    step.after_index_score = lambda l: ev_pairs[-1].__setitem__(2, side_event())
+    step.on_attn = lambda l: attn_pairs.append([l, side_event(), None])
+    step.after_attn = lambda l: attn_pairs[-1].__setitem__(2, side_event())
     g = torch.cuda.CUDAGraph()
-    step.on_index_score, step.after_index_score = on_scan, after_scan
-    step.on_attn, step.after_attn = on_attn, after_attn
     with torch.cuda.graph(g, stream=stream):
         for _ in range(K):
             step.run(stream)
         join = torch.cuda.Event()
         join.record(side)
         stream.wait_event(join)
-    step.on_index_score = step.after_index_score = None
-    step.on_attn = step.after_attn = None
+    step.on_index_score = step.after_index_score = step.on_attn = step.after_attn = None
     with torch.cuda.stream(stream):
         g.replay()                   # untimed: first replay of the instantiated graph
     stream.synchronize()
 
+    # ---- timed region: replays of the K-step graph until min_seconds have passed
     sampler = ClockSampler(local)
     if rank == 0:
         sampler.start()
-    if world > 1:
-        import torch.distributed as dist
-        dist.barrier()
-    torch.cuda.synchronize()
+    replay_ms, scan_ms, attn_ms, per_layer = [], [], [], {}
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     sampler.mark(True)
-    with torch.cuda.stream(stream):  # the graph replays on the current stream
-        t_start.record(stream)
-        g.replay()
-        t_end.record(stream)
-    stream.synchronize()
+    t_wall = time.time()
+    while len(replay_ms) < 3 or time.time() - t_wall < args.min_seconds:
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):  # the graph replays on the current stream
+            t_start.record(stream)
+            g.replay()
+            t_end.record(stream)
+        stream.synchronize()
+        torch.cuda.synchronize()
+        replay_ms.append(t_start.elapsed_time(t_end))
+        for l, a, b in ev_pairs:
+            ms = a.elapsed_time(b)
+            scan_ms.append(ms)
+            per_layer.setdefault(l, []).append(ms)
+        attn_ms.extend(a.elapsed_time(b) for _, a, b in attn_pairs)
     sampler.mark(False)
-    torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
-    ms_total = t_start.elapsed_time(t_end)
     if rank == 0:
         sampler.stop()
     rc = csa2.check_device_error(stream)
     if rc != 0:
         raise RuntimeError(f"device error status {rc} in the timed region")
-    scan_ms = [a.elapsed_time(b) for _, a, b in ev_pairs]
-    per_layer = {}
-    for (l, _, _), ms in zip(ev_pairs, scan_ms):
-        per_layer.setdefault(l, []).append(ms)
-    scan_ms_total = sum(scan_ms)
-    attn_ms = [a.elapsed_time(b) for a, b in attn_pairs]
-    ms_total = max_over_ranks(ms_total, dev)
+    ms_replay = max_over_ranks(statistics.median(replay_ms), dev)
+    ms_per_step = ms_replay / K
 
     # ---- end to end: pinned host inputs -> device, step, outputs -> pinned host.
     # Every step copies all of its query-side inputs in and all 38 attention
@@ -370,75 +684,96 @@ def main():
     with torch.cuda.stream(stream):
         g2.replay()
     stream.synchronize()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        e0.record(stream)
-        g2.replay()
-        e1.record(stream)
-    stream.synchronize()
-    e2e_ms = e0.elapsed_time(e1)
-    e2e_ms = max_over_ranks(e2e_ms, dev)
+    e2e_runs = []
+    for _ in range(3):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            g2.replay()
+            e1.record(stream)
+        stream.synchronize()
+        e2e_runs.append(e0.elapsed_time(e1))
+    e2e_ms = max_over_ranks(statistics.median(e2e_runs), dev)
+
+    hbm_peak, bf16_peak, bf16_sust, peak_kind = _peaks()
+    cpu_path = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu_path = _save_cpu_sample(step, lambda t: t.detach().cpu().numpy())
+    del g, g2
+    n_full = sum(1 for l in step.layers if ds.role_of(l) == "full")
+    n_reidx = sum(1 for l in step.layers if ds.role_of(l) == "reindex")
+    n_layers = len(step.layers)
+    del step
+    torch.cuda.empty_cache()
+
+    # ---- the prefill chunk and the decode Reindex at 1M, measured in the same run
+    extra = {}
+    if not args.no_workloads:
+        extra.update(measure_prefill(dev, stream, 20, 2 * bf16_peak, 2 * bf16_sust))
+        extra.update(measure_reindex(dev, stream, 20, hbm_peak))
 
     if rank != 0:
         if world > 1:
             dist.destroy_process_group()
         return
 
-    peak, peak_kind = _peaks()
-    bf16_peak = _bf16_peak()
     traffic_per_key = _scan_traffic_per_key()
-    ms_per_step = ms_total / K
-    value = whole_job_rate(keys_per_step, K, world, ms_total)
-    scan_launches = len(scan_ms)
-    scan_bytes_per_launch = scan_bytes_per_step * K / scan_launches
-    achieved = scan_bytes_per_step * K / (scan_ms_total / 1e3) / 1e9
+    value = whole_job_rate(keys_per_step, K, world, ms_replay)
+    scan_bytes_per_launch = scan_bytes_per_step * K / (len(ev_pairs))
+    scan_avg = statistics.mean(scan_ms)
+    achieved = scan_bytes_per_launch / (scan_avg / 1e3) / 1e9
+    attn_avg = statistics.mean(attn_ms)
     # our kernels launched per step: a Full layer runs compress, the scan and the
     # two select passes (filter, final); a Reindex layer the pool gather and the
     # final select; every layer one clustered attention launch (the histogram
     # memsets are not kernels)
-    from serving_lightning_indexer_gb300 import decode_step as ds
-    n_full = sum(1 for l in step.layers if ds.role_of(l) == "full")
-    n_reidx = sum(1 for l in step.layers if ds.role_of(l) == "reindex")
-    launches_per_step = n_full * 4 + n_reidx * 2 + len(step.layers)
+    launches_per_step = n_full * 4 + n_reidx * 2 + n_layers
     cpu = None
-    if not args.no_cpu_baseline:
-        v, cores, sample = cpu_baseline(step, args.cpu_budget, lambda t: t.detach().cpu().numpy())
-        cpu = {"value": v, "unit": "keys/s", "cores": cores, "kind": "oracle", "sample": sample}
+    if cpu_path:
+        try:
+            cpu = cpu_baseline(cpu_path, args.cpu_budget)
+        finally:
+            os.remove(cpu_path)
     out = {
         "metric": METRIC, "value": value, "unit": "keys/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
         "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "e4m3 (indexer, fp32 accumulate) + bf16 (attention)", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "batch": len(LENGTHS), "context_lengths": LENGTHS, "layers": 38,
+        "config": {"workload": WORKLOAD, "batch": len(LENGTHS), "context_lengths": LENGTHS, "layers": n_layers,
                    "keys_scored_per_step": keys_per_step, "attn_query_layers_per_step": attn_per_step,
-                   "timing": "K steps in one CUDA graph; inputs larger than L2 (no flush)",
+                   "timing": (f"K steps in one CUDA graph, replayed {len(replay_ms)} times over >= "
+                              f"{args.min_seconds} s, median replay; inputs larger than L2 (no flush)"),
                    "parallelism": f"replicas x{world}"},
-        "attn_query_layers_per_s": whole_job_rate(attn_per_step, K, world, ms_total),
+        "replays": len(replay_ms), "replay_ms": {"median": statistics.median(replay_ms), "min": min(replay_ms),
+                                                 "max": max(replay_ms)},
+        "attn_query_layers_per_s": whole_job_rate(attn_per_step, K, world, ms_replay),
         "roofline": {"bound": "hbm", "kernel": "index_tiles_kernel<1,scan> (decode Lightning-Indexer scan)",
-                     "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "achieved": achieved, "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
                      "peak_source": peak_kind,
                      "traffic": (None if traffic_per_key is None
                                  else traffic_per_key * scan_bytes_per_launch / INDEX_KEY_BYTES),
                      "traffic_source": "ncu dram bytes per key of the committed scan capture, scaled to the "
                                        "keys of an average launch",
                      "algorithmic_bytes_per_launch": scan_bytes_per_launch,
-                     "avg_launch_ms": scan_ms_total / scan_launches, "launches_timed": scan_launches,
+                     "avg_launch_ms": scan_avg, "launches_timed": len(scan_ms),
                      "per_layer_ms": {str(l): statistics.mean(v) for l, v in per_layer.items()}},
-        # the sparse attention, the step's largest time share: latency-bound at
-        # 8 rows a launch, reported beside the scan against both rooflines
+        # the sparse attention: latency-bound at 8 rows a launch, reported
+        # beside the scan against both rooflines
         "roofline_attention": {
             "bound": "latency", "kernel": "sparse_attn_tc_kernel (8 rows x 64 heads x 640 keys)",
-            "avg_launch_ms": statistics.mean(attn_ms), "launches_timed": len(attn_ms),
-            "share_of_step": sum(attn_ms) / ms_total,
+            "avg_launch_ms": attn_avg, "launches_timed": len(attn_ms),
+            "share_of_step": attn_avg * n_layers / ms_per_step,
             "algorithmic_bytes_per_launch": ATTN_ROW_BYTES * len(LENGTHS),
-            "hbm_frac": ATTN_ROW_BYTES * len(LENGTHS) / (statistics.mean(attn_ms) / 1e3) / 1e9 / peak,
+            "hbm_frac": ATTN_ROW_BYTES * len(LENGTHS) / (attn_avg / 1e3) / 1e9 / hbm_peak,
             "flop_per_launch": ATTN_ROW_FLOP * len(LENGTHS),
-            "bf16_tensor_frac": ATTN_ROW_FLOP * len(LENGTHS) / (statistics.mean(attn_ms) / 1e3) / 1e12 / bf16_peak,
-            "peaks": {"hbm_gbs": peak, "bf16_tflops": bf16_peak, "source": peak_kind}},
+            "bf16_tensor_frac": ATTN_ROW_FLOP * len(LENGTHS) / (attn_avg / 1e3) / 1e12 / bf16_sust,
+            "peaks": {"hbm_gbs": hbm_peak, "bf16_tflops_sustained": bf16_sust, "source": peak_kind}},
+        **extra,
         "cpu_baseline": cpu,
         "e2e": {"value": whole_job_rate(keys_per_step, Ke, world, e2e_ms), "unit": "keys/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "steps": Ke},
-        "gpu_launches": launches_per_step * K,
+                "d2h_bytes_per_step": d2h, "steps": Ke, "replays": len(e2e_runs)},
+        "gpu_launches": launches_per_step * K * len(replay_ms),
+        "gpu_launches_per_step": launches_per_step,
         "clocks": sampler.summary(),
     }
     print(json.dumps(out), flush=True)
@@ -468,10 +803,10 @@ def reference_arm(args, rank, world):
 
     for i in range(args.warmup):
         one(i % 2)
-    t0 = time.perf_counter()
+    t0, c0 = time.perf_counter(), time.process_time()
     for i in range(args.steps):
         one(i % 2)
-    dt = time.perf_counter() - t0
+    dt, cpu_s = time.perf_counter() - t0, time.process_time() - c0
     cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
     v = n * args.steps / dt
     sample = f"per step one decoder Full-layer row prefix of {n} entries: score + top-512 + pool"
@@ -480,7 +815,8 @@ def reference_arm(args, rank, world):
         "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": WORKLOAD, "sample_entries_per_step": n},
-        "cpu_baseline": {"value": v, "unit": "keys/s", "cores": cores, "kind": "oracle", "sample": sample},
+        "cpu_baseline": {"value": v, "unit": "keys/s", "cores": cores, "kind": "oracle", "sample": sample,
+                         "threads": round(cpu_s / dt, 2), "model": cpu_model()},
         "e2e": {"value": v, "unit": "keys/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }), flush=True)
 

@@ -184,11 +184,20 @@ CSA2_API int csa2_topk_with_candidates(const csa2_topk_args* args, void* workspa
  * operator interface that passes only inputs and outputs, an engine whose
  * allocator cannot serve extra buffers, a path that must not call cudaMalloc).
  * The scratch is a static device array of CSA2_TOPK_NOALLOC_SCRATCH_BYTES that
- * every GPU loading the library holds until exit.  A row longer than 16,384
- * elements needs about 2 B of it per element plus 8 KB (a 1M-entry row and its
- * pool about 2.3 MB); calls needing more return CSA2_ERR_WORKSPACE.  The
- * library allocates nothing during the call.  The first call on each device
- * looks up the array's device address, so make it before any stream capture.
+ * every GPU loading the library holds until exit.  A call needs exactly what
+ * csa2_workspace_size(CSA2_CALL_TOPK, args, ...) reports: nothing when
+ * L <= 16384, else
+ *     V * H + round_up(V * c * 4, 256) + V * c * 8192 bytes,
+ * with L = ld_scores (the larger of ld_scores and ld_block_max when
+ * pool_blocks is set), c = ceil(L / 4096), V = T (2T with a pool: the block
+ * maxima are a second row per query) and H = 8192 (0 when hist is given).
+ * That is about 2 B per element of L per row: a 1M-entry row needs 2.1 MB,
+ * 4.2 MB with its pool, so the 8 MiB array takes three 1M rows, or one with
+ * its pool, or seven 262,144-entry rows with their pools.  Calls needing more
+ * return CSA2_ERR_WORKSPACE.  The library allocates nothing during the call.
+ * The first call on each device looks up the array's device address, so make
+ * it before any stream capture; the address is kept for the life of the
+ * process, so do not use this call on a device after cudaDeviceReset.
  * All calls share the array: calls that overlap on the GPU race. */
 #define CSA2_TOPK_NOALLOC_SCRATCH_BYTES ((size_t)8 << 20)
 CSA2_API int csa2_topk_with_candidates_noalloc(const csa2_topk_args* args, void* stream);
@@ -314,8 +323,23 @@ enum { CSA2_CALL_INDEX_SCORE = 1, CSA2_CALL_TOPK = 2, CSA2_CALL_REINDEX = 3, CSA
 CSA2_API int csa2_workspace_size(int which_call, const void* args, size_t* bytes);
 /* Synchronises the stream, then returns CSA2_ERR_DEVICE_BOUNDS or
  * CSA2_ERR_DEVICE_TIMEOUT if a kernel on this device recorded one since the
- * last check (and clears the record), else CSA2_OK. */
+ * last check (and clears the record), else CSA2_OK.  The record is one word
+ * per device for the whole process: every stream and every call of the
+ * library on that device reports into it, so a check made after work on
+ * stream A also reports an error that a kernel on stream B recorded, and
+ * clears it for B's check.  Only the given stream is synchronised; the word
+ * is read with a blocking copy. */
 CSA2_API int csa2_check_device_error(void* stream);
+/* Diagnostic (no counterpart in the pages): one CTA waits, with the bounded
+ * wait every kernel of the library uses, on an mbarrier that nothing arrives
+ * at and no copy completes; after `polls` polls (1..2^20; each poll may
+ * suspend the thread for a short, hardware-defined time) it gives up and
+ * records a timeout, so the next csa2_check_device_error returns
+ * CSA2_ERR_DEVICE_TIMEOUT.  It exercises the failure path of the bounded
+ * waits without a fault: nothing is left in flight and the context stays
+ * usable.  In the kernels a wait gives up after 2^26 polls or 1 s of the
+ * global timer without progress. */
+CSA2_API int csa2_debug_bounded_wait(uint32_t polls, void* stream);
 /* Library version string. */
 CSA2_API const char* csa2_version(void);
 

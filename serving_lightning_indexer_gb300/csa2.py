@@ -68,7 +68,8 @@ class CompressArgs(C.Structure):
 CALL_INDEX_SCORE, CALL_TOPK, CALL_REINDEX, CALL_SPARSE_ATTN = 1, 2, 3, 4
 EXPORTED = ("csa2_status_string", "csa2_last_error_detail", "csa2_index_score", "csa2_topk_with_candidates",
             "csa2_reindex", "csa2_sparse_attn", "csa2_compress_m2", "csa2_workspace_size",
-            "csa2_check_device_error", "csa2_version", "csa2_topk_with_candidates_noalloc")
+            "csa2_check_device_error", "csa2_version", "csa2_topk_with_candidates_noalloc",
+            "csa2_debug_bounded_wait")
 
 _lib = None
 
@@ -105,6 +106,8 @@ def load(build_if_missing: bool = False) -> C.CDLL:
     lib.csa2_workspace_size.argtypes = [C.c_int, _P, C.POINTER(C.c_size_t)]
     lib.csa2_check_device_error.restype = C.c_int
     lib.csa2_check_device_error.argtypes = [_P]
+    lib.csa2_debug_bounded_wait.restype = C.c_int
+    lib.csa2_debug_bounded_wait.argtypes = [C.c_uint32, _P]
     _lib = lib
     return lib
 

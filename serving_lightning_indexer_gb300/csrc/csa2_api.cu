@@ -9,6 +9,7 @@
 #include <mutex>
 #include <string>
 
+#include "csa2_device.cuh"
 #include "csa2_internal.h"
 
 namespace {
@@ -221,23 +222,23 @@ int csa2_index_score(const csa2_index_score_args* a, void* ws, size_t ws_bytes, 
 }  // extern "C"
 
 // Validates top-k arguments and fills the internal launch description; shared
-// by every top-k entry point.
-int csa2::topk_prepare(const csa2_topk_args* a, csa2::SelectLaunch* S) {
-  if (!a) return fail(CSA2_ERR_NULL, "csa2_topk_with_candidates: args is NULL");
-  int rc = rows_check(a->rows, "csa2_topk_with_candidates");
+// by every top-k entry point (`who` names the entry point in error details).
+int csa2::topk_prepare(const csa2_topk_args* a, csa2::SelectLaunch* S, const char* who) {
+  if (!a) return fail(CSA2_ERR_NULL, "%s: args is NULL", who);
+  int rc = rows_check(a->rows, who);
   if (rc) return rc;
-  if (!a->scores || !a->topk_pos) return fail(CSA2_ERR_NULL, "csa2_topk_with_candidates: scores/topk_pos is NULL");
-  if (a->k < 1 || a->k > CSA2_MAX_TOPK) return fail(CSA2_ERR_SHAPE, "csa2_topk_with_candidates: k=%d not in 1..2048", a->k);
-  if (a->ld_topk < a->k) return fail(CSA2_ERR_SHAPE, "csa2_topk_with_candidates: ld_topk < k");
+  if (!a->scores || !a->topk_pos) return fail(CSA2_ERR_NULL, "%s: scores/topk_pos is NULL", who);
+  if (a->k < 1 || a->k > CSA2_MAX_TOPK) return fail(CSA2_ERR_SHAPE, "%s: k=%d not in 1..2048", who, a->k);
+  if (a->ld_topk < a->k) return fail(CSA2_ERR_SHAPE, "%s: ld_topk < k", who);
   if (!aligned16(a->scores) || (a->ld_scores & 3) || a->ld_scores < 1)
-    return fail(CSA2_ERR_ALIGN, "csa2_topk_with_candidates: scores must be 16-B aligned, ld a positive multiple of 4");
-  if (a->topk_slot && !a->page_table) return fail(CSA2_ERR_NULL, "csa2_topk_with_candidates: topk_slot needs page_table");
+    return fail(CSA2_ERR_ALIGN, "%s: scores must be 16-B aligned, ld a positive multiple of 4", who);
+  if (a->topk_slot && !a->page_table) return fail(CSA2_ERR_NULL, "%s: topk_slot needs page_table", who);
   if (a->pool_blocks) {
-    if (!a->block_max) return fail(CSA2_ERR_NULL, "csa2_topk_with_candidates: the pool needs block_max");
+    if (!a->block_max) return fail(CSA2_ERR_NULL, "%s: the pool needs block_max", who);
     if (a->pool_n < 1 || a->pool_n > CSA2_MAX_TOPK)
-      return fail(CSA2_ERR_SHAPE, "csa2_topk_with_candidates: pool_n=%d not in 1..2048", a->pool_n);
+      return fail(CSA2_ERR_SHAPE, "%s: pool_n=%d not in 1..2048", who, a->pool_n);
     if (!aligned16(a->block_max) || (a->ld_block_max & 3) || a->ld_block_max < 1)
-      return fail(CSA2_ERR_ALIGN, "csa2_topk_with_candidates: block_max must be 16-B aligned, ld a positive multiple of 4");
+      return fail(CSA2_ERR_ALIGN, "%s: block_max must be 16-B aligned, ld a positive multiple of 4", who);
   }
   *S = csa2::SelectLaunch{};
   S->kind = 0;
@@ -254,7 +255,7 @@ int csa2::topk_prepare(const csa2_topk_args* a, csa2::SelectLaunch* S) {
   S->ld_topk = a->ld_topk;
   S->pool_out = a->pool_blocks;
   S->pool_n = a->pool_blocks ? a->pool_n : 0;
-  if (a->hist && !aligned16(a->hist)) return fail(CSA2_ERR_ALIGN, "csa2_topk_with_candidates: hist must be 16-B aligned");
+  if (a->hist && !aligned16(a->hist)) return fail(CSA2_ERR_ALIGN, "%s: hist must be 16-B aligned", who);
   S->hist = a->hist;
   return CSA2_OK;
 }
@@ -263,7 +264,7 @@ extern "C" {
 
 int csa2_topk_with_candidates(const csa2_topk_args* a, void* ws, size_t ws_bytes, void* stream) {
   csa2::SelectLaunch S;
-  int rc = csa2::topk_prepare(a, &S);
+  int rc = csa2::topk_prepare(a, &S, "csa2_topk_with_candidates");
   if (rc) return rc;
   const size_t need = csa2::select_workspace_bytes(S);
   if (need && (!ws || ws_bytes < need))
@@ -466,7 +467,7 @@ int csa2_workspace_size(int which, const void* args, size_t* bytes) {
       return CSA2_OK;
     case CSA2_CALL_TOPK: {
       csa2::SelectLaunch S;
-      int rc = csa2::topk_prepare(static_cast<const csa2_topk_args*>(args), &S);
+      int rc = csa2::topk_prepare(static_cast<const csa2_topk_args*>(args), &S, "csa2_workspace_size");
       if (rc) return rc;
       *bytes = csa2::select_workspace_bytes(S);
       return CSA2_OK;
@@ -487,6 +488,36 @@ int csa2_workspace_size(int which, const void* args, size_t* bytes) {
     default:
       return fail(CSA2_ERR_UNSUPPORTED, "csa2_workspace_size: unknown call %d", which);
   }
+}
+
+}  // extern "C"
+
+namespace {
+// One CTA waits, with the library's bounded wait, on an mbarrier that nothing
+// arrives at and no copy completes; the wait gives up and records a timeout
+// in the device error word exactly as the kernels of the library do.
+__global__ void bounded_wait_probe_kernel(uint32_t polls, uint32_t* err) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    csa2::mbar_init(&bar, 1);
+    csa2::fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0 && !csa2::mbar_wait_polls(&bar, 0u, nullptr, polls)) csa2::set_error(err, csa2::kErrTimeout);
+}
+}  // namespace
+
+extern "C" {
+
+int csa2_debug_bounded_wait(uint32_t polls, void* stream) {
+  if (polls < 1 || polls > (1u << 20)) return fail(CSA2_ERR_SHAPE, "csa2_debug_bounded_wait: polls=%u not in 1..2^20", polls);
+  DeviceCtx ctx;
+  cudaError_t e = csa2::device_ctx(&ctx);
+  if (e != cudaSuccess) return cuda_fail(e, "csa2_debug_bounded_wait: device");
+  bounded_wait_probe_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(polls, ctx.err);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "csa2_debug_bounded_wait: launch");
+  return CSA2_OK;
 }
 
 int csa2_check_device_error(void* stream) {

@@ -16,8 +16,10 @@ constexpr uint32_t kErrTimeout = 2u;
 
 // A bounded wait gives up after this many polls of an mbarrier (each poll of
 // try_wait may itself suspend the thread for a short, hardware-defined time),
-// i.e. after well over a second of no progress.
+// or after kWaitLimitNs of the global timer without progress, whichever
+// comes first.
 constexpr uint32_t kSpinLimit = 1u << 26;
+constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s
 
 __device__ __forceinline__ void set_error(uint32_t* err, uint32_t bit) {
   if (err) atomicOr(err, bit);
@@ -52,14 +54,30 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-// Waits for the phase of the given parity to complete; false after kSpinLimit
-// polls or when *abort becomes non-zero.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
-  for (uint32_t i = 0; i < kSpinLimit; ++i) {
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+// Waits for the phase of the given parity to complete; false after max_polls
+// polls, after kWaitLimitNs, or when *abort becomes non-zero (checked every
+// 1024 polls, like the clock).
+__device__ __forceinline__ bool mbar_wait_polls(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                                uint32_t max_polls) {
+  uint64_t t0 = 0;
+  for (uint32_t i = 0; i < max_polls; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 1023u) == 1023u && abort && *abort) return false;
+    if ((i & 1023u) == 1023u) {
+      if (abort && *abort) return false;
+      const uint64_t now = global_ns();
+      if (t0 == 0) t0 = now;
+      else if (now - t0 > kWaitLimitNs) return false;
+    }
   }
   return false;
+}
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
+  return mbar_wait_polls(bar, parity, abort, kSpinLimit);
 }
 
 // ---------------------------------------------------------------- TMA / bulk copies

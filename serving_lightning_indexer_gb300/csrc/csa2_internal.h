@@ -149,8 +149,9 @@ struct CompressLaunch {
 };
 cudaError_t launch_compress(const CompressLaunch& a, const DeviceCtx& ctx, cudaStream_t st);
 
-// Shared by the top-k entry points: argument checks + launch description.
-int topk_prepare(const csa2_topk_args* a, SelectLaunch* S);
+// Shared by the top-k entry points: argument checks + launch description;
+// `who` names the entry point in the error detail.
+int topk_prepare(const csa2_topk_args* a, SelectLaunch* S, const char* who);
 // Records the per-thread detail string returned by csa2_last_error_detail().
 int set_error_detail(int code, const char* detail);
 

@@ -47,7 +47,7 @@ cudaError_t scratch_address(int dev, void** out) {
 
 extern "C" int csa2_topk_with_candidates_noalloc(const csa2_topk_args* a, void* stream) {
   csa2::SelectLaunch S;
-  int rc = csa2::topk_prepare(a, &S);
+  int rc = csa2::topk_prepare(a, &S, "csa2_topk_with_candidates_noalloc");
   if (rc) return rc;
   const size_t need = csa2::select_workspace_bytes(S);
   if (need > CSA2_TOPK_NOALLOC_SCRATCH_BYTES) {

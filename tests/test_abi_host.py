@@ -142,6 +142,7 @@ def test_validation_returns_codes_without_launch(lib):
     assert lib.csa2_compress_m2(C.byref(ca), None) == 3
     for code in range(9):
         assert lib.csa2_status_string(code)
+    assert lib.csa2_debug_bounded_wait(0, None) == 2                             # polls out of range: no launch
 
 
 def test_binding_refuses_cpu_tensors(lib):
@@ -151,3 +152,40 @@ def test_binding_refuses_cpu_tensors(lib):
     x = torch.zeros(4, 32, 128, dtype=torch.uint8)
     with pytest.raises(ValueError):
         csa2.index_score(x, x, x, x, x, csa2.Rows(1, 1, None, None, None, 1), x)
+
+
+def _topk_scratch_rule(T, L, pool, hist_given):
+    """The top-k scratch rule include/csa2.h states for the no-allocation call
+    (and that csa2_workspace_size reports for the workspace call)."""
+    if L <= 16384:
+        return 0
+    V = T * (2 if pool else 1)
+    c = -(-L // 4096)
+    return V * (0 if hist_given else 8192) + (V * c * 4 + 255) // 256 * 256 + V * c * 8192
+
+
+@pytest.mark.parametrize("T,ld_scores,ld_bm,pool,hist", [
+    (1, 1 << 20, 1 << 17, True, False),     # a 1M row with its pool: 4,212,736 B
+    (1, 1 << 20, 1 << 17, False, False),    # without the pool: 2.1 MB
+    (3, 1 << 20, 1 << 17, False, False),    # three 1M rows fit the 8 MiB array
+    (7, 262144, 32768, True, False),        # seven 262,144-entry rows with pools fit
+    (8, 262144, 32768, True, False),        # eight do not
+    (5, 100000, 12500, True, True),         # histograms given: no histogram part
+    (4, 16384, 2048, True, False),          # direct path: no scratch
+    (2, 20000, 40000, True, False),         # the pool row is the longer one
+])
+def test_topk_workspace_size_follows_the_documented_rule(lib, T, ld_scores, ld_bm, pool, hist):
+    from serving_lightning_indexer_gb300 import csa2
+    t = csa2.TopkArgs(FAKE, ld_scores, FAKE, ld_bm, FAKE, 8, csa2.Rows(T, T, None, None, FAKE, 1), 512, FAKE, FAKE,
+                      512, FAKE if pool else None, 2048, FAKE if hist else None)
+    n = C.c_size_t(0)
+    assert lib.csa2_workspace_size(csa2.CALL_TOPK, C.cast(C.byref(t), C.c_void_p), C.byref(n)) == 0
+    L = max(ld_scores, ld_bm) if pool else ld_scores
+    assert n.value == _topk_scratch_rule(T, L, pool, hist)
+    limit = 8 << 20
+    if (T, ld_scores, pool) == (1, 1 << 20, True):
+        assert n.value == 4_212_736
+    if (T, ld_scores, pool) == (7, 262144, True):
+        assert n.value == 7_458_304 <= limit
+    if (T, ld_scores, pool) == (8, 262144, True):
+        assert n.value == 8_523_776 > limit
