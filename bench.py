@@ -452,7 +452,7 @@ def run_case(args):
         ld = (n + 127) // 128 * 128
         scores = torch.empty(B, ld, dtype=torch.float32, device=dev)
         bm = torch.empty(B, ld // 8, dtype=torch.float32, device=dev)
-        hist = torch.empty(2, B, 2048, dtype=torch.int32, device=dev)
+        hist = torch.zeros(2, B, 2048, dtype=torch.int32, device=dev)
         if args.case == "scan":
             ms = _time_calls(lambda: csa2.index_score(iq.q_fp8, iq.q_scale, iq.w, pc.index_k, pc.page_table, r, scores,
                                                       bm, hist=hist), args.iters, st)

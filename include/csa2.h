@@ -140,11 +140,16 @@ typedef struct {
   csa2_rows rows;
   float* scores; int64_t ld_scores;           /* [T, ld_scores] */
   float* block_max; int64_t ld_block_max;     /* optional [T, ld_block_max] */
-  /* optional [2, T, 2048] uint32, decode path only (else must be NULL): receives
-   * 2048-bin histograms of the top 11 bits of the order-preserving key of every
-   * finite visible score (rows 0..T-1) and of every finite block maximum (rows
-   * T..2T-1, the newest block counted as +inf; zero when block_max is NULL).  Passing it on
-   * to csa2_topk_with_candidates saves that call a pass over the scores. */
+  /* optional [2, T, 2048] uint32, decode path only (else must be NULL): 2048-bin
+   * histograms of the top 11 bits of the order-preserving key of every finite
+   * visible score (rows 0..T-1) and of every finite block maximum (rows
+   * T..2T-1, the newest block counted as +inf; untouched when block_max is
+   * NULL).  The call ADDS into the buffer, which must hold zeros on entry:
+   * zero it once when it is allocated; csa2_topk_with_candidates (or its
+   * no-allocation variant) given the same buffer reads it and sets it back to
+   * zero, so a step that pairs every scan with its top-k call needs no memset
+   * between layers.  Passing it on saves the top-k call a pass over the
+   * scores. */
   uint32_t* hist;
   int32_t index_k_format;     /* CSA2_INDEX_FP8 (0) or CSA2_INDEX_FP4 */
 } csa2_index_score_args;
@@ -172,8 +177,9 @@ typedef struct {
   int64_t ld_topk;                             /* >= k */
   int32_t* pool_blocks;                        /* [T, pool_n] or NULL */
   int32_t pool_n;                              /* 1..2048 when pool_blocks is set */
-  const uint32_t* hist;                        /* optional: the histograms csa2_index_score wrote
-                                                  for these scores and block maxima */
+  uint32_t* hist;                              /* optional: the histograms csa2_index_score wrote
+                                                  for these scores and block maxima; read, then set
+                                                  back to zero (both halves, also without a pool) */
 } csa2_topk_args;
 CSA2_API int csa2_topk_with_candidates(const csa2_topk_args* args, void* workspace, size_t ws_bytes, void* stream);
 
@@ -210,8 +216,7 @@ CSA2_API int csa2_topk_with_candidates_noalloc(const csa2_topk_args* args, void*
  * csa2_topk_with_candidates, reported as positions and slots.
  * pool_scores (optional, [T, 8*pool_n]) receives the candidate scores.
  * Workspace: csa2_workspace_size(CSA2_CALL_REINDEX, args, &bytes): the
- * candidate scores (unless pool_scores is given) and a T x 2048 key histogram
- * of them that the scoring kernel builds for the selection. */
+ * candidate scores, unless pool_scores is given (then none). */
 typedef struct {
   const uint8_t* q_fp8; const float* q_scale; const float* w;  /* as in index_score */
   const uint8_t* index_k; int64_t index_k_pages;

@@ -165,7 +165,12 @@ def index_format(index_k) -> int:
 
 
 def rows(T, B, row_seq=None, row_pos=None, n_visible=None, ratio_m=1) -> Rows:
-    return Rows(T, B, _ptr(row_seq), _ptr(row_pos), _ptr(n_visible), ratio_m)
+    """Row description of a call.  The struct holds device pointers; it also
+    keeps the tensors themselves, so that they stay allocated as long as the
+    struct is in use."""
+    r = Rows(T, B, _ptr(row_seq), _ptr(row_pos), _ptr(n_visible), ratio_m)
+    r._tensors = (row_seq, row_pos, n_visible)
+    return r
 
 
 # ---------------------------------------------------------------- calls

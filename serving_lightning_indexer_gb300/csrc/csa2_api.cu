@@ -256,7 +256,7 @@ int csa2::topk_prepare(const csa2_topk_args* a, csa2::SelectLaunch* S, const cha
   S->pool_out = a->pool_blocks;
   S->pool_n = a->pool_blocks ? a->pool_n : 0;
   if (a->hist && !aligned16(a->hist)) return fail(CSA2_ERR_ALIGN, "%s: hist must be 16-B aligned", who);
-  S->hist = a->hist;
+  S->hist = const_cast<uint32_t*>(a->hist);
   return CSA2_OK;
 }
 
@@ -278,13 +278,10 @@ int csa2_topk_with_candidates(const csa2_topk_args* a, void* ws, size_t ws_bytes
   return CSA2_OK;
 }
 
-// Reindex workspace: [candidate scores, unless pool_scores is given][T x 2048
-// key histogram of the candidate scores, built by the gather kernel]
-static size_t reindex_scores_bytes(const csa2_reindex_args* a) {
-  return a->pool_scores ? 0 : ((static_cast<size_t>(a->rows.T) * a->pool_n * 8 * 4 + 255) & ~size_t(255));
-}
+// Reindex workspace: the candidate scores, unless pool_scores is given (the
+// selection builds their histogram itself).
 static size_t reindex_ws(const csa2_reindex_args* a) {
-  return reindex_scores_bytes(a) + static_cast<size_t>(a->rows.T) * 2048 * 4;
+  return a->pool_scores ? 0 : ((static_cast<size_t>(a->rows.T) * a->pool_n * 8 * 4 + 255) & ~size_t(255));
 }
 
 int csa2_reindex(const csa2_reindex_args* a, void* ws, size_t ws_bytes, void* stream) {
@@ -305,7 +302,6 @@ int csa2_reindex(const csa2_reindex_args* a, void* ws, size_t ws_bytes, void* st
   cudaError_t e = csa2::device_ctx(&ctx);
   if (e != cudaSuccess) return cuda_fail(e, "csa2_reindex: device");
   float* ps = a->pool_scores ? a->pool_scores : static_cast<float*>(ws);
-  uint32_t* hist = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(ws) + reindex_scores_bytes(a));
   csa2::IndexLaunch L{};
   L.q_fp8 = a->q_fp8;
   L.q_scale = a->q_scale;
@@ -320,7 +316,6 @@ int csa2_reindex(const csa2_reindex_args* a, void* ws, size_t ws_bytes, void* st
   L.ld_out = static_cast<long long>(a->pool_n) * 8;
   L.pool_blocks = a->pool_blocks;
   L.pool_n = a->pool_n;
-  L.hist = hist;
   const char* why = "launch";
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   e = csa2::launch_index_tiles(L, 1, 1, ctx, st, &why);
@@ -338,7 +333,6 @@ int csa2_reindex(const csa2_reindex_args* a, void* ws, size_t ws_bytes, void* st
   S.ld_topk = a->ld_topk;
   S.pool_in = a->pool_blocks;
   S.pool_in_n = a->pool_n;
-  S.hist = hist;
   e = csa2::launch_select(S, nullptr, 0, ctx, st);
   if (e != cudaSuccess) return cuda_fail(e, "csa2_reindex: select launch");
   return CSA2_OK;

@@ -87,7 +87,7 @@ struct SelectLaunch {
   int pool_n;
   const int* pool_in;     // kind 2: the pool the candidates come from [T, pool_in_n]
   int pool_in_n;
-  const uint32_t* hist;   // optional precomputed key histograms [V][2048]
+  uint32_t* hist;         // optional precomputed key histograms [V][2048] (returned to zero)
 };
 size_t select_workspace_bytes(const SelectLaunch& a);
 cudaError_t launch_select(const SelectLaunch& a, void* ws, size_t ws_bytes, const DeviceCtx& ctx, cudaStream_t st);

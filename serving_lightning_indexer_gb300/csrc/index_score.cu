@@ -787,16 +787,12 @@ cudaError_t launch_variant(const IndexLaunch& a, const DeviceCtx& ctx, cudaStrea
   p.pool_blocks = a.pool_blocks;
   p.pool_n = a.pool_n;
   p.err = ctx.err;
-  if (a.hist) {
-    if (NQ != 1) {
-      *why = "score histograms are produced on the decode and Reindex paths only";
-      return cudaErrorInvalidValue;
-    }
-    // scan: [2][T][2048] (scores, block maxima); gather: [T][2048] (candidate scores)
-    const size_t words = static_cast<size_t>(MODE == kModeScan ? 2 : 1) * a.rows.T * kHistBins;
-    cudaError_t e0 = cudaMemsetAsync(a.hist, 0, words * 4, st);
-    if (e0 != cudaSuccess) return e0;
+  if (a.hist && NQ != 1) {
+    *why = "score histograms are produced on the decode and Reindex paths only";
+    return cudaErrorInvalidValue;
   }
+  // the histograms accumulate into the caller's zeroed buffer: [2][T][2048]
+  // (scores, block maxima); the top-k call that reads them zeroes them again
   const size_t smem = Cfg::smem_bytes(nqb);
   auto kern = index_tiles_kernel<NQ, MODE, F4>;
   cudaError_t e = prefer_max_smem(kern, smem);

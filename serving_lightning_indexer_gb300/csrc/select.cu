@@ -64,8 +64,9 @@ struct SelParams {
   int pool_n;
   const int* pool_in;
   int pool_in_n;
-  const uint32_t* hist;  // [V][kBins]: given, or built by the hist pass in `hist_ws`
-  int hist_full;         // hist covers every row (given by the caller), not only the long ones
+  uint32_t* hist;        // [V][kBins]: given, or built by the hist pass in `hist_ws`
+  int hist_full;         // hist covers every row (given by the caller), not only the long ones;
+                         // the final pass returns the caller's rows to zero after reading them
   uint32_t* hist_ws;
   uint32_t* cnt;         // [V][nchunks]: candidates found by each filter CTA (may exceed kRegion)
   uint2* cand;           // [V][nchunks][kRegion]: (key, index) of each filter CTA's candidates
@@ -180,6 +181,16 @@ __device__ __forceinline__ void stage_hist(uint32_t* dst, const uint32_t* src) {
   const uint4* s4 = reinterpret_cast<const uint4*>(src);
   uint4* d4 = reinterpret_cast<uint4*>(dst);
   for (int i = threadIdx.x; i < kBins / 4; i += blockDim.x) d4[i] = s4[i];
+}
+// As stage_hist, and sets the global histogram back to zero (the caller's
+// histogram, read by nothing after the final pass).
+__device__ __forceinline__ void stage_hist_clear(uint32_t* dst, uint32_t* src) {
+  uint4* s4 = reinterpret_cast<uint4*>(src);
+  uint4* d4 = reinterpret_cast<uint4*>(dst);
+  for (int i = threadIdx.x; i < kBins / 4; i += blockDim.x) {
+    d4[i] = s4[i];
+    s4[i] = make_uint4(0u, 0u, 0u, 0u);
+  }
 }
 
 // Exclusive block-wide prefix sum of x (every thread calls); *total gets the sum.
@@ -509,6 +520,11 @@ __global__ void __launch_bounds__(kFinalThreads, 1) sel_final_kernel(const __gri
   const VRow r = vrow_of(P, v);
   const int tid = threadIdx.x;
   if (tid < 4) sm.counters[tid] = 0;
+  if (P.hist_full && P.kind == 0 && P.pool_out == nullptr) {
+    // the scan's block-maximum histogram of this row has no pool row to read it
+    uint4* hb = reinterpret_cast<uint4*>(P.hist + (static_cast<long long>(P.rows.T) + v) * kBins);
+    for (int i = tid; i < kBins / 4; i += blockDim.x) hb[i] = make_uint4(0u, 0u, 0u, 0u);
+  }
 
   // 1. the 2048-bin histogram of the top 11 key bits: the caller's (scan or
   //    gather epilogue) or the hist pass's, else built here from the values of
@@ -536,7 +552,7 @@ __global__ void __launch_bounds__(kFinalThreads, 1) sel_final_kernel(const __gri
       val[4 * q + 3] = v4.w;
     }
     if (P.hist_full) {
-      stage_hist(sm.hist, P.hist + static_cast<long long>(v) * kBins);
+      stage_hist_clear(sm.hist, P.hist + static_cast<long long>(v) * kBins);
     } else {
       for (int i = tid; i < kBins; i += blockDim.x) sm.hist[i] = 0;
     }
@@ -554,7 +570,8 @@ __global__ void __launch_bounds__(kFinalThreads, 1) sel_final_kernel(const __gri
     mode = (nch <= kMaxChunks) ? 1 : 2;
     if (mode == 1)
       for (int i = tid; i < nch; i += blockDim.x) scnt[i] = P.cnt[static_cast<long long>(v) * P.nchunks + i];
-    stage_hist(sm.hist, P.hist + static_cast<long long>(v) * kBins);
+    if (P.hist_full) stage_hist_clear(sm.hist, P.hist + static_cast<long long>(v) * kBins);
+    else stage_hist(sm.hist, P.hist + static_cast<long long>(v) * kBins);
 #pragma unroll
     for (int j = 0; j < kPerThread; ++j) ord[j] = 0u;
   }

@@ -136,7 +136,7 @@ class DecodeStep:
             topk_pos=torch.empty(self.B, W.TOPK, dtype=torch.int32, device=dev),
         )
         # key histograms produced by the scan and reused by the top-k of the same layer
-        self.buf.hist = torch.empty(2, self.B, 2048, dtype=torch.int32, device=dev)
+        self.buf.hist = torch.zeros(2, self.B, 2048, dtype=torch.int32, device=dev)
         for ci, c in enumerate(self.caches):
             if c is not None:
                 self.buf.topk_slot[ci] = torch.empty(self.B, W.TOPK, dtype=torch.int32, device=dev)

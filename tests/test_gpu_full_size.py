@@ -139,7 +139,7 @@ def test_decode_full_and_reuse_batch32_64k_128k():
     ld = (max(lengths) + 127) // 128 * 128
     scores = torch.empty(B, ld, dtype=torch.float32, device=dev)
     bm = torch.empty(B, ld // 8, dtype=torch.float32, device=dev)
-    hist = torch.empty(2, B, 2048, dtype=torch.int32, device=dev)
+    hist = torch.zeros(2, B, 2048, dtype=torch.int32, device=dev)
     r = csa2.rows(B, B, n_visible=pc.n_entries)
     pos = torch.empty(B, 512, dtype=torch.int32, device=dev)
     slot = torch.empty_like(pos)
@@ -352,7 +352,7 @@ def test_decode_fp4_index_keys_batch8_1m():
     ld = max(lengths)
     scores = torch.empty(B, ld, dtype=torch.float32, device=dev)
     bm = torch.empty(B, ld // 8, dtype=torch.float32, device=dev)
-    hist = torch.empty(2, B, 2048, dtype=torch.int32, device=dev)
+    hist = torch.zeros(2, B, 2048, dtype=torch.int32, device=dev)
     pos = torch.empty(B, 512, dtype=torch.int32, device=dev)
     slot = torch.empty(B, 512, dtype=torch.int32, device=dev)
     pool = torch.empty(B, 2048, dtype=torch.int32, device=dev)

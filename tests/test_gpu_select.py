@@ -184,7 +184,9 @@ def test_reindex_equals_full_topk_when_pool_covers_all():
 
 
 def test_fused_histograms_give_identical_selection():
-    # the decode scan's key histograms, passed on to the top-k, must not change any result
+    # the decode scan's key histograms, passed on to the top-k, must not change
+    # any result; the top-k returns them to zero, so the same buffer serves the
+    # next layer's scan without a memset
     dev = need_gpu()
     lengths = [70000, 140001, 20000]
     B = len(lengths)
@@ -194,31 +196,43 @@ def test_fused_histograms_give_identical_selection():
     ld = 140032
     scores = torch.empty(B, ld, dtype=torch.float32, device=dev)
     bm = torch.empty(B, ld // 8, dtype=torch.float32, device=dev)
-    hist = torch.full((2, B, 2048), 99, dtype=torch.int32, device=dev)
+    hist = torch.zeros((2, B, 2048), dtype=torch.int32, device=dev)
+    runs = []
+    for rep in range(2):
+        csa2.index_score(iq.q_fp8, iq.q_scale, iq.w, pc.index_k, pc.page_table, r, scores, bm, hist=hist)
+        h = np_(hist).astype(np.int64)
+        outs = []
+        for hh in (None, hist):
+            pos = torch.empty(B, 512, dtype=torch.int32, device=dev)
+            slot = torch.empty_like(pos)
+            pool = torch.empty(B, 2048, dtype=torch.int32, device=dev)
+            csa2.topk_with_candidates(scores, r, 512, pos, slot, pc.page_table, bm, pool, hist=hh)
+            outs.append((np_(pos), np_(slot), np_(pool)))
+        torch.cuda.synchronize()
+        assert csa2.check_device_error() == 0
+        for a, b in zip(*outs):
+            assert np.array_equal(a, b)
+        assert not np_(hist).any(), "the top-k call leaves the histograms at zero"
+        runs.append(outs[1])
+        # the histograms count exactly the visible scores and block maxima, in their top-11-bit bins
+        for b_, n in enumerate(lengths):
+            s = np_(scores[b_, :n])
+            key = s.view(np.uint32).astype(np.int64)
+            key = np.where(key & 0x80000000, ~key & 0xFFFFFFFF, key | 0x80000000)
+            assert np.array_equal(h[0, b_], np.bincount(key >> 21, minlength=2048))
+            nb = (n + 7) // 8
+            bmk = np_(bm[b_, :nb]).view(np.uint32).astype(np.int64)
+            bmk = np.where(bmk & 0x80000000, ~bmk & 0xFFFFFFFF, bmk | 0x80000000)
+            bmk[-1] = 0xFFFFFFFF
+            assert np.array_equal(h[1, b_], np.bincount(bmk >> 21, minlength=2048))
+    for a, b in zip(*runs):
+        assert np.array_equal(a, b), "a second scan + top-k on the returned buffer gives the same selection"
+    # without a pool the top-k also clears the block-maximum half
     csa2.index_score(iq.q_fp8, iq.q_scale, iq.w, pc.index_k, pc.page_table, r, scores, bm, hist=hist)
-    outs = []
-    for h in (None, hist):
-        pos = torch.empty(B, 512, dtype=torch.int32, device=dev)
-        slot = torch.empty_like(pos)
-        pool = torch.empty(B, 2048, dtype=torch.int32, device=dev)
-        csa2.topk_with_candidates(scores, r, 512, pos, slot, pc.page_table, bm, pool, hist=h)
-        outs.append((np_(pos), np_(slot), np_(pool)))
+    pos = torch.empty(B, 512, dtype=torch.int32, device=dev)
+    csa2.topk_with_candidates(scores, r, 512, pos, None, None, hist=hist)
     torch.cuda.synchronize()
-    assert csa2.check_device_error() == 0
-    for a, b in zip(*outs):
-        assert np.array_equal(a, b)
-    # the histograms count exactly the visible scores and block maxima, in their top-11-bit bins
-    h = np_(hist).astype(np.int64)
-    for b_, n in enumerate(lengths):
-        s = np_(scores[b_, :n])
-        key = s.view(np.uint32).astype(np.int64)
-        key = np.where(key & 0x80000000, ~key & 0xFFFFFFFF, key | 0x80000000)
-        assert np.array_equal(h[0, b_], np.bincount(key >> 21, minlength=2048))
-        nb = (n + 7) // 8
-        bmk = np_(bm[b_, :nb]).view(np.uint32).astype(np.int64)
-        bmk = np.where(bmk & 0x80000000, ~bmk & 0xFFFFFFFF, bmk | 0x80000000)
-        bmk[-1] = 0xFFFFFFFF
-        assert np.array_equal(h[1, b_], np.bincount(bmk >> 21, minlength=2048))
+    assert not np_(hist).any()
 
 
 def test_reindex_fp4_index_keys_match_oracle():

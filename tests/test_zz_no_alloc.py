@@ -54,14 +54,21 @@ def _args(scores, bm, pt, r, out, hist=None):
                          hist.data_ptr() if hist is not None else None)
 
 
-def _compare(lib, scores, bm, pt, nvis, hist=None, what=""):
-    """The no-allocation call against the workspace call on the same inputs: bit-exact."""
+def _compare(lib, scores, bm, pt, nvis, hist=None, what="", before=None):
+    """The no-allocation call against the workspace call on the same inputs: bit-exact.
+    `before` (if given) runs ahead of each of the two calls: a top-k call that
+    is given the scan's histograms returns them to zero, so the scan writes
+    them again for the next one."""
     dev = scores.device
     T = scores.shape[0]
     r = csa2.rows(T, T, n_visible=nvis)
     want = _outputs(T, dev)
+    if before:
+        before()
     csa2.topk_with_candidates(scores, r, 512, want[0], want[1], pt, bm, want[2], hist=hist)
     got = _outputs(T, dev)
+    if before:
+        before()
     a = _args(scores, bm, pt, r, got, hist)
     assert lib.csa2_topk_with_candidates_noalloc(C.byref(a), torch.cuda.current_stream().cuda_stream) == 0, \
         lib.csa2_last_error_detail()
@@ -100,10 +107,14 @@ def test_noalloc_topk_with_the_scan_histograms():
     ld = (max(lengths) + 127) // 128 * 128
     scores = torch.empty(B, ld, dtype=torch.float32, device=dev)
     bm = torch.empty(B, ld // 8, dtype=torch.float32, device=dev)
-    hist = torch.empty(2, B, 2048, dtype=torch.int32, device=dev)
-    csa2.index_score(iq.q_fp8, iq.q_scale, iq.w, pc.index_k, pc.page_table, r, scores, bm, hist=hist)
+    hist = torch.zeros(2, B, 2048, dtype=torch.int32, device=dev)
+
+    def scan():
+        csa2.index_score(iq.q_fp8, iq.q_scale, iq.w, pc.index_k, pc.page_table, r, scores, bm, hist=hist)
     for call in range(2):
-        _compare(lib, scores, bm, pc.page_table, pc.n_entries, hist=hist, what=f"with histograms, call {call}")
+        _compare(lib, scores, bm, pc.page_table, pc.n_entries, hist=hist, what=f"with histograms, call {call}",
+                 before=scan)
+        assert not np_(hist).any(), "the call returns the histograms to zero"
 
 
 def test_noalloc_topk_just_under_and_just_over_the_static_scratch():
