@@ -93,6 +93,14 @@ enum {
 /* Index-K page formats (the index_k_format field of the scoring calls). */
 enum { CSA2_INDEX_FP8 = 0, CSA2_INDEX_FP4 = 1 };
 
+/* Order of the reported top-k positions (the order field of the top-k and
+ * Reindex calls).  The pages leave it open; the set is the same either way. */
+enum {
+  CSA2_ORDER_POSITION = 0, /* ascending position (groups a row's slot reads by page) */
+  CSA2_ORDER_SCORE = 1     /* best first: score descending, ties to the lower position,
+                              so the first k' < k entries are the row's top-k' */
+};
+
 /* Static description of a status code. */
 CSA2_API const char* csa2_status_string(int status);
 /* Human-readable detail of the last error returned on the calling thread
@@ -157,8 +165,9 @@ CSA2_API int csa2_index_score(const csa2_index_score_args* args, void* workspace
 
 /* ---- 2. top-k with slot translation and the candidate pool ------------------
  * Per row: the k (<= 2048) positions s < E_t with the largest finite scores
- * (ties go to the lower position), in ascending position order, -1 filled
- * when fewer than k are finite (DSA page, "Top-k：选的是 token，不是 block").  topk_slot[t][i] = slot of topk_pos[t][i] (-1 kept).
+ * (ties go to the lower position), in the order given by `order` (ascending
+ * position by default), -1 filled when fewer than k are finite (DSA page,
+ * "Top-k：选的是 token，不是 block").  topk_slot[t][i] = slot of topk_pos[t][i] (-1 kept).
  * Pool (pool_blocks not NULL; CSA2 page, "Hierarchical Sparse Indexer",
  * "attention 计算的落点" select_candidate_blocks): block scores are
  * block_max[t][0..ceil(E_t/8)); the newest block ceil(E_t/8)-1 is always kept
@@ -180,6 +189,7 @@ typedef struct {
   uint32_t* hist;                              /* optional: the histograms csa2_index_score wrote
                                                   for these scores and block maxima; read, then set
                                                   back to zero (both halves, also without a pool) */
+  int32_t order;                               /* CSA2_ORDER_POSITION (0) or CSA2_ORDER_SCORE (1) */
 } csa2_topk_args;
 CSA2_API int csa2_topk_with_candidates(const csa2_topk_args* args, void* workspace, size_t ws_bytes, void* stream);
 
@@ -227,6 +237,7 @@ typedef struct {
   int32_t* topk_pos; int32_t* topk_slot; int64_t ld_topk;
   float* pool_scores;                          /* optional [T, 8*pool_n] */
   int32_t index_k_format;                      /* CSA2_INDEX_FP8 (0) or CSA2_INDEX_FP4 */
+  int32_t order;                               /* CSA2_ORDER_POSITION (0) or CSA2_ORDER_SCORE (1) */
 } csa2_reindex_args;
 CSA2_API int csa2_reindex(const csa2_reindex_args* args, void* workspace, size_t ws_bytes, void* stream);
 

@@ -39,14 +39,15 @@ class IndexScoreArgs(C.Structure):
 class TopkArgs(C.Structure):
     _fields_ = [("scores", _P), ("ld_scores", _I64), ("block_max", _P), ("ld_block_max", _I64),
                 ("page_table", _P), ("pt_stride", _I32), ("rows", Rows), ("k", _I32), ("topk_pos", _P),
-                ("topk_slot", _P), ("ld_topk", _I64), ("pool_blocks", _P), ("pool_n", _I32), ("hist", _P)]
+                ("topk_slot", _P), ("ld_topk", _I64), ("pool_blocks", _P), ("pool_n", _I32), ("hist", _P),
+                ("order", _I32)]
 
 
 class ReindexArgs(C.Structure):
     _fields_ = [("q_fp8", _P), ("q_scale", _P), ("w", _P), ("index_k", _P), ("index_k_pages", _I64),
                 ("page_table", _P), ("pt_stride", _I32), ("rows", Rows), ("pool_blocks", _P), ("pool_n", _I32),
                 ("k", _I32), ("topk_pos", _P), ("topk_slot", _P), ("ld_topk", _I64), ("pool_scores", _P),
-                ("index_k_format", _I32)]
+                ("index_k_format", _I32), ("order", _I32)]
 
 
 class SparseAttnArgs(C.Structure):
@@ -185,13 +186,13 @@ def index_score(q_fp8, q_scale, w, index_k, page_table, r: Rows, scores, block_m
 
 
 def topk_with_candidates(scores, r: Rows, k, topk_pos, topk_slot=None, page_table=None, block_max=None,
-                         pool_blocks=None, stream=None, ws=None, hist=None):
+                         pool_blocks=None, stream=None, ws=None, hist=None, order=0):
     """Top-k positions / slots and the optional candidate pool (csa2_topk_with_candidates)."""
     lib = load()
     a = TopkArgs(_ptr(scores), scores.shape[-1], _ptr(block_max), block_max.shape[-1] if block_max is not None else 0,
                  _ptr(page_table), page_table.shape[-1] if page_table is not None else 0, r, k, _ptr(topk_pos),
                  _ptr(topk_slot), topk_pos.shape[-1], _ptr(pool_blocks),
-                 pool_blocks.shape[-1] if pool_blocks is not None else 0, _ptr(hist))
+                 pool_blocks.shape[-1] if pool_blocks is not None else 0, _ptr(hist), order)
     need = C.c_size_t(0)
     _check(lib.csa2_workspace_size(CALL_TOPK, C.cast(C.byref(a), _P), C.byref(need)), "csa2_workspace_size")
     buf = ws if ws is not None else workspace(need.value, scores.device, "topk")
@@ -200,7 +201,7 @@ def topk_with_candidates(scores, r: Rows, k, topk_pos, topk_slot=None, page_tabl
 
 
 def topk_with_candidates_noalloc(scores, r: Rows, k, topk_pos, topk_slot=None, page_table=None, block_max=None,
-                                 pool_blocks=None, stream=None, hist=None):
+                                 pool_blocks=None, stream=None, hist=None, order=0):
     """csa2_topk_with_candidates_noalloc: the same selection without a workspace; its
     scratch is a static device array inside the library (for callers that cannot
     allocate device memory)."""
@@ -208,17 +209,17 @@ def topk_with_candidates_noalloc(scores, r: Rows, k, topk_pos, topk_slot=None, p
     a = TopkArgs(_ptr(scores), scores.shape[-1], _ptr(block_max), block_max.shape[-1] if block_max is not None else 0,
                  _ptr(page_table), page_table.shape[-1] if page_table is not None else 0, r, k, _ptr(topk_pos),
                  _ptr(topk_slot), topk_pos.shape[-1], _ptr(pool_blocks),
-                 pool_blocks.shape[-1] if pool_blocks is not None else 0, _ptr(hist))
+                 pool_blocks.shape[-1] if pool_blocks is not None else 0, _ptr(hist), order)
     _check(lib.csa2_topk_with_candidates_noalloc(C.byref(a), _stream(stream)), "csa2_topk_with_candidates_noalloc")
 
 
 def reindex(q_fp8, q_scale, w, index_k, page_table, r: Rows, pool_blocks, k, topk_pos, topk_slot=None,
-            pool_scores=None, stream=None, ws=None):
+            pool_scores=None, stream=None, ws=None, order=0):
     """Pool-only rescoring and top-k of a Reindex layer (csa2_reindex)."""
     lib = load()
     a = ReindexArgs(_ptr(q_fp8), _ptr(q_scale), _ptr(w), _ptr(index_k), index_k.shape[0], _ptr(page_table),
                     page_table.shape[-1], r, _ptr(pool_blocks), pool_blocks.shape[-1], k, _ptr(topk_pos),
-                    _ptr(topk_slot), topk_pos.shape[-1], _ptr(pool_scores), index_format(index_k))
+                    _ptr(topk_slot), topk_pos.shape[-1], _ptr(pool_scores), index_format(index_k), order)
     need = C.c_size_t(0)
     _check(lib.csa2_workspace_size(CALL_REINDEX, C.cast(C.byref(a), _P), C.byref(need)), "csa2_workspace_size")
     buf = ws if ws is not None else workspace(need.value, q_fp8.device, "reindex")

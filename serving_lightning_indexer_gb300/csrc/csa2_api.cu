@@ -257,6 +257,9 @@ int csa2::topk_prepare(const csa2_topk_args* a, csa2::SelectLaunch* S, const cha
   S->pool_n = a->pool_blocks ? a->pool_n : 0;
   if (a->hist && !aligned16(a->hist)) return fail(CSA2_ERR_ALIGN, "%s: hist must be 16-B aligned", who);
   S->hist = const_cast<uint32_t*>(a->hist);
+  if (a->order != CSA2_ORDER_POSITION && a->order != CSA2_ORDER_SCORE)
+    return fail(CSA2_ERR_SHAPE, "%s: order=%d must be 0 (positions) or 1 (best first)", who, a->order);
+  S->order = a->order;
   return CSA2_OK;
 }
 
@@ -295,6 +298,8 @@ int csa2_reindex(const csa2_reindex_args* a, void* ws, size_t ws_bytes, void* st
   if (a->k < 1 || a->k > CSA2_MAX_TOPK) return fail(CSA2_ERR_SHAPE, "csa2_reindex: k=%d not in 1..2048", a->k);
   if (a->ld_topk < a->k) return fail(CSA2_ERR_SHAPE, "csa2_reindex: ld_topk < k");
   if (a->pool_scores && !aligned16(a->pool_scores)) return fail(CSA2_ERR_ALIGN, "csa2_reindex: pool_scores must be 16-B aligned");
+  if (a->order != CSA2_ORDER_POSITION && a->order != CSA2_ORDER_SCORE)
+    return fail(CSA2_ERR_SHAPE, "csa2_reindex: order=%d must be 0 (positions) or 1 (best first)", a->order);
   const size_t need = reindex_ws(a);
   if (need && (!ws || ws_bytes < need)) return fail(CSA2_ERR_WORKSPACE, "csa2_reindex: workspace of %zu bytes needed", need);
   if (need && !aligned16(ws)) return fail(CSA2_ERR_ALIGN, "csa2_reindex: workspace must be 16-B aligned");
@@ -333,6 +338,7 @@ int csa2_reindex(const csa2_reindex_args* a, void* ws, size_t ws_bytes, void* st
   S.ld_topk = a->ld_topk;
   S.pool_in = a->pool_blocks;
   S.pool_in_n = a->pool_n;
+  S.order = a->order;
   e = csa2::launch_select(S, nullptr, 0, ctx, st);
   if (e != cudaSuccess) return cuda_fail(e, "csa2_reindex: select launch");
   return CSA2_OK;

@@ -88,6 +88,7 @@ struct SelectLaunch {
   const int* pool_in;     // kind 2: the pool the candidates come from [T, pool_in_n]
   int pool_in_n;
   uint32_t* hist;         // optional precomputed key histograms [V][2048] (returned to zero)
+  int order;              // 0: ascending positions, 1: best first
 };
 size_t select_workspace_bytes(const SelectLaunch& a);
 cudaError_t launch_select(const SelectLaunch& a, void* ws, size_t ws_bytes, const DeviceCtx& ctx, cudaStream_t st);

@@ -65,6 +65,7 @@ struct SelParams {
   const int* pool_in;
   int pool_in_n;
   uint32_t* hist;        // [V][kBins]: given, or built by the hist pass in `hist_ws`
+  int order;             // 0: ascending positions, 1: best first (score desc, index asc)
   int hist_full;         // hist covers every row (given by the caller), not only the long ones;
                          // the final pass returns the caller's rows to zero after reading them
   uint32_t* hist_ws;
@@ -724,7 +725,20 @@ __global__ void __launch_bounds__(kFinalThreads, 1) sel_final_kernel(const __gri
     __syncthreads();
   }
 
-  // 5. write: sel holds the survivors' element indices in ascending order
+  // best first: the survivors' 64-bit keys sorted descending (ties of the
+  // score go to the lower index through ~index in the low word)
+  if (P.order == 1 && !r.pool) {
+    for (int i = tid; i < got; i += blockDim.x) {
+      const uint32_t id = static_cast<uint32_t>(sm.sel[i]);
+      sm.sel[i] = key64(elem_key(r, r.src[id], static_cast<int>(id)), id);
+    }
+    __syncthreads();
+    sort_desc(sm, got);
+    for (int i = tid; i < got; i += blockDim.x) sm.sel[i] = ~static_cast<uint32_t>(sm.sel[i]);
+    __syncthreads();
+  }
+
+  // 5. write: sel holds the survivors' element indices in ascending order (or best first)
   const int t = r.t;
   const int b = row_seq_of(P.rows, t);
   if (r.pool) {
@@ -805,6 +819,7 @@ cudaError_t launch_select(const SelectLaunch& a, void* ws, size_t ws_bytes, cons
   P.pool_n = a.pool_n;
   P.pool_in = a.pool_in;
   P.pool_in_n = a.pool_in_n;
+  P.order = a.order;
   P.err = ctx.err;
   const int V = a.rows.T * ((a.kind == 0 && a.pool_out) ? 2 : 1);
   P.hist = a.hist;

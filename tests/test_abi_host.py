@@ -117,6 +117,10 @@ def test_validation_returns_codes_without_launch(lib):
     t.ld_scores, t.ld_block_max = 32768, 4096                                    # rows past the direct path
     assert lib.csa2_workspace_size(2, C.cast(C.byref(t), C.c_void_p), C.byref(n)) == 0 and n.value > 0
     assert lib.csa2_topk_with_candidates(C.byref(t), None, 0, None) == 7         # workspace missing
+    t.order = 2
+    assert lib.csa2_topk_with_candidates(C.byref(t), None, 0, None) == 2         # order is 0 or 1
+    assert b"order" in lib.csa2_last_error_detail()
+    t.order = 0
 
     s = csa2.SparseAttnArgs(FAKE, FAKE, 10, FAKE, 512, 512, FAKE, 10, FAKE, 129, 129, FAKE, 0.0, 1, 0, FAKE, None)
     assert lib.csa2_sparse_attn(C.byref(s), None, 0, None) == 2                  # n_swa > 128

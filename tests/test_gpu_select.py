@@ -260,3 +260,70 @@ def test_reindex_fp4_index_keys_match_oracle():
         want = o.topk_positions(full, 512)
         assert np_(pos[b]).tolist() == want.tolist()
         assert np_(slot[b]).tolist() == o.slots_of(want, pt[b]).tolist()
+
+
+@pytest.mark.parametrize("lengths", [[300, 511, 5000, 16384], [70_001, 200_000, 16_385]])
+def test_best_first_order(lengths):
+    # order = 1 (CSA2_ORDER_SCORE): the same top-k set, reported score
+    # descending with ties to the lower position, so every prefix k' of the row
+    # is the row's top-k'; slots follow their positions; the pool is unchanged
+    dev = need_gpu()
+    rng = np.random.default_rng(len(lengths))
+    T, ld = len(lengths), (max(lengths) + 3) & ~3
+    s = rng.normal(size=(T, ld)).astype(np.float32)
+    s[:, 100:140] = 0.25                                 # ties inside the selection
+    scores = torch.tensor(s, device=dev)
+    nbld = (ld + 7) // 8 + 3 & ~3
+    bm_np = np.full((T, nbld), -np.inf, dtype=np.float32)
+    for t, n in enumerate(lengths):
+        v = s[t, :n]
+        bm_np[t, :(n + 7) // 8] = np.pad(v, (0, -n % 8), constant_values=-np.inf).reshape(-1, 8).max(1)
+    bm = torch.tensor(bm_np, device=dev)
+    pt_np = np.stack([rng.permutation(1 << 16)[: (ld + 63) // 64] for _ in range(T)]).astype(np.int32)
+    pt = torch.tensor(pt_np, device=dev)
+    r = csa2.rows(T, T, n_visible=torch.tensor(lengths, dtype=torch.int32, device=dev))
+    outs = []
+    for order in (0, 1):
+        pos = torch.full((T, 512), -7, dtype=torch.int32, device=dev)
+        slot = torch.full((T, 512), -7, dtype=torch.int32, device=dev)
+        pool = torch.full((T, 2048), -7, dtype=torch.int32, device=dev)
+        csa2.topk_with_candidates(scores, r, 512, pos, slot, pt, bm, pool, order=order)
+        outs.append((np_(pos), np_(slot), np_(pool)))
+    torch.cuda.synchronize()
+    assert csa2.check_device_error() == 0
+    (p0, s0, q0), (p1, s1, q1) = outs
+    assert np.array_equal(q0, q1)
+    for t, n in enumerate(lengths):
+        want = o.topk_positions(s[t, :n], 512)
+        assert p0[t].tolist() == want.tolist()
+        sel = want[want >= 0]
+        best = sel[np.lexsort((sel, -s[t, sel].astype(np.float64)))]   # score desc, position asc
+        got = p1[t]
+        assert got[:len(best)].tolist() == best.tolist() and (got[len(best):] == -1).all(), f"row {t}"
+        assert s1[t].tolist() == o.slots_of(got, pt_np[t]).tolist()
+
+
+def test_reindex_best_first_order():
+    dev = need_gpu()
+    lengths = [30000, 16384 * 8 + 5, 700]
+    B = len(lengths)
+    pc = W.make_paged_cache(lengths, seed=41, device=dev, with_main=False)
+    iq = W.make_indexer_query(B, seed=42, device=dev)
+    pool = W.make_pool(lengths, seed=43, device=dev)
+    r = csa2.rows(B, B, n_visible=torch.tensor(lengths, dtype=torch.int32, device=dev))
+    res = []
+    for order in (0, 1):
+        pos = torch.empty(B, 512, dtype=torch.int32, device=dev)
+        ps = torch.empty(B, 2048 * 8, dtype=torch.float32, device=dev)
+        csa2.reindex(iq.q_fp8, iq.q_scale, iq.w, pc.index_k, pc.page_table, r, pool, 512, pos, None, ps, order=order)
+        res.append((np_(pos), np_(ps)))
+    torch.cuda.synchronize()
+    assert csa2.check_device_error() == 0
+    (p0, ps0), (p1, ps1) = res
+    for b, n in enumerate(lengths):
+        full = np.full(n, -np.inf, dtype=np.float32)
+        pp = o.pool_positions(np_(pool[b]), n)
+        full[pp[pp >= 0]] = ps0[b][pp >= 0]
+        sel = p0[b][p0[b] >= 0]
+        best = sel[np.lexsort((sel, -full[sel].astype(np.float64)))]
+        assert p1[b][:len(best)].tolist() == best.tolist(), f"row {b}"

@@ -145,3 +145,23 @@ def test_index_key_bytes_decode_through_the_page_readers():
     # the generator's independent FP4 encoder writes the same bytes
     gc, gu = W.fp4_encode_blocks(torch.tensor(k))
     assert np.array_equal(gc.numpy(), c4) and np.array_equal(gu.numpy(), u4)
+
+
+def test_record_comparison_rule_accepts_the_oracle_and_catches_planted_errors():
+    """The FP4 record comparison the GPU tests use (boundary rule, then every
+    decoded value within half its local grid spacing of the float64 latent)
+    accepts the oracle's own encoding and rejects a flipped code or scale."""
+    import pytest as _pytest
+    from gpu_util import assert_records_match_except_near_boundaries
+    rng = np.random.default_rng(0)
+    lat = rng.normal(size=(500, 512))
+    rec = o.fp4_encode_records(lat)
+    assert_records_match_except_near_boundaries(rec, lat)
+    bad = rec.copy()
+    bad[5, 10] ^= 0x11
+    with _pytest.raises(AssertionError):
+        assert_records_match_except_near_boundaries(bad, lat)
+    bad = rec.copy()
+    bad[7, 256] += 1
+    with _pytest.raises(AssertionError):
+        assert_records_match_except_near_boundaries(bad, lat)
