@@ -426,6 +426,38 @@ def measure_reindex(dev, stream, iters: int, hbm_peak: float) -> dict:
         "attn_hbm_frac": ATTN_ROW_BYTES * REINDEX_B / (attn / 1e3) / 1e9 / hbm_peak}}
 
 
+def measure_kv_project(dev, stream, iters: int, hbm_peak: float) -> dict:
+    """The hidden-state projection C = H W of a Full layer's new tokens (the
+    entry build's input; outside the step, which takes C as given): 16 rows
+    (decoder, m = 1) and 32 rows (encoder, m = 2, two tokens a sequence), hidden
+    width 7168, weight 7168 x 512 bf16."""
+    import torch
+
+    from serving_lightning_indexer_gb300 import csa2
+    from serving_lightning_indexer_gb300 import workloads as W
+    res = {}
+    for T in (16, 32):
+        H, w = W.make_hidden_projection(T, seed=400 + T, device=dev)
+        out = torch.empty(T, 512, dtype=torch.bfloat16, device=dev)
+        # ten weight copies (73 MB) cycled so that each call reads its weight from HBM
+        # rather than from the previous call's L2 lines
+        ws = [w] + [w.clone() for _ in range(9)]
+        k = [0]
+
+        def call():
+            csa2.kv_project(H, ws[k[0] % 10], out)
+            k[0] += 1
+        ms = _time_calls(call, iters * 10, stream)
+        nbytes = w.numel() * 2 + H.numel() * 2 + out.numel() * 2
+        gbs = nbytes / (ms / 1e3) / 1e9
+        res[f"rows_{T}"] = {"avg_launch_ms": ms, "algorithmic_bytes_per_launch": nbytes, "achieved": gbs,
+                            "frac": gbs / hbm_peak}
+        del ws, H, w, out
+    torch.cuda.empty_cache()
+    return {"roofline_kv_project": {"bound": "hbm", "kernel": "kv_project_kernel (csa2_kv_project)",
+                                    "hidden": W.HIDDEN, "peak": hbm_peak, "unit": "GB/s", **res}}
+
+
 # ---------------------------------------------------------------------------
 # single-call cases for profilers
 # ---------------------------------------------------------------------------
@@ -482,6 +514,11 @@ def run_case(args):
         ms = _time_calls(lambda: csa2.sparse_attn(al.q, pc.main_kv, slot, al.swa_kv, al.swa_slot, al.sink, out),
                          args.iters, st)
         res.update(ms=ms, query_layers=B)
+    elif args.case == "project":
+        H, w = W.make_hidden_projection(B, seed=8, device=dev)
+        out = torch.empty(B, 512, dtype=torch.bfloat16, device=dev)
+        ms = _time_calls(lambda: csa2.kv_project(H, w, out), args.iters, st)
+        res.update(ms=ms, rows=B, hidden=W.HIDDEN)
     else:  # prefill: the query-blocked indexer over one sequence, m = 2, T queries at the end of n entries
         T = args.queries
         pc = W.make_paged_cache([n], seed=6, device=dev, with_main=False)
@@ -514,7 +551,7 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-workloads", action="store_true", help="skip the prefill and Reindex workloads")
-    ap.add_argument("--case", choices=["scan", "topk", "reindex", "attn", "prefill"])
+    ap.add_argument("--case", choices=["scan", "topk", "reindex", "attn", "prefill", "project"])
     ap.add_argument("--iters", type=int, default=3)
     ap.add_argument("--batch", type=int, default=8)
     ap.add_argument("--entries", type=int, default=262144)
@@ -712,6 +749,7 @@ def main():
     if not args.no_workloads:
         extra.update(measure_prefill(dev, stream, 20, 2 * bf16_peak, 2 * bf16_sust))
         extra.update(measure_reindex(dev, stream, 20, hbm_peak))
+        extra.update(measure_kv_project(dev, stream, 20, hbm_peak))
 
     if rank != 0:
         if world > 1:

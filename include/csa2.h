@@ -333,6 +333,25 @@ typedef struct {
 } csa2_compress_args;
 CSA2_API int csa2_compress_m2(const csa2_compress_args* args, void* stream);
 
+/* ---- hidden-state projection of the entry build's inputs ---------------------
+ * out[t] = hidden[t] W (fp32 accumulation, rounded to bf16) for t < T: the
+ * per-token 512-vector the entry build takes as C (and, for m = 2, as Z).
+ * CSA2 page item 3: with m = 1 the main-KV entry is one linear projection of
+ * the token; CED (CSA2 page, report reading): the decoder layers' global KV
+ * comes from the encoder output, C = H_{L/2} W^KV, the encoder layers' C and
+ * Z from their own hidden states.  Sized for decode batches (T <= 4096 rows;
+ * the cost is the weight read, hidden_dim x 1 KB); a prefill chunk's
+ * projection is a dense GEMM outside this call.  No workspace.
+ * Alignment: hidden, w, out 16 B; hidden_dim a multiple of 256. */
+typedef struct {
+  const uint16_t* hidden;      /* [T, hidden_dim] bf16 */
+  const uint16_t* w;           /* [hidden_dim, 512] bf16 (row = input dim) */
+  int32_t T;                   /* 1..4096 */
+  int32_t hidden_dim;          /* 256..65536, multiple of 256 */
+  uint16_t* out;               /* [T, 512] bf16 */
+} csa2_kv_project_args;
+CSA2_API int csa2_kv_project(const csa2_kv_project_args* args, void* stream);
+
 /* ---- workspace, device errors ------------------------------------------------ */
 enum { CSA2_CALL_INDEX_SCORE = 1, CSA2_CALL_TOPK = 2, CSA2_CALL_REINDEX = 3, CSA2_CALL_SPARSE_ATTN = 4 };
 /* Bytes of workspace the call needs with these arguments (0 if none). */

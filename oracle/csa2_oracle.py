@@ -402,6 +402,20 @@ def attention_row(q_bf16_values, main_cache, topk_slot_row, swa_cache, swa_slot_
 # Main-KV entry build (m = 1 or 2)
 # ---------------------------------------------------------------------------
 
+def kv_project(hidden: np.ndarray, w_kv: np.ndarray) -> np.ndarray:
+    """Per-token inputs of the entry build from the hidden states: C = H W.
+
+    CSA2 page, "一层 CSA2 的 attention 具体怎么算" item 3: with m = 1 the
+    main-KV entry is one linear projection of the token (weight identically 1
+    in the compression); CSA2 page and report reading, CED: the decoder layers'
+    C_l = H_{L/2} W^KV_l, the encoder layers' C and Z from their own hidden
+    state.  H is [n_tokens, hidden], W is [hidden, 512] (row = input dim).
+    Readings: the pages give no V4.1 hidden width; the DSA page's V3.2 figure,
+    7168, is taken; the weights are random (no trained weights).
+    """
+    return np.asarray(hidden, dtype=np.float64) @ np.asarray(w_kv, dtype=np.float64)
+
+
 def compress_latent(C: np.ndarray, Z, ratio_m: int, gamma: np.ndarray, eps: float,
                     positions: np.ndarray, rope_theta: float, apply_rope: bool = True) -> np.ndarray:
     """Latent [n_entries,512] of the main-KV entries, before quantisation.

@@ -66,11 +66,15 @@ class CompressArgs(C.Structure):
                 ("index_k_pages", _I64), ("index_k_format", _I32), ("index_latent_out", _P)]
 
 
+class KvProjectArgs(C.Structure):
+    _fields_ = [("hidden", _P), ("w", _P), ("T", _I32), ("hidden_dim", _I32), ("out", _P)]
+
+
 CALL_INDEX_SCORE, CALL_TOPK, CALL_REINDEX, CALL_SPARSE_ATTN = 1, 2, 3, 4
 EXPORTED = ("csa2_status_string", "csa2_last_error_detail", "csa2_index_score", "csa2_topk_with_candidates",
             "csa2_reindex", "csa2_sparse_attn", "csa2_compress_m2", "csa2_workspace_size",
             "csa2_check_device_error", "csa2_version", "csa2_topk_with_candidates_noalloc",
-            "csa2_debug_bounded_wait")
+            "csa2_debug_bounded_wait", "csa2_kv_project")
 
 _lib = None
 
@@ -107,6 +111,8 @@ def load(build_if_missing: bool = False) -> C.CDLL:
     lib.csa2_workspace_size.argtypes = [C.c_int, _P, C.POINTER(C.c_size_t)]
     lib.csa2_check_device_error.restype = C.c_int
     lib.csa2_check_device_error.argtypes = [_P]
+    lib.csa2_kv_project.restype = C.c_int
+    lib.csa2_kv_project.argtypes = [C.POINTER(KvProjectArgs), _P]
     lib.csa2_debug_bounded_wait.restype = C.c_int
     lib.csa2_debug_bounded_wait.argtypes = [C.c_uint32, _P]
     _lib = lib
@@ -262,6 +268,13 @@ def compress_m2(Cm, Z, ratio_m, gamma, main_kv, page_table=None, entry_slot=None
                      _ptr(w_ik), _ptr(k_gamma), _ptr(index_k), index_k.shape[0] if index_k is not None else 0,
                      index_format(index_k) if index_k is not None else 0, _ptr(index_latent_out))
     _check(lib.csa2_compress_m2(C.byref(a), _stream(stream)), "csa2_compress_m2")
+
+
+def kv_project(hidden, w, out, stream=None):
+    """out [T,512] bf16 = hidden [T,H] bf16 @ w [H,512] bf16 (csa2_kv_project)."""
+    lib = load()
+    a = KvProjectArgs(_ptr(hidden), _ptr(w), hidden.shape[0], hidden.shape[1], _ptr(out))
+    _check(lib.csa2_kv_project(C.byref(a), _stream(stream)), "csa2_kv_project")
 
 
 def check_device_error(stream=None) -> int:

@@ -312,6 +312,74 @@ __global__ void __launch_bounds__(256) compress_kernel(const __grid_constant__ C
   }
 }
 
+
+// ---------------------------------------------------------------- hidden-state projection
+// C = H W for the per-token inputs of the entry build (CSA2 page item 3: with
+// m = 1 the main-KV entry is one linear projection of the token; CED: the
+// decoder layers' C = H_{L/2} W^KV, the encoder layers' C and Z from their
+// own hidden state).  Decode-sized row counts: the weight read (hidden x 512
+// bf16) is the cost.  CTA = 8 output columns; thread (column c, slice s)
+// accumulates rows 8 s + 256 i .. + 7 for every i, with one 16-B load of each
+// hidden row per block of 8; the 32 slices are summed by shuffles and through
+// shared memory.
+constexpr int kPjD = 512;        // width of the projected token vector
+constexpr int kPjCols = 8;
+constexpr int kPjThreads = 256;   // 8 columns x 32 row slices
+constexpr int kPjRows = 16;       // hidden rows per pass
+
+__global__ void __launch_bounds__(kPjThreads) kv_project_kernel(const __nv_bfloat16* __restrict__ H,
+                                                                const __nv_bfloat16* __restrict__ W, int T,
+                                                                int hidden, __nv_bfloat16* __restrict__ out) {
+  __shared__ float red[kPjThreads / 32][kPjRows][kPjCols];
+  pdl_wait();
+  pdl_trigger();
+  const int c = threadIdx.x & (kPjCols - 1), sl = threadIdx.x >> 3;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int col = blockIdx.x * kPjCols + c;
+  for (int t0 = 0; t0 < T; t0 += kPjRows) {
+    const int nt = min(kPjRows, T - t0);
+    float acc[kPjRows];
+#pragma unroll
+    for (int t = 0; t < kPjRows; ++t) acc[t] = 0.f;
+    for (int k0 = 8 * sl; k0 < hidden; k0 += 8 * (kPjThreads / kPjCols)) {
+      float wv[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) wv[j] = __bfloat162float(W[static_cast<long long>(k0 + j) * kPjD + col]);
+#pragma unroll
+      for (int t = 0; t < kPjRows; ++t) {
+        if (t < nt) {
+          const uint4 hv = __ldg(reinterpret_cast<const uint4*>(H + static_cast<long long>(t0 + t) * hidden + k0));
+          const uint32_t hw[4] = {hv.x, hv.y, hv.z, hv.w};
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&hw[j]));
+            acc[t] = fmaf(f.x, wv[2 * j], acc[t]);
+            acc[t] = fmaf(f.y, wv[2 * j + 1], acc[t]);
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int t = 0; t < kPjRows; ++t) {
+      acc[t] += __shfl_xor_sync(0xffffffffu, acc[t], 8);
+      acc[t] += __shfl_xor_sync(0xffffffffu, acc[t], 16);
+    }
+    if (lane < kPjCols) {
+#pragma unroll
+      for (int t = 0; t < kPjRows; ++t) red[warp][t][c] = acc[t];
+    }
+    __syncthreads();
+    if (threadIdx.x < nt * kPjCols) {
+      const int t = threadIdx.x / kPjCols, cc = threadIdx.x % kPjCols;
+      float v = 0.f;
+#pragma unroll
+      for (int w = 0; w < kPjThreads / 32; ++w) v += red[w][t][cc];
+      out[static_cast<long long>(t0 + t) * kPjD + blockIdx.x * kPjCols + cc] = __float2bfloat16_rn(v);
+    }
+    __syncthreads();
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_compress(const CompressLaunch& a, const DeviceCtx& ctx, cudaStream_t st) {
@@ -360,6 +428,15 @@ cudaError_t launch_compress(const CompressLaunch& a, const DeviceCtx& ctx, cudaS
   cudaError_t e = prefer_max_smem(compress_kernel<true, 8>, smem);
   if (e != cudaSuccess) return e;
   return launch_pdl(compress_kernel<true, 8>, dim3(static_cast<unsigned>(blocks)), dim3(256), smem, st, p);
+}
+
+cudaError_t launch_kv_project(const uint16_t* H, const uint16_t* W, int T, int hidden, uint16_t* out,
+                              cudaStream_t st) {
+  cudaError_t e = prefer_max_smem(kv_project_kernel, 0);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(kv_project_kernel, dim3(kPjD / kPjCols), dim3(kPjThreads), 0, st,
+                    reinterpret_cast<const __nv_bfloat16*>(H), reinterpret_cast<const __nv_bfloat16*>(W), T, hidden,
+                    reinterpret_cast<__nv_bfloat16*>(out));
 }
 
 }  // namespace csa2

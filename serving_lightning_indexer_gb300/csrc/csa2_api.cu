@@ -459,6 +459,21 @@ int csa2_compress_m2(const csa2_compress_args* a, void* stream) {
   return CSA2_OK;
 }
 
+int csa2_kv_project(const csa2_kv_project_args* a, void* stream) {
+  if (!a) return fail(CSA2_ERR_NULL, "csa2_kv_project: args is NULL");
+  if (!a->hidden || !a->w || !a->out) return fail(CSA2_ERR_NULL, "csa2_kv_project: hidden/w/out is NULL");
+  if (a->T < 1 || a->T > 4096) return fail(CSA2_ERR_SHAPE, "csa2_kv_project: T=%d not in 1..4096", a->T);
+  if (a->hidden_dim < 256 || a->hidden_dim > 65536 || (a->hidden_dim & 255))
+    return fail(CSA2_ERR_SHAPE, "csa2_kv_project: hidden_dim=%d must be a multiple of 256 in 256..65536",
+                a->hidden_dim);
+  if (!aligned16(a->hidden) || !aligned16(a->w) || !aligned16(a->out))
+    return fail(CSA2_ERR_ALIGN, "csa2_kv_project: hidden, w, out must be 16-B aligned");
+  cudaError_t e = csa2::launch_kv_project(a->hidden, a->w, a->T, a->hidden_dim, a->out,
+                                          static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "csa2_kv_project: launch");
+  return CSA2_OK;
+}
+
 int csa2_workspace_size(int which, const void* args, size_t* bytes) {
   if (!args || !bytes) return fail(CSA2_ERR_NULL, "csa2_workspace_size: null argument");
   *bytes = 0;

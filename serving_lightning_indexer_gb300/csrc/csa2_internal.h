@@ -149,6 +149,9 @@ struct CompressLaunch {
   float* index_latent_out;
 };
 cudaError_t launch_compress(const CompressLaunch& a, const DeviceCtx& ctx, cudaStream_t st);
+// C = H W (bf16 in and out, fp32 accumulation) for T hidden rows of width `hidden`.
+cudaError_t launch_kv_project(const uint16_t* H, const uint16_t* W, int T, int hidden, uint16_t* out,
+                              cudaStream_t st);
 
 // Shared by the top-k entry points: argument checks + launch description;
 // `who` names the entry point in the error detail.

@@ -282,6 +282,18 @@ def make_index_projection(seed: int, device="cpu"):
     return w.contiguous(), k_gamma.contiguous()
 
 
+HIDDEN = 7168   # model width of the hidden states (the DSA page's figure; no V4.1 width is given)
+
+
+def make_hidden_projection(n_tokens: int, seed: int, device="cpu", hidden: int = HIDDEN):
+    """Hidden states H [n_tokens,hidden] bf16 ~ N(0,1) and W^KV [hidden,512]
+    bf16 ~ N(0,1)/sqrt(hidden) (a random initialisation: no trained weights)."""
+    g = _gen(seed, device)
+    H = torch.randn(n_tokens, hidden, generator=g, device=device).to(torch.bfloat16)
+    w = (torch.randn(hidden, ATT_DIM, generator=g, device=device) / math.sqrt(hidden)).to(torch.bfloat16)
+    return H.contiguous(), w.contiguous()
+
+
 # ---------------------------------------------------------------------------
 # the five workloads
 # ---------------------------------------------------------------------------

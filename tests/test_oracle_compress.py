@@ -165,3 +165,24 @@ def test_record_comparison_rule_accepts_the_oracle_and_catches_planted_errors():
     bad[7, 256] += 1
     with _pytest.raises(AssertionError):
         assert_records_match_except_near_boundaries(bad, lat)
+
+
+def test_kv_project_brute_force_and_selector():
+    """C = H W written out as a triple loop on a tiny case; a selector W (the
+    identity on the first 512 input dims) returns those dims of H; a scaled
+    hidden state scales C (linearity)."""
+    rng = np.random.default_rng(3)
+    H = rng.normal(size=(3, 40))
+    Wt = rng.normal(size=(40, 7))
+    want = np.zeros((3, 7))
+    for t in range(3):
+        for n in range(7):
+            for k in range(40):
+                want[t, n] += H[t, k] * Wt[k, n]
+    assert np.allclose(o.kv_project(H, Wt), want, rtol=1e-13, atol=1e-13)
+    H2 = rng.normal(size=(2, 7168))
+    sel = np.zeros((7168, 512))
+    sel[np.arange(512), np.arange(512)] = 1.0
+    assert np.array_equal(o.kv_project(H2, sel), H2[:, :512])
+    W2 = rng.normal(size=(7168, 512))
+    assert np.allclose(o.kv_project(2.5 * H2, W2), 2.5 * o.kv_project(H2, W2), rtol=1e-12)
