@@ -429,25 +429,25 @@ def measure_reindex(dev, stream, iters: int, hbm_peak: float) -> dict:
 def measure_kv_project(dev, stream, iters: int, hbm_peak: float) -> dict:
     """The hidden-state projection C = H W of a Full layer's new tokens (the
     entry build's input; outside the step, which takes C as given): 16 rows
-    (decoder, m = 1) and 32 rows (encoder, m = 2, two tokens a sequence), hidden
-    width 7168, weight 7168 x 512 bf16."""
+    rows, batch 8: 8 (decoder, m = 1) and 16 (encoder, m = 2, two tokens a
+    sequence), hidden width 7168, weight 7168 x 512 bf16."""
     import torch
 
     from serving_lightning_indexer_gb300 import csa2
     from serving_lightning_indexer_gb300 import workloads as W
     res = {}
-    for T in (16, 32):
+    for T in (8, 16):
         H, w = W.make_hidden_projection(T, seed=400 + T, device=dev)
         out = torch.empty(T, 512, dtype=torch.bfloat16, device=dev)
-        # ten weight copies (73 MB) cycled so that each call reads its weight from HBM
-        # rather than from the previous call's L2 lines
-        ws = [w] + [w.clone() for _ in range(9)]
+        # 24 weight copies (176 MB, more than L2) cycled so that each call reads
+        # its weight from HBM
+        ws = [w] + [w.clone() for _ in range(23)]
         k = [0]
 
         def call():
-            csa2.kv_project(H, ws[k[0] % 10], out)
+            csa2.kv_project(H, ws[k[0] % 24], out)
             k[0] += 1
-        ms = _time_calls(call, iters * 10, stream)
+        ms = _time_calls(call, iters * 24, stream)
         nbytes = w.numel() * 2 + H.numel() * 2 + out.numel() * 2
         gbs = nbytes / (ms / 1e3) / 1e9
         res[f"rows_{T}"] = {"avg_launch_ms": ms, "algorithmic_bytes_per_launch": nbytes, "achieved": gbs,

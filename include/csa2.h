@@ -238,6 +238,15 @@ typedef struct {
   float* pool_scores;                          /* optional [T, 8*pool_n] */
   int32_t index_k_format;                      /* CSA2_INDEX_FP8 (0) or CSA2_INDEX_FP4 */
   int32_t order;                               /* CSA2_ORDER_POSITION (0) or CSA2_ORDER_SCORE (1) */
+  /* 1: rows, pool_blocks, page_table and index_k were written at least two
+   * launches before this call on the stream (a Reindex layer reads its group's
+   * Full-layer caches and pool), so the candidate blocks are located and
+   * prefetched into L2 before the previous launch completes; q_fp8, q_scale
+   * and w are still read after it.  The two launches before the call must be
+   * ordinary launches or kernels that signal their dependents only after their
+   * own dependency wait (as every kernel of this library does).  0: everything
+   * is read after the previous launch. */
+  int32_t kv_ready;
 } csa2_reindex_args;
 CSA2_API int csa2_reindex(const csa2_reindex_args* args, void* workspace, size_t ws_bytes, void* stream);
 
@@ -339,15 +348,17 @@ CSA2_API int csa2_compress_m2(const csa2_compress_args* args, void* stream);
  * CSA2 page item 3: with m = 1 the main-KV entry is one linear projection of
  * the token; CED (CSA2 page, report reading): the decoder layers' global KV
  * comes from the encoder output, C = H_{L/2} W^KV, the encoder layers' C and
- * Z from their own hidden states.  Sized for decode batches (T <= 4096 rows;
+ * Z from their own hidden states.  Sized for decode batches (T <= 64 rows;
  * the cost is the weight read, hidden_dim x 1 KB); a prefill chunk's
- * projection is a dense GEMM outside this call.  No workspace.
- * Alignment: hidden, w, out 16 B; hidden_dim a multiple of 256. */
+ * projection is a dense GEMM outside this call.  No workspace.  w is read
+ * before the previous launch on the stream completes (weights are not
+ * written by the step): it must not be written by the launch just before
+ * this call.  Alignment: hidden, w, out 16 B. */
 typedef struct {
   const uint16_t* hidden;      /* [T, hidden_dim] bf16 */
   const uint16_t* w;           /* [hidden_dim, 512] bf16 (row = input dim) */
-  int32_t T;                   /* 1..4096 */
-  int32_t hidden_dim;          /* 256..65536, multiple of 256 */
+  int32_t T;                   /* 1..64 */
+  int32_t hidden_dim;          /* 512..16384, multiple of 512 */
   uint16_t* out;               /* [T, 512] bf16 */
 } csa2_kv_project_args;
 CSA2_API int csa2_kv_project(const csa2_kv_project_args* args, void* stream);

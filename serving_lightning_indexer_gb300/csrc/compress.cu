@@ -317,67 +317,148 @@ __global__ void __launch_bounds__(256) compress_kernel(const __grid_constant__ C
 // C = H W for the per-token inputs of the entry build (CSA2 page item 3: with
 // m = 1 the main-KV entry is one linear projection of the token; CED: the
 // decoder layers' C = H_{L/2} W^KV, the encoder layers' C and Z from their
-// own hidden state).  Decode-sized row counts: the weight read (hidden x 512
-// bf16) is the cost.  CTA = 8 output columns; thread (column c, slice s)
-// accumulates rows 8 s + 256 i .. + 7 for every i, with one 16-B load of each
-// hidden row per block of 8; the 32 slices are summed by shuffles and through
-// shared memory.
-constexpr int kPjD = 512;        // width of the projected token vector
-constexpr int kPjCols = 8;
-constexpr int kPjThreads = 256;   // 8 columns x 32 row slices
-constexpr int kPjRows = 16;       // hidden rows per pass
+// own hidden state).  Decode-sized row counts (T <= 64): the weight read
+// (hidden x 1 KB) is the cost, so every SM streams a share of it at once.
+// Grid: 16 column blocks of 32 x 8 slices of the hidden dimension; the 8 CTAs
+// of a column block form a cluster and add their partial sums through
+// distributed shared memory.  A thread owns 8 columns (one 16-B weight load)
+// of one row in each round of 64 rows; a batch of up to 16 rounds of weights
+// is loaded into registers at once (the first batch before the dependency
+// wait: weights are not produced by the step), the batch's hidden-state
+// columns are staged in shared memory, and 4 rows of H at a time are
+// accumulated with packed fp32x2 FMAs.  The 64 threads of a column chunk are
+// reduced by a shuffle reduce-scatter (xor 16, 8, 4) and through shared memory.
+constexpr int kPjD = 512;           // width of the projected token vector
+constexpr int kPjCols = 32;         // output columns per CTA
+constexpr int kPjSplit = 8;         // CTAs (slices of the hidden dimension) per column block
+constexpr int kPjThreads = 256;     // 64 rows x 4 column chunks of 8
+constexpr int kPjRounds = 16;       // rounds of 64 rows per batch
+constexpr int kPjBatch = 64 * kPjRounds;
+constexpr int kPjMaxT = 64;
 
-__global__ void __launch_bounds__(kPjThreads) kv_project_kernel(const __nv_bfloat16* __restrict__ H,
-                                                                const __nv_bfloat16* __restrict__ W, int T,
-                                                                int hidden, __nv_bfloat16* __restrict__ out) {
-  __shared__ float red[kPjThreads / 32][kPjRows][kPjCols];
-  pdl_wait();
-  pdl_trigger();
-  const int c = threadIdx.x & (kPjCols - 1), sl = threadIdx.x >> 3;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int col = blockIdx.x * kPjCols + c;
-  for (int t0 = 0; t0 < T; t0 += kPjRows) {
-    const int nt = min(kPjRows, T - t0);
-    float acc[kPjRows];
+size_t kv_project_smem(int T, int hidden) {
+  const int batch = min(hidden / kPjSplit, kPjBatch);
+  return static_cast<size_t>(T) * batch * 2 + 8 * 4 * 32 * 4 + static_cast<size_t>(T) * kPjCols * 4;
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t x) { return __uint_as_float(x << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t x) { return __uint_as_float(x & 0xFFFF0000u); }
+
+__global__ void __launch_bounds__(kPjThreads, 1) kv_project_kernel(const __nv_bfloat16* __restrict__ H,
+                                                                   const __nv_bfloat16* __restrict__ W, int T,
+                                                                   int hidden, __nv_bfloat16* __restrict__ out) {
+  extern __shared__ __align__(16) uint8_t pj_smem[];
+  const int hs = hidden / kPjSplit;       // rows of this CTA's slice (a multiple of 64)
+  const int batch = min(hs, kPjBatch);
+  __nv_bfloat16* h_s = reinterpret_cast<__nv_bfloat16*>(pj_smem);            // [T][batch]
+  float* red = reinterpret_cast<float*>(pj_smem + static_cast<size_t>(T) * batch * 2);  // [8 warps][4 chunks][32]
+  float* part = red + 8 * 4 * 32;                                              // [T][32]
+  const uint32_t rank = cluster_rank();
+  const int col0 = blockIdx.x * kPjCols;
+  const int tid = threadIdx.x, cc = tid & 3, rsub = tid >> 2;
+  const int lane = tid & 31, warp = tid >> 5;
+  const int k_begin = static_cast<int>(rank) * hs;
+  for (int i = tid; i < T * kPjCols; i += kPjThreads) part[i] = 0.f;
+  bool waited = false;
+  for (int kb = k_begin; kb < k_begin + hs; kb += batch) {
+    const int nb = min(batch, k_begin + hs - kb);  // a multiple of 64
+    uint4 wv[kPjRounds];
 #pragma unroll
-    for (int t = 0; t < kPjRows; ++t) acc[t] = 0.f;
-    for (int k0 = 8 * sl; k0 < hidden; k0 += 8 * (kPjThreads / kPjCols)) {
-      float wv[8];
+    for (int i = 0; i < kPjRounds; ++i) {
+      wv[i] = make_uint4(0u, 0u, 0u, 0u);
+      if (i * 64 < nb)
+        wv[i] = __ldg(reinterpret_cast<const uint4*>(W + static_cast<long long>(kb + i * 64 + rsub) * kPjD + col0 +
+                                                     cc * 8));
+    }
+    if (!waited) {
+      pdl_wait();
+      pdl_trigger();
+      waited = true;
+    }
+    __syncthreads();  // the previous batch's h_s is no longer read
+    const int per_row = nb / 8;
+    for (int i = tid; i < T * per_row; i += kPjThreads) {
+      const int t = i / per_row, u = i - t * per_row;
+      *reinterpret_cast<uint4*>(h_s + t * batch + u * 8) =
+          __ldg(reinterpret_cast<const uint4*>(H + static_cast<long long>(t) * hidden + kb + u * 8));
+    }
+    __syncthreads();
+    for (int t0 = 0; t0 < T; t0 += 4) {
+      uint64_t acc[4][4];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) wv[j] = __bfloat162float(W[static_cast<long long>(k0 + j) * kPjD + col]);
+      for (int tt = 0; tt < 4; ++tt)
 #pragma unroll
-      for (int t = 0; t < kPjRows; ++t) {
-        if (t < nt) {
-          const uint4 hv = __ldg(reinterpret_cast<const uint4*>(H + static_cast<long long>(t0 + t) * hidden + k0));
-          const uint32_t hw[4] = {hv.x, hv.y, hv.z, hv.w};
+        for (int jp = 0; jp < 4; ++jp) acc[tt][jp] = 0ull;
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&hw[j]));
-            acc[t] = fmaf(f.x, wv[2 * j], acc[t]);
-            acc[t] = fmaf(f.y, wv[2 * j + 1], acc[t]);
+      for (int i = 0; i < kPjRounds; ++i) {
+        if (i * 64 < nb) {
+          const int kl = i * 64 + rsub;
+          const uint32_t w32[4] = {wv[i].x, wv[i].y, wv[i].z, wv[i].w};
+          uint64_t wp[4];
+#pragma unroll
+          for (int jp = 0; jp < 4; ++jp) wp[jp] = pack_f32x2(bf16_lo(w32[jp]), bf16_hi(w32[jp]));
+#pragma unroll
+          for (int tt = 0; tt < 4; ++tt) {
+            const float h = (t0 + tt < T) ? __bfloat162float(h_s[(t0 + tt) * batch + kl]) : 0.f;
+            const uint64_t hh = pack_f32x2(h, h);
+#pragma unroll
+            for (int jp = 0; jp < 4; ++jp) acc[tt][jp] = fma_f32x2(hh, wp[jp], acc[tt][jp]);
           }
         }
       }
-    }
+      // value q = 8 tt + j of this thread (row t0 + tt, column cc * 8 + j)
+      float v[32];
 #pragma unroll
-    for (int t = 0; t < kPjRows; ++t) {
-      acc[t] += __shfl_xor_sync(0xffffffffu, acc[t], 8);
-      acc[t] += __shfl_xor_sync(0xffffffffu, acc[t], 16);
-    }
-    if (lane < kPjCols) {
+      for (int tt = 0; tt < 4; ++tt)
 #pragma unroll
-      for (int t = 0; t < kPjRows; ++t) red[warp][t][c] = acc[t];
-    }
-    __syncthreads();
-    if (threadIdx.x < nt * kPjCols) {
-      const int t = threadIdx.x / kPjCols, cc = threadIdx.x % kPjCols;
-      float v = 0.f;
+        for (int jp = 0; jp < 4; ++jp) {
+          const float2 f = unpack_f32x2(acc[tt][jp]);
+          v[tt * 8 + 2 * jp] = f.x;
+          v[tt * 8 + 2 * jp + 1] = f.y;
+        }
+      // reduce-scatter over the 8 lanes of the warp that hold chunk cc: after
+      // the xor-16, -8 and -4 steps lane l holds values (l >> 2) * 4 + i, i < 4
 #pragma unroll
-      for (int w = 0; w < kPjThreads / 32; ++w) v += red[w][t][cc];
-      out[static_cast<long long>(t0 + t) * kPjD + blockIdx.x * kPjCols + cc] = __float2bfloat16_rn(v);
+      for (int i = 0; i < 16; ++i) {
+        const bool hi = lane & 16;
+        const float keep = hi ? v[16 + i] : v[i], send = hi ? v[i] : v[16 + i];
+        v[i] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const bool hi = lane & 8;
+        const float keep = hi ? v[8 + i] : v[i], send = hi ? v[i] : v[8 + i];
+        v[i] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const bool hi = lane & 4;
+        const float keep = hi ? v[4 + i] : v[i], send = hi ? v[i] : v[4 + i];
+        v[i] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
+      }
+      *reinterpret_cast<float4*>(red + (warp * 4 + cc) * 32 + (lane >> 2) * 4) = make_float4(v[0], v[1], v[2], v[3]);
+      __syncthreads();
+      if (tid < 128) {
+        const int c2 = tid >> 5, q = tid & 31;
+        float sum = 0.f;
+#pragma unroll
+        for (int w = 0; w < 8; ++w) sum += red[(w * 4 + c2) * 32 + q];
+        const int tt = q >> 3, j = q & 7;
+        if (t0 + tt < T) part[(t0 + tt) * kPjCols + c2 * 8 + j] += sum;
+      }
+      __syncthreads();  // red is rewritten by the next rows
     }
-    __syncthreads();
   }
+  cluster_sync();  // every slice's partial sums are final
+  // the column block's T x 32 outputs, split over the cluster's CTAs
+  for (int o = static_cast<int>(rank) * kPjThreads + tid; o < T * kPjCols; o += kPjSplit * kPjThreads) {
+    const uint32_t a = smem_u32(part + o);
+    float sum = 0.f;
+#pragma unroll
+    for (int r = 0; r < kPjSplit; ++r) sum += ld_cluster_f32(map_rank(a, static_cast<uint32_t>(r)));
+    out[static_cast<long long>(o / kPjCols) * kPjD + col0 + (o % kPjCols)] = __float2bfloat16_rn(sum);
+  }
+  cluster_sync();  // no CTA leaves while its partial sums may still be read
 }
 
 }  // namespace
@@ -432,11 +513,25 @@ cudaError_t launch_compress(const CompressLaunch& a, const DeviceCtx& ctx, cudaS
 
 cudaError_t launch_kv_project(const uint16_t* H, const uint16_t* W, int T, int hidden, uint16_t* out,
                               cudaStream_t st) {
-  cudaError_t e = prefer_max_smem(kv_project_kernel, 0);
+  const size_t smem = kv_project_smem(T, hidden);
+  cudaError_t e = prefer_max_smem(kv_project_kernel, smem);
   if (e != cudaSuccess) return e;
-  return launch_pdl(kv_project_kernel, dim3(kPjD / kPjCols), dim3(kPjThreads), 0, st,
-                    reinterpret_cast<const __nv_bfloat16*>(H), reinterpret_cast<const __nv_bfloat16*>(W), T, hidden,
-                    reinterpret_cast<__nv_bfloat16*>(out));
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(kPjD / kPjCols, kPjSplit);
+  cfg.blockDim = dim3(kPjThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = 1;
+  attr[1].val.clusterDim.y = kPjSplit;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, kv_project_kernel, reinterpret_cast<const __nv_bfloat16*>(H),
+                            reinterpret_cast<const __nv_bfloat16*>(W), T, hidden, reinterpret_cast<__nv_bfloat16*>(out));
 }
 
 }  // namespace csa2

@@ -321,6 +321,7 @@ int csa2_reindex(const csa2_reindex_args* a, void* ws, size_t ws_bytes, void* st
   L.ld_out = static_cast<long long>(a->pool_n) * 8;
   L.pool_blocks = a->pool_blocks;
   L.pool_n = a->pool_n;
+  L.kv_ready = a->kv_ready != 0;
   const char* why = "launch";
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   e = csa2::launch_index_tiles(L, 1, 1, ctx, st, &why);
@@ -462,9 +463,9 @@ int csa2_compress_m2(const csa2_compress_args* a, void* stream) {
 int csa2_kv_project(const csa2_kv_project_args* a, void* stream) {
   if (!a) return fail(CSA2_ERR_NULL, "csa2_kv_project: args is NULL");
   if (!a->hidden || !a->w || !a->out) return fail(CSA2_ERR_NULL, "csa2_kv_project: hidden/w/out is NULL");
-  if (a->T < 1 || a->T > 4096) return fail(CSA2_ERR_SHAPE, "csa2_kv_project: T=%d not in 1..4096", a->T);
-  if (a->hidden_dim < 256 || a->hidden_dim > 65536 || (a->hidden_dim & 255))
-    return fail(CSA2_ERR_SHAPE, "csa2_kv_project: hidden_dim=%d must be a multiple of 256 in 256..65536",
+  if (a->T < 1 || a->T > 64) return fail(CSA2_ERR_SHAPE, "csa2_kv_project: T=%d not in 1..64", a->T);
+  if (a->hidden_dim < 512 || a->hidden_dim > 16384 || (a->hidden_dim & 511))
+    return fail(CSA2_ERR_SHAPE, "csa2_kv_project: hidden_dim=%d must be a multiple of 512 in 512..16384",
                 a->hidden_dim);
   if (!aligned16(a->hidden) || !aligned16(a->w) || !aligned16(a->out))
     return fail(CSA2_ERR_ALIGN, "csa2_kv_project: hidden, w, out must be 16-B aligned");
