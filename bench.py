@@ -60,6 +60,7 @@ INDEX_PAIR_FLOP = 2 * 32 * 128           # one (query, entry) pair of the indexe
 PREFILL_PREFIX, PREFILL_T, PREFILL_M = 1 << 18, 4096, 2
 # decode Reindex: batch 16 at 1M context, 2048-block x 8 pools
 REINDEX_B, REINDEX_N = 16, 1 << 20
+REINDEX_POOLS = 6
 
 
 def _scan_traffic_per_key():
@@ -282,6 +283,10 @@ def cpu_baseline(path: str, budget: float) -> dict:
         "model": cpu_model(), "value_1thread": one["keys_per_s"],
         "attn_query_layers_per_s": multi["attn_query_layers_per_s"],
         "attn_query_layers_per_s_1thread": one["attn_query_layers_per_s"],
+        # a query of the 4096-query prefill chunk scores 131,072..133,120 entries
+        # (132,096 on average), the same work per entry as the decode row sampled
+        "prefill_query_rows_per_s": multi["keys_per_s"] / 132096,
+        "prefill_chunk_s_extrapolated": 4096 * 132096 / multi["keys_per_s"],
         "sample": (f"{multi['index_rows']} x one decoder Full-layer row prefix of 131072 entries (score + top-512 + "
                    f"pool) and {multi['attn_rows']} x one attention query-layer (64 heads, 128 SWA + 512 main keys, "
                    f"sink), float64 numpy oracle"),
@@ -292,21 +297,34 @@ def cpu_baseline(path: str, budget: float) -> dict:
 # GPU measurement helpers
 # ---------------------------------------------------------------------------
 
-def _time_calls(fn, iters: int, stream, warm: int = 2) -> float:
-    """Average ms of fn() over iters back-to-back calls on the stream (CUDA events)."""
+def _time_calls(fn, iters: int, stream, warm: int = 2, replays: int = 7) -> float:
+    """Device time in ms of one fn() call: iters back-to-back calls captured in
+    one CUDA graph (so host launch overhead does not starve the GPU), replayed
+    `replays` times, median replay over iters (CUDA events on the stream)."""
     import torch
+    torch.cuda.synchronize()   # inputs made on other streams are complete
     with torch.cuda.stream(stream):
         for _ in range(warm):
             fn()
     stream.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        e0.record(stream)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
         for _ in range(iters):
             fn()
-        e1.record(stream)
+    with torch.cuda.stream(stream):
+        g.replay()
     stream.synchronize()
-    return e0.elapsed_time(e1) / iters
+    runs = []
+    for _ in range(replays):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            g.replay()
+            e1.record(stream)
+        stream.synchronize()
+        runs.append(e0.elapsed_time(e1) / iters)
+    del g
+    return statistics.median(runs)
 
 
 def prefill_case(dev, seed=300):
@@ -356,17 +374,27 @@ def reindex_case(dev, seed=200):
     iq = W.make_indexer_query(B, seed=seed + 1, device=dev)
     dirs = (iq.w[:, :, None] * iq.q_float).sum(dim=1)
     pc = W.make_paged_cache(lengths, seed=seed, device=dev, plant_dirs=dirs, plant_frac=0.1, plant_shift=3.0)
-    pool = W.make_pool(lengths, seed=seed + 2, device=dev)
+    # REINDEX_POOLS different pools (and their selections) are cycled through,
+    # so that the candidate blocks one call reads (34.6 MB) were last read
+    # REINDEX_POOLS - 1 calls earlier and L2 (129 MB) no longer holds them
+    pools = [W.make_pool(lengths, seed=seed + 2 + 97 * j, device=dev) for j in range(REINDEX_POOLS)]
     layers = [W.make_attn_layer(B, seed=seed + 10 + i, device=dev) for i in range(4)]
     r = csa2.rows(B, B, n_visible=pc.n_entries)
-    pos = torch.empty(B, 512, dtype=torch.int32, device=dev)
-    slot = torch.empty_like(pos)
+    pos = [torch.empty(B, 512, dtype=torch.int32, device=dev) for _ in pools]
+    slot = [torch.empty_like(p_) for p_ in pos]
     outs = [torch.empty(B, 64, 512, dtype=torch.bfloat16, device=dev) for _ in layers]
-    calls = {"reindex": lambda: csa2.reindex(iq.q_fp8, iq.q_scale, iq.w, pc.index_k, pc.page_table, r, pool, 512,
-                                             pos, slot)}
+    turn = {"reindex": 0, **{f"attn{i}": 0 for i in range(4)}}
+
+    def nxt(name):
+        j = turn[name] % REINDEX_POOLS
+        turn[name] += 1
+        return j
+
+    calls = {"reindex": lambda: (lambda j: csa2.reindex(iq.q_fp8, iq.q_scale, iq.w, pc.index_k, pc.page_table, r,
+                                                        pools[j], 512, pos[j], slot[j]))(nxt("reindex"))}
     for i, (al, o_) in enumerate(zip(layers, outs)):
-        calls[f"attn{i}"] = (lambda al=al, o_=o_, i=i: csa2.sparse_attn(al.q, pc.main_kv, slot, al.swa_kv,
-                                                                       al.swa_slot, al.sink, o_, kv_ready=i > 0))
+        calls[f"attn{i}"] = (lambda al=al, o_=o_, i=i: (lambda j: csa2.sparse_attn(
+            al.q, pc.main_kv, slot[j], al.swa_kv, al.swa_slot, al.sink, o_, kv_ready=i > 0))(nxt(f"attn{i}")))
     keys = int(sum(min(n, W.POOL_BLOCKS * W.POOL_BLOCK) for _ in range(B)))
     return calls, dict(rows=B, keys=keys)
 
@@ -391,7 +419,7 @@ def measure_prefill(dev, stream, iters: int, peak_fp8: float, peak_fp8_sust: flo
             "achieved": achieved, "peak": peak_fp8, "unit": "TFLOP/s", "frac": achieved / peak_fp8,
             "frac_vs_sustained": achieved / peak_fp8_sust,
             "peak_source": "FP8 dense = 2 x the measured bf16 burst (nominal FP8:BF16 ratio); sustained likewise",
-            "flop_per_launch": info["flop"], "avg_launch_ms": ms["index_score"], "launches_timed": iters,
+            "flop_per_launch": info["flop"], "avg_launch_ms": ms["index_score"], "launches_timed": iters * 7,
             "traffic": None},
         "prefill_chunk": {
             "workload": "prefill chunk: 4096 queries after a 256K-token prefix, m=2",
@@ -408,8 +436,11 @@ def measure_reindex(dev, stream, iters: int, hbm_peak: float) -> dict:
     import torch
     calls, info = reindex_case(dev)
     with torch.cuda.stream(stream):
-        for fn in calls.values():
-            fn()
+        for _ in range(REINDEX_POOLS):   # every pool's selection, before any attention reads it
+            calls["reindex"]()
+        for name, fn in calls.items():
+            if name != "reindex":
+                fn()
     stream.synchronize()
     ms = {name: _time_calls(fn, iters, stream) for name, fn in calls.items()}
     attn = statistics.mean(ms[f"attn{i}"] for i in range(4))
@@ -421,7 +452,9 @@ def measure_reindex(dev, stream, iters: int, hbm_peak: float) -> dict:
         "workload": "decode Reindex at 1M context, batch 16 x 16384 pool candidates, 10% planted blocks",
         "keys_per_s": info["keys"] / (ms["reindex"] / 1e3), "achieved": gbs, "peak": hbm_peak, "unit": "GB/s",
         "frac": gbs / hbm_peak, "algorithmic_bytes_per_launch": info["keys"] * INDEX_KEY_BYTES,
-        "avg_launch_ms": ms["reindex"], "launches_timed": iters, "traffic": None,
+        "avg_launch_ms": ms["reindex"], "launches_timed": iters * 7, "traffic": None,
+        "timing": (f"CUDA graph of {iters} calls replayed 7 times, median; {REINDEX_POOLS} pools cycled so the "
+                   "candidate blocks are not L2-resident"),
         "attn_avg_launch_ms": attn, "attn_query_layers_per_s": REINDEX_B / (attn / 1e3),
         "attn_hbm_frac": ATTN_ROW_BYTES * REINDEX_B / (attn / 1e3) / 1e9 / hbm_peak}}
 
@@ -472,7 +505,7 @@ def run_case(args):
     from serving_lightning_indexer_gb300 import csa2
     from serving_lightning_indexer_gb300 import workloads as W
     dev = torch.device("cuda:0")
-    st = torch.cuda.current_stream()
+    st = torch.cuda.Stream(device=dev)   # graph capture needs a non-default stream
     B, n = args.batch, args.entries
     res = {"case": args.case}
     if args.case in ("scan", "topk", "reindex"):

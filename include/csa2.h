@@ -238,15 +238,6 @@ typedef struct {
   float* pool_scores;                          /* optional [T, 8*pool_n] */
   int32_t index_k_format;                      /* CSA2_INDEX_FP8 (0) or CSA2_INDEX_FP4 */
   int32_t order;                               /* CSA2_ORDER_POSITION (0) or CSA2_ORDER_SCORE (1) */
-  /* 1: rows, pool_blocks, page_table and index_k were written at least two
-   * launches before this call on the stream (a Reindex layer reads its group's
-   * Full-layer caches and pool), so the candidate blocks are located and
-   * prefetched into L2 before the previous launch completes; q_fp8, q_scale
-   * and w are still read after it.  The two launches before the call must be
-   * ordinary launches or kernels that signal their dependents only after their
-   * own dependency wait (as every kernel of this library does).  0: everything
-   * is read after the previous launch. */
-  int32_t kv_ready;
 } csa2_reindex_args;
 CSA2_API int csa2_reindex(const csa2_reindex_args* args, void* workspace, size_t ws_bytes, void* stream);
 

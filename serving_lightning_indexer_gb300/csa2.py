@@ -47,7 +47,7 @@ class ReindexArgs(C.Structure):
     _fields_ = [("q_fp8", _P), ("q_scale", _P), ("w", _P), ("index_k", _P), ("index_k_pages", _I64),
                 ("page_table", _P), ("pt_stride", _I32), ("rows", Rows), ("pool_blocks", _P), ("pool_n", _I32),
                 ("k", _I32), ("topk_pos", _P), ("topk_slot", _P), ("ld_topk", _I64), ("pool_scores", _P),
-                ("index_k_format", _I32), ("order", _I32), ("kv_ready", _I32)]
+                ("index_k_format", _I32), ("order", _I32)]
 
 
 class SparseAttnArgs(C.Structure):
@@ -220,13 +220,12 @@ def topk_with_candidates_noalloc(scores, r: Rows, k, topk_pos, topk_slot=None, p
 
 
 def reindex(q_fp8, q_scale, w, index_k, page_table, r: Rows, pool_blocks, k, topk_pos, topk_slot=None,
-            pool_scores=None, stream=None, ws=None, order=0, kv_ready=False):
+            pool_scores=None, stream=None, ws=None, order=0):
     """Pool-only rescoring and top-k of a Reindex layer (csa2_reindex)."""
     lib = load()
     a = ReindexArgs(_ptr(q_fp8), _ptr(q_scale), _ptr(w), _ptr(index_k), index_k.shape[0], _ptr(page_table),
                     page_table.shape[-1], r, _ptr(pool_blocks), pool_blocks.shape[-1], k, _ptr(topk_pos),
-                    _ptr(topk_slot), topk_pos.shape[-1], _ptr(pool_scores), index_format(index_k), order,
-                    1 if kv_ready else 0)
+                    _ptr(topk_slot), topk_pos.shape[-1], _ptr(pool_scores), index_format(index_k), order)
     need = C.c_size_t(0)
     _check(lib.csa2_workspace_size(CALL_REINDEX, C.cast(C.byref(a), _P), C.byref(need)), "csa2_workspace_size")
     buf = ws if ws is not None else workspace(need.value, q_fp8.device, "reindex")

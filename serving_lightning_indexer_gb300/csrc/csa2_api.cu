@@ -321,7 +321,6 @@ int csa2_reindex(const csa2_reindex_args* a, void* ws, size_t ws_bytes, void* st
   L.ld_out = static_cast<long long>(a->pool_n) * 8;
   L.pool_blocks = a->pool_blocks;
   L.pool_n = a->pool_n;
-  L.kv_ready = a->kv_ready != 0;
   const char* why = "launch";
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   e = csa2::launch_index_tiles(L, 1, 1, ctx, st, &why);

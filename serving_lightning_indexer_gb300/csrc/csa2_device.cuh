@@ -104,10 +104,6 @@ __device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* m
       : "memory");
 }
 // Untiled bulk copy global -> shared (16-B aligned addresses, size multiple of 16).
-// Prefetch of [gsrc, gsrc + bytes) into L2 (16-B aligned, bytes a multiple of 16).
-__device__ __forceinline__ void bulk_prefetch_l2(const void* gsrc, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(gsrc), "r"(bytes) : "memory");
-}
 __device__ __forceinline__ void bulk_load(void* smem_dst, const void* gsrc, uint32_t bytes, uint64_t* bar,
                                           uint64_t policy) {
   asm volatile(

@@ -64,7 +64,6 @@ struct IndexLaunch {
   const int* pool_blocks;
   int pool_n;
   int fp4;  // index-K pages: 0 FP8 (8448 B), 1 FP4 (4352 B)
-  int kv_ready;  // gather: rows, pool, page table and index-K were written two launches back or earlier
 };
 cudaError_t launch_index_tiles(const IndexLaunch& a, int mode, int nq, const DeviceCtx& ctx, cudaStream_t st,
                                const char** why);

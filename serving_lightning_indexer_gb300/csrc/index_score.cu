@@ -63,7 +63,6 @@ struct IdxParams {
   const int* pool_blocks;
   int pool_n;
   uint32_t* err;
-  int kv_ready;    // gather: the candidate blocks may be located and prefetched before the dependency wait
 };
 
 constexpr int kHistBins = 2048;  // top 11 bits of the order-preserving key
@@ -226,17 +225,8 @@ __global__ void __launch_bounds__(kThreads, IdxCfg<NQ, F4>::kCtasPerSm)
     tmem_alloc(s_tmem, Cfg::kTmemCols);
     tmem_relinquish();
   }
-  // Global memory is touched only after the previous kernel completed, except
-  // in a gather whose rows, pool, page table and index-K pages were written at
-  // least two launches back (a Reindex layer reads the caches and pool of its
-  // group's Full layer): then the CTA locates its candidate blocks and pulls
-  // them into L2 while the previous kernel still runs, and waits before it
-  // reads the query.
-  const bool early = MODE == kModeGather && p.kv_ready;
-  if (!early) {
-    pdl_wait();
-    pdl_trigger();
-  }
+  pdl_wait();  // global memory is touched only after the previous kernel completed
+  pdl_trigger();
   for (int i = threadIdx.x; i < nqb; i += blockDim.x) s_prefix[i + 1] = qb_tiles<NQ, MODE>(p, i, &s_seq[i], &s_emax[i]);
   __syncthreads();
   if (warp == 0) {  // inclusive scan of the tile counts by one warp
@@ -264,24 +254,6 @@ __global__ void __launch_bounds__(kThreads, IdxCfg<NQ, F4>::kCtasPerSm)
   const long long total = s_prefix[nqb];
   const long long g_begin = total * blockIdx.x / gridDim.x;
   const long long g_end = total * (blockIdx.x + 1) / gridDim.x;
-  if (early) {
-    if (warp == 0) {  // one candidate block (codes, then scales) per lane, two tiles a pass
-      constexpr uint32_t kCodeBytes = F4 ? 64 : kRowBytes;  // per key
-      for (long long gl = g_begin + lane / 16; gl < g_end; gl += 2) {
-        const int qbl = find_qb(s_prefix, nqb, gl);
-        const int cb = static_cast<int>(gl - s_prefix[qbl]) * 16 + (lane & 15);
-        const int blk = (cb < p.pool_n) ? __ldg(p.pool_blocks + static_cast<long long>(qbl) * p.pool_n + cb) : -1;
-        if (blk < 0 || blk * 8 >= s_emax[qbl] || (blk >> 3) >= p.pt_stride) continue;
-        const int phys = __ldg(p.page_table + static_cast<long long>(s_seq[qbl]) * p.pt_stride + (blk >> 3));
-        if (phys < 0 || phys >= p.n_pages) continue;  // reported by the producer
-        const uint8_t* page = p.index_k + static_cast<long long>(phys) * Fmt::kBytes;
-        bulk_prefetch_l2(page + (blk & 7) * 8 * kCodeBytes, 8 * kCodeBytes);
-        bulk_prefetch_l2(page + Fmt::kScaleOff + (blk & 7) * 8 * 4, 32);
-      }
-    }
-    pdl_wait();
-    pdl_trigger();
-  }
 
   if (g_begin < g_end) {
     if (warp == 0) {
@@ -815,7 +787,6 @@ cudaError_t launch_variant(const IndexLaunch& a, const DeviceCtx& ctx, cudaStrea
   p.pool_blocks = a.pool_blocks;
   p.pool_n = a.pool_n;
   p.err = ctx.err;
-  p.kv_ready = a.kv_ready;
   if (a.hist && NQ != 1) {
     *why = "score histograms are produced on the decode and Reindex paths only";
     return cudaErrorInvalidValue;

@@ -193,10 +193,8 @@ class DecodeStep:
                                           b.pool if ci == 3 else None, stream=stream, hist=b.hist)
                 del sc, bm
             elif role == "reindex":
-                # the pool, the cache and the rows were written by layer 20's calls, many
-                # launches back: the candidate blocks are prefetched early
                 csa2.reindex(li.iq.q_fp8, li.iq.q_scale, li.iq.w, c.pc.index_k, c.pc.page_table, self.rows[ci],
-                             b.pool, W.TOPK, b.topk_pos, b.topk_slot[ci], stream=stream, kv_ready=True)
+                             b.pool, W.TOPK, b.topk_pos, b.topk_slot[ci], stream=stream)
             at = li.attn
             # a Reuse layer's slots and caches were written by its Full or Reindex
             # layer's calls, at least two launches back: its keys are gathered early

@@ -130,9 +130,8 @@ def test_end_to_end_selection_from_cache():
         assert set((np_(pos[b]) // 8).tolist()) <= set(p.tolist())
 
 
-@pytest.mark.parametrize("kv_ready", [False, True])
 @pytest.mark.parametrize("lengths", [[3000, 16384], [40000, 1_000_003]])
-def test_reindex_matches_oracle(lengths, kv_ready):
+def test_reindex_matches_oracle(lengths):
     dev = need_gpu()
     B = len(lengths)
     pc = W.make_paged_cache(lengths, seed=13, device=dev, with_main=False)
@@ -143,8 +142,7 @@ def test_reindex_matches_oracle(lengths, kv_ready):
     pos = torch.empty(B, 512, dtype=torch.int32, device=dev)
     slot = torch.empty(B, 512, dtype=torch.int32, device=dev)
     ps = torch.empty(B, 2048 * 8, dtype=torch.float32, device=dev)
-    csa2.reindex(iq.q_fp8, iq.q_scale, iq.w, pc.index_k, pc.page_table, r, pool, 512, pos, slot, ps,
-                 kv_ready=kv_ready)
+    csa2.reindex(iq.q_fp8, iq.q_scale, iq.w, pc.index_k, pc.page_table, r, pool, 512, pos, slot, ps)
     torch.cuda.synchronize()
     assert csa2.check_device_error() == 0
     cache, pt = np_(pc.index_k), np_(pc.page_table)
@@ -248,8 +246,7 @@ def test_reindex_fp4_index_keys_match_oracle():
     pos = torch.empty(B, 512, dtype=torch.int32, device=dev)
     slot = torch.empty(B, 512, dtype=torch.int32, device=dev)
     ps = torch.empty(B, 2048 * 8, dtype=torch.float32, device=dev)
-    csa2.reindex(iq.q_fp8, iq.q_scale, iq.w, pc.index_k, pc.page_table, r, pool, 512, pos, slot, ps,
-                 kv_ready=kv_ready)
+    csa2.reindex(iq.q_fp8, iq.q_scale, iq.w, pc.index_k, pc.page_table, r, pool, 512, pos, slot, ps)
     torch.cuda.synchronize()
     assert csa2.check_device_error() == 0
     cache, pt = np_(pc.index_k), np_(pc.page_table)
@@ -331,35 +328,3 @@ def test_reindex_best_first_order():
         best = sel[np.lexsort((sel, -full[sel].astype(np.float64)))]
         assert p1[b][:len(best)].tolist() == best.tolist(), f"row {b}"
 
-
-@pytest.mark.parametrize("fp4", [False, True])
-def test_reindex_prefetched_candidates_give_the_same_result(fp4):
-    """kv_ready = 1 (candidate blocks located and prefetched before the
-    dependency wait) after two unrelated launches: the same scores, positions
-    and slots as kv_ready = 0, bit for bit, with pool entries that are -1,
-    beyond the visible entries, or in the newest block."""
-    dev = need_gpu()
-    lengths = [70_001, 16_384 * 5 + 3, 900]
-    B = len(lengths)
-    pc = W.make_paged_cache(lengths, seed=51, device=dev, with_main=False, index_fp4=fp4)
-    iq = W.make_indexer_query(B, seed=52, device=dev)
-    pool = W.make_pool(lengths, seed=53, device=dev)
-    pool[0, 5] = -1
-    pool[1, 7] = (lengths[1] + 7) // 8 + 40      # beyond the visible entries: -inf candidates
-    r = csa2.rows(B, B, n_visible=torch.tensor(lengths, dtype=torch.int32, device=dev))
-    ld = (max(lengths) + 127) // 128 * 128
-    scores = torch.empty(B, ld, dtype=torch.float32, device=dev)
-    res = []
-    for ready in (False, True):
-        pos = torch.full((B, 512), -7, dtype=torch.int32, device=dev)
-        slot = torch.full((B, 512), -7, dtype=torch.int32, device=dev)
-        ps = torch.full((B, 2048 * 8), 7.0, dtype=torch.float32, device=dev)
-        for _ in range(2):   # two launches in front that touch none of the call's inputs
-            csa2.index_score(iq.q_fp8, iq.q_scale, iq.w, pc.index_k, pc.page_table, r, scores)
-        csa2.reindex(iq.q_fp8, iq.q_scale, iq.w, pc.index_k, pc.page_table, r, pool, 512, pos, slot, ps,
-                     kv_ready=ready)
-        res.append((np_(pos), np_(slot), np_(ps)))
-    torch.cuda.synchronize()
-    assert csa2.check_device_error() == 0
-    for a, b in zip(*res):
-        assert np.array_equal(a, b)
