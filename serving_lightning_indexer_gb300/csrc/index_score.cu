@@ -652,10 +652,16 @@ __global__ void __launch_bounds__(kThreads, IdxCfg<NQ, F4>::kCtasPerSm)
           float acc0 = 0.f, acc1 = 0.f;
           if constexpr (F4) {
             // q . k = sum over the 4 blocks of 2^(u_b - 127) * (q . e2m1 codes of
-            // block b); 16 heads at a time
-            float sb[4];
+            // block b); 16 heads at a time, two heads per packed fp32x2 FMA (each
+            // element rounded as by fmaf: the same values as one head at a time)
+            uint64_t sb[4];
 #pragma unroll
-            for (int b = 0; b < 4; ++b) sb[b] = ue8m0_to_float((ub >> (8 * b)) & 0xFFu);
+            for (int b = 0; b < 4; ++b) {
+              const float f = ue8m0_to_float((ub >> (8 * b)) & 0xFFu);
+              sb[b] = pack_f32x2(f, f);
+            }
+            const uint64_t nz = pack_f32x2(-0.f, -0.f);  // x * y + (-0) == x * y, zeros' signs included
+            uint64_t acc = pack_f32x2(0.f, 0.f);        // heads 2i (low) and 2i + 1 (high)
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh) {
               // the four blocks' loads are issued together, then one wait
@@ -664,23 +670,20 @@ __global__ void __launch_bounds__(kThreads, IdxCfg<NQ, F4>::kCtasPerSm)
               for (int b = 0; b < 4; ++b) tmem_ld32x16_async(tq + b * 32 + hh * 16, d[b]);
 #pragma unroll
               for (int b = 0; b < 4; ++b) tmem_wait_ld16(d[b]);
-              float v[16];
 #pragma unroll
-              for (int i = 0; i < 16; ++i) {
-                v[i] = __uint_as_float(d[0][i]) * sb[0];
-                v[i] = fmaf(__uint_as_float(d[1][i]), sb[1], v[i]);
-                v[i] = fmaf(__uint_as_float(d[2][i]), sb[2], v[i]);
-                v[i] = fmaf(__uint_as_float(d[3][i]), sb[3], v[i]);
-              }
-#pragma unroll
-              for (int h4 = 0; h4 < 4; ++h4) {
-                const float4 ww = w4[4 * hh + h4];
-                acc0 = fmaf(ww.x, fmaxf(v[4 * h4 + 0], 0.f), acc0);
-                acc1 = fmaf(ww.y, fmaxf(v[4 * h4 + 1], 0.f), acc1);
-                acc0 = fmaf(ww.z, fmaxf(v[4 * h4 + 2], 0.f), acc0);
-                acc1 = fmaf(ww.w, fmaxf(v[4 * h4 + 3], 0.f), acc1);
+              for (int i = 0; i < 16; i += 2) {
+                uint64_t x = fma_f32x2(pack_f32x2(__uint_as_float(d[0][i]), __uint_as_float(d[0][i + 1])), sb[0], nz);
+                x = fma_f32x2(pack_f32x2(__uint_as_float(d[1][i]), __uint_as_float(d[1][i + 1])), sb[1], x);
+                x = fma_f32x2(pack_f32x2(__uint_as_float(d[2][i]), __uint_as_float(d[2][i + 1])), sb[2], x);
+                x = fma_f32x2(pack_f32x2(__uint_as_float(d[3][i]), __uint_as_float(d[3][i + 1])), sb[3], x);
+                const float2 v = unpack_f32x2(x);
+                const float2 ww = reinterpret_cast<const float2*>(w4)[8 * hh + i / 2];
+                acc = fma_f32x2(pack_f32x2(fmaxf(v.x, 0.f), fmaxf(v.y, 0.f)), pack_f32x2(ww.x, ww.y), acc);
               }
             }
+            const float2 a2 = unpack_f32x2(acc);
+            acc0 = a2.x;
+            acc1 = a2.y;
           } else {
             float v[32];
             tmem_ld32(tq + j * 32, v);
