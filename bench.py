@@ -703,54 +703,76 @@ def main():
 
     # ---- end to end: pinned host inputs -> device, step, outputs -> pinned host.
     # Every step copies all of its query-side inputs in and all 38 attention
-    # outputs out.  The copies run on two copy streams: layer l waits only for
-    # its own inputs, and its output is read back while later layers compute;
-    # the next step starts after the last read-back.
-    in_by_layer, h2d, host_out = {}, 0, {}
+    # outputs out.  The inputs of all layers sit in one pinned host buffer; on
+    # the device there are two such buffers, and the step's input tensors are
+    # views into the one of the current step.  While step k computes, step
+    # k + 1's inputs are copied into the other buffer, so no layer of a step
+    # waits on a copy (a wait between two kernels of the step would cut their
+    # programmatic overlap); the first step's copy runs before it.  Each
+    # layer's output is read back on a second copy stream while later layers
+    # compute; the next step starts after the last read-back.
+    layout, off = [], 0
     for l in step.layers:
         li = step.inputs[l]
-        ts = [li.attn.q]
+        fields = [(li.attn, "q")]
         if li.iq is not None:
-            ts += [li.iq.q_fp8, li.iq.q_scale, li.iq.w]
+            fields += [(li.iq, "q_fp8"), (li.iq, "q_scale"), (li.iq, "w")]
         if li.C is not None:
-            ts += [li.C] + ([li.Z] if li.Z is not None else [])
-        in_by_layer[l] = [(t.detach().cpu().pin_memory(), t) for t in ts]
-        h2d += sum(t.numel() * t.element_size() for t in ts)
-        host_out[l] = step.buf.out[l].detach().cpu().pin_memory()
+            fields += [(li, "C")] + ([(li, "Z")] if li.Z is not None else [])
+        for obj, name in fields:
+            t = getattr(obj, name)
+            nb = t.numel() * t.element_size()
+            layout.append((obj, name, t, off, nb))
+            off = (off + nb + 255) // 256 * 256
+    dbufs = [torch.empty(off, dtype=torch.uint8, device=dev) for _ in range(2)]
+    hbuf = torch.empty(off, dtype=torch.uint8).pin_memory()
+    views = [[], []]
+    for obj, name, t, o, nb in layout:
+        hbuf[o:o + nb].copy_(t.detach().contiguous().cpu().view(torch.uint8).reshape(-1))
+        for k in range(2):
+            view = dbufs[k][o:o + nb].view(t.dtype).view(t.shape)
+            view.copy_(t)
+            views[k].append((obj, name, view))
+    h2d = off
+    host_out = {l: step.buf.out[l].detach().cpu().pin_memory() for l in step.layers}
     d2h = sum(t.numel() * t.element_size() for t in host_out.values())
     cp_in = torch.cuda.Stream(device=dev)
     cp_out = torch.cuda.Stream(device=dev)
     Ke = max(1, min(K, 20))
+
+    def load_inputs(k):
+        """Copy a step's inputs into buffer k % 2 on cp_in, after the work so far on the stream."""
+        mark = torch.cuda.Event()
+        mark.record(stream)
+        cp_in.wait_event(mark)
+        with torch.cuda.stream(cp_in):
+            dbufs[k % 2].copy_(hbuf, non_blocking=True)
+            done = torch.cuda.Event()
+            done.record(cp_in)
+        return done
+
+    def after(l):
+        done = torch.cuda.Event()
+        done.record(stream)
+        cp_out.wait_event(done)
+        with torch.cuda.stream(cp_out):
+            host_out[l].copy_(step.buf.out[l], non_blocking=True)
+
     g2 = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g2, stream=stream):
-        for _ in range(Ke):
-            begin = torch.cuda.Event()
-            begin.record(stream)
-            cp_in.wait_event(begin)
-            ready = {}
-            with torch.cuda.stream(cp_in):
-                for l in step.layers:
-                    for h, d in in_by_layer[l]:
-                        d.copy_(h, non_blocking=True)
-                    ready[l] = torch.cuda.Event()
-                    ready[l].record(cp_in)
-
-            def before(l, ready=ready):
-                stream.wait_event(ready[l])
-
-            def after(l):
-                done = torch.cuda.Event()
-                done.record(stream)
-                cp_out.wait_event(done)
-                with torch.cuda.stream(cp_out):
-                    host_out[l].copy_(step.buf.out[l], non_blocking=True)
-
-            step.before_layer, step.after_layer = before, after
+        ready = load_inputs(0)
+        for k in range(Ke):
+            stream.wait_event(ready)             # this step's inputs are in its buffer
+            if k + 1 < Ke:
+                ready = load_inputs(k + 1)       # the next step's, while this one computes
+            for obj, name, view in views[k % 2]:
+                setattr(obj, name, view)
+            step.after_layer = after
             step.run(stream)
             finished = torch.cuda.Event()
             finished.record(cp_out)
             stream.wait_event(finished)
-        step.before_layer = step.after_layer = None
+        step.after_layer = None
     with torch.cuda.stream(stream):
         g2.replay()
     stream.synchronize()
