@@ -527,9 +527,9 @@ __global__ void __launch_bounds__(kFinalThreads, 1) sel_final_kernel(const __gri
     for (int i = tid; i < kBins / 4; i += blockDim.x) hb[i] = make_uint4(0u, 0u, 0u, 0u);
   }
 
-  // 1. the 2048-bin histogram of the top 11 key bits: the caller's (scan or
-  //    gather epilogue) or the hist pass's, else built here from the values of
-  //    a short row (kept in registers)
+  // 1. the 2048-bin histogram of the top 11 key bits: the caller's (the
+  //    scan's) or the hist pass's, else built here from the values of a short
+  //    row (kept in registers)
   int mode;  // 0: short row, 1: candidate list, 2: overflowed candidate list (stream the row)
   uint32_t ord[kPerThread];  // direct rows: elements e0 .. e0 + kPerThread - 1 of this thread
   const int e0 = tid * kPerThread;
