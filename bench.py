@@ -661,15 +661,24 @@ def main():
         join.record(side)
         stream.wait_event(join)
     step.on_index_score = step.after_index_score = step.on_attn = step.after_attn = None
+    # the same K steps without the timing events: the step time comes from this
+    # graph (the event nodes of the other cost ~1 % of the step)
+    g_plain = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_plain, stream=stream):
+        for _ in range(K):
+            step.run(stream)
     with torch.cuda.stream(stream):
-        g.replay()                   # untimed: first replay of the instantiated graph
+        g.replay()                   # untimed: first replays of the instantiated graphs
+        g_plain.replay()
     stream.synchronize()
 
-    # ---- timed region: replays of the K-step graph until min_seconds have passed
+    # ---- timed region: replays of the K-step graph until min_seconds have
+    # passed; each round replays the plain graph (the step time) and the graph
+    # with the timing events (the scan and attention launch times)
     sampler = ClockSampler(local)
     if rank == 0:
         sampler.start()
-    replay_ms, scan_ms, attn_ms, per_layer = [], [], [], {}
+    replay_ms, marked_ms, scan_ms, attn_ms, per_layer = [], [], [], [], {}
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     sampler.mark(True)
@@ -680,11 +689,17 @@ def main():
         torch.cuda.synchronize()
         with torch.cuda.stream(stream):  # the graph replays on the current stream
             t_start.record(stream)
-            g.replay()
+            g_plain.replay()
             t_end.record(stream)
         stream.synchronize()
         torch.cuda.synchronize()
         replay_ms.append(t_start.elapsed_time(t_end))
+        with torch.cuda.stream(stream):
+            t_start.record(stream)
+            g.replay()
+            t_end.record(stream)
+        stream.synchronize()
+        marked_ms.append(t_start.elapsed_time(t_end))
         for l, a, b in ev_pairs:
             ms = a.elapsed_time(b)
             scan_ms.append(ms)
@@ -707,10 +722,11 @@ def main():
     # the device there are two such buffers, and the step's input tensors are
     # views into the one of the current step.  While step k computes, step
     # k + 1's inputs are copied into the other buffer, so no layer of a step
-    # waits on a copy (a wait between two kernels of the step would cut their
-    # programmatic overlap); the first step's copy runs before it.  Each
-    # layer's output is read back on a second copy stream while later layers
-    # compute; the next step starts after the last read-back.
+    # waits on a copy (a wait or an event between two kernels of the step would
+    # cut their programmatic overlap); the first step's copy runs before it.
+    # Likewise the outputs go to one of two device buffers and a step's are
+    # read back in one copy while the next step computes; the last step's
+    # read-back ends the timed replay.
     layout, off = [], 0
     for l in step.layers:
         li = step.inputs[l]
@@ -734,8 +750,14 @@ def main():
             view.copy_(t)
             views[k].append((obj, name, view))
     h2d = off
-    host_out = {l: step.buf.out[l].detach().cpu().pin_memory() for l in step.layers}
-    d2h = sum(t.numel() * t.element_size() for t in host_out.values())
+    # the 38 outputs of a step in one buffer (two, alternating by step): a
+    # step's outputs are read back in one copy while the next step computes
+    o0 = step.buf.out[step.layers[0]]
+    obufs = [torch.empty((len(step.layers),) + tuple(o0.shape), dtype=o0.dtype, device=dev) for _ in range(2)]
+    oviews = [{l: ob[i] for i, l in enumerate(step.layers)} for ob in obufs]
+    host_obuf = torch.empty(tuple(obufs[0].shape), dtype=o0.dtype).pin_memory()
+    d2h = obufs[0].numel() * obufs[0].element_size()
+    out_orig = step.buf.out
     cp_in = torch.cuda.Stream(device=dev)
     cp_out = torch.cuda.Stream(device=dev)
     Ke = max(1, min(K, 20))
@@ -751,28 +773,29 @@ def main():
             done.record(cp_in)
         return done
 
-    def after(l):
-        done = torch.cuda.Event()
-        done.record(stream)
-        cp_out.wait_event(done)
-        with torch.cuda.stream(cp_out):
-            host_out[l].copy_(step.buf.out[l], non_blocking=True)
-
     g2 = torch.cuda.CUDAGraph()
+    read_back = [None, None]
     with torch.cuda.graph(g2, stream=stream):
         ready = load_inputs(0)
         for k in range(Ke):
             stream.wait_event(ready)             # this step's inputs are in its buffer
+            if read_back[k % 2] is not None:     # its output buffer has been read back
+                stream.wait_event(read_back[k % 2])
             if k + 1 < Ke:
                 ready = load_inputs(k + 1)       # the next step's, while this one computes
             for obj, name, view in views[k % 2]:
                 setattr(obj, name, view)
-            step.after_layer = after
+            step.buf.out = oviews[k % 2]
             step.run(stream)
-            finished = torch.cuda.Event()
-            finished.record(cp_out)
-            stream.wait_event(finished)
-        step.after_layer = None
+            end = torch.cuda.Event()
+            end.record(stream)
+            cp_out.wait_event(end)
+            with torch.cuda.stream(cp_out):      # this step's outputs, while the next one computes
+                host_obuf.copy_(obufs[k % 2], non_blocking=True)
+                read_back[k % 2] = torch.cuda.Event()
+                read_back[k % 2].record(cp_out)
+        stream.wait_event(read_back[(Ke - 1) % 2])   # the last step's outputs are on the host
+    step.buf.out = out_orig
     with torch.cuda.stream(stream):
         g2.replay()
     stream.synchronize()
@@ -835,10 +858,13 @@ def main():
         "config": {"workload": WORKLOAD, "batch": len(LENGTHS), "context_lengths": LENGTHS, "layers": n_layers,
                    "keys_scored_per_step": keys_per_step, "attn_query_layers_per_step": attn_per_step,
                    "timing": (f"K steps in one CUDA graph, replayed {len(replay_ms)} times over >= "
-                              f"{args.min_seconds} s, median replay; inputs larger than L2 (no flush)"),
+                              f"{args.min_seconds} s, median replay; inputs larger than L2 (no flush); "
+                              "each replay followed by one of the same steps with side-stream timing events, "
+                              "which give the per-launch scan and attention times"),
                    "parallelism": f"replicas x{world}"},
         "replays": len(replay_ms), "replay_ms": {"median": statistics.median(replay_ms), "min": min(replay_ms),
-                                                 "max": max(replay_ms)},
+                                                 "max": max(replay_ms),
+                                                 "with_timing_events_median": statistics.median(marked_ms)},
         "attn_query_layers_per_s": whole_job_rate(attn_per_step, K, world, ms_replay),
         "roofline": {"bound": "hbm", "kernel": "index_tiles_kernel<1,scan> (decode Lightning-Indexer scan)",
                      "achieved": achieved, "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
@@ -865,7 +891,7 @@ def main():
         "cpu_baseline": cpu,
         "e2e": {"value": whole_job_rate(keys_per_step, Ke, world, e2e_ms), "unit": "keys/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": Ke, "replays": len(e2e_runs)},
-        "gpu_launches": launches_per_step * K * len(replay_ms),
+        "gpu_launches": launches_per_step * K * (len(replay_ms) + len(marked_ms)),
         "gpu_launches_per_step": launches_per_step,
         "clocks": sampler.summary(),
     }
