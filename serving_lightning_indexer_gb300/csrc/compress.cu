@@ -35,7 +35,7 @@ struct CompressParams {
   const float* gamma;
   float eps;
   int apply_rope;
-  double inv_freq[32];     // theta^(-2i/64), computed on the host in double
+  uint64_t inv_freq[32];   // theta^(-2i/64) as a fixed-point turn rate (rope_turn_rate)
   long long first_entry;
   const int* entry_pos;
   uint8_t* main_kv;
@@ -117,6 +117,15 @@ __global__ void __launch_bounds__(256) compress_kernel(const __grid_constant__ C
   long long pos = 0, slot = -1;
   bool slot_ok = false;
   if (warp < EPC) {
+  // the entry's position and destination slot are requested with its tokens
+  pos = p.entry_pos ? static_cast<long long>(__ldg(p.entry_pos + e)) : (p.first_entry + e) * p.ratio_m;
+  if (p.entry_slot) {
+    slot = __ldg(p.entry_slot + e);
+  } else {
+    const long long ent = p.first_entry + e;
+    const long long lp = ent >> 6;
+    slot = (lp < p.pt_len) ? static_cast<long long>(__ldg(p.page_table + lp)) * 64 + (ent & 63) : -1;
+  }
   float x[16];
   if (p.ratio_m == 1) {
     load16_bf16(p.C + e * 512 + c0, x);
@@ -144,7 +153,6 @@ __global__ void __launch_bounds__(256) compress_kernel(const __grid_constant__ C
   float y[16];
 #pragma unroll
   for (int i = 0; i < 16; ++i) y[i] = x[i] * inv * gam[i];
-  pos = p.entry_pos ? static_cast<long long>(__ldg(p.entry_pos + e)) : (p.first_entry + e) * p.ratio_m;
   if constexpr (IK) {  // the latent before RoPE feeds the index key
 #pragma unroll
     for (int i = 0; i < 16; ++i) s_ik[(c0 + i) * EPC + warp] = y[i];
@@ -183,14 +191,6 @@ __global__ void __launch_bounds__(256) compress_kernel(const __grid_constant__ C
   for (int i = 0; i < 16; ++i) {
     const uint32_t code = e2m1_code(ldexpf(y[i], 127 - u));
     packed[i >> 3] |= code << (4 * (i & 7));
-  }
-  // destination slot
-  if (p.entry_slot) {
-    slot = __ldg(p.entry_slot + e);
-  } else {
-    const long long ent = p.first_entry + e;
-    const long long lp = ent >> 6;
-    slot = (lp < p.pt_len) ? static_cast<long long>(__ldg(p.page_table + lp)) * 64 + (ent & 63) : -1;
   }
   slot_ok = slot >= 0 && slot < p.main_slots;
   if (active && !slot_ok && lane == 0) set_error(p.err, kErrBounds);
@@ -334,7 +334,6 @@ constexpr int kPjSplit = 8;         // CTAs (slices of the hidden dimension) per
 constexpr int kPjThreads = 256;     // 64 rows x 4 column chunks of 8
 constexpr int kPjRounds = 16;       // rounds of 64 rows per batch
 constexpr int kPjBatch = 64 * kPjRounds;
-constexpr int kPjMaxT = 64;
 
 size_t kv_project_smem(int T, int hidden) {
   const int batch = min(hidden / kPjSplit, kPjBatch);
@@ -472,7 +471,7 @@ cudaError_t launch_compress(const CompressLaunch& a, const DeviceCtx& ctx, cudaS
   p.gamma = a.gamma;
   p.eps = a.eps;
   p.apply_rope = a.apply_rope;
-  for (int i = 0; i < 32; ++i) p.inv_freq[i] = pow(static_cast<double>(a.rope_theta), -2.0 * i / 64.0);
+  for (int i = 0; i < 32; ++i) p.inv_freq[i] = rope_turn_rate(static_cast<double>(a.rope_theta), i);
   p.first_entry = a.first_entry;
   p.entry_pos = a.entry_pos;
   p.main_kv = a.main_kv;

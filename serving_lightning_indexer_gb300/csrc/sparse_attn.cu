@@ -65,7 +65,7 @@ struct AttnParams {
   const int* q_pos;          // [T] query positions (inverse RoPE, bounded replay)
   const int* swa_seg_start;  // [T] bounded-replay segment starts, or null
   int inv_rope;              // rotate the output's last 64 dims back by the query's RoPE
-  double inv_freq[32];       // theta^(-2p/64)
+  uint64_t inv_freq[32];     // theta^(-2p/64) as a fixed-point turn rate (rope_turn_rate)
   uint32_t* err;
 };
 
@@ -452,7 +452,7 @@ __global__ void __launch_bounds__(512, 1) sparse_attn_kernel(const __grid_consta
       float a0 = o[nt][0] * f0, b0 = o[nt][1] * f0, a1 = o[nt][2] * f1, b1 = o[nt][3] * f1;
       if (p.inv_rope && d >= kD - 64) {  // (d, d + 1) is RoPE pair (d - 448) / 2
         const long long pos = __ldg(p.q_pos + t);
-        const double fr = p.inv_freq[(d - (kD - 64)) >> 1];
+        const uint64_t fr = p.inv_freq[(d - (kD - 64)) >> 1];
         inv_rope_pair(a0, b0, pos, fr);
         inv_rope_pair(a1, b1, pos, fr);
       }
@@ -639,7 +639,7 @@ struct TcParams {
   const int* q_pos;          // [T] query positions (inverse RoPE, bounded replay)
   const int* swa_seg_start;  // [T] bounded-replay segment starts, or null
   int inv_rope;              // rotate the output's last 64 dims back by the query's RoPE
-  double inv_freq[32];       // theta^(-2p/64)
+  uint64_t inv_freq[32];     // theta^(-2p/64) as a fixed-point turn rate (rope_turn_rate)
 };
 
 __device__ __forceinline__ int key_slot_tc(const TcParams& p, int t, int j, int* kind) {
@@ -1158,7 +1158,7 @@ static cudaError_t launch_sparse_attn_tc(const AttnLaunch& a, void* ws, const De
   p.q_pos = a.q_pos;
   p.swa_seg_start = a.swa_seg_start;
   p.inv_rope = a.inv_rope;
-  for (int i = 0; i < 32; ++i) p.inv_freq[i] = pow(static_cast<double>(a.rope_theta), -2.0 * i / 64.0);
+  for (int i = 0; i < 32; ++i) p.inv_freq[i] = rope_turn_rate(static_cast<double>(a.rope_theta), i);
   // q viewed as [T*64 rows of 1024 B]; a 128-B x 64-row box is one swizzled atom
   CUtensorMap map_q;
   if (encode_tmap_2d_u8(&map_q, a.q, static_cast<uint64_t>(kD) * 2, static_cast<uint64_t>(a.T) * kH,
@@ -1219,7 +1219,7 @@ cudaError_t launch_sparse_attn(const AttnLaunch& a, void* ws, size_t ws_bytes, c
   p.q_pos = a.q_pos;
   p.swa_seg_start = a.swa_seg_start;
   p.inv_rope = a.inv_rope;
-  for (int i = 0; i < 32; ++i) p.inv_freq[i] = pow(static_cast<double>(a.rope_theta), -2.0 * i / 64.0);
+  for (int i = 0; i < 32; ++i) p.inv_freq[i] = rope_turn_rate(static_cast<double>(a.rope_theta), i);
   const int L = a.n_swa + a.k;
   const int nchunks = (L + kCK - 1) / kCK;
   const int nsplit = attn_num_splits(a.T, L, ctx.num_sms);
