@@ -71,6 +71,26 @@ __device__ __forceinline__ void load16_bf16(const __nv_bfloat16* src, float (&v)
 
 // e2m1 code of a value already divided by its group scale: nearest magnitude
 // among 0, .5, 1, 1.5, 2, 3, 4, 6 with ties to the even code, saturating.
+// The FP4 block exponent: the smallest k with 6 * 2^k >= a, for a finite a > 0
+// (a = f * 2^ex with f in [0.5, 1): k = ex - 3 when f <= 0.75, else ex - 2),
+// read from the bits of a; frexpf for a subnormal a.
+__device__ __forceinline__ int fp4_block_exp(float a) {
+  const uint32_t b = __float_as_uint(a);
+  const int e = static_cast<int>(b >> 23);
+  if (e == 0) {
+    int ex;
+    const float f = frexpf(a, &ex);
+    return (f <= 0.75f) ? ex - 3 : ex - 2;
+  }
+  return ((b & 0x7FFFFFu) <= 0x400000u) ? e - 129 : e - 128;  // ex = e - 126; f <= 0.75 iff mantissa <= 2^22
+}
+// 2^(127 - u) for a scale byte u in 0..254, exact (2^-127 is subnormal):
+// multiplying by it equals ldexpf(v, 127 - u), rounding included.
+__device__ __forceinline__ float fp4_unscale(int u) {
+  const int e = 254 - u;
+  return e >= 1 ? __uint_as_float(static_cast<uint32_t>(e) << 23) : __uint_as_float(0x00400000u);
+}
+
 __device__ __forceinline__ uint32_t e2m1_code(float v) {
   const float a = fabsf(v);
   uint32_t c = (a > 0.25f) + (a >= 0.75f) + (a > 1.25f) + (a >= 1.75f) + (a > 2.5f) + (a >= 3.5f) + (a > 5.0f);
@@ -116,6 +136,7 @@ __global__ void __launch_bounds__(256) compress_kernel(const __grid_constant__ C
   const long long e = active ? e_raw : p.n_entries - 1;
   long long pos = 0, slot = -1;
   bool slot_ok = false;
+  float rope_sn = 0.f, rope_cs = 1.f;  // RoPE pair `lane` of the entry (below)
   if (warp < EPC) {
   // the entry's position and destination slot are requested with its tokens
   pos = p.entry_pos ? static_cast<long long>(__ldg(p.entry_pos + e)) : (p.first_entry + e) * p.ratio_m;
@@ -126,6 +147,10 @@ __global__ void __launch_bounds__(256) compress_kernel(const __grid_constant__ C
     const long long lp = ent >> 6;
     slot = (lp < p.pt_len) ? static_cast<long long>(__ldg(p.page_table + lp)) * 64 + (ent & 63) : -1;
   }
+  // RoPE pair `lane` of the entry (the latent's dims 448 + 2 lane, +1, and the
+  // index key's 64 + 2 lane, +1 turn by the same angle): one angle a lane,
+  // handed to the lanes that rotate the pair by shuffles
+  if (p.apply_rope) rope_angle(pos, p.inv_freq[lane], &rope_sn, &rope_cs);
   float x[16];
   if (p.ratio_m == 1) {
     load16_bf16(p.C + e * 512 + c0, x);
@@ -158,15 +183,16 @@ __global__ void __launch_bounds__(256) compress_kernel(const __grid_constant__ C
     for (int i = 0; i < 16; ++i) s_ik[(c0 + i) * EPC + warp] = y[i];
   }
   // RoPE on dims 448..511: interleaved pairs, angle pos * theta^(-2i/64)
-  if (p.apply_rope && lane >= 28) {
+  if (p.apply_rope) {
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-      const int i = (c0 - 448) / 2 + j;
-      float sn, cs;
-      rope_angle(pos, p.inv_freq[i], &sn, &cs);
-      const float a = y[2 * j], b = y[2 * j + 1];
-      y[2 * j] = a * cs - b * sn;
-      y[2 * j + 1] = a * sn + b * cs;
+      const int i = lane >= 28 ? (c0 - 448) / 2 + j : j;  // pair i (every lane takes part in the shuffle)
+      const float sn = __shfl_sync(0xffffffffu, rope_sn, i), cs = __shfl_sync(0xffffffffu, rope_cs, i);
+      if (lane >= 28) {
+        const float a = y[2 * j], b = y[2 * j + 1];
+        y[2 * j] = a * cs - b * sn;
+        y[2 * j + 1] = a * sn + b * cs;
+      }
     }
   }
   if (p.latent_out && active) {
@@ -180,16 +206,12 @@ __global__ void __launch_bounds__(256) compress_kernel(const __grid_constant__ C
   for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(y[i]));
   amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
   int u = 127;
-  if (amax > 0.f) {
-    int ex;
-    const float f = frexpf(amax, &ex);           // amax = f * 2^ex, f in [0.5, 1)
-    const int k = (f <= 0.75f) ? ex - 3 : ex - 2;  // smallest k with 6 * 2^k >= amax
-    u = min(max(k + 127, 0), 254);
-  }
+  if (amax > 0.f) u = min(max(fp4_block_exp(amax) + 127, 0), 254);  // smallest k with 6 * 2^k >= amax
+  const float unscale = fp4_unscale(u);
   uint32_t packed[2] = {0u, 0u};
 #pragma unroll
   for (int i = 0; i < 16; ++i) {
-    const uint32_t code = e2m1_code(ldexpf(y[i], 127 - u));
+    const uint32_t code = e2m1_code(y[i] * unscale);
     packed[i >> 3] |= code << (4 * (i & 7));
   }
   slot_ok = slot >= 0 && slot < p.main_slots;
@@ -260,14 +282,16 @@ __global__ void __launch_bounds__(256) compress_kernel(const __grid_constant__ C
   kk[1] *= inv2 * kg.y;
   kk[2] *= inv2 * kg.z;
   kk[3] *= inv2 * kg.w;
-  if (p.apply_rope && lane >= 16) {  // dims 64..127: pairs (4l, 4l+1), (4l+2, 4l+3) = pair 2l-32, 2l-31
+  if (p.apply_rope) {  // dims 64..127: pairs (4l, 4l+1), (4l+2, 4l+3) = pair 2l-32, 2l-31
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
-      float sn, cs;
-      rope_angle(pos, p.inv_freq[2 * lane - 32 + h], &sn, &cs);
-      const float a = kk[2 * h], b = kk[2 * h + 1];
-      kk[2 * h] = a * cs - b * sn;
-      kk[2 * h + 1] = a * sn + b * cs;
+      const int i = lane >= 16 ? 2 * lane - 32 + h : h;
+      const float sn = __shfl_sync(0xffffffffu, rope_sn, i), cs = __shfl_sync(0xffffffffu, rope_cs, i);
+      if (lane >= 16) {
+        const float a = kk[2 * h], b = kk[2 * h + 1];
+        kk[2 * h] = a * cs - b * sn;
+        kk[2 * h + 1] = a * sn + b * cs;
+      }
     }
   }
   if (!active) return;
@@ -297,15 +321,11 @@ __global__ void __launch_bounds__(256) compress_kernel(const __grid_constant__ C
 #pragma unroll
     for (int o = 4; o > 0; o >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
     int ue = 127;
-    if (am > 0.f) {
-      int ex;
-      const float f = frexpf(am, &ex);
-      const int k = (f <= 0.75f) ? ex - 3 : ex - 2;
-      ue = min(max(k + 127, 0), 254);
-    }
+    if (am > 0.f) ue = min(max(fp4_block_exp(am) + 127, 0), 254);
+    const float unscale = fp4_unscale(ue);
     uint32_t half = 0u;
 #pragma unroll
-    for (int j = 0; j < 4; ++j) half |= e2m1_code(ldexpf(kk[j], 127 - ue)) << (4 * j);
+    for (int j = 0; j < 4; ++j) half |= e2m1_code(kk[j] * unscale) << (4 * j);
     uint8_t* pg = p.index_k + page * 4352;
     *reinterpret_cast<uint16_t*>(pg + row * 64 + 2 * lane) = static_cast<uint16_t>(half);
     if ((lane & 7) == 0) pg[4096 + row * 4 + (lane >> 3)] = static_cast<uint8_t>(ue);
