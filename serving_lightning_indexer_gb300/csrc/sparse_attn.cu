@@ -600,8 +600,8 @@ struct TcSmem {
   static constexpr int kOffRaw = kOffP + 2 * kQAtom;            // [kTcKeys][kRawStride]
   static constexpr int kOffKind = kOffRaw + kTcKeys * kRawStride;  // int[kTcKeys]
   static constexpr int kOffStat = kOffKind + kTcKeys * 4;       // float m[64], l[64], sink[64]
-  static constexpr int kOffBar = kOffStat + 3 * kH * 4;             // raw, S done, O halves done, q
-  static constexpr int kOffTmem = kOffBar + 5 * 8;
+  static constexpr int kOffBar = kOffStat + 3 * kH * 4;             // raw, S done, O halves done, q halves
+  static constexpr int kOffTmem = kOffBar + 6 * 8;
   static constexpr int kBytes = kOffTmem + 8;
   static constexpr int kAlloc = kBytes + 1024;                  // the base is rounded up to 1024 B
   static_assert(kKAtom % 1024 == 0 && kOffK % 1024 == 0 && kOffP % 1024 == 0, "swizzle atoms are 1024-B aligned");
@@ -736,7 +736,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   uint64_t* bar_raw = reinterpret_cast<uint64_t*>(sm + TcSmem::kOffBar);
   uint64_t* bar_s = bar_raw + 1;
   uint64_t* bar_o = bar_raw + 2;  // [2]
-  uint64_t* bar_q = bar_raw + 4;  // the row's q tile
+  uint64_t* bar_q = bar_raw + 4;  // the row's q tile: dims 0-255 on bar_q[0], 256-511 on bar_q[1]
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(sm + TcSmem::kOffTmem);
 
   const int tid = threadIdx.x;
@@ -752,6 +752,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     mbar_init(bar_o, 1);
     mbar_init(bar_o + 1, 1);
     mbar_init(bar_q, 1);
+    mbar_init(bar_q + 1, 1);
     fence_mbar_init();
   }
   if (warp == 0) {
@@ -823,8 +824,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     if (wave == 1) mma_commit(bar_s);
   };
-  auto wait_q = [&]() {
-    if (!mbar_wait(bar_q, 0u, nullptr)) set_error(p.err, kErrTimeout);
+  auto wait_q = [&](int half) {  // the S MMAs of a wave need that half of q only
+    if (!mbar_wait(bar_q + half, 0u, nullptr)) set_error(p.err, kErrTimeout);
   };
 
   if (p.kv_ready) {  // the keys are ready before the previous launch completes
@@ -835,18 +836,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   }
   pdl_wait();
   pdl_trigger();
-  // the row's q: eight 64-head x 64-dim atoms, swizzled by the tensor copy
+  // the row's q: eight 64-head x 64-dim atoms, swizzled by the tensor copy,
+  // in two halves so that the first wave's S MMAs start on the first half
   if (tid == kTcMmaThread) {
-    mbar_arrive_expect_tx(bar_q, kH * kD * 2);
+    mbar_arrive_expect_tx(bar_q, kH * kD);
+    mbar_arrive_expect_tx(bar_q + 1, kH * kD);
 #pragma unroll
     for (int a = 0; a < 8; ++a)
-      tma_load_2d(sQ + a * TcSmem::kQAtom, &map_q, a * 128, t * kH, bar_q, l2_policy_evict_first());
+      tma_load_2d(sQ + a * TcSmem::kQAtom, &map_q, a * 128, t * kH, bar_q + (a >> 2), l2_policy_evict_first());
   }
   if (tid < kH) sSink[tid] = __ldg(p.sink + tid) * kLog2e;
   if (p.kv_ready) {
     if (tid == kTcMmaThread) {
-      wait_q();
+      wait_q(0);
       issue_s(0);
+      wait_q(1);
       issue_s(1);
     }
   } else {  // the first wave's S MMAs run while the second wave is dequantised
@@ -854,11 +858,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     wait_records();
     dequant_wave(0);
     if (tid == kTcMmaThread) {
-      wait_q();
+      wait_q(0);
       issue_s(0);
     }
     dequant_wave(1);
-    if (tid == kTcMmaThread) issue_s(1);
+    if (tid == kTcMmaThread) {
+      wait_q(1);
+      issue_s(1);
+    }
   }
 
   // ---- softmax of the chunk: warps 0-3, one per TMEM lane quadrant q (an
