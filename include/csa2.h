@@ -248,7 +248,11 @@ CSA2_API int csa2_reindex(const csa2_reindex_args* args, void* workspace, size_t
  *   out[t,i] = sum_j e^(logit_j - M) kv_j / (sum_j e^(logit_j - M) + e^(sink[i] - M))
  * kv_j is the dequantised 512-vector (K = V); the sink is not scaled.
  * lse[t,i] = M + ln(denominator) (natural log, sink included).
- * softmax_scale == 0 selects 1/sqrt(512).  Alignment: q, main_kv, swa_kv, out 16 B. */
+ * softmax_scale == 0 selects 1/sqrt(512).  Alignment: q, main_kv, swa_kv, out 16 B.
+ * Two kernels: while rows x ceil((n_swa + k) / 80) is at most the SM count
+ * (decode layers), each row's keys are split over a cluster of CTAs and merged
+ * through L2 in the workspace (csa2_workspace_size); beyond, split-K CTAs walk
+ * a row's keys with an online softmax and merge on chip (no workspace). */
 typedef struct {
   const uint16_t* q;                           /* [T,64,512] bf16 */
   const uint8_t* main_kv; int64_t main_kv_slots;   /* 288-B records */

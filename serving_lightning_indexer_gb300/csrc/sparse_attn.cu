@@ -1117,18 +1117,24 @@ int attn_num_splits(int T, int n_keys, int num_sms) {
 
 // The tensor-core path takes rows of 1..16 chunks (up to 1280 keys), one CTA
 // per chunk, in launches of at most kTcRowsPerLaunch rows sharing one scratch.
+// It is a latency design (a row's chunks in parallel on a cluster, merged
+// through L2): it is taken while all rows' CTAs fit one wave (rows x chunks
+// <= SMs, e.g. 8-row decode layers).  Beyond that the split-K kernel, fewer
+// CTAs a row each walking its chunks with an online softmax, measured faster
+// (640 keys a row: 28 against 31 us at 32 rows, 477 against 785 us at 1,024
+// rows, 1.84 against 3.14 ms for a 4,096-query prefill chunk; 16 against
+// 10.6 us at 8 rows).
 constexpr int kTcRowsPerLaunch = 256;
-static bool use_tc_path(int n_keys) {
+static bool use_tc_path(int T, int n_keys, int num_sms) {
   const int nchunks = (n_keys + kTcKeys - 1) / kTcKeys;
-  return nchunks >= 1 && nchunks <= kMaxCluster;
+  return nchunks >= 1 && nchunks <= kMaxCluster && static_cast<long long>(T) * nchunks <= num_sms;
 }
 static size_t tc_part_bytes(int rows, int nchunks) {
   return static_cast<size_t>(rows) * nchunks * (kPartChunkBytes + kH * sizeof(float2));
 }
 
 size_t attn_workspace_bytes(int T, int n_keys, int num_sms) {
-  (void)num_sms;
-  if (!use_tc_path(n_keys)) return 0;  // the split-K kernel merges on chip
+  if (!use_tc_path(T, n_keys, num_sms)) return 0;  // the split-K kernel merges on chip
   const int nchunks = (n_keys + kTcKeys - 1) / kTcKeys;
   const int rows = T < kTcRowsPerLaunch ? T : kTcRowsPerLaunch;
   return tc_part_bytes(rows, nchunks);
@@ -1203,7 +1209,7 @@ static cudaError_t launch_sparse_attn_tc(const AttnLaunch& a, void* ws, const De
 cudaError_t launch_sparse_attn(const AttnLaunch& a, void* ws, size_t ws_bytes, const DeviceCtx& ctx,
                                cudaStream_t st) {
   (void)ws_bytes;
-  if (use_tc_path(a.n_swa + a.k)) return launch_sparse_attn_tc(a, ws, ctx, st);
+  if (use_tc_path(a.T, a.n_swa + a.k, ctx.num_sms)) return launch_sparse_attn_tc(a, ws, ctx, st);
   AttnParams p;
   p.q = reinterpret_cast<const __nv_bfloat16*>(a.q);
   p.main_kv = a.main_kv;
