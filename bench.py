@@ -338,6 +338,8 @@ def prefill_case(dev, seed=300):
     n_tok = prefix + T
     n_ent = n_tok // m
     pc = W.make_paged_cache([n_ent], seed=seed, device=dev)
+    # the same entries' index keys as FP4 pages (scored on the per-row scan)
+    pc4 = W.make_paged_cache([n_ent], seed=seed, device=dev, with_main=False, index_fp4=True)
     Cm, Z, gamma = W.make_compress_inputs(n_tok, seed=seed + 1, device=dev)
     iq = W.make_indexer_query(T, seed=seed + 2, device=dev)
     row_pos = torch.arange(prefix, n_tok, dtype=torch.int32, device=dev)
@@ -355,9 +357,11 @@ def prefill_case(dev, seed=300):
         "index_score": lambda: csa2.index_score(iq.q_fp8, iq.q_scale, iq.w, pc.index_k, pc.page_table, r, scores),
         "topk": lambda: csa2.topk_with_candidates(scores, r, 512, pos, slot, pc.page_table),
         "attn": lambda: csa2.sparse_attn(al.q, pc.main_kv, slot, al.swa_kv, al.swa_slot, al.sink, out),
+        "index_score_fp4": lambda: csa2.index_score(iq.q_fp8, iq.q_scale, iq.w, pc4.index_k, pc4.page_table, r,
+                                                    scores),
     }
-    flop = float(sum((p + 1) // m for p in range(prefix, n_tok))) * INDEX_PAIR_FLOP
-    return calls, dict(n_entries=n_ent, tokens=n_tok, queries=T, flop=flop)
+    pairs = float(sum((p + 1) // m for p in range(prefix, n_tok)))
+    return calls, dict(n_entries=n_ent, tokens=n_tok, queries=T, flop=pairs * INDEX_PAIR_FLOP, pairs=pairs)
 
 
 def reindex_case(dev, seed=200):
@@ -409,6 +413,8 @@ def measure_prefill(dev, stream, iters: int, peak_fp8: float, peak_fp8_sust: flo
     stream.synchronize()
     ms = {name: _time_calls(calls[name], iters if name == "index_score" else max(3, iters // 4), stream)
           for name in ("compress", "index_score", "topk", "attn")}
+    # FP4 pages last (they overwrite the scores the top-k above read)
+    fp4_ms = _time_calls(calls["index_score_fp4"], 3, stream)
     achieved = info["flop"] / (ms["index_score"] / 1e3) / 1e12
     del calls
     torch.cuda.empty_cache()
@@ -427,6 +433,12 @@ def measure_prefill(dev, stream, iters: int, peak_fp8: float, peak_fp8_sust: flo
             "attn_query_layers_per_s": PREFILL_T / (ms["attn"] / 1e3),
             "entries_built_per_s": info["n_entries"] / (ms["compress"] / 1e3),
             "topk_rows_per_s": PREFILL_T / (ms["topk"] / 1e3)},
+        "prefill_index_fp4": {
+            "workload": "the same 4096 queries over FP4 index-K pages of the 133120 entries",
+            "path": "per-row scan (M = 128 keys x 32 heads a tile, 4 block accumulators; each query reads the "
+                    "keys again, from L2)",
+            "avg_launch_ms": fp4_ms, "pairs_per_s": info["pairs"] / (fp4_ms / 1e3),
+            "vs_fp8_gemm": ms["index_score"] / fp4_ms},
     }
 
 

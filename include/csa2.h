@@ -133,10 +133,13 @@ typedef struct {
  * block j (8 positions) for j < ceil(E_t / 8), if block_max is not NULL.
  * Alignment: q_fp8, index_k 16 B (32 B for FP4 pages); ld_scores and
  * ld_block_max multiples of 4.
- * Prefill (row_pos given, B == 1, T >= 64) runs the query-blocked tensor-core
- * path (8 queries x 32 heads per MMA); everything else the per-row scan.
- * FP4 index-K pages are scored on the per-row scan (CSA2_ERR_UNSUPPORTED on
- * the prefill path): k = sum over its 4 blocks of 2^(u_b-127) * e2m1 codes. */
+ * Prefill (row_pos given, B == 1, T >= 64, FP8 pages; T <= 16384) runs the
+ * query-blocked tensor-core path (8 queries x 32 heads per MMA); everything
+ * else the per-row scan (one query's 32 heads per MMA), which takes calls of
+ * any T in launches of 2048 rows (hist: T <= 2048).  FP4 index-K pages are
+ * scored on the per-row scan at every shape, prefill included (each query then
+ * reads the keys anew, from L2 for a prefill chunk):
+ * k = sum over its 4 blocks of 2^(u_b-127) * e2m1 codes. */
 typedef struct {
   const uint8_t* q_fp8;       /* [T,32,128] e4m3 codes */
   const float* q_scale;       /* [T,32] >= 0 */

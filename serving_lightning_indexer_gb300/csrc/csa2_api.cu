@@ -186,36 +186,59 @@ int csa2_index_score(const csa2_index_score_args* a, void* ws, size_t ws_bytes, 
     return fail(CSA2_ERR_ALIGN, "csa2_index_score: scores must be 16-B aligned with ld_scores a multiple of 4");
   if (a->block_max && (!aligned16(a->block_max) || (a->ld_block_max & 3) || a->ld_block_max < 1))
     return fail(CSA2_ERR_ALIGN, "csa2_index_score: block_max must be 16-B aligned with ld a positive multiple of 4");
-  const bool prefill = a->rows.row_pos && a->rows.B == 1 && a->rows.T >= 64;
+  // FP4 pages take the per-row scan at every shape (prefill included)
+  const bool fp4 = a->index_k_format == CSA2_INDEX_FP4;
+  const bool prefill = a->rows.row_pos && a->rows.B == 1 && a->rows.T >= 64 && !fp4;
   const int nq = prefill ? 8 : 1;
-  if ((a->rows.T + nq - 1) / nq > 2048)
-    return fail(CSA2_ERR_SHAPE, "csa2_index_score: at most %d rows per call on this path", 2048 * nq);
+  if (prefill && a->rows.T > csa2::kIndexQueryBlocksPerLaunch * 8)
+    return fail(CSA2_ERR_SHAPE, "csa2_index_score: at most %d rows per call on the prefill path",
+                csa2::kIndexQueryBlocksPerLaunch * 8);
   if (a->hist && prefill)
-    return fail(CSA2_ERR_UNSUPPORTED, "csa2_index_score: hist is produced on the decode path only (pass NULL)");
-  if (prefill && a->index_k_format == CSA2_INDEX_FP4)
-    return fail(CSA2_ERR_UNSUPPORTED, "csa2_index_score: FP4 index-K pages are scored on the decode path only");
+    return fail(CSA2_ERR_UNSUPPORTED, "csa2_index_score: hist is produced on the per-row scan only (pass NULL)");
+  if (a->hist && a->rows.T > csa2::kIndexQueryBlocksPerLaunch)
+    return fail(CSA2_ERR_SHAPE, "csa2_index_score: hist needs at most %d rows per call", csa2::kIndexQueryBlocksPerLaunch);
   if (a->hist && !aligned16(a->hist)) return fail(CSA2_ERR_ALIGN, "csa2_index_score: hist must be 16-B aligned");
   DeviceCtx ctx;
   cudaError_t e = csa2::device_ctx(&ctx);
   if (e != cudaSuccess) return cuda_fail(e, "csa2_index_score: device");
-  csa2::IndexLaunch L{};
-  L.q_fp8 = a->q_fp8;
-  L.q_scale = a->q_scale;
-  L.w = a->w;
-  L.index_k = a->index_k;
-  L.n_pages = a->index_k_pages;
-  L.fp4 = a->index_k_format == CSA2_INDEX_FP4;
-  L.page_table = a->page_table;
-  L.pt_stride = a->pt_stride;
-  L.rows = rows_host(a->rows);
-  L.out = a->scores;
-  L.ld_out = a->ld_scores;
-  L.block_max = a->block_max;
-  L.ld_bm = a->ld_block_max;
-  L.hist = a->hist;
-  const char* why = "launch";
-  e = csa2::launch_index_tiles(L, 0, nq, ctx, static_cast<cudaStream_t>(stream), &why);
-  if (e != cudaSuccess) return cuda_fail(e, why);
+  // The per-row scan takes at most kIndexQueryBlocksPerLaunch rows a launch: rows
+  // [t0, t0 + n) go with q, w, the outputs and the row arrays offset by t0.
+  // Without row_seq the row is its own sequence, so the page table rows and
+  // n_visible move along, and rows past the last sequence see nothing (no
+  // launch).
+  const int step = prefill ? a->rows.T : csa2::kIndexQueryBlocksPerLaunch;
+  for (int t0 = 0; t0 < a->rows.T; t0 += step) {
+    const int n = (a->rows.T - t0) < step ? (a->rows.T - t0) : step;
+    csa2::IndexLaunch L{};
+    L.q_fp8 = a->q_fp8 + static_cast<size_t>(t0) * 32 * 128;
+    L.q_scale = a->q_scale + static_cast<size_t>(t0) * 32;
+    L.w = a->w + static_cast<size_t>(t0) * 32;
+    L.index_k = a->index_k;
+    L.n_pages = a->index_k_pages;
+    L.fp4 = fp4;
+    L.page_table = a->page_table;
+    L.pt_stride = a->pt_stride;
+    L.rows = rows_host(a->rows);
+    L.rows.T = n;
+    if (a->rows.row_pos) L.rows.row_pos = a->rows.row_pos + t0;
+    if (a->rows.row_seq) {
+      L.rows.row_seq = a->rows.row_seq + t0;
+    } else if (t0 > 0) {
+      const int b_left = a->rows.B - t0;
+      if (b_left <= 0) break;
+      L.rows.B = b_left < n ? b_left : n;
+      L.page_table = a->page_table + static_cast<size_t>(t0) * a->pt_stride;
+      if (a->rows.n_visible) L.rows.n_visible = a->rows.n_visible + t0;
+    }
+    L.out = a->scores + static_cast<size_t>(t0) * a->ld_scores;
+    L.ld_out = a->ld_scores;
+    L.block_max = a->block_max ? a->block_max + static_cast<size_t>(t0) * a->ld_block_max : nullptr;
+    L.ld_bm = a->ld_block_max;
+    L.hist = a->hist;
+    const char* why = "launch";
+    e = csa2::launch_index_tiles(L, 0, nq, ctx, static_cast<cudaStream_t>(stream), &why);
+    if (e != cudaSuccess) return cuda_fail(e, why);
+  }
   return CSA2_OK;
 }
 
@@ -292,7 +315,8 @@ int csa2_reindex(const csa2_reindex_args* a, void* ws, size_t ws_bytes, void* st
   int rc = check_index_common(a->q_fp8, a->q_scale, a->w, a->index_k, a->index_k_pages, a->page_table, a->pt_stride,
                               a->rows, a->index_k_format, "csa2_reindex");
   if (rc) return rc;
-  if (a->rows.T > 2048) return fail(CSA2_ERR_SHAPE, "csa2_reindex: at most 2048 rows per call");
+  if (a->rows.T > csa2::kIndexQueryBlocksPerLaunch)
+    return fail(CSA2_ERR_SHAPE, "csa2_reindex: at most %d rows per call", csa2::kIndexQueryBlocksPerLaunch);
   if (!a->pool_blocks || !a->topk_pos) return fail(CSA2_ERR_NULL, "csa2_reindex: pool_blocks/topk_pos is NULL");
   if (a->pool_n < 1 || a->pool_n > CSA2_MAX_TOPK) return fail(CSA2_ERR_SHAPE, "csa2_reindex: pool_n=%d not in 1..2048", a->pool_n);
   if (a->k < 1 || a->k > CSA2_MAX_TOPK) return fail(CSA2_ERR_SHAPE, "csa2_reindex: k=%d not in 1..2048", a->k);

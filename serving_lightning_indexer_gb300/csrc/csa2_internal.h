@@ -12,6 +12,11 @@ namespace csa2 {
 constexpr uint32_t kErrBoundsBit = 1u;
 constexpr uint32_t kErrTimeoutBit = 2u;
 
+// Query blocks one indexer launch takes (the kernel keeps a table of them in
+// shared memory): rows on the per-row scan and Reindex, blocks of 8 rows on
+// the prefill path.
+constexpr int kIndexQueryBlocksPerLaunch = 2048;
+
 struct RowsHost {
   int T, B;
   const int* row_seq;

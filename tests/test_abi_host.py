@@ -100,10 +100,15 @@ def test_validation_returns_codes_without_launch(lib):
     a.index_k = FAKE + 16
     assert lib.csa2_index_score(C.byref(a), None, 0, None) == 3                  # FP4 pages need 32-B alignment
     a.index_k = FAKE
-    a.rows = csa2.Rows(64, 1, FAKE, FAKE, None, 2)
-    assert lib.csa2_index_score(C.byref(a), None, 0, None) == 4                  # FP4 keys: decode path only
-    assert b"FP4" in lib.csa2_last_error_detail()
+    a.rows = csa2.Rows(2049, 1, FAKE, FAKE, None, 2)
+    a.hist = FAKE
+    assert lib.csa2_index_score(C.byref(a), None, 0, None) == 2                  # FP4 prefill rows: per-row scan,
+    assert b"hist" in lib.csa2_last_error_detail()                               # whose hist takes <= 2048 rows
     a.index_k_format = csa2.INDEX_FP8
+    assert lib.csa2_index_score(C.byref(a), None, 0, None) == 4                  # FP8 prefill path: no hist
+    a.hist = None
+    a.rows = csa2.Rows(16385, 1, FAKE, FAKE, None, 2)
+    assert lib.csa2_index_score(C.byref(a), None, 0, None) == 2                  # prefill path: <= 16384 rows
 
     t = csa2.TopkArgs(FAKE, 128, None, 0, None, 0, csa2.Rows(2, 2, None, None, FAKE, 1), 4096, FAKE, None, 4096,
                       None, 0)

@@ -112,6 +112,77 @@ def test_prefill_query_blocked_path(T, ratio, n_entries):
         assert np.all(bm_all[t, nb:] == 7.0), f"row {t}: block maxima written past the visible blocks"
 
 
+def _check_rows(scores, bm, iq, cache, pt_rows, visible, rows_to_check, fp4, what):
+    """Scores of the given rows against the oracle, -inf up to the row's last
+    128-entry tile, block maxima equal to the max over the kernel's own scores."""
+    ld = scores.shape[1]
+    for t in rows_to_check:
+        e = visible[t]
+        got = np_(scores[t])
+        if e:
+            ref = o.index_scores_row(np_(iq.q_fp8[t]), np_(iq.q_scale[t]), np_(iq.w[t]), cache, pt_rows[t], e,
+                                     fp4=fp4)
+            assert_scores_close(got[:e], ref, f"{what} row {t}")
+        assert np.all(np.isneginf(got[e:min(ld, (e + 127) // 128 * 128)])), f"{what} row {t}: tail"
+        assert np.all(got[(e + 127) // 128 * 128:] == 7.0), f"{what} row {t}: written past its last tile"
+        nb = (e + 7) // 8
+        want = [got[8 * j:min(8 * j + 8, e)].max() for j in range(nb)]
+        assert np.array_equal(np_(bm[t, :nb]), np.array(want, dtype=np.float32)), f"{what} row {t}: block maxima"
+        assert np.all(np_(bm[t, nb:]) == 7.0)
+
+
+@pytest.mark.parametrize("T,ratio,n_entries", [(100, 2, 3000), (2100, 1, 2500)])
+def test_prefill_fp4_index_keys_take_the_per_row_scan(T, ratio, n_entries):
+    # FP4 pages at a prefill shape (row_pos, one sequence, T >= 64) are scored
+    # by the per-row scan, in launches of 2048 rows
+    dev = need_gpu()
+    pc = W.make_paged_cache([n_entries], seed=31, device=dev, with_main=False, index_fp4=True)
+    iq = W.make_indexer_query(T, seed=32, device=dev)
+    first = n_entries * ratio - T
+    row_pos = torch.arange(first, first + T, dtype=torch.int32, device=dev)
+    ld = (n_entries + 127) // 128 * 128 + 128
+    scores = torch.full((T, ld), 7.0, dtype=torch.float32, device=dev)
+    bm = torch.full((T, ld // 8), 7.0, dtype=torch.float32, device=dev)
+    r = csa2.rows(T, 1, row_seq=torch.zeros(T, dtype=torch.int32, device=dev), row_pos=row_pos, ratio_m=ratio)
+    csa2.index_score(iq.q_fp8, iq.q_scale, iq.w, pc.index_k, pc.page_table, r, scores, bm)
+    torch.cuda.synchronize()
+    assert csa2.check_device_error() == 0
+    pt = np_(pc.page_table)
+    visible = [o.visible_entries(first + t, ratio) for t in range(T)]
+    rows = sorted(set([0, 1, T // 2, T - 1] + ([2047, 2048] if T > 2048 else [])))
+    _check_rows(scores, bm, iq, np_(pc.index_k), [pt[0]] * T, visible, rows, True, "fp4 prefill")
+
+
+@pytest.mark.parametrize("with_row_seq", [True, False])
+def test_per_row_scan_takes_more_than_2048_rows_in_launches(with_row_seq):
+    # 2100 rows: launches of rows 0..2047 and 2048..2099.  With row_seq, three
+    # sequences shared by the rows; without, every row is its own sequence
+    # (page-table rows and n_visible follow the row)
+    dev = need_gpu()
+    T = 2100
+    rng = np.random.default_rng(41)
+    lengths = [300, 1000, 129] if with_row_seq else [int(x) for x in rng.integers(1, 300, size=T)]
+    pc = W.make_paged_cache(lengths, seed=42, device=dev, with_main=False)
+    iq = W.make_indexer_query(T, seed=43, device=dev)
+    ld = (max(lengths) + 127) // 128 * 128 + 128
+    scores = torch.full((T, ld), 7.0, dtype=torch.float32, device=dev)
+    bm = torch.full((T, ld // 8), 7.0, dtype=torch.float32, device=dev)
+    nvis = torch.tensor(lengths, dtype=torch.int32, device=dev)
+    if with_row_seq:
+        seq = rng.integers(0, 3, size=T)
+        r = csa2.rows(T, 3, row_seq=torch.tensor(seq, dtype=torch.int32, device=dev), n_visible=nvis)
+    else:
+        seq = np.arange(T)
+        r = csa2.rows(T, T, n_visible=nvis)
+    csa2.index_score(iq.q_fp8, iq.q_scale, iq.w, pc.index_k, pc.page_table, r, scores, bm)
+    torch.cuda.synchronize()
+    assert csa2.check_device_error() == 0
+    pt = np_(pc.page_table)
+    visible = [lengths[seq[t]] for t in range(T)]
+    _check_rows(scores, bm, iq, np_(pc.index_k), [pt[seq[t]] for t in range(T)], visible,
+                [0, 1, 1000, 2046, 2047, 2048, 2049, 2099], False, "split")
+
+
 @pytest.mark.parametrize("lengths", [[1], [127, 128, 129], [4096], [100, 1000, 4133, 64, 65, 8191]])
 def test_decode_fp4_index_keys_match_oracle(lengths):
     # FP4 index-K pages (e2m1 + ue8m0 per 32 dims): the same scan, the e2m1 keys
