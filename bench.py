@@ -691,7 +691,7 @@ def main():
     sampler = ClockSampler(local)
     if rank == 0:
         sampler.start()
-    replay_ms, marked_ms, scan_ms, attn_ms, per_layer = [], [], [], [], {}
+    replay_ms, marked_ms, scan_ms, attn_ms, per_layer, attn_role = [], [], [], [], {}, {}
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     sampler.mark(True)
@@ -717,7 +717,10 @@ def main():
             ms = a.elapsed_time(b)
             scan_ms.append(ms)
             per_layer.setdefault(l, []).append(ms)
-        attn_ms.extend(a.elapsed_time(b) for _, a, b in attn_pairs)
+        for l, a, b in attn_pairs:
+            ms = a.elapsed_time(b)
+            attn_ms.append(ms)
+            attn_role.setdefault(ds.role_of(l), []).append(ms)
     sampler.mark(False)
     if world > 1:
         dist.barrier()
@@ -895,6 +898,9 @@ def main():
         "roofline_attention": {
             "bound": "latency", "kernel": "sparse_attn_tc_kernel (8 rows x 64 heads x 640 keys)",
             "avg_launch_ms": attn_avg, "launches_timed": len(attn_ms),
+            # Reuse layers gather their keys before the dependency wait; Full and
+            # Reindex layers read slots written by the launch just before
+            "avg_launch_ms_by_role": {r: statistics.mean(v) for r, v in attn_role.items()},
             "share_of_step": attn_avg * n_layers / ms_per_step,
             "algorithmic_bytes_per_launch": ATTN_ROW_BYTES * len(LENGTHS),
             "hbm_frac": ATTN_ROW_BYTES * len(LENGTHS) / (attn_avg / 1e3) / 1e9 / hbm_peak,
