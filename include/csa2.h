@@ -206,10 +206,11 @@ CSA2_API int csa2_topk_with_candidates(const csa2_topk_args* args, void* workspa
  * every GPU loading the library holds until exit.  A call needs exactly what
  * csa2_workspace_size(CSA2_CALL_TOPK, args, ...) reports: nothing when
  * L <= 16384, else
- *     V * H + round_up(V * c * 4, 256) + V * c * 8192 bytes,
+ *     V * H + R + round_up(V * c * 4, 256) + V * c * 8192 bytes,
  * with L = ld_scores (the larger of ld_scores and ld_block_max when
  * pool_blocks is set), c = ceil(L / 4096), V = T (2T with a pool: the block
- * maxima are a second row per query) and H = 8192 (0 when hist is given).
+ * maxima are a second row per query), H = 8192 and R = round_up(V * 8, 256)
+ * (H = R = 0 when hist is given).
  * That is about 2 B per element of L per row: a 1M-entry row needs 2.1 MB,
  * 4.2 MB with its pool, so the 8 MiB array takes three 1M rows, or one with
  * its pool, or seven 262,144-entry rows with their pools.  Calls needing more

@@ -69,6 +69,8 @@ struct SelParams {
   int hist_full;         // hist covers every row (given by the caller), not only the long ones;
                          // the final pass returns the caller's rows to zero after reading them
   uint32_t* hist_ws;
+  uint32_t* hist_done;   // [V]: hist CTAs finished per row (zeroed with hist_ws), or null
+  int* thr;              // [V]: threshold bin of each row found by its last hist CTA (-1: take all), or null
   uint32_t* cnt;         // [V][nchunks]: candidates found by each filter CTA (may exceed kRegion)
   uint2* cand;           // [V][nchunks][kRegion]: (key, index) of each filter CTA's candidates
   int nchunks;           // filter CTAs per row
@@ -247,6 +249,27 @@ __global__ void __launch_bounds__(kStreamThreads) sel_hist_kernel(const __grid_c
   uint32_t* gh = P.hist_ws + static_cast<long long>(v) * kBins;
   for (int i = threadIdx.x; i < kBins; i += blockDim.x)
     if (h[i]) atomicAdd(gh + i, h[i]);
+  // The row's last CTA to finish searches the complete histogram once for the
+  // threshold bin, so that the filter CTAs read one word instead of each
+  // searching the 8-KB histogram (the usual last-block pattern: each CTA's
+  // additions are fenced before it counts itself done).
+  __shared__ int last;
+  __shared__ int res[4];
+  __shared__ uint32_t wsum[32];
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const unsigned nblk = static_cast<unsigned>((r.n + kChunk - 1) / kChunk);
+    last = atomicAdd(P.hist_done + v, 1u) == nblk - 1;
+    res[0] = -1;
+  }
+  __syncthreads();
+  if (!last) return;
+  __threadfence();
+  for (int i = threadIdx.x; i < kBins; i += blockDim.x) h[i] = __ldcg(gh + i);
+  __syncthreads();
+  block_find_bin(h, static_cast<uint32_t>(r.k), res, wsum);
+  if (threadIdx.x == 0) P.thr[v] = res[0];
 }
 
 __global__ void __launch_bounds__(kStreamThreads) sel_filter_kernel(const __grid_constant__ SelParams P) {
@@ -281,11 +304,16 @@ __global__ void __launch_bounds__(kStreamThreads) sel_filter_kernel(const __grid
     vals[4 * q + 2] = v4.z;
     vals[4 * q + 3] = v4.w;
   }
-  stage_hist(h, P.hist + static_cast<long long>(v) * kBins);
-  if (threadIdx.x == 0) res[0] = -1;
-  __syncthreads();
-  block_find_bin(h, static_cast<uint32_t>(r.k), res, wsum);
-  const int b1 = res[0];
+  int b1;
+  if (P.thr) {  // found once per row by the hist pass
+    b1 = __ldcg(P.thr + v);
+  } else {
+    stage_hist(h, P.hist + static_cast<long long>(v) * kBins);
+    if (threadIdx.x == 0) res[0] = -1;
+    __syncthreads();
+    block_find_bin(h, static_cast<uint32_t>(r.k), res, wsum);
+    b1 = res[0];
+  }
   const uint32_t thr = b1 < 0 ? 0u : static_cast<uint32_t>(b1);
   uint32_t keys[kFilterPer];
   uint32_t mine = 0;
@@ -790,13 +818,15 @@ static long long select_maxn(const SelectLaunch& a) {
 static size_t select_cnt_bytes(long long V, long long nch) {
   return (static_cast<size_t>(V) * nch * 4 + 255) & ~size_t(255);
 }
+// the hist pass's per-row words: a done count and the threshold bin
+static size_t select_row_words_bytes(long long V) { return (static_cast<size_t>(V) * 8 + 255) & ~size_t(255); }
 
 size_t select_workspace_bytes(const SelectLaunch& a) {
   const long long maxn = select_maxn(a);
   if (maxn <= kDirect) return 0;
   const long long V = static_cast<long long>(a.rows.T) * (a.pool_out ? 2 : 1);
   const long long nch = (maxn + kFilterChunk - 1) / kFilterChunk;
-  const size_t hist = a.hist ? 0 : static_cast<size_t>(V) * kBins * 4;
+  const size_t hist = a.hist ? 0 : static_cast<size_t>(V) * kBins * 4 + select_row_words_bytes(V);
   return hist + select_cnt_bytes(V, nch) + static_cast<size_t>(V) * nch * kRegion * 8;
 }
 
@@ -825,6 +855,8 @@ cudaError_t launch_select(const SelectLaunch& a, void* ws, size_t ws_bytes, cons
   P.hist = a.hist;
   P.hist_full = a.hist != nullptr;
   P.hist_ws = nullptr;
+  P.hist_done = nullptr;
+  P.thr = nullptr;
   P.cnt = nullptr;
   P.cand = nullptr;
   P.nchunks = 0;
@@ -837,8 +869,12 @@ cudaError_t launch_select(const SelectLaunch& a, void* ws, size_t ws_bytes, cons
       P.hist_ws = reinterpret_cast<uint32_t*>(w);
       P.hist = P.hist_ws;
       w += static_cast<size_t>(V) * kBins * 4;
-      // the histogram pass accumulates: zero it (the only memset; given histograms need none)
-      e = cudaMemsetAsync(P.hist_ws, 0, static_cast<size_t>(V) * kBins * 4, st);
+      P.hist_done = reinterpret_cast<uint32_t*>(w);
+      P.thr = reinterpret_cast<int*>(w + static_cast<size_t>(V) * 4);
+      w += select_row_words_bytes(V);
+      // the histogram pass accumulates and counts its CTAs: zero both (the
+      // only memset; given histograms need none)
+      e = cudaMemsetAsync(P.hist_ws, 0, static_cast<size_t>(V) * kBins * 4 + select_row_words_bytes(V), st);
       if (e != cudaSuccess) return e;
     }
     P.cnt = reinterpret_cast<uint32_t*>(w);

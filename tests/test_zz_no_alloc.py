@@ -25,7 +25,7 @@ def _scratch_bytes(T, L, pool, hist_given=False):
         return 0
     V = T * (2 if pool else 1)
     c = -(-L // 4096)
-    return V * (0 if hist_given else 8192) + (V * c * 4 + 255) // 256 * 256 + V * c * 8192
+    return (0 if hist_given else V * 8192 + (V * 8 + 255) // 256 * 256) + (V * c * 4 + 255) // 256 * 256 + V * c * 8192
 
 
 def _inputs(seed, lengths, dev):
@@ -118,8 +118,8 @@ def test_noalloc_topk_with_the_scan_histograms():
 
 
 def test_noalloc_topk_just_under_and_just_over_the_static_scratch():
-    """Seven rows of 262,144 entries with pools fit the 8 MiB array (7,458,304 B);
-    eight (8,523,776 B) are rejected before any launch."""
+    """Seven rows of 262,144 entries with pools fit the 8 MiB array (7,458,560 B);
+    eight (8,524,032 B) are rejected before any launch."""
     dev = need_gpu()
     lib = csa2.load()
     n = 262_144
