@@ -73,7 +73,8 @@ struct SelParams {
   int* thr;              // [V]: threshold bin of each row found by its last hist CTA (-1: take all), or null
   uint32_t* cnt;         // [V][nchunks]: candidates found by each filter CTA (may exceed kRegion)
   uint2* cand;           // [V][nchunks][kRegion]: (key, index) of each filter CTA's candidates
-  int nchunks;           // filter CTAs per row
+  int nchunks;           // filter chunks of 4096 elements per row
+  int filter_cpc;        // chunks per filter CTA
   uint32_t* err;
 };
 
@@ -278,32 +279,39 @@ __global__ void __launch_bounds__(kStreamThreads) sel_filter_kernel(const __grid
   const int v = blockIdx.y;
   const VRow r = vrow_of(P, v);
   if (r.n <= kDirect) return;
-  const int i0 = blockIdx.x * kFilterChunk;
-  if (i0 >= r.n) return;
+  // chunks filter_cpc * blockIdx.x .. of 4096 elements, one after the other
+  // (several per CTA only when the rows x chunks make many waves of CTAs)
+  const int ch0 = blockIdx.x * P.filter_cpc;
+  if (ch0 * kFilterChunk >= r.n) return;
+  const int ch1 = min(ch0 + P.filter_cpc, (r.n + kFilterChunk - 1) / kFilterChunk);
   __shared__ __align__(16) uint32_t h[kBins];
   __shared__ int res[4];
   __shared__ uint32_t wsum[32];
-  // this thread's kFilterPer consecutive elements, loaded before the histogram
-  // is searched so that the two latencies overlap
-  const int i = i0 + threadIdx.x * kFilterPer;
-  const int i1 = min(i0 + kFilterChunk, r.n);
+  // this thread's kFilterPer consecutive elements of chunk ch
   float vals[kFilterPer];
+  auto load_chunk = [&](int ch) {
+    const int i = ch * kFilterChunk + threadIdx.x * kFilterPer;
+    const int i1 = min(ch * kFilterChunk + kFilterChunk, r.n);
 #pragma unroll
-  for (int q = 0; q < kFilterPer / 4; ++q) {
-    const int e = i + 4 * q;
-    float4 v4 = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-    if (e + 3 < i1) {
-      v4 = *reinterpret_cast<const float4*>(r.src + e);
-    } else if (e < i1) {
-      v4.x = r.src[e];
-      if (e + 1 < i1) v4.y = r.src[e + 1];
-      if (e + 2 < i1) v4.z = r.src[e + 2];
+    for (int q = 0; q < kFilterPer / 4; ++q) {
+      const int e = i + 4 * q;
+      float4 v4 = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+      if (e + 3 < i1) {
+        v4 = *reinterpret_cast<const float4*>(r.src + e);
+      } else if (e < i1) {
+        v4.x = r.src[e];
+        if (e + 1 < i1) v4.y = r.src[e + 1];
+        if (e + 2 < i1) v4.z = r.src[e + 2];
+      }
+      vals[4 * q] = v4.x;
+      vals[4 * q + 1] = v4.y;
+      vals[4 * q + 2] = v4.z;
+      vals[4 * q + 3] = v4.w;
     }
-    vals[4 * q] = v4.x;
-    vals[4 * q + 1] = v4.y;
-    vals[4 * q + 2] = v4.z;
-    vals[4 * q + 3] = v4.w;
-  }
+  };
+  // the first chunk's elements are requested before the threshold, so that
+  // the two latencies overlap
+  load_chunk(ch0);
   int b1;
   if (P.thr) {  // found once per row by the hist pass
     b1 = __ldcg(P.thr + v);
@@ -315,27 +323,32 @@ __global__ void __launch_bounds__(kStreamThreads) sel_filter_kernel(const __grid
     b1 = res[0];
   }
   const uint32_t thr = b1 < 0 ? 0u : static_cast<uint32_t>(b1);
-  uint32_t keys[kFilterPer];
-  uint32_t mine = 0;
+  for (int ch = ch0; ch < ch1; ++ch) {
+    const int i = ch * kFilterChunk + threadIdx.x * kFilterPer;
+    const int i1 = min(ch * kFilterChunk + kFilterChunk, r.n);
+    uint32_t keys[kFilterPer];
+    uint32_t mine = 0;
 #pragma unroll
-  for (int j = 0; j < kFilterPer; ++j) {
-    const uint32_t key = (i + j < i1) ? elem_key(r, vals[j], i + j) : 0u;
-    keys[j] = (key && (key >> 21) >= thr) ? key : 0u;
-    mine += keys[j] ? 1u : 0u;
-  }
-  // this CTA's own region, in element order (each thread holds consecutive
-  // elements; a block prefix sum places them), and its true count: no counter
-  // shared across CTAs, nothing to zero
-  uint32_t total;
-  uint32_t slot = block_excl_scan(mine, wsum, &total);
-  uint2* cand = P.cand + (static_cast<long long>(v) * P.nchunks + blockIdx.x) * kRegion;
+    for (int j = 0; j < kFilterPer; ++j) {
+      const uint32_t key = (i + j < i1) ? elem_key(r, vals[j], i + j) : 0u;
+      keys[j] = (key && (key >> 21) >= thr) ? key : 0u;
+      mine += keys[j] ? 1u : 0u;
+    }
+    if (ch + 1 < ch1) load_chunk(ch + 1);  // in flight during this chunk's compaction
+    // the chunk's own region, in element order (each thread holds consecutive
+    // elements; a block prefix sum places them), and its true count: no
+    // counter shared across CTAs, nothing to zero
+    uint32_t total;
+    uint32_t slot = block_excl_scan(mine, wsum, &total);
+    uint2* cand = P.cand + (static_cast<long long>(v) * P.nchunks + ch) * kRegion;
 #pragma unroll
-  for (int j = 0; j < kFilterPer; ++j) {
-    if (!keys[j]) continue;
-    if (slot < static_cast<uint32_t>(kRegion)) cand[slot] = make_uint2(keys[j], static_cast<uint32_t>(i + j));
-    ++slot;
+    for (int j = 0; j < kFilterPer; ++j) {
+      if (!keys[j]) continue;
+      if (slot < static_cast<uint32_t>(kRegion)) cand[slot] = make_uint2(keys[j], static_cast<uint32_t>(i + j));
+      ++slot;
+    }
+    if (threadIdx.x == 0) P.cnt[static_cast<long long>(v) * P.nchunks + ch] = total;
   }
-  if (threadIdx.x == 0) P.cnt[static_cast<long long>(v) * P.nchunks + blockIdx.x] = total;
 }
 
 // ---------------------------------------------------------------- final select
@@ -860,6 +873,7 @@ cudaError_t launch_select(const SelectLaunch& a, void* ws, size_t ws_bytes, cons
   P.cnt = nullptr;
   P.cand = nullptr;
   P.nchunks = 0;
+  P.filter_cpc = 1;
   cudaError_t e;
   const long long maxn = select_maxn(a);
   if (maxn > kDirect) {
@@ -880,8 +894,17 @@ cudaError_t launch_select(const SelectLaunch& a, void* ws, size_t ws_bytes, cons
     P.cnt = reinterpret_cast<uint32_t*>(w);
     P.cand = reinterpret_cast<uint2*>(w + select_cnt_bytes(V, nch));
     P.nchunks = static_cast<int>(nch);
+    // one filter chunk per CTA while the rows' chunks make at most 8 waves of
+    // CTAs (decode), else up to 8 chunks per CTA, which spreads the CTA's
+    // setup (row, threshold) and overlaps a chunk's loads with the previous
+    // chunk's compaction (prefill: thousands of rows)
+    const long long wave = static_cast<long long>(ctx.num_sms) * 4;  // 256-thread CTAs at 64 registers: 4 an SM
+    const long long fct = static_cast<long long>(V) * nch;
+    long long cpc = fct > 8 * wave ? (fct + 4 * wave - 1) / (4 * wave) : 1;
+    cpc = cpc < 1 ? 1 : (cpc > 8 ? 8 : cpc);
+    P.filter_cpc = static_cast<int>(cpc);
     const dim3 grid(static_cast<unsigned>((maxn + kChunk - 1) / kChunk), static_cast<unsigned>(V));
-    const dim3 fgrid(static_cast<unsigned>(nch), static_cast<unsigned>(V));
+    const dim3 fgrid(static_cast<unsigned>((nch + cpc - 1) / cpc), static_cast<unsigned>(V));
     if ((e = prefer_max_smem(sel_hist_kernel, 0)) != cudaSuccess) return e;
     if ((e = prefer_max_smem(sel_filter_kernel, 0)) != cudaSuccess) return e;
     if (!a.hist && (e = launch_pdl(sel_hist_kernel, grid, dim3(kStreamThreads), 0, st, P)) != cudaSuccess) return e;
