@@ -18,7 +18,7 @@ query-layers per second is reported beside it.  The same run also measures
     row, 10 % planted blocks) and the attention of its four layers.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-  python bench.py --case scan|topk|reindex|attn|prefill [--iters N]   (one call, for profilers)
+  python bench.py --case scan|topk|reindex|attn|prefill|prefill_chunk|project [--iters N]   (for profilers)
 
 Timing: W eager warm-up steps, then K steps captured in one CUDA graph; the
 graph is replayed (each replay timed with CUDA events between two device
@@ -560,6 +560,15 @@ def run_case(args):
         ms = _time_calls(lambda: csa2.sparse_attn(al.q, pc.main_kv, slot, al.swa_kv, al.swa_slot, al.sink, out),
                          args.iters, st)
         res.update(ms=ms, query_layers=B)
+    elif args.case == "prefill_chunk":
+        # the 4,096-query prefill chunk after a 256K-token prefix, its four calls
+        # in order, args.iters times (for an ncu launch list of the chunk)
+        calls, info = prefill_case(dev)
+        order = ("compress", "index_score", "topk", "attn")
+        ms = {}
+        for name in order:
+            ms[name] = _time_calls(calls[name], args.iters, st, warm=1, replays=1)
+        res.update(call_ms=ms, queries=info["queries"], entries=info["n_entries"])
     elif args.case == "project":
         H, w = W.make_hidden_projection(B, seed=8, device=dev)
         out = torch.empty(B, 512, dtype=torch.bfloat16, device=dev)
@@ -597,7 +606,7 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-workloads", action="store_true", help="skip the prefill and Reindex workloads")
-    ap.add_argument("--case", choices=["scan", "topk", "reindex", "attn", "prefill", "project"])
+    ap.add_argument("--case", choices=["scan", "topk", "reindex", "attn", "prefill", "prefill_chunk", "project"])
     ap.add_argument("--iters", type=int, default=3)
     ap.add_argument("--batch", type=int, default=8)
     ap.add_argument("--entries", type=int, default=262144)
