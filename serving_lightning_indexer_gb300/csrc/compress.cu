@@ -105,7 +105,7 @@ constexpr int ik_smem_floats() { return 512 * EPC + 8 * EPC * 128; }
 // IK: also the index keys (W^IK given); EPC: entries per CTA (8, or 1 so that
 // few entries spread over more SMs: the other warps then only help project)
 template <bool IK, int EPC>
-__global__ void __launch_bounds__(256) compress_kernel(const __grid_constant__ CompressParams p) {
+__global__ void __launch_bounds__(256, IK ? 1 : 4) compress_kernel(const __grid_constant__ CompressParams p) {
   extern __shared__ float s_ik[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // W^IK is a weight (no earlier kernel writes it): this warp's 64 rows, lane
@@ -155,17 +155,28 @@ __global__ void __launch_bounds__(256) compress_kernel(const __grid_constant__ C
   if (p.ratio_m == 1) {
     load16_bf16(p.C + e * 512 + c0, x);
   } else {
-    float ca[16], cb[16], za[16], zb[16];
+    // the two tokens' 16 channels of C and Z, kept packed (bf16) until used
     const long long r0 = e * 2;
-    load16_bf16(p.C + r0 * 512 + c0, ca);
-    load16_bf16(p.C + (r0 + 1) * 512 + c0, cb);
-    load16_bf16(p.Z + r0 * 512 + c0, za);
-    load16_bf16(p.Z + (r0 + 1) * 512 + c0, zb);
+    uint4 pk[4][2];  // C token 0, C token 1, Z token 0, Z token 1; 8 channels each
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      pk[0][h] = __ldg(reinterpret_cast<const uint4*>(p.C + r0 * 512 + c0) + h);
+      pk[1][h] = __ldg(reinterpret_cast<const uint4*>(p.C + (r0 + 1) * 512 + c0) + h);
+      pk[2][h] = __ldg(reinterpret_cast<const uint4*>(p.Z + r0 * 512 + c0) + h);
+      pk[3][h] = __ldg(reinterpret_cast<const uint4*>(p.Z + (r0 + 1) * 512 + c0) + h);
+    }
+    auto chan = [&](int s_, int i) {  // channel c0 + i of stream s_ as fp32 (exact)
+      const uint4& q = pk[s_][i >> 3];
+      const int w = (i >> 1) & 3;
+      const uint32_t word = w == 0 ? q.x : (w == 1 ? q.y : (w == 2 ? q.z : q.w));
+      return __uint_as_float((i & 1) ? (word & 0xFFFF0000u) : (word << 16));
+    };
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
-      const float zm = fmaxf(za[i], zb[i]);
-      const float ea = expf(za[i] - zm), eb = expf(zb[i] - zm);
-      x[i] = (ea * ca[i] + eb * cb[i]) / (ea + eb);
+      const float za = chan(2, i), zb = chan(3, i);
+      const float zm = fmaxf(za, zb);
+      const float ea = expf(za - zm), eb = expf(zb - zm);
+      x[i] = (ea * chan(0, i) + eb * chan(1, i)) / (ea + eb);
     }
   }
   // RMSNorm over the 512 channels

@@ -95,6 +95,33 @@ def test_exact_massive_ties_fall_back_to_streaming_select():
     assert pool[0].tolist() == o.candidate_pool(bm_np[0, :12_500].astype(np.float64), 2048).tolist()
 
 
+@pytest.mark.parametrize("kind", ["normal", "ties"])
+def test_exact_many_long_rows_multi_chunk_passes(kind):
+    # 2,500 rows of 16,385..20,000 scores without histograms: enough chunks
+    # that each filter CTA takes several 4096-score chunks and each hist CTA
+    # 65,536 scores, with the threshold bin found once per row by the hist
+    # pass.  "ties": scores in steps of 0.5, so the threshold bin is crowded
+    # and the radix refinement breaks ties by position.
+    dev = need_gpu()
+    T, ld = 2500, 20000
+    rng = np.random.default_rng(77 if kind == "normal" else 78)
+    lengths = rng.integers(16385, ld + 1, size=T)
+    lengths[::97] = ld
+    s = rng.normal(size=(T, ld)).astype(np.float32)
+    if kind == "ties":
+        s = (np.round(s * 2) / 2).astype(np.float32)
+    scores = torch.tensor(s, device=dev)
+    pos = torch.full((T, 512), -7, dtype=torch.int32, device=dev)
+    nvis = torch.tensor(lengths, dtype=torch.int32, device=dev)
+    csa2.topk_with_candidates(scores, csa2.rows(T, T, n_visible=nvis), 512, pos)
+    torch.cuda.synchronize()
+    assert csa2.check_device_error() == 0
+    got = np_(pos)
+    for t in sorted(set(range(0, T, 23)) | {1, T - 1}):
+        want = o.topk_positions(s[t, :lengths[t]], 512)
+        assert got[t].tolist() == want.tolist(), f"row {t} ({kind}): positions differ"
+
+
 def test_exact_all_excluded_rows():
     s = np.full((2, 1024), -np.inf, dtype=np.float32)
     s[1, 5] = 1.0
