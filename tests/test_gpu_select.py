@@ -95,21 +95,32 @@ def test_exact_massive_ties_fall_back_to_streaming_select():
     assert pool[0].tolist() == o.candidate_pool(bm_np[0, :12_500].astype(np.float64), 2048).tolist()
 
 
-@pytest.mark.parametrize("kind", ["normal", "ties"])
-def test_exact_many_long_rows_multi_chunk_passes(kind):
-    # 2,500 rows of 16,385..20,000 scores without histograms: enough chunks
-    # that each filter CTA takes several 4096-score chunks and each hist CTA
-    # 65,536 scores, with the threshold bin found once per row by the hist
-    # pass.  "ties": scores in steps of 0.5, so the threshold bin is crowded
-    # and the radix refinement breaks ties by position.
+@pytest.mark.parametrize("T,ld,kind", [
+    (2500, 20000, "normal"),    # many long rows: hist CTAs of 65,536 scores, filter
+                                # CTAs of several 4096-score chunks, the threshold
+                                # bin found once per row
+    (2500, 20000, "ties"),      # crowded threshold bin, ties broken by position
+    (400, 20000, "equal"),      # every score equal: the candidate lists overflow
+                                # and the streaming radix select takes over
+    (400, 20000, "sparse"),     # 300 selectable scores a row: all of them
+    (300, 280000, "normal"),    # fewer, longer rows, the same multi-chunk passes
+])
+def test_exact_many_long_rows(T, ld, kind):
+    # long rows without histograms (the hist, filter and final passes)
     dev = need_gpu()
-    T, ld = 2500, 20000
-    rng = np.random.default_rng(77 if kind == "normal" else 78)
-    lengths = rng.integers(16385, ld + 1, size=T)
+    rng = np.random.default_rng(T + ld + len(kind))
+    lengths = rng.integers(ld * 4 // 5, ld + 1, size=T)
     lengths[::97] = ld
     s = rng.normal(size=(T, ld)).astype(np.float32)
     if kind == "ties":
         s = (np.round(s * 2) / 2).astype(np.float32)
+    elif kind == "equal":
+        s[:] = 1.0
+    elif kind == "sparse":
+        keep = np.zeros((T, ld), dtype=bool)
+        for t in range(T):
+            keep[t, rng.choice(int(lengths[t]), size=300, replace=False)] = True
+        s[~keep] = -np.inf
     scores = torch.tensor(s, device=dev)
     pos = torch.full((T, 512), -7, dtype=torch.int32, device=dev)
     nvis = torch.tensor(lengths, dtype=torch.int32, device=dev)
@@ -117,7 +128,8 @@ def test_exact_many_long_rows_multi_chunk_passes(kind):
     torch.cuda.synchronize()
     assert csa2.check_device_error() == 0
     got = np_(pos)
-    for t in sorted(set(range(0, T, 23)) | {1, T - 1}):
+    step = max(1, T // 100)
+    for t in sorted(set(range(0, T, step)) | {1, T - 1}):
         want = o.topk_positions(s[t, :lengths[t]], 512)
         assert got[t].tolist() == want.tolist(), f"row {t} ({kind}): positions differ"
 
