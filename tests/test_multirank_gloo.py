@@ -62,3 +62,23 @@ def test_reference_arm_runs_on_rank_zero_only():
     with redirect_stdout(buf):
         bench.reference_arm(SimpleNamespace(steps=1, warmup=0), rank=1, world=2)
     assert buf.getvalue() == ""      # the other ranks exit without work or output
+
+
+def test_reference_arm_prints_the_contract_line_on_rank_zero():
+    # the oracle on the host cores: one JSON line with the metric, its unit,
+    # the CPU record and an e2e object without host-device copies
+    sys.path.insert(0, ROOT)
+    import json
+    import bench
+    buf = io.StringIO()
+    with redirect_stdout(buf):
+        bench.reference_arm(SimpleNamespace(steps=1, warmup=0), rank=0, world=1)
+    lines = [ln for ln in buf.getvalue().splitlines() if ln.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["metric"] == bench.METRIC and d["unit"] == "keys/s"
+    assert d["value"] > 0 and d["higher_is_better"] is True and d["steps"] == 1 and d["n_gpus"] == 1
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == d["value"] and cb["sample"]
+    assert d["e2e"] == {"value": d["value"], "unit": "keys/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+    assert d["config"]["workload"]
