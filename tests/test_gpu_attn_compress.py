@@ -57,7 +57,10 @@ def _attn_case(T, k, n_swa, seed, holes=0.0, out_bf16=False, n_entries=5000, inv
 
 @pytest.mark.parametrize("T,k,n_swa", [(1, 512, 128), (3, 512, 128), (16, 512, 128), (200, 512, 128),
                                        (2, 100, 0), (2, 0, 37), (5, 2048, 128), (1, 1, 0),
-                                       (2, 1152, 128), (2, 1153, 128), (3, 33, 48)])
+                                       (2, 1152, 128), (2, 1153, 128), (3, 33, 48),
+                                       # 19 rows x 8 chunks = 152 CTAs: the last launch of the
+                                       # cluster kernel on 152 SMs; 20 rows: the split-K kernel
+                                       (19, 512, 128), (20, 512, 128)])
 def test_attention_matches_oracle(T, k, n_swa):
     _attn_case(T, k, n_swa, seed=T * 7 + k + n_swa)
 
