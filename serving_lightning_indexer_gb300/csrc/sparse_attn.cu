@@ -839,43 +839,45 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (!mbar_wait(bar_q + half, 0u, nullptr)) set_error(p.err, kErrTimeout);
   };
 
-  if (p.kv_ready) {  // the keys are ready before the previous launch completes
-    issue_records();
-    wait_records();
-    dequant_wave(0);
-    dequant_wave(1);
-  }
-  pdl_wait();
-  pdl_trigger();
-  // the row's q: eight 64-head x 64-dim atoms, swizzled by the tensor copy,
-  // in two halves so that the first wave's S MMAs start on the first half
-  if (tid == kTcMmaThread) {
-    mbar_arrive_expect_tx(bar_q, kH * kD);
-    mbar_arrive_expect_tx(bar_q + 1, kH * kD);
+  // Records and S waves each have one call site (a loop that is not
+  // unrolled), so every launch runs the same copy of their code whether the
+  // keys are gathered before the dependency wait (kv_ready, pass 0) or after
+  // it (pass 1): instruction fetches of code a previous launch has run are
+  // cheaper on the critical path.
+  const int rec_pass = p.kv_ready ? 0 : 1;
+#pragma unroll 1
+  for (int pass = 0; pass < 2; ++pass) {
+    if (pass == 1) {
+      pdl_wait();
+      pdl_trigger();
+      // the row's q: eight 64-head x 64-dim atoms, swizzled by the tensor copy,
+      // in two halves so that the first wave's S MMAs start on the first half
+      if (tid == kTcMmaThread) {
+        mbar_arrive_expect_tx(bar_q, kH * kD);
+        mbar_arrive_expect_tx(bar_q + 1, kH * kD);
 #pragma unroll
-    for (int a = 0; a < 8; ++a)
-      tma_load_2d(sQ + a * TcSmem::kQAtom, &map_q, a * 128, t * kH, bar_q + (a >> 2), l2_policy_evict_first());
+        for (int a = 0; a < 8; ++a)
+          tma_load_2d(sQ + a * TcSmem::kQAtom, &map_q, a * 128, t * kH, bar_q + (a >> 2), l2_policy_evict_first());
+      }
+      if (tid < kH) sSink[tid] = __ldg(p.sink + tid) * kLog2e;
+    }
+    if (pass == rec_pass) {
+      issue_records();
+      wait_records();
+      if (pass == 0) {  // kv_ready: both waves before the wait
+        dequant_wave(0);
+        dequant_wave(1);
+      }
+    }
   }
-  if (tid < kH) sSink[tid] = __ldg(p.sink + tid) * kLog2e;
-  if (p.kv_ready) {
+  // the S MMAs: after the wait, the first wave's MMAs run while the second
+  // wave is dequantised (keys gathered after the wait)
+#pragma unroll 1
+  for (int w = 0; w < 2; ++w) {
+    if (!p.kv_ready) dequant_wave(w);
     if (tid == kTcMmaThread) {
-      wait_q(0);
-      issue_s(0);
-      wait_q(1);
-      issue_s(1);
-    }
-  } else {  // the first wave's S MMAs run while the second wave is dequantised
-    issue_records();
-    wait_records();
-    dequant_wave(0);
-    if (tid == kTcMmaThread) {
-      wait_q(0);
-      issue_s(0);
-    }
-    dequant_wave(1);
-    if (tid == kTcMmaThread) {
-      wait_q(1);
-      issue_s(1);
+      wait_q(w);
+      issue_s(w);
     }
   }
 
