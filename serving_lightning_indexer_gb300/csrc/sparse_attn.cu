@@ -746,8 +746,13 @@ __device__ __noinline__ void tc_dequant_wave(const uint8_t* sRaw, uint8_t* sK, c
   __syncthreads();
 }
 
+// NS: the cluster size when fixed at compile time (8: the 640-key decode row,
+// whose instantiation has the combine's per-chunk loops at 8 instead of 16,
+// less code on the critical path), or 0 (p.nsplit, up to 16 chunks).
+template <int NS>
 __global__ void __launch_bounds__(kTcThreads, 1)
     sparse_attn_tc_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ TcParams p) {
+  constexpr int kMaxNs = NS > 0 ? NS : kMaxCluster;
   extern __shared__ uint8_t tc_smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(tc_smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = sm + TcSmem::kOffQ;
@@ -767,7 +772,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
   const int rank = blockIdx.x;  // the cluster spans gridDim.x
-  const int ns = p.nsplit;
+  const int ns = NS > 0 ? NS : p.nsplit;
   const int tl = blockIdx.y;    // row within this launch
   const int t = p.t_base + tl;
 
@@ -1052,10 +1057,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // both arrive in one round trip to L2
     uint4 pv[8];
     load_batch(0, pv);
-    float wr[kMaxCluster], ml_l[kMaxCluster];
+    float wr[kMaxNs], ml_l[kMaxNs];
     float M = sSink[h];
 #pragma unroll
-    for (int r = 0; r < kMaxCluster; ++r) {
+    for (int r = 0; r < kMaxNs; ++r) {
       float2 ml = make_float2(-INFINITY, 0.f);
       if (r < ns) ml = __ldcg(p.part_ml + (rowbase + r) * kH + h);
       wr[r] = ml.x;
@@ -1064,7 +1069,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     float D = ex2_approx(sSink[h] - M);
 #pragma unroll
-    for (int r = 0; r < kMaxCluster; ++r) {
+    for (int r = 0; r < kMaxNs; ++r) {
       wr[r] = (wr[r] == -INFINITY) ? 0.f : ex2_approx(wr[r] - M) * ml_l[r];
       D += wr[r];
     }
@@ -1072,7 +1077,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (c == 0 && p.lse) p.lse[static_cast<long long>(t) * kH + h] = (M + log2f(D)) * kLn2;
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int r0 = 0; r0 < kMaxCluster; r0 += 8) {  // 8 chunks' loads in flight at a time
+    for (int r0 = 0; r0 < kMaxNs; r0 += 8) {  // 8 chunks' loads in flight at a time
       if (r0 > 0) {
         if (r0 >= ns) break;
         load_batch(r0, pv);
@@ -1190,10 +1195,13 @@ static cudaError_t launch_sparse_attn_tc(const AttnLaunch& a, void* ws, const De
   if (encode_tmap_2d_u8(&map_q, a.q, static_cast<uint64_t>(kD) * 2, static_cast<uint64_t>(a.T) * kH,
                         static_cast<uint64_t>(kD) * 2, 128, kH) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
-  cudaError_t e = prefer_max_smem(sparse_attn_tc_kernel, TcSmem::kAlloc);
+  // rows of 8 chunks (640 keys: 128 SWA + 512) take the instantiation with the
+  // cluster size fixed at 8
+  auto kern = nchunks == 8 ? sparse_attn_tc_kernel<8> : sparse_attn_tc_kernel<0>;
+  cudaError_t e = prefer_max_smem(kern, TcSmem::kAlloc);
   if (e != cudaSuccess) return e;
   if (nchunks > 8) {
-    e = cudaFuncSetAttribute(sparse_attn_tc_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e != cudaSuccess) return e;
   }
   for (int t0 = 0; t0 < a.T; t0 += kTcRowsPerLaunch) {
@@ -1213,7 +1221,7 @@ static cudaError_t launch_sparse_attn_tc(const AttnLaunch& a, void* ws, const De
     attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    e = cudaLaunchKernelEx(&cfg, sparse_attn_tc_kernel, map_q, p);
+    e = cudaLaunchKernelEx(&cfg, kern, map_q, p);
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;
